@@ -1,0 +1,172 @@
+/*
+ * tokenselect.h - C ABI of the token-level KV selection decode path (sm_103a).
+ *
+ * The method: TokenSelect ("TokenSelect: Efficient Long-Context Inference and
+ * Length Extrapolation for LLMs via Dynamic Token-Level KV Cache Selection").
+ * One decode step of one layer is, per sequence of the batch:
+ *
+ *   1. Selection Cache check: cos(Q, C_Q) >= theta reuses the cached indices
+ *      (deep notes, Appendix Algorithm 1; review, section 3.2).
+ *   2. Paged dot product: l[h][i] = alpha <q_h, K_{h/G}[i]> over all N cached
+ *      tokens of the paged cache (deep notes, Appendix Algorithm 2).
+ *   3. Head soft vote: v[i] = sum_h softmax_h(l[h])[i] (deep notes, "Head soft
+ *      vote", equation T_head-soft-vote).
+ *   4. Selection: TopK(v) over the candidates [s, N-w), or the shortest
+ *      (vote desc, index asc) prefix with mass >= p*H, united with the sinks
+ *      [0, s) and the local window [N-w, N) (review, section 4.2, "2K+512").
+ *   5. Sparse attention over the selected tokens (deep notes, "Formalising
+ *      selective sparse attention", equation for O-hat).
+ *
+ * Conventions for every call below:
+ *  - Tensor arguments are DEVICE pointers owned by the caller. The library
+ *    never frees them. A context owns its own device scratch; a cache handle
+ *    owns C_Q and C_T. Both are freed by their destroy call.
+ *  - Layouts are dense row-major. KV pools are [num_pages][H_kv][P][d] (fp32
+ *    or bf16, 16-byte aligned base); token i of sequence b lives in page
+ *    page_table[b * max_pages_per_seq + i / P] at slot i % P (page tables are
+ *    int32 [B][max_pages_per_seq], entries past a sequence unused). Queries are
+ *    fp32 [B][H][d]. Query head h reads KV head h / (H / H_kv).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL is the legacy default
+ *    stream) and returns before it runs. Argument and shape errors are
+ *    reported synchronously by the return value, before anything is enqueued.
+ *    Errors found on the device (a page id outside the pool, an output that
+ *    does not fit, a wait that ran out) are recorded in the context's status
+ *    word and read back with ts_get_status. Nothing aborts or traps.
+ *  - A context is bound to the device current at ts_create and is not thread
+ *    safe: calls on one context must be serialised by the caller, and calls
+ *    that share a context's scratch must go to one stream (or be ordered).
+ */
+#ifndef TOKENSELECT_H
+#define TOKENSELECT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ts_ctx ts_ctx;     /* opaque; library-owned */
+typedef struct ts_cache ts_cache; /* opaque; library-owned */
+
+typedef enum {
+  TS_OK = 0,
+  TS_ERR_INVALID_ARG = 1,      /* null pointer, bad enum, negative size        */
+  TS_ERR_SHAPE = 2,            /* sizes beyond what the context was created for */
+  TS_ERR_UNSUPPORTED = 3,      /* head geometry without a compiled kernel       */
+  TS_ERR_CUDA = 4,             /* a CUDA runtime call failed                    */
+  TS_ERR_PAGE_OOB = 5,         /* device: page-table entry outside the pool     */
+  TS_ERR_CAPACITY = 6,         /* device: selection larger than its buffer      */
+  TS_ERR_TIMEOUT = 7,          /* device: a bounded wait ran out                */
+  TS_ERR_COOP_UNAVAILABLE = 8, /* a cooperative launch was refused              */
+  TS_ERR_SEQ_LEN = 9           /* device: seq_lens[b] < 0 or above the maximum  */
+} ts_status;
+
+enum { TS_KV_F32 = 0, TS_KV_BF16 = 1 };
+enum { TS_SELECT_TOPK = 0, TS_SELECT_TOPP = 1 };
+
+/* Shape of the model's attention and of the caller's pools, fixed per context. */
+typedef struct {
+  int n_q_heads;          /* H                                                  */
+  int n_kv_heads;         /* H_kv, divides H                                    */
+  int head_dim;           /* d (64 or 128)                                      */
+  int page_size;          /* P tokens per page (16)                             */
+  int kv_dtype;           /* TS_KV_F32 or TS_KV_BF16                            */
+  int max_batch;          /* largest B of any call                              */
+  int max_pages_per_seq;  /* page-table row stride; max tokens = this * P       */
+  int64_t num_pages;      /* pool size in pages; larger page ids are errors     */
+} ts_config;
+
+/* Selection parameters (review, section 4.2: k = 2048, 4 sinks, 512 local;
+ * deep notes, Algorithm 1: theta = 0.9). */
+typedef struct {
+  int mode;               /* TS_SELECT_TOPK or TS_SELECT_TOPP                   */
+  int k;                  /* top-k budget over the candidates                   */
+  int n_sink;             /* s: tokens [0, s) always kept                       */
+  int n_local;            /* w: tokens [N-w, N) always kept                     */
+  float top_p;            /* mass fraction for TOPP; >= 1 keeps every token     */
+  float theta;            /* cache threshold; > 1 never hits                    */
+  float softmax_scale;    /* alpha; 0 means 1/sqrt(d)                           */
+} ts_select_params;
+
+/* Context: validates and records cfg, allocates the device scratch for
+ * max_batch sequences of max_pages_per_seq * page_size tokens on the current
+ * device. Returns TS_ERR_UNSUPPORTED for a head geometry with no kernel. */
+ts_status ts_create(ts_ctx** out, const ts_config* cfg);
+ts_status ts_destroy(ts_ctx* ctx);
+
+/* Selection Cache for n_layers layers of max_batch sequences: per (sequence,
+ * layer) a first-query flag, C_Q (fp32 H*d) and C_T (int32, `capacity`
+ * entries). Starts empty (every first query misses). */
+ts_status ts_cache_create(ts_ctx* ctx, ts_cache** out, int n_layers, int capacity);
+ts_status ts_cache_destroy(ts_cache* cache);
+/* Marks every (sequence, layer) as empty again; enqueued on `stream`. */
+ts_status ts_cache_reset(ts_cache* cache, void* stream);
+
+/* Algorithm 1's test for one layer: hit[b] = 1 iff the entry of (b, layer)
+ * is filled, and cos(q_b, C_Q) >= theta over the H*d query (fp32).
+ * q [B][H][d]; hit uint8 [B]; cos_out fp32 [B] or NULL (NaN when empty). */
+ts_status ts_cache_check(ts_ctx* ctx, ts_cache* cache, int layer, const float* q, int B,
+                         float theta, uint8_t* hit, float* cos_out, void* stream);
+
+/* Paged dot product + fused per-head softmax normaliser + head soft vote.
+ * For each b with skip == NULL or skip[b] == 0:
+ *   vote[b * vote_stride + i] = sum_h exp(l[h][i] - L_h),  i < seq_lens[b],
+ * with l = scale * <q_h, K_{h/G}[i]> and L_h = log sum_i exp(l[h][i]).
+ * The H x N logits are context scratch and are not returned. scale 0 means
+ * 1/sqrt(d). seq_lens int32 [B] on the device, each in [0, max_pages_per_seq
+ * * page_size]; vote_stride >= max_pages_per_seq * page_size. Entries past
+ * seq_lens[b] and skipped rows are left untouched. */
+ts_status ts_score(ts_ctx* ctx, const float* q, const void* k_pool, const int32_t* page_table,
+                   const int32_t* seq_lens, int B, const uint8_t* skip, float scale,
+                   float* vote, int64_t vote_stride, void* stream);
+
+/* Selection (top-k or top-p) united with sinks and window, ascending.
+ * For each b: if hit != NULL and hit[b] != 0, the index set is rebuilt from
+ * the cache entry (cached part within [s, N-w), plus the current sinks and
+ * window); otherwise it is selected from vote and, if cache != NULL, the
+ * entry of (b, layer) takes the selected part and q_b (Algorithm 1). Ties in
+ * the vote go to the lower index. idx int32 [B][idx_stride] receives the
+ * count[b] indices; a count above idx_stride (or a selected part above the
+ * cache capacity) records TS_ERR_CAPACITY and writes nothing past the end.
+ * q may be NULL when cache is NULL. */
+ts_status ts_select(ts_ctx* ctx, ts_cache* cache, int layer, const float* q, const float* vote,
+                    int64_t vote_stride, const int32_t* seq_lens, int B, const uint8_t* hit,
+                    const ts_select_params* params, int32_t* idx, int64_t idx_stride,
+                    int32_t* count, void* stream);
+
+/* Sparse attention: out[b][h] = softmax_i(scale q_h.K_i) V_i over the count[b]
+ * indices idx[b * idx_stride + j] (split over the index list, merged by
+ * log-sum-exp). out fp32 [B][H][d]; lse fp32 [B][H] or NULL. An empty index
+ * list gives out = 0 and lse = -inf. */
+ts_status ts_sparse_attend(ts_ctx* ctx, const float* q, const void* k_pool, const void* v_pool,
+                           const int32_t* page_table, const int32_t* idx, int64_t idx_stride,
+                           const int32_t* count, int B, float scale, float* out, float* lse,
+                           void* stream);
+
+/* One whole decode step of one layer, stream-ordered, no host synchronisation:
+ * cache check (when cache != NULL and theta <= 1), score and vote for the
+ * sequences that miss, selection (and cache update), sparse attention.
+ * hit uint8 [B] (may be NULL) receives the cache decisions. vote receives the
+ * votes of the missing sequences (may be NULL: context scratch is used). */
+ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q,
+                         const void* k_pool, const void* v_pool, const int32_t* page_table,
+                         const int32_t* seq_lens, int B, const ts_select_params* params,
+                         float* vote, int64_t vote_stride, int32_t* idx, int64_t idx_stride,
+                         int32_t* count, float* out, float* lse, uint8_t* hit, void* stream);
+
+/* Synchronises `stream`, then reads and clears the device status word.
+ * *device_status receives TS_OK or the first device error since the last read. */
+ts_status ts_get_status(ts_ctx* ctx, ts_status* device_status, void* stream);
+
+/* Static text for a status code. */
+const char* ts_status_str(ts_status s);
+
+/* Library version, e.g. 100 for 0.1.0. */
+int ts_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOKENSELECT_H */

@@ -1,0 +1,96 @@
+"""GPU decode path against the CPU oracle, through the C ABI, on seeded inputs.
+
+Small sizes check every output of every step (several score CTAs, ragged last
+pages, several selection chunks); the full sizes of the 128K, batched and
+top-p workloads run the same comparison on fewer steps, and the 1M-token layer
+on one step.
+"""
+import pytest
+import torch
+
+import workloads as W
+from parity import run_trajectory
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _run(sp, steps, **kw):
+    wl = W.generate(sp, DEV)
+    rep = run_trajectory(wl, steps, **kw)
+    print(f"{sp.name}: steps={rep.steps} hits={rep.hits} replays={rep.replays} "
+          f"band_swaps={rep.band_swaps} worst_vote_rel={rep.worst_vote_rel:.2e}")
+    return rep
+
+
+def test_tiny_fp32_trajectory_with_cache():
+    rep = _run(W.spec(0), 8)
+    assert rep.steps == 8
+
+
+def test_tiny_fp32_separate_calls_all_miss():
+    _run(W.spec(0), 4, separate_calls=True)
+
+
+@pytest.mark.parametrize("overrides", [
+    dict(n0=(3001,), steps=3, k=256, n_local=64),                              # GQA 32/8, ragged
+    dict(n0=(5000,), steps=2, k=2048),                                         # k close to |C|
+    dict(n0=(70,), steps=3, k=2048),                                           # N < k+s+w: all tokens
+])
+def test_llama_geometry_small(overrides):
+    sp = W.spec(1, **overrides)
+    _run(sp, sp.steps, theta=2.0)
+    _run(sp, sp.steps)
+
+
+def test_qwen_geometry_batched_small():
+    sp = W.spec(2, n0=(1000, 4099, 2500), n0_range=None, batch=3, steps=3, k=300, n_local=50)
+    _run(sp, 3)
+    _run(sp, 2, theta=2.0)
+
+
+@pytest.mark.parametrize("geom", [
+    dict(n_q_heads=8, n_kv_heads=2, head_dim=64, kv_dtype="f32"),
+    dict(n_q_heads=32, n_kv_heads=8, head_dim=128, kv_dtype="f32"),
+    dict(n_q_heads=8, n_kv_heads=8, head_dim=128, kv_dtype="bf16"),
+    dict(n_q_heads=8, n_kv_heads=4, head_dim=64, kv_dtype="bf16"),
+    dict(n_q_heads=16, n_kv_heads=2, head_dim=128, kv_dtype="bf16"),
+])
+def test_other_geometries(geom):
+    sp = W.spec(1, n0=(2300,), steps=2, k=200, n_local=32, key_scale="logu3", needles="lnN2", **geom)
+    _run(sp, 2, theta=2.0)
+
+
+def test_topp_small():
+    for p in (0.9, 0.99):
+        sp = W.spec(4, n0=(6000, 6000, 7000, 9000), steps=3, top_p=p)
+        _run(sp, 3)
+        _run(sp, 2, theta=2.0)
+
+
+def test_topp_all_tokens_when_p_is_one():
+    sp = W.spec(4, n0=(300,) * 4, steps=1, top_p=1.0, needles="lnN2")
+    _run(sp, 1, theta=2.0)
+
+
+# ------------------------------------------------------------ full sizes
+
+def test_llama_128k_full():
+    sp = W.spec(1, steps=6)
+    _run(sp, 6)
+
+
+def test_qwen_batched_full():
+    sp = W.spec(2, steps=2)
+    _run(sp, 2, theta=2.0)
+
+
+def test_topp_256k_full():
+    sp = W.spec(4, steps=2)
+    _run(sp, 2)
+
+
+def test_llama_1m_one_layer_full():
+    sp = W.spec(3, layers=1, steps=1)
+    _run(sp, 1, theta=2.0)
+    torch.cuda.empty_cache()

@@ -1,0 +1,277 @@
+// C ABI of libtokenselect: argument validation, context and cache lifetime,
+// and the stream-ordered composition of one decode step.
+#include <cmath>
+#include <cstdlib>
+#include <new>
+
+#include "ts_internal.h"
+
+using namespace ts;
+
+namespace {
+
+template <typename T>
+cudaError_t alloc(T** p, size_t n) {
+  *p = nullptr;
+  if (n == 0) n = 1;
+  return cudaMalloc(reinterpret_cast<void**>(p), n * sizeof(T));
+}
+
+void free_ctx_buffers(ts_ctx* c) {
+  cudaFree(c->status);
+  cudaFree(c->logits);
+  cudaFree(c->partials);
+  cudaFree(c->stats);
+  cudaFree(c->counters);
+  cudaFree(c->sel_state);
+  cudaFree(c->hist);
+  cudaFree(c->mass_hist);
+  cudaFree(c->chunk_counts);
+  cudaFree(c->attn_part);
+  cudaFree(c->vote);
+  cudaFree(c->hit);
+}
+
+float resolve_scale(const ts_ctx* ctx, float scale) {
+  return scale == 0.f ? 1.f / std::sqrt((float)ctx->cfg.head_dim) : scale;
+}
+
+bool valid_params(const ts_select_params* p) {
+  if (!p) return false;
+  if (p->mode != TS_SELECT_TOPK && p->mode != TS_SELECT_TOPP) return false;
+  if (p->k < 0 || p->n_sink < 0 || p->n_local < 0) return false;
+  if (p->mode == TS_SELECT_TOPP && !(p->top_p > 0.f)) return false;
+  if (std::isnan(p->theta) || std::isnan(p->softmax_scale)) return false;
+  return true;
+}
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+}  // namespace
+
+extern "C" {
+
+int ts_version(void) { return 100; }
+
+const char* ts_status_str(ts_status s) {
+  switch (s) {
+    case TS_OK: return "ok";
+    case TS_ERR_INVALID_ARG: return "invalid argument";
+    case TS_ERR_SHAPE: return "shape outside the context's limits";
+    case TS_ERR_UNSUPPORTED: return "head geometry not compiled";
+    case TS_ERR_CUDA: return "CUDA runtime error";
+    case TS_ERR_PAGE_OOB: return "page-table entry outside the pool";
+    case TS_ERR_CAPACITY: return "selection larger than its output buffer";
+    case TS_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case TS_ERR_COOP_UNAVAILABLE: return "cooperative launch refused";
+    case TS_ERR_SEQ_LEN: return "sequence length outside [0, max tokens]";
+  }
+  return "unknown status";
+}
+
+ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
+  if (!out || !cfg) return TS_ERR_INVALID_ARG;
+  *out = nullptr;
+  const ts_config& c = *cfg;
+  if (c.n_q_heads < 1 || c.n_kv_heads < 1 || c.n_q_heads % c.n_kv_heads != 0) return TS_ERR_INVALID_ARG;
+  if (c.max_batch < 1 || c.max_pages_per_seq < 1 || c.num_pages < 1 || c.head_dim < 1) return TS_ERR_INVALID_ARG;
+  if (c.kv_dtype != TS_KV_F32 && c.kv_dtype != TS_KV_BF16) return TS_ERR_INVALID_ARG;
+  if (c.page_size != kPage) return TS_ERR_UNSUPPORTED;
+  if (c.n_kv_heads > kCounterSlots - 2 || c.n_q_heads > 256) return TS_ERR_UNSUPPORTED;
+  if ((int64_t)c.max_pages_per_seq * kPage > (int64_t)1 << 30) return TS_ERR_SHAPE;
+  if (!score_supported(c)) return TS_ERR_UNSUPPORTED;
+
+  ts_ctx* ctx = new (std::nothrow) ts_ctx();
+  if (!ctx) return TS_ERR_CUDA;
+  ctx->cfg = c;
+  if (cudaGetDevice(&ctx->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess) {
+    delete ctx;
+    return TS_ERR_CUDA;
+  }
+  const size_t B = c.max_batch, H = c.n_q_heads, HKV = c.n_kv_heads, G = H / HKV, D = c.head_dim;
+  ctx->max_tokens = c.max_pages_per_seq * kPage;
+  ctx->score_max_chunks = (c.max_pages_per_seq + kScorePagesPerCta - 1) / kScorePagesPerCta;
+  ctx->sel_max_chunks = (ctx->max_tokens + kSelChunk - 1) / kSelChunk;
+  ctx->attn_splits = kAttnMaxSplits;
+  const size_t T = ctx->max_tokens;
+  cudaError_t e = cudaSuccess;
+  auto chk = [&](cudaError_t r) {
+    if (e == cudaSuccess) e = r;
+  };
+  chk(alloc(&ctx->status, 1));
+  chk(alloc(&ctx->logits, B * H * T));
+  chk(alloc(&ctx->partials, B * ctx->score_max_chunks * H));
+  chk(alloc(&ctx->stats, B * H));
+  chk(alloc(&ctx->counters, B * kCounterSlots));
+  chk(alloc(&ctx->sel_state, B));
+  chk(alloc(&ctx->hist, B * 2048));
+  chk(alloc(&ctx->mass_hist, B * 2048));
+  chk(alloc(&ctx->chunk_counts, B * ctx->sel_max_chunks));
+  chk(alloc(&ctx->attn_part, B * HKV * kAttnMaxSplits * G * (D + 2)));
+  chk(alloc(&ctx->vote, B * T));
+  chk(alloc(&ctx->hit, B));
+  if (e == cudaSuccess) chk(cudaMemset(ctx->status, 0, sizeof(int)));
+  if (e == cudaSuccess) chk(cudaMemset(ctx->counters, 0, B * kCounterSlots * sizeof(unsigned)));
+  if (e == cudaSuccess) chk(cudaMemset(ctx->hist, 0, B * 2048 * sizeof(unsigned)));
+  if (e == cudaSuccess) chk(cudaMemset(ctx->mass_hist, 0, B * 2048 * sizeof(unsigned long long)));
+  if (e == cudaSuccess) chk(cudaMemset(ctx->hit, 0, B));
+  if (e == cudaSuccess) chk(cudaDeviceSynchronize());
+  if (e != cudaSuccess) {
+    free_ctx_buffers(ctx);
+    delete ctx;
+    return TS_ERR_CUDA;
+  }
+  *out = ctx;
+  return TS_OK;
+}
+
+ts_status ts_destroy(ts_ctx* ctx) {
+  if (!ctx) return TS_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  free_ctx_buffers(ctx);
+  delete ctx;
+  return TS_OK;
+}
+
+ts_status ts_cache_create(ts_ctx* ctx, ts_cache** out, int n_layers, int capacity) {
+  if (!ctx || !out || n_layers < 1 || capacity < 1) return TS_ERR_INVALID_ARG;
+  *out = nullptr;
+  ts_cache* c = new (std::nothrow) ts_cache();
+  if (!c) return TS_ERR_CUDA;
+  c->ctx = ctx;
+  c->n_layers = n_layers;
+  c->capacity = capacity;
+  const size_t LB = (size_t)n_layers * ctx->cfg.max_batch;
+  const size_t HD = (size_t)ctx->cfg.n_q_heads * ctx->cfg.head_dim;
+  cudaError_t e = alloc(&c->cq, LB * HD);
+  if (e == cudaSuccess) e = alloc(&c->ct, LB * capacity);
+  if (e == cudaSuccess) e = alloc(&c->ct_count, LB);
+  if (e == cudaSuccess) e = alloc(&c->filled, LB);
+  if (e == cudaSuccess) e = cudaMemset(c->filled, 0, LB);
+  if (e == cudaSuccess) e = cudaMemset(c->ct_count, 0, LB * sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cudaFree(c->cq);
+    cudaFree(c->ct);
+    cudaFree(c->ct_count);
+    cudaFree(c->filled);
+    delete c;
+    return TS_ERR_CUDA;
+  }
+  *out = c;
+  return TS_OK;
+}
+
+ts_status ts_cache_destroy(ts_cache* c) {
+  if (!c) return TS_ERR_INVALID_ARG;
+  cudaDeviceSynchronize();
+  cudaFree(c->cq);
+  cudaFree(c->ct);
+  cudaFree(c->ct_count);
+  cudaFree(c->filled);
+  delete c;
+  return TS_OK;
+}
+
+ts_status ts_cache_reset(ts_cache* c, void* stream) {
+  if (!c) return TS_ERR_INVALID_ARG;
+  return launch_cache_reset(c, as_stream(stream));
+}
+
+ts_status ts_cache_check(ts_ctx* ctx, ts_cache* cache, int layer, const float* q, int B, float theta,
+                         uint8_t* hit, float* cos_out, void* stream) {
+  if (!ctx || !cache || !q || !hit || cache->ctx != ctx) return TS_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= cache->n_layers || B < 1 || B > ctx->cfg.max_batch) return TS_ERR_SHAPE;
+  if (std::isnan(theta)) return TS_ERR_INVALID_ARG;
+  return launch_cache_check(ctx, cache, layer, q, B, theta, hit, cos_out, as_stream(stream));
+}
+
+ts_status ts_score(ts_ctx* ctx, const float* q, const void* k_pool, const int32_t* page_table,
+                   const int32_t* seq_lens, int B, const uint8_t* skip, float scale, float* vote,
+                   int64_t vote_stride, void* stream) {
+  if (!ctx || !q || !k_pool || !page_table || !seq_lens || !vote) return TS_ERR_INVALID_ARG;
+  if (B < 1 || B > ctx->cfg.max_batch || vote_stride < ctx->max_tokens) return TS_ERR_SHAPE;
+  if (std::isnan(scale)) return TS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(k_pool) % 16 != 0) return TS_ERR_INVALID_ARG;
+  ScoreCall c{q, k_pool, page_table, seq_lens, skip, B, resolve_scale(ctx, scale), vote, vote_stride};
+  return launch_score(ctx, c, as_stream(stream));
+}
+
+ts_status ts_select(ts_ctx* ctx, ts_cache* cache, int layer, const float* q, const float* vote,
+                    int64_t vote_stride, const int32_t* seq_lens, int B, const uint8_t* hit,
+                    const ts_select_params* params, int32_t* idx, int64_t idx_stride, int32_t* count,
+                    void* stream) {
+  if (!ctx || !vote || !seq_lens || !idx || !count || !valid_params(params)) return TS_ERR_INVALID_ARG;
+  if (B < 1 || B > ctx->cfg.max_batch || vote_stride < ctx->max_tokens || idx_stride < 1) return TS_ERR_SHAPE;
+  if (hit && !cache) return TS_ERR_INVALID_ARG;
+  if (cache) {
+    if (cache->ctx != ctx || !q) return TS_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= cache->n_layers) return TS_ERR_SHAPE;
+  }
+  SelectCall c{cache, layer, q, vote, vote_stride, seq_lens, B, hit, *params, idx, idx_stride, count};
+  return launch_select(ctx, c, as_stream(stream));
+}
+
+ts_status ts_sparse_attend(ts_ctx* ctx, const float* q, const void* k_pool, const void* v_pool,
+                           const int32_t* page_table, const int32_t* idx, int64_t idx_stride,
+                           const int32_t* count, int B, float scale, float* out, float* lse, void* stream) {
+  if (!ctx || !q || !k_pool || !v_pool || !page_table || !idx || !count || !out) return TS_ERR_INVALID_ARG;
+  if (B < 1 || B > ctx->cfg.max_batch || idx_stride < 1) return TS_ERR_SHAPE;
+  if (std::isnan(scale)) return TS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(k_pool) % 16 != 0 || reinterpret_cast<uintptr_t>(v_pool) % 16 != 0)
+    return TS_ERR_INVALID_ARG;
+  AttendCall c{q, k_pool, v_pool, page_table, idx, idx_stride, count, B, resolve_scale(ctx, scale), out, lse};
+  return launch_attend(ctx, c, as_stream(stream));
+}
+
+ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q, const void* k_pool,
+                         const void* v_pool, const int32_t* page_table, const int32_t* seq_lens, int B,
+                         const ts_select_params* params, float* vote, int64_t vote_stride, int32_t* idx,
+                         int64_t idx_stride, int32_t* count, float* out, float* lse, uint8_t* hit,
+                         void* stream) {
+  if (!ctx || !q || !k_pool || !v_pool || !page_table || !seq_lens || !idx || !count || !out ||
+      !valid_params(params))
+    return TS_ERR_INVALID_ARG;
+  if (B < 1 || B > ctx->cfg.max_batch || idx_stride < 1) return TS_ERR_SHAPE;
+  if (cache && (cache->ctx != ctx || layer < 0 || layer >= cache->n_layers)) return TS_ERR_INVALID_ARG;
+  if (!vote) {
+    vote = ctx->vote;
+    vote_stride = ctx->max_tokens;
+  }
+  if (vote_stride < ctx->max_tokens) return TS_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(k_pool) % 16 != 0 || reinterpret_cast<uintptr_t>(v_pool) % 16 != 0)
+    return TS_ERR_INVALID_ARG;
+  cudaStream_t s = as_stream(stream);
+  const float scale = resolve_scale(ctx, params->softmax_scale);
+  const bool use_cache = cache != nullptr && params->theta <= 1.f;
+  uint8_t* hbuf = hit ? hit : ctx->hit;
+  ts_status st = TS_OK;
+  if (use_cache) {
+    st = launch_cache_check(ctx, cache, layer, q, B, params->theta, hbuf, nullptr, s);
+    if (st != TS_OK) return st;
+  } else if (hit) {
+    if (cudaMemsetAsync(hit, 0, B, s) != cudaSuccess) return TS_ERR_CUDA;
+  }
+  const uint8_t* skip = use_cache ? hbuf : nullptr;
+  ScoreCall sc{q, k_pool, page_table, seq_lens, skip, B, scale, vote, vote_stride};
+  st = launch_score(ctx, sc, s);
+  if (st != TS_OK) return st;
+  SelectCall sel{cache, layer, q, vote, vote_stride, seq_lens, B, skip, *params, idx, idx_stride, count};
+  st = launch_select(ctx, sel, s);
+  if (st != TS_OK) return st;
+  AttendCall ac{q, k_pool, v_pool, page_table, idx, idx_stride, count, B, scale, out, lse};
+  return launch_attend(ctx, ac, s);
+}
+
+ts_status ts_get_status(ts_ctx* ctx, ts_status* device_status, void* stream) {
+  if (!ctx || !device_status) return TS_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return TS_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, ctx->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TS_ERR_CUDA;
+  if (cudaMemset(ctx->status, 0, sizeof(int)) != cudaSuccess) return TS_ERR_CUDA;
+  *device_status = static_cast<ts_status>(v);
+  return TS_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,290 @@
+// Selective sparse attention over the selected tokens.
+//
+// TokenSelect deep notes, "Formalising selective sparse attention", equation
+// for O-hat: per head, softmax(q K_sel^T / sqrt(d)) V_sel over the selected
+// tokens (which include the current one). Only indices cross from the
+// selection (deep notes, "Paged Dot Product Kernel design": O(k) index I/O
+// instead of moving 2kd values); the rows are gathered here through the page
+// table.
+//
+// Grid: (split, KV head, sequence). A CTA takes a contiguous slice of the
+// index list, stages the K and V rows of 64 tokens at a time into shared
+// memory with one 1-D bulk copy per row (all in flight at once, one mbarrier),
+// and runs an online softmax for the G query heads of its KV head. The splits
+// are merged by log-sum-exp in split order by the last CTA of each
+// (sequence, KV head).
+#include "ts_common.cuh"
+
+namespace ts {
+namespace {
+
+constexpr int cpow2(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+template <typename KT, int D, int G>
+struct AttShape {
+  static constexpr int EPC = KV<KT>::kPerChunk;  // elements per 16-byte chunk
+  static constexpr int LPT = D / EPC;            // lanes per token row
+  static constexpr int TPW = 32 / LPT;           // tokens per warp step
+  static constexpr int GP = cpow2(G);
+  static constexpr int WARPS = 4;
+  static constexpr int THREADS = WARPS * 32;
+  static constexpr int GROUPS = WARPS * TPW;     // independent softmax states per CTA
+  static constexpr int SUB = 64;                 // tokens staged per round
+  static constexpr int ROW_BYTES = D * (int)sizeof(KT);
+  static_assert(32 % LPT == 0 && LPT <= 32 && GP <= LPT, "lane split");
+  static_assert(ROW_BYTES % 16 == 0, "row copies");
+  static constexpr size_t smem_bytes() {
+    return 2ull * SUB * ROW_BYTES + (size_t)GROUPS * G * (D + 2) * sizeof(float) + SUB * sizeof(int) + 16;
+  }
+};
+
+struct AttKArgs {
+  const float* q;
+  const unsigned char* k_pool;
+  const unsigned char* v_pool;
+  const int32_t* page_table;
+  int pt_stride;
+  int64_t num_pages;
+  int max_tokens;
+  const int32_t* idx;
+  int64_t idx_stride;
+  const int32_t* count;
+  int H, HKV;
+  float scale;
+  float* out;
+  float* lse;
+  float* part;  // [B][HKV][nsplit][G*(D+2)]
+  unsigned* counters;
+  int* status;
+};
+
+template <typename KT, int D, int G>
+__global__ void __launch_bounds__(AttShape<KT, D, G>::THREADS) attend_kernel(AttKArgs a) {
+  using S = AttShape<KT, D, G>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  KT* Ks = reinterpret_cast<KT*>(smem);
+  KT* Vs = Ks + S::SUB * D;
+  float* mg = reinterpret_cast<float*>(Vs + S::SUB * D);  // [GROUPS][G][D] then m, l
+  float* mm = mg + (size_t)S::GROUPS * G * D;             // [GROUPS][G]
+  float* ml = mm + S::GROUPS * G;                          // [GROUPS][G]
+  int* tokflag = reinterpret_cast<int*>(ml + S::GROUPS * G);
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_last;
+
+  const int split = blockIdx.x, nsplit = gridDim.x, g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cnt = (int)min((int64_t)max(a.count[b], 0), a.idx_stride);  // never read past the index row
+  const int per = (cnt + nsplit - 1) / nsplit;
+  const int t_begin = min(cnt, split * per), t_end = min(cnt, t_begin + per);
+  const int lt = lane % S::LPT;                       // chunk of the row this lane reads
+  const int slot = warp * S::TPW + lane / S::LPT;     // token group of this lane
+
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  float qr[S::GP][S::EPC];
+#pragma unroll
+  for (int j = 0; j < S::GP; ++j)
+#pragma unroll
+    for (int e = 0; e < S::EPC; ++e)
+      qr[j][e] = (j < G) ? a.q[((size_t)b * a.H + g * G + j) * D + lt * S::EPC + e] : 0.f;
+  float m[G], l[G], o[G][S::EPC];
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    m[j] = -INFINITY;
+    l[j] = 0.f;
+#pragma unroll
+    for (int e = 0; e < S::EPC; ++e) o[j][e] = 0.f;
+  }
+  __syncthreads();
+
+  const int32_t* ib = a.idx + (size_t)b * a.idx_stride;
+  const int32_t* pt = a.page_table + (size_t)b * a.pt_stride;
+  uint32_t phase = 0;
+  bool ok = true;
+  for (int s0 = t_begin; s0 < t_end && ok; s0 += S::SUB) {
+    const int ns = min(S::SUB, t_end - s0);
+    __syncthreads();  // the previous round is fully consumed
+    if (tid == 0) mbar_arrive_expect_tx(&bar, 2u * ns * S::ROW_BYTES);
+    __syncthreads();
+    for (int i = tid; i < 2 * ns; i += S::THREADS) {
+      const int j = i >> 1;
+      const int t = ib[s0 + j];
+      int page = -1;
+      if (t >= 0 && t < a.max_tokens) page = pt[t / kPage];
+      const bool valid = page >= 0 && (int64_t)page < a.num_pages;
+      const size_t off = valid ? (((size_t)page * a.HKV + g) * kPage + (t % kPage)) * S::ROW_BYTES : 0;
+      if (i & 1) {
+        bulk_g2s(Vs + (size_t)j * D, a.v_pool + off, S::ROW_BYTES, &bar);
+      } else {
+        bulk_g2s(Ks + (size_t)j * D, a.k_pool + off, S::ROW_BYTES, &bar);
+        tokflag[j] = valid;
+        if (!valid) set_error(a.status, TS_ERR_PAGE_OOB);
+      }
+    }
+    const bool landed = mbar_wait(&bar, phase);
+    phase ^= 1u;
+    ok = __syncthreads_and(landed) != 0;  // block-uniform
+    if (!ok) {
+      if (tid == 0) set_error(a.status, TS_ERR_TIMEOUT);
+      break;
+    }
+    for (int j0 = 0; j0 < ns; j0 += S::GROUPS) {
+      const int j = j0 + slot;
+      const bool act = j < ns;
+      const int jj = act ? j : 0;
+      float kf[S::EPC], vf[S::EPC];
+      KV<KT>::unpack(lds128(Ks + (size_t)jj * D + lt * S::EPC), kf);
+      KV<KT>::unpack(lds128(Vs + (size_t)jj * D + lt * S::EPC), vf);
+      float acc[S::GP];
+#pragma unroll
+      for (int h = 0; h < S::GP; ++h) {
+        float x = 0.f;
+#pragma unroll
+        for (int e = 0; e < S::EPC; ++e) x = fmaf(qr[h][e], kf[e], x);
+        acc[h] = x;
+      }
+      int which;
+      const float red = transpose_reduce<S::GP, S::LPT>(acc, lane, which);
+      const bool live = act && tokflag[jj] != 0;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float dot = __shfl_sync(kFull, red, (lane & ~(S::LPT - 1)) + h * (S::LPT / S::GP));
+        if (live) {
+          const float s = dot * a.scale;
+          const float mn = fmaxf(m[h], s);
+          const float corr = expf(m[h] - mn);
+          const float p = expf(s - mn);
+          l[h] = l[h] * corr + p;
+#pragma unroll
+          for (int e = 0; e < S::EPC; ++e) o[h][e] = fmaf(p, vf[e], o[h][e] * corr);
+          m[h] = mn;
+        }
+      }
+    }
+  }
+  // In-flight copies must land before shared memory is reused or released.
+  if (!ok && tid == 0) mbar_wait(&bar, phase ^ 1u);
+  __syncthreads();
+
+  // ---- merge the token groups of this CTA
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+#pragma unroll
+    for (int e = 0; e < S::EPC; ++e) mg[((size_t)slot * G + h) * D + lt * S::EPC + e] = o[h][e];
+    if (lt == 0) {
+      mm[slot * G + h] = m[h];
+      ml[slot * G + h] = l[h];
+    }
+  }
+  __syncthreads();
+  const int W = G * (D + 2);
+  float* pb = a.part + (((size_t)b * a.HKV + g) * nsplit + split) * W;
+  for (int i = tid; i < G * D; i += S::THREADS) {
+    const int h = i / D;
+    float M = -INFINITY;
+    for (int r = 0; r < S::GROUPS; ++r) M = fmaxf(M, mm[r * G + h]);
+    float num = 0.f, den = 0.f;
+    if (M > -INFINITY) {
+      for (int r = 0; r < S::GROUPS; ++r) {
+        const float w = expf(mm[r * G + h] - M);
+        num = fmaf(w, mg[(size_t)r * G * D + i], num);
+        den = fmaf(w, ml[r * G + h], den);
+      }
+    }
+    pb[i] = num;
+    if ((i % D) == 0) {
+      pb[G * D + h] = M;
+      pb[G * D + G + h] = den;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&a.counters[(size_t)b * kCounterSlots + 2 + g], 1u) == (unsigned)(nsplit - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ---- the last CTA merges the splits in split order
+  const float* pg = a.part + ((size_t)b * a.HKV + g) * nsplit * W;
+  for (int i = tid; i < G * D; i += S::THREADS) {
+    const int h = i / D;
+    float M = -INFINITY;
+    for (int r = 0; r < nsplit; ++r) M = fmaxf(M, __ldcg(pg + (size_t)r * W + G * D + h));
+    float num = 0.f, den = 0.f;
+    if (M > -INFINITY) {
+      for (int r = 0; r < nsplit; ++r) {
+        const float* pr = pg + (size_t)r * W;
+        const float w = expf(__ldcg(pr + G * D + h) - M);
+        num = fmaf(w, __ldcg(pr + i), num);
+        den = fmaf(w, __ldcg(pr + G * D + G + h), den);
+      }
+    }
+    const int qh = g * G + h;
+    a.out[((size_t)b * a.H + qh) * D + (i % D)] = den > 0.f ? num / den : 0.f;
+    if (a.lse && (i % D) == 0) a.lse[(size_t)b * a.H + qh] = den > 0.f ? M + logf(den) : -INFINITY;
+  }
+  if (tid == 0) a.counters[(size_t)b * kCounterSlots + 2 + g] = 0u;
+}
+
+template <typename KT, int D, int G>
+ts_status run_attend(ts_ctx* ctx, const AttendCall& c, cudaStream_t s) {
+  using S = AttShape<KT, D, G>;
+  const ts_config& cfg = ctx->cfg;
+  auto kern = attend_kernel<KT, D, G>;
+  const size_t smem = S::smem_bytes();
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return TS_ERR_CUDA;
+  AttKArgs a;
+  a.q = c.q;
+  a.k_pool = static_cast<const unsigned char*>(c.k_pool);
+  a.v_pool = static_cast<const unsigned char*>(c.v_pool);
+  a.page_table = c.page_table;
+  a.pt_stride = cfg.max_pages_per_seq;
+  a.num_pages = cfg.num_pages;
+  a.max_tokens = ctx->max_tokens;
+  a.idx = c.idx;
+  a.idx_stride = c.idx_stride;
+  a.count = c.count;
+  a.H = cfg.n_q_heads;
+  a.HKV = cfg.n_kv_heads;
+  a.scale = c.scale;
+  a.out = c.out;
+  a.lse = c.lse;
+  a.part = ctx->attn_part;
+  a.counters = ctx->counters;
+  a.status = ctx->status;
+  int nsplit = (2 * ctx->num_sms + cfg.n_kv_heads * c.B - 1) / (cfg.n_kv_heads * c.B);
+  nsplit = nsplit < 1 ? 1 : (nsplit > kAttnMaxSplits ? kAttnMaxSplits : nsplit);
+  kern<<<dim3(nsplit, cfg.n_kv_heads, c.B), S::THREADS, smem, s>>>(a);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+#define TS_ATTEND_GEOMETRIES(X)        \
+  X(TS_KV_F32, float, 64, 1)           \
+  X(TS_KV_F32, float, 64, 4)           \
+  X(TS_KV_F32, float, 128, 4)          \
+  X(TS_KV_BF16, __nv_bfloat16, 128, 4) \
+  X(TS_KV_BF16, __nv_bfloat16, 128, 7) \
+  X(TS_KV_BF16, __nv_bfloat16, 128, 1) \
+  X(TS_KV_BF16, __nv_bfloat16, 64, 2)  \
+  X(TS_KV_BF16, __nv_bfloat16, 128, 8)
+
+ts_status launch_attend(ts_ctx* ctx, const AttendCall& a, cudaStream_t s) {
+  const ts_config& c = ctx->cfg;
+  const int G = c.n_q_heads / c.n_kv_heads;
+#define X(DT, T, D_, G_) \
+  if (c.kv_dtype == DT && c.head_dim == D_ && G == G_) return run_attend<T, D_, G_>(ctx, a, s);
+  TS_ATTEND_GEOMETRIES(X)
+#undef X
+  return TS_ERR_UNSUPPORTED;
+}
+
+}  // namespace ts

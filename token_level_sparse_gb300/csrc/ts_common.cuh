@@ -1,0 +1,206 @@
+// Device helpers shared by the token-selection kernels (sm_103a).
+//
+// Bulk copies (cp.async.bulk, the 1-D form of TMA) complete on shared-memory
+// mbarriers. Every wait here is bounded by %globaltimer: when it runs out the
+// kernel records TS_ERR_TIMEOUT in the status word and returns instead of
+// spinning forever.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ts_internal.h"
+
+namespace ts {
+
+constexpr unsigned kFull = 0xffffffffu;
+// Upper bound on any single wait inside a kernel (nanoseconds).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+__device__ __forceinline__ void set_error(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete; false after the limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` of transaction on `bar`.
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// ----------------------------------------------------------- value access
+
+template <typename T>
+struct KV;
+
+// 16 bytes of fp32 = 4 elements.
+template <>
+struct KV<float> {
+  static constexpr int kPerChunk = 4;
+  __device__ __forceinline__ static void unpack(const uint4& c, float* o) {
+    o[0] = __uint_as_float(c.x);
+    o[1] = __uint_as_float(c.y);
+    o[2] = __uint_as_float(c.z);
+    o[3] = __uint_as_float(c.w);
+  }
+};
+
+// 16 bytes of bf16 = 8 elements; a bf16 is the top half of the fp32 with the same bits.
+template <>
+struct KV<__nv_bfloat16> {
+  static constexpr int kPerChunk = 8;
+  __device__ __forceinline__ static void unpack(const uint4& c, float* o) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      o[2 * i] = __uint_as_float(w[i] << 16);
+      o[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  }
+};
+
+__device__ __forceinline__ uint4 lds128(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+
+__device__ __forceinline__ uint4 ldg_nc128(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// ------------------------------------------------------------- reductions
+
+// Sums NV per-lane values over groups of LPR consecutive lanes (both powers of
+// two, NV <= LPR). Each butterfly level keeps half of the values and ships the
+// other half to the partner, so after log2(NV) levels a lane holds one value;
+// the remaining levels add plainly. Returns the full sum of value `which`.
+template <int NV, int LPR>
+__device__ __forceinline__ float transpose_reduce(float (&v)[NV], int lane, int& which) {
+  static_assert(NV >= 1 && LPR >= 1 && NV <= LPR, "bad transpose_reduce shape");
+  int base = 0;
+  int n = NV;
+#pragma unroll
+  for (int d = LPR / 2; d >= 1; d >>= 1) {
+    const bool upper = (lane & d) != 0;
+    if (n > 1) {
+      const int half = n / 2;
+#pragma unroll
+      for (int i = 0; i < NV / 2; ++i) {
+        if (i < half) {
+          const float send = upper ? v[i] : v[i + half];
+          const float keep = upper ? v[i + half] : v[i];
+          v[i] = keep + __shfl_xor_sync(kFull, send, d);
+        }
+      }
+      if (upper) base += half;
+      n = half;
+    } else {
+      v[0] += __shfl_xor_sync(kFull, v[0], d);
+    }
+  }
+  which = base;
+  return v[0];
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, d));
+  return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) x += __shfl_xor_sync(kFull, x, d);
+  return x;
+}
+
+__device__ __forceinline__ double warp_sum_f64(double x) {
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) x += __shfl_xor_sync(kFull, x, d);
+  return x;
+}
+
+__device__ __forceinline__ int warp_sum_i(int x) {
+#pragma unroll
+  for (int d = 16; d >= 1; d >>= 1) x += __shfl_xor_sync(kFull, x, d);
+  return x;
+}
+
+// Compensated (Kahan) accumulation in fp32.
+struct KahanF {
+  float s = 0.f, c = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float y = x - c;
+    const float t = s + y;
+    c = (t - s) - y;
+    s = t;
+  }
+};
+
+// Token segments of a sequence of n tokens: sinks [0, s_end), candidates
+// [s_end, local_start), window [local_start, n).
+__device__ __forceinline__ void budget_segments(int n, int n_sink, int n_local, int& s_end,
+                                                int& local_start) {
+  s_end = min(n_sink, n);
+  local_start = max(s_end, n - n_local);
+}
+
+}  // namespace ts

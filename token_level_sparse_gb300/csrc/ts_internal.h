@@ -1,0 +1,125 @@
+// Host-side internals of libtokenselect: context, cache and the launchers each
+// kernel file exports to the C ABI layer.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/tokenselect.h"
+
+namespace ts {
+
+constexpr int kPage = 16;            // tokens per page (the only page size compiled)
+constexpr int kScorePagesPerCta = 16;  // pages of one sequence per score CTA
+constexpr int kSelThreads = 512;     // select kernels: threads per CTA
+constexpr int kSelPerThread = 8;     // consecutive tokens per thread
+constexpr int kSelChunk = kSelThreads * kSelPerThread;
+constexpr int kAttnMaxSplits = 64;   // CTAs per (sequence, KV head) in the attention
+
+// Per-sequence state of the radix selection (device resident).
+struct SelState {
+  uint32_t prefix;               // fixed high bits of the threshold
+  uint32_t mask;                 // which bits of prefix are fixed
+  int32_t k_rem;                 // top-k: tokens still to take at/under prefix
+  int32_t n_gt;                  // tokens strictly above the prefix range
+  unsigned long long mass_rem;   // top-p: fixed-point mass still to reach
+  int32_t all;                   // 1: every token of the domain is selected
+  int32_t ties;                  // tokens equal to the threshold to take (by index)
+};
+
+struct ChunkCount {              // per selection chunk, written by the count pass
+  int gt_all, eq_all, gt_cand, eq_cand, eq_pre;
+};
+
+}  // namespace ts
+
+struct ts_ctx {
+  ts_config cfg;
+  int device = 0;
+  int num_sms = 0;
+  int max_tokens = 0;            // max_pages_per_seq * page size
+  int score_max_chunks = 0;      // score CTAs per sequence (upper bound)
+  int sel_max_chunks = 0;        // selection chunks per sequence (upper bound)
+  int attn_splits = 0;           // attention CTAs per (sequence, KV head)
+  // device scratch
+  int* status = nullptr;                 // first device error since last read
+  float* logits = nullptr;               // [max_batch][H][max_tokens]
+  float2* partials = nullptr;            // [max_batch][score_max_chunks][H]  (max, sum)
+  float2* stats = nullptr;               // [max_batch][H]  (max, 1/sum)
+  unsigned* counters = nullptr;          // last-CTA counters, kCounterSlots per sequence
+  ts::SelState* sel_state = nullptr;     // [max_batch]
+  unsigned* hist = nullptr;              // [max_batch][2048]
+  unsigned long long* mass_hist = nullptr;  // [max_batch][2048]
+  ts::ChunkCount* chunk_counts = nullptr;   // [max_batch][sel_max_chunks]
+  float* attn_part = nullptr;            // [max_batch][H_kv][attn_splits][G*(D+2)]
+  float* vote = nullptr;                 // [max_batch][max_tokens] (decode step)
+  uint8_t* hit = nullptr;                // [max_batch] (decode step)
+};
+
+struct ts_cache {
+  ts_ctx* ctx = nullptr;
+  int n_layers = 0;
+  int capacity = 0;
+  float* cq = nullptr;           // [n_layers][max_batch][H*d]
+  int32_t* ct = nullptr;         // [n_layers][max_batch][capacity]
+  int32_t* ct_count = nullptr;   // [n_layers][max_batch]
+  uint8_t* filled = nullptr;     // [n_layers][max_batch]
+};
+
+namespace ts {
+
+// Counter slots per sequence: [0] score, [1] select, [2 .. 2+H_kv) attention.
+constexpr int kCounterSlots = 2 + 64;
+
+struct ScoreCall {
+  const float* q;
+  const void* k_pool;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const uint8_t* skip;
+  int B;
+  float scale;
+  float* vote;
+  int64_t vote_stride;
+};
+
+struct SelectCall {
+  ts_cache* cache;
+  int layer;
+  const float* q;
+  const float* vote;
+  int64_t vote_stride;
+  const int32_t* seq_lens;
+  int B;
+  const uint8_t* hit;
+  ts_select_params params;
+  int32_t* idx;
+  int64_t idx_stride;
+  int32_t* count;
+};
+
+struct AttendCall {
+  const float* q;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* page_table;
+  const int32_t* idx;
+  int64_t idx_stride;
+  const int32_t* count;
+  int B;
+  float scale;
+  float* out;
+  float* lse;
+};
+
+bool score_supported(const ts_config& c);
+ts_status launch_score(ts_ctx* ctx, const ScoreCall& a, cudaStream_t s);
+ts_status launch_select(ts_ctx* ctx, const SelectCall& a, cudaStream_t s);
+ts_status launch_attend(ts_ctx* ctx, const AttendCall& a, cudaStream_t s);
+ts_status launch_cache_check(ts_ctx* ctx, ts_cache* cache, int layer, const float* q, int B,
+                             float theta, uint8_t* hit, float* cos_out, cudaStream_t s);
+ts_status launch_cache_reset(ts_cache* cache, cudaStream_t s);
+
+inline ts_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TS_OK : TS_ERR_CUDA; }
+
+}  // namespace ts
