@@ -102,7 +102,8 @@ def head_logits(q: np.ndarray, k_pool: np.ndarray, page_row: np.ndarray, n: int,
 
     Per-head criticality of every cached token (TS-notes, "Head soft vote":
     Q^h . K_cache^h^T; Appendix Algorithm 2: s = <q, k> per head and token).
-    GQA mapping g(h) = h // G (reading R5).
+    GQA mapping g(h) = h // G (reading R5). Each logit is its own row-wise dot
+    product, so equal keys give equal logits and ties stay ties (reading R8).
     """
     q = np.asarray(q, dtype=np.float64)
     H, d = q.shape
@@ -117,7 +118,7 @@ def head_logits(q: np.ndarray, k_pool: np.ndarray, page_row: np.ndarray, n: int,
         K = gather_rows(k_pool, page_row, tokens, g)          # [n, d]
         for j in range(G):
             h = g * G + j
-            out[h] = alpha * (K @ q[h])
+            out[h] = alpha * np.einsum("nd,d->n", K, q[h])
     return out
 
 

@@ -16,7 +16,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 MUTATIONS = {
     "gqa index h % G": ("h = g * G + j\n            out[h] = alpha", "h = j * Hkv + g\n            out[h] = alpha"),
-    "vote without scale": ("out[h] = alpha * (K @ q[h])", "out[h] = (K @ q[h])"),
+    "vote without scale": ('out[h] = alpha * np.einsum("nd,d->n", K, q[h])',
+                           'out[h] = np.einsum("nd,d->n", K, q[h])'),
     "normaliser drops max": ("m + np.log(np.exp(logits - m[:, None]).sum(axis=1))",
                              "np.log(np.exp(logits - m[:, None]).sum(axis=1))"),
     "vote not normalised": ("v += np.exp(logits[h] - L[h])", "v += np.exp(logits[h])"),

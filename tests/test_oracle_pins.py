@@ -434,3 +434,21 @@ def test_decode_step_keeps_last_miss_query():
         q = np.array([[math.cos(r), math.sin(r)]])
         hits.append(O.decode_step(st, q, kp, vp, pt, n, k=4, n_sink=1, n_local=2, theta=theta)["hit"])
     assert hits == [False, True, False]
+
+
+def test_equal_keys_tie_exactly_and_go_to_lower_index():
+    # Identical keys must give identical votes; the tie then goes to the lower index.
+    rng = np.random.default_rng(95)
+    d, n = 64, 300
+    kp = rng.standard_normal((n // 16 + 1, 2, 16, d))
+    pt = rng.permutation(n // 16 + 1).astype(np.int32)
+    q = rng.standard_normal((4, d))
+    tied = [17, 90, 144, 201, 260]
+    for g in range(2):                       # the same key at every tied position, in every KV head
+        key = 3.0 * q[2 * g] / np.linalg.norm(q[2 * g])
+        for i in tied:
+            kp[pt[i // 16], g, i % 16] = key
+    v = O.soft_vote(O.head_logits(q, kp, pt, n))
+    assert len(set(v[tied].tolist())) == 1
+    _, part = O.select_topk(v, n, 3, 0, 0)
+    assert list(part) == tied[:3]
