@@ -162,6 +162,32 @@ ts_status ts_get_status(ts_ctx* ctx, ts_status* device_status, void* stream);
 /* Static text for a status code. */
 const char* ts_status_str(ts_status s);
 
+/* Kernel timing (tracing). While enabled, every kernel launch of the library is
+ * bracketed by a pair of CUDA events on its stream, tagged with its family;
+ * inside a CUDA graph capture the events become event-record nodes that each
+ * replay re-records. At most 256 brackets are held; later ones are dropped. */
+enum {
+  TS_PROF_CHECK = 0,   /* Selection Cache test                     */
+  TS_PROF_SCORE = 1,   /* paged dot product + per-CTA normaliser    */
+  TS_PROF_VOTE = 2,    /* head soft vote                            */
+  TS_PROF_SELECT = 3,  /* radix selection, refresh and compaction   */
+  TS_PROF_ATTEND = 4,  /* sparse attention + merge                  */
+  TS_PROF_N = 5
+};
+typedef struct {
+  double ms[TS_PROF_N];        /* summed device time per family */
+  int64_t launches[TS_PROF_N]; /* brackets summed per family    */
+} ts_profile;
+ts_status ts_profile_enable(ts_ctx* ctx, int on);
+/* Waits for the recorded brackets and ADDS their durations into *out. With
+ * keep == 0 the brackets are released; keep != 0 leaves them registered so a
+ * replayed CUDA graph can be read again after each replay. */
+ts_status ts_profile_read(ts_ctx* ctx, ts_profile* out, int keep);
+
+/* Number of kernel launches this context has issued (or captured into a CUDA
+ * graph) since ts_create, counted on the host at each launch. */
+ts_status ts_kernel_count(ts_ctx* ctx, int64_t* out);
+
 /* Library version, e.g. 100 for 0.1.0. */
 int ts_version(void);
 

@@ -9,7 +9,10 @@ Tolerances (written here, used by every parity test):
   is within TIE_REL * p * H of p * H. TIE_REL = 1e-6 is the stated tolerance
   of the method's parity target.
 * attention output: max_j |o_j - r_j| / max_j |r_j| <= ATTN_REL per (seq, head)
-  row, ATTN_REL = 2e-3 (the stated tolerance for bf16 inputs).
+  row, ATTN_REL = 2e-3 (the stated tolerance for bf16 inputs). When the GPU
+  set differs from the oracle's only inside the tie band, both are correct
+  selections (equal votes may be broken either way within rounding), so the
+  GPU output is checked against the definition evaluated on the GPU's set.
 * lse: |lse - ref| <= LSE_ABS. fp32 dot products, exp and log over a few
   thousand terms carry a relative error of a few 1e-6 on values below ~100,
   so 1e-3 leaves a wide margin without hiding a wrong term.
@@ -280,6 +283,14 @@ def run_trajectory(wl, steps, layers=(0,), theta=None, mode=None, top_p=None, ch
                             tau = ov[order[m - 1]]
                             bad = [i for i in gi ^ oi if i >= lm["n"] or abs(ov[i] - tau) > TIE_REL * tau]
                             assert not bad, f"{where}: top-p hit set differs outside the band"
-                check_attention(g["out"][b], g["lse"][b], r["out"], r["lse"], where)
+                gi = np.asarray(g["idx"][b])
+                if np.array_equal(gi, r["idx"]):
+                    check_attention(g["out"][b], g["lse"][b], r["out"], r["lse"], where)
+                else:
+                    # The sets differ only inside the tie band (checked above): both are
+                    # correct selections, so the GPU attention is checked against the
+                    # definition evaluated on the GPU's own (valid) set.
+                    vo, vl = O.sparse_attention(r["q"], ora.kp[l], ora.vp[l], ora.pt[b], gi)
+                    check_attention(g["out"][b], g["lse"][b], vo, vl, where + " (tie-band set)")
             rep.steps += 1
     return rep

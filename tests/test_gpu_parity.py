@@ -29,7 +29,7 @@ def test_tiny_fp32_trajectory_with_cache():
 
 
 def test_tiny_fp32_separate_calls_all_miss():
-    _run(W.spec(0), 4, separate_calls=True)
+    _run(W.spec(0), 4, separate_calls=True, theta=2.0)
 
 
 @pytest.mark.parametrize("overrides", [

@@ -13,14 +13,15 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import POINTER, c_char_p, c_float, c_int, c_int64, c_void_p
+from ctypes import POINTER, c_char_p, c_double, c_float, c_int, c_int64, c_void_p
 
 __all__ = [
     "TokenSelectError", "Config", "SelectParams", "library", "library_path",
     "TS_KV_F32", "TS_KV_BF16", "TS_SELECT_TOPK", "TS_SELECT_TOPP", "STATUS",
     "ts_create", "ts_destroy", "ts_cache_create", "ts_cache_destroy", "ts_cache_reset",
     "ts_cache_check", "ts_score", "ts_select", "ts_sparse_attend", "ts_decode_step",
-    "ts_get_status", "ts_status_str", "ts_version", "Context", "Cache",
+    "ts_get_status", "ts_status_str", "ts_version", "ts_profile_enable", "ts_profile_read",
+    "ts_kernel_count", "Context", "Cache", "Profile", "PROF_FAMILIES",
 ]
 
 TS_KV_F32, TS_KV_BF16 = 0, 1
@@ -45,6 +46,13 @@ class Config(ctypes.Structure):
     _fields_ = [("n_q_heads", c_int), ("n_kv_heads", c_int), ("head_dim", c_int),
                 ("page_size", c_int), ("kv_dtype", c_int), ("max_batch", c_int),
                 ("max_pages_per_seq", c_int), ("num_pages", c_int64)]
+
+
+class Profile(ctypes.Structure):
+    _fields_ = [("ms", c_double * 5), ("launches", c_int64 * 5)]
+
+
+PROF_FAMILIES = ("check", "score", "vote", "select", "attend")
 
 
 class SelectParams(ctypes.Structure):
@@ -73,6 +81,9 @@ _SIGS = {
                                c_void_p, c_int, POINTER(SelectParams), c_void_p, c_int64, c_void_p,
                                c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "ts_get_status": (c_int, [c_void_p, POINTER(c_int), c_void_p]),
+    "ts_profile_enable": (c_int, [c_void_p, c_int]),
+    "ts_profile_read": (c_int, [c_void_p, c_void_p, c_int]),
+    "ts_kernel_count": (c_int, [c_void_p, POINTER(c_int64)]),
 }
 
 
@@ -189,6 +200,23 @@ def ts_decode_step(ctx, cache, layer, q, k_pool, v_pool, page_table, seq_lens, B
 def ts_get_status(ctx, stream=None) -> int:
     v = c_int(0)
     _check(library().ts_get_status(ctx, ctypes.byref(v), _s(stream)), "ts_get_status")
+    return v.value
+
+
+def ts_profile_enable(ctx, on: bool) -> None:
+    _check(library().ts_profile_enable(ctx, 1 if on else 0), "ts_profile_enable")
+
+
+def ts_profile_read(ctx, keep: bool = False) -> dict:
+    """{family: (ms, launches)} added up over the recorded brackets."""
+    p = Profile()
+    _check(library().ts_profile_read(ctx, ctypes.byref(p), 1 if keep else 0), "ts_profile_read")
+    return {f: (p.ms[i], p.launches[i]) for i, f in enumerate(PROF_FAMILIES)}
+
+
+def ts_kernel_count(ctx) -> int:
+    v = c_int64(0)
+    _check(library().ts_kernel_count(ctx, ctypes.byref(v)), "ts_kernel_count")
     return v.value
 
 

@@ -18,6 +18,11 @@ cudaError_t alloc(T** p, size_t n) {
 }
 
 void free_ctx_buffers(ts_ctx* c) {
+  for (auto& b : c->prof) {
+    if (b.begin) cudaEventDestroy(b.begin);
+    if (b.end) cudaEventDestroy(b.end);
+    b.begin = b.end = nullptr;
+  }
   cudaFree(c->status);
   cudaFree(c->logits);
   cudaFree(c->partials);
@@ -262,6 +267,38 @@ ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q
   if (st != TS_OK) return st;
   AttendCall ac{q, k_pool, v_pool, page_table, idx, idx_stride, count, B, scale, out, lse};
   return launch_attend(ctx, ac, s);
+}
+
+ts_status ts_kernel_count(ts_ctx* ctx, int64_t* out) {
+  if (!ctx || !out) return TS_ERR_INVALID_ARG;
+  *out = ctx->kernels;
+  return TS_OK;
+}
+
+ts_status ts_profile_enable(ts_ctx* ctx, int on) {
+  if (!ctx) return TS_ERR_INVALID_ARG;
+  if (on) {
+    for (auto& b : ctx->prof) {
+      if (!b.begin && cudaEventCreate(&b.begin) != cudaSuccess) return TS_ERR_CUDA;
+      if (!b.end && cudaEventCreate(&b.end) != cudaSuccess) return TS_ERR_CUDA;
+    }
+  }
+  ctx->prof_on = on != 0;
+  return TS_OK;
+}
+
+ts_status ts_profile_read(ts_ctx* ctx, ts_profile* out, int keep) {
+  if (!ctx || !out) return TS_ERR_INVALID_ARG;
+  for (int i = 0; i < ctx->prof_used; ++i) {
+    ProfBracket& b = ctx->prof[i];
+    if (cudaEventSynchronize(b.end) != cudaSuccess) return TS_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, b.begin, b.end) != cudaSuccess) return TS_ERR_CUDA;
+    out->ms[b.family] += ms;
+    out->launches[b.family] += 1;
+  }
+  if (!keep) ctx->prof_used = 0;
+  return TS_OK;
 }
 
 ts_status ts_get_status(ts_ctx* ctx, ts_status* device_status, void* stream) {

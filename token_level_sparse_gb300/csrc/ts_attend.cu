@@ -238,8 +238,7 @@ ts_status run_attend(ts_ctx* ctx, const AttendCall& c, cudaStream_t s) {
   const ts_config& cfg = ctx->cfg;
   auto kern = attend_kernel<KT, D, G>;
   const size_t smem = S::smem_bytes();
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-    return TS_ERR_CUDA;
+  if (!ensure_smem(kern, smem, ctx->device)) return TS_ERR_CUDA;
   AttKArgs a;
   a.q = c.q;
   a.k_pool = static_cast<const unsigned char*>(c.k_pool);
@@ -261,6 +260,8 @@ ts_status run_attend(ts_ctx* ctx, const AttendCall& c, cudaStream_t s) {
   a.status = ctx->status;
   int nsplit = (2 * ctx->num_sms + cfg.n_kv_heads * c.B - 1) / (cfg.n_kv_heads * c.B);
   nsplit = nsplit < 1 ? 1 : (nsplit > kAttnMaxSplits ? kAttnMaxSplits : nsplit);
+  ProfScope ps(ctx, TS_PROF_ATTEND, s);
+  ctx->kernels += 1;
   kern<<<dim3(nsplit, cfg.n_kv_heads, c.B), S::THREADS, smem, s>>>(a);
   return cuda_status(cudaGetLastError());
 }

@@ -63,6 +63,8 @@ ts_status launch_cache_check(ts_ctx* ctx, ts_cache* cache, int layer, const floa
   const ts_config& cfg = ctx->cfg;
   const int HD = cfg.n_q_heads * cfg.head_dim;
   const size_t mb = (size_t)cfg.max_batch;
+  ProfScope ps(ctx, TS_PROF_CHECK, s);
+  ctx->kernels += 1;
   cache_check_kernel<<<B, kCheckThreads, 0, s>>>(q, cache->cq + (size_t)layer * mb * HD,
                                                   cache->filled + (size_t)layer * mb, HD, theta, hit,
                                                   cos_out);

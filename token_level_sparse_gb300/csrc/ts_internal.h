@@ -33,6 +33,14 @@ struct ChunkCount {              // per selection chunk, written by the count pa
 
 }  // namespace ts
 
+namespace ts {
+struct ProfBracket {
+  cudaEvent_t begin = nullptr, end = nullptr;
+  int family = 0;
+};
+constexpr int kProfMax = 256;
+}  // namespace ts
+
 struct ts_ctx {
   ts_config cfg;
   int device = 0;
@@ -54,6 +62,11 @@ struct ts_ctx {
   float* attn_part = nullptr;            // [max_batch][H_kv][attn_splits][G*(D+2)]
   float* vote = nullptr;                 // [max_batch][max_tokens] (decode step)
   uint8_t* hit = nullptr;                // [max_batch] (decode step)
+  int64_t kernels = 0;           // kernel launches issued
+  // kernel timing
+  bool prof_on = false;
+  int prof_used = 0;
+  ts::ProfBracket prof[ts::kProfMax];
 };
 
 struct ts_cache {
@@ -121,5 +134,44 @@ ts_status launch_cache_check(ts_ctx* ctx, ts_cache* cache, int layer, const floa
 ts_status launch_cache_reset(ts_cache* cache, cudaStream_t s);
 
 inline ts_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TS_OK : TS_ERR_CUDA; }
+
+// Raises a kernel's dynamic shared-memory limit once per device (never inside
+// a stream capture after the first launch on that device).
+template <typename K>
+inline bool ensure_smem(K kernel, size_t bytes, int device) {
+  static unsigned long long done = 0ull;  // one bit per device
+  const unsigned long long bit = 1ull << (device & 63);
+  if (done & bit) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+    return false;
+  done |= bit;
+  return true;
+}
+
+// Brackets the launches made during its lifetime with a pair of timing events
+// when the context's profiling is on.
+class ProfScope {
+ public:
+  ProfScope(ts_ctx* ctx, int family, cudaStream_t s) : s_(s) {
+    if (!ctx->prof_on || ctx->prof_used >= kProfMax) return;
+    b_ = &ctx->prof[ctx->prof_used];
+    if (!b_->begin || !b_->end) {  // events are made by ts_profile_enable, never during a capture
+      b_ = nullptr;
+      return;
+    }
+    ++ctx->prof_used;
+    b_->family = family;
+    cudaEventRecord(b_->begin, s_);
+  }
+  ~ProfScope() {
+    if (b_) cudaEventRecord(b_->end, s_);
+  }
+  ProfScope(const ProfScope&) = delete;
+  ProfScope& operator=(const ProfScope&) = delete;
+
+ private:
+  ProfBracket* b_ = nullptr;
+  cudaStream_t s_;
+};
 
 }  // namespace ts

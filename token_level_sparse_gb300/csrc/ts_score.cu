@@ -290,8 +290,7 @@ ts_status run_score(ts_ctx* ctx, const ScoreCall& c, cudaStream_t s) {
   const int H = ctx->cfg.n_q_heads;
   const size_t smem = S::smem_bytes(H);
   auto kern = score_logits_kernel<KT, D, HKV, G>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return TS_ERR_CUDA;
+  if (!ensure_smem(kern, S::smem_bytes(HKV * G), ctx->device)) return TS_ERR_CUDA;  // H = H_kv * G
   ScoreKArgs a;
   a.q = c.q;
   a.k_pool = c.k_pool;
@@ -309,9 +308,16 @@ ts_status run_score(ts_ctx* ctx, const ScoreCall& c, cudaStream_t s) {
   a.stats = ctx->stats;
   a.counters = ctx->counters;
   a.status = ctx->status;
-  kern<<<dim3(ctx->score_max_chunks, c.B), S::THREADS, smem, s>>>(a);
+  {
+    ProfScope ps(ctx, TS_PROF_SCORE, s);
+    kern<<<dim3(ctx->score_max_chunks, c.B), S::THREADS, smem, s>>>(a);
+  }
+  ctx->kernels += 2;
   VoteKArgs v{c.seq_lens, c.skip, H, ctx->logits, ctx->max_tokens, ctx->stats, c.vote, c.vote_stride};
-  score_vote_kernel<<<dim3((ctx->max_tokens + kVoteTile - 1) / kVoteTile, c.B), kVoteThreads, 0, s>>>(v);
+  {
+    ProfScope ps(ctx, TS_PROF_VOTE, s);
+    score_vote_kernel<<<dim3((ctx->max_tokens + kVoteTile - 1) / kVoteTile, c.B), kVoteThreads, 0, s>>>(v);
+  }
   return cuda_status(cudaGetLastError());
 }
 

@@ -514,6 +514,8 @@ ts_status launch_select(ts_ctx* ctx, const SelectCall& c, cudaStream_t s) {
     a.filled = nullptr;
     a.cap = 0;
   }
+  ProfScope ps(ctx, TS_PROF_SELECT, s);
+  ctx->kernels += 5 + (c.hit ? 1 : 0);
   if (c.hit) sel_refresh_kernel<<<c.B, 256, 0, s>>>(a);
   const dim3 grid(ctx->sel_max_chunks, c.B);
   for (int pass = 0; pass < 3; ++pass) {
