@@ -199,3 +199,39 @@ def test_cache_always_and_never():
     always = GpuRunner(wl, theta=-1.0)
     hits = [bool(always.step(t)["hit"][0]) for t in range(4)]
     assert hits == [False, True, True, True]
+
+
+def test_graph_capture_replay_and_kernel_timing():
+    T = tsl()
+    sp = W.spec(1, n0=(20000,), steps=2)
+    wl = W.generate(sp, DEV)
+    B, H, d = 1, sp.n_q_heads, sp.head_dim
+    ctx = T.Context(H, sp.n_kv_heads, d, T.TS_KV_BF16, B, wl.page_table.shape[1], wl.num_pages)
+    prm = T.params(theta=2.0)
+    cap = sp.k + sp.n_sink + sp.n_local
+    q = wl.q[0][0].clone()
+    seq = wl.seq_lens(0)
+    idx = torch.zeros(B, cap, dtype=torch.int32, device=DEV)
+    cnt = torch.zeros(B, dtype=torch.int32, device=DEV)
+    out = torch.zeros(B, H, d, device=DEV)
+    ctx.decode_step(q, wl.k_pool[0], wl.v_pool[0], wl.page_table, seq, prm, idx, cnt, out)
+    torch.cuda.synchronize()
+    direct = (idx.clone(), out.clone())
+    T.ts_profile_enable(ctx.handle, True)
+    k0 = T.ts_kernel_count(ctx.handle)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        ctx.decode_step(q, wl.k_pool[0], wl.v_pool[0], wl.page_table, seq, prm, idx, cnt, out)
+    per_replay = T.ts_kernel_count(ctx.handle) - k0
+    assert per_replay >= 8
+    idx.zero_()
+    out.zero_()
+    for _ in range(3):
+        g.replay()
+        torch.cuda.synchronize()
+        prof = T.ts_profile_read(ctx.handle, keep=True)
+        for fam in ("score", "vote", "select", "attend"):
+            ms, n = prof[fam]
+            assert n >= 1 and ms > 0, (fam, prof)
+    assert torch.equal(idx, direct[0]) and torch.equal(out, direct[1])
+    assert ctx.status() == 0

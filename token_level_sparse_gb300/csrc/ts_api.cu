@@ -291,6 +291,7 @@ ts_status ts_profile_read(ts_ctx* ctx, ts_profile* out, int keep) {
   if (!ctx || !out) return TS_ERR_INVALID_ARG;
   for (int i = 0; i < ctx->prof_used; ++i) {
     ProfBracket& b = ctx->prof[i];
+    if (!b.recorded) continue;
     if (cudaEventSynchronize(b.end) != cudaSuccess) return TS_ERR_CUDA;
     float ms = 0.f;
     if (cudaEventElapsedTime(&ms, b.begin, b.end) != cudaSuccess) return TS_ERR_CUDA;

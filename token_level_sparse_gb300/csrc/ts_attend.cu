@@ -238,7 +238,7 @@ ts_status run_attend(ts_ctx* ctx, const AttendCall& c, cudaStream_t s) {
   const ts_config& cfg = ctx->cfg;
   auto kern = attend_kernel<KT, D, G>;
   const size_t smem = S::smem_bytes();
-  if (!ensure_smem(kern, smem, ctx->device)) return TS_ERR_CUDA;
+  if (!ensure_smem<attend_kernel<KT, D, G>>(smem, ctx->device)) return TS_ERR_CUDA;
   AttKArgs a;
   a.q = c.q;
   a.k_pool = static_cast<const unsigned char*>(c.k_pool);

@@ -37,6 +37,7 @@ namespace ts {
 struct ProfBracket {
   cudaEvent_t begin = nullptr, end = nullptr;
   int family = 0;
+  bool recorded = false;  // both events were recorded
 };
 constexpr int kProfMax = 256;
 }  // namespace ts
@@ -135,14 +136,15 @@ ts_status launch_cache_reset(ts_cache* cache, cudaStream_t s);
 
 inline ts_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TS_OK : TS_ERR_CUDA; }
 
-// Raises a kernel's dynamic shared-memory limit once per device (never inside
-// a stream capture after the first launch on that device).
-template <typename K>
-inline bool ensure_smem(K kernel, size_t bytes, int device) {
+// Raises one kernel's dynamic shared-memory limit once per device (so no
+// attribute call happens inside a stream capture after the first launch on
+// that device). Templated on the kernel itself: one flag set per kernel.
+template <auto Kernel>
+inline bool ensure_smem(size_t bytes, int device) {
   static unsigned long long done = 0ull;  // one bit per device
   const unsigned long long bit = 1ull << (device & 63);
   if (done & bit) return true;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
+  if (cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
     return false;
   done |= bit;
   return true;
@@ -161,10 +163,16 @@ class ProfScope {
     }
     ++ctx->prof_used;
     b_->family = family;
-    cudaEventRecord(b_->begin, s_);
+    b_->recorded = false;
+    // Inside a stream capture only an "external" record becomes an event-record
+    // node that each graph replay executes.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s_, &cs) != cudaSuccess) cs = cudaStreamCaptureStatusNone;
+    flags_ = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+    if (cudaEventRecordWithFlags(b_->begin, s_, flags_) != cudaSuccess) b_ = nullptr;
   }
   ~ProfScope() {
-    if (b_) cudaEventRecord(b_->end, s_);
+    if (b_) b_->recorded = cudaEventRecordWithFlags(b_->end, s_, flags_) == cudaSuccess;
   }
   ProfScope(const ProfScope&) = delete;
   ProfScope& operator=(const ProfScope&) = delete;
@@ -172,6 +180,7 @@ class ProfScope {
  private:
   ProfBracket* b_ = nullptr;
   cudaStream_t s_;
+  unsigned flags_ = cudaEventRecordDefault;
 };
 
 }  // namespace ts

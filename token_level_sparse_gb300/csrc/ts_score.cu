@@ -290,7 +290,8 @@ ts_status run_score(ts_ctx* ctx, const ScoreCall& c, cudaStream_t s) {
   const int H = ctx->cfg.n_q_heads;
   const size_t smem = S::smem_bytes(H);
   auto kern = score_logits_kernel<KT, D, HKV, G>;
-  if (!ensure_smem(kern, S::smem_bytes(HKV * G), ctx->device)) return TS_ERR_CUDA;  // H = H_kv * G
+  if (!ensure_smem<score_logits_kernel<KT, D, HKV, G>>(S::smem_bytes(HKV * G), ctx->device))  // H = H_kv * G
+    return TS_ERR_CUDA;
   ScoreKArgs a;
   a.q = c.q;
   a.k_pool = c.k_pool;
