@@ -47,7 +47,29 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--no-extras", action="store_true", help="skip the 1M, miss-only and hit-only passes")
     p.add_argument("--cpu-baseline-only", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--case", choices=sorted(CASES),
+                   help="run --steps decode steps of one workload and exit (for ncu captures; no timing)")
     return p.parse_args(argv)
+
+
+# workload index, theta for the profiling cases
+CASES = {"n128k": (1, 0.9), "n128k-miss": (1, 2.0), "n1m-miss": (3, 2.0), "n1m-1layer-miss": ("3x1", 2.0),
+         "qwen-b8-miss": (2, 2.0), "topp-b4": (4, 0.9)}
+
+
+def case_main(args):
+    """Plain decode steps of one workload (graph replays, no flush, no timing)."""
+    import torch
+
+    import workloads as W
+    cfg, theta = CASES[args.case]
+    sp = W.spec(3, layers=1) if cfg == "3x1" else W.spec(cfg)
+    if sp.mode == "topp":
+        raise SystemExit("the top-p workload has no graph bench yet")
+    b = DecodeBench(sp, "cuda:0", theta=theta)
+    b.run(args.steps, 0, flush=False)
+    torch.cuda.synchronize()
+    print(f"case {args.case}: {args.steps} steps, kernels per step {b.kernels_per_step}")
 
 
 # ------------------------------------------------------------ distributed
@@ -468,6 +490,9 @@ def main(argv=None):
         return
     if args.impl == "reference":
         reference_main(args)
+        return
+    if args.case:
+        case_main(args)
         return
     import torch
 
