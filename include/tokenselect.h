@@ -59,7 +59,8 @@ typedef enum {
   TS_ERR_CAPACITY = 6,         /* device: selection larger than its buffer      */
   TS_ERR_TIMEOUT = 7,          /* device: a bounded wait ran out                */
   TS_ERR_COOP_UNAVAILABLE = 8, /* a cooperative launch was refused              */
-  TS_ERR_SEQ_LEN = 9           /* device: seq_lens[b] < 0 or above the maximum  */
+  TS_ERR_SEQ_LEN = 9,          /* device: seq_lens[b] < 0 or above the maximum  */
+  TS_ERR_SCRATCH_LIMIT = 10    /* beyond the fixed scratch of the no-alloc call */
 } ts_status;
 
 enum { TS_KV_F32 = 0, TS_KV_BF16 = 1 };
@@ -143,6 +144,35 @@ ts_status ts_sparse_attend(ts_ctx* ctx, const float* q, const void* k_pool, cons
                            const int32_t* page_table, const int32_t* idx, int64_t idx_stride,
                            const int32_t* count, int B, float scale, float* out, float* lse,
                            void* stream);
+
+/* Sparse attention for callers that cannot allocate device memory: the same
+ * computation and the same kernel as ts_sparse_attend, but with no context.
+ * The paper has no counterpart; this exists for callers that run where
+ * cudaMalloc is unavailable or forbidden - inside a memory pool or arena they
+ * do not own, under a framework allocator that must see every allocation, or
+ * in a process that has to keep device memory fixed after start-up - and
+ * so cannot create a context (ts_create allocates its scratch).
+ * Its scratch (split partials, merge counters, a fallback status slot) is one
+ * fixed static device array of 4 MiB + 16 KiB in the library, held by every
+ * GPU that loads the library until the process exits. Limits: B <= 48 and
+ * B * H_kv * G * (d + 2) <= 2^20 floats (one split per (sequence, KV head)
+ * at that size); beyond them the call returns TS_ERR_SCRATCH_LIMIT and
+ * enqueues nothing. It calls no cudaMalloc/cudaFree. The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) and the
+ * SM count: make that first call before any stream capture on that device.
+ * Every call clears the merge counters, then uses the shared array: calls
+ * that overlap on the GPU (other streams, other threads) race on it and must
+ * be serialised by the caller. Geometry: n_q_heads, n_kv_heads, head_dim,
+ * kv_dtype as in ts_config; pools of num_pages pages; page_table int32
+ * [B][max_pages_per_seq]. status: int32 on the device or NULL; receives the
+ * first device error (0 otherwise is left unchanged). Other arguments as in
+ * ts_sparse_attend. */
+ts_status ts_sparse_attend_noalloc(int n_q_heads, int n_kv_heads, int head_dim, int kv_dtype,
+                                   const float* q, const void* k_pool, const void* v_pool,
+                                   int64_t num_pages, const int32_t* page_table,
+                                   int max_pages_per_seq, const int32_t* idx, int64_t idx_stride,
+                                   const int32_t* count, int B, float scale, float* out, float* lse,
+                                   int32_t* status, void* stream);
 
 /* One whole decode step of one layer, stream-ordered, no host synchronisation:
  * cache check (when cache != NULL and theta <= 1), score and vote for the

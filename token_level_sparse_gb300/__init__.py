@@ -21,7 +21,7 @@ __all__ = [
     "ts_create", "ts_destroy", "ts_cache_create", "ts_cache_destroy", "ts_cache_reset",
     "ts_cache_check", "ts_score", "ts_select", "ts_sparse_attend", "ts_decode_step",
     "ts_get_status", "ts_status_str", "ts_version", "ts_profile_enable", "ts_profile_read",
-    "ts_kernel_count", "Context", "Cache", "Profile", "PROF_FAMILIES",
+    "ts_kernel_count", "ts_sparse_attend_noalloc", "Context", "Cache", "Profile", "PROF_FAMILIES",
 ]
 
 TS_KV_F32, TS_KV_BF16 = 0, 1
@@ -29,7 +29,7 @@ TS_SELECT_TOPK, TS_SELECT_TOPP = 0, 1
 STATUS = {
     0: "TS_OK", 1: "TS_ERR_INVALID_ARG", 2: "TS_ERR_SHAPE", 3: "TS_ERR_UNSUPPORTED",
     4: "TS_ERR_CUDA", 5: "TS_ERR_PAGE_OOB", 6: "TS_ERR_CAPACITY", 7: "TS_ERR_TIMEOUT",
-    8: "TS_ERR_COOP_UNAVAILABLE", 9: "TS_ERR_SEQ_LEN",
+    8: "TS_ERR_COOP_UNAVAILABLE", 9: "TS_ERR_SEQ_LEN", 10: "TS_ERR_SCRATCH_LIMIT",
 }
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
@@ -84,6 +84,9 @@ _SIGS = {
     "ts_profile_enable": (c_int, [c_void_p, c_int]),
     "ts_profile_read": (c_int, [c_void_p, c_void_p, c_int]),
     "ts_kernel_count": (c_int, [c_void_p, POINTER(c_int64)]),
+    "ts_sparse_attend_noalloc": (c_int, [c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p, c_int64,
+                                         c_void_p, c_int, c_void_p, c_int64, c_void_p, c_int, c_float,
+                                         c_void_p, c_void_p, c_void_p, c_void_p]),
 }
 
 
@@ -195,6 +198,16 @@ def ts_decode_step(ctx, cache, layer, q, k_pool, v_pool, page_table, seq_lens, B
                                     _p(seq_lens), B, ctypes.byref(params), _p(vote), vote_stride, _p(idx),
                                     idx_stride, _p(count), _p(out), _p(lse), _p(hit), _s(stream)),
            "ts_decode_step")
+
+
+def ts_sparse_attend_noalloc(n_q_heads, n_kv_heads, head_dim, kv_dtype, q, k_pool, v_pool, num_pages,
+                             page_table, max_pages_per_seq, idx, idx_stride, count, B, scale, out, lse=None,
+                             status=None, stream=None) -> None:
+    """Sparse attention with no context and no allocation (fixed static scratch)."""
+    _check(library().ts_sparse_attend_noalloc(n_q_heads, n_kv_heads, head_dim, kv_dtype, _p(q), _p(k_pool),
+                                              _p(v_pool), num_pages, _p(page_table), max_pages_per_seq, _p(idx),
+                                              idx_stride, _p(count), B, scale, _p(out), _p(lse), _p(status),
+                                              _s(stream)), "ts_sparse_attend_noalloc")
 
 
 def ts_get_status(ctx, stream=None) -> int:

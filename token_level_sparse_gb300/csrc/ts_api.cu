@@ -70,6 +70,7 @@ const char* ts_status_str(ts_status s) {
     case TS_ERR_TIMEOUT: return "a bounded device wait ran out";
     case TS_ERR_COOP_UNAVAILABLE: return "cooperative launch refused";
     case TS_ERR_SEQ_LEN: return "sequence length outside [0, max tokens]";
+    case TS_ERR_SCRATCH_LIMIT: return "size beyond the fixed scratch of the no-alloc call";
   }
   return "unknown status";
 }

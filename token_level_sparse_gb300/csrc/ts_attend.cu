@@ -289,3 +289,122 @@ ts_status launch_attend(ts_ctx* ctx, const AttendCall& a, cudaStream_t s) {
 }
 
 }  // namespace ts
+
+// ---------------------------------------------------------------------------
+// The no-alloc variant of the sparse attention (ts_sparse_attend_noalloc).
+// For callers that may not call cudaMalloc: the scratch lives in one fixed
+// static device array instead of a context. Layout: [0, 16 KiB) merge
+// counters (kCounterSlots per sequence) and a fallback status slot,
+// [16 KiB, end) split partials.
+
+#include <mutex>
+
+namespace ts {
+namespace {
+
+constexpr int kNoAllocMaxBatch = 48;
+constexpr size_t kNoAllocHeadBytes = 16384;
+constexpr size_t kNoAllocPartFloats = size_t(1) << 20;
+constexpr size_t kNoAllocBytes = kNoAllocHeadBytes + kNoAllocPartFloats * sizeof(float);
+static_assert(kNoAllocMaxBatch * kCounterSlots * sizeof(unsigned) + sizeof(int) <= kNoAllocHeadBytes,
+              "counters must fit the head of the array");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+struct NoAllocDevice {
+  unsigned char* base = nullptr;  // device address of g_noalloc_scratch
+  int num_sms = 0;
+};
+constexpr int kNoAllocMaxDevices = 64;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of the array on the current device (looked up once per device).
+ts_status noalloc_setup(int device, NoAllocDevice& out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc_dev[device];
+  if (!d.base) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return TS_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return TS_ERR_CUDA;
+    d.num_sms = sms;
+    d.base = static_cast<unsigned char*>(p);
+  }
+  out = d;
+  return TS_OK;
+}
+
+template <typename KT, int D, int G>
+ts_status run_attend_noalloc(const AttKArgs& proto, int B, int HKV, int device, const NoAllocDevice& dev,
+                             cudaStream_t s) {
+  using S = AttShape<KT, D, G>;
+  const size_t per_split = (size_t)B * HKV * G * (D + 2);
+  if (per_split > kNoAllocPartFloats) return TS_ERR_SCRATCH_LIMIT;
+  int nsplit = (2 * dev.num_sms + HKV * B - 1) / (HKV * B);
+  nsplit = nsplit < 1 ? 1 : (nsplit > kAttnMaxSplits ? kAttnMaxSplits : nsplit);
+  const int fit = (int)(kNoAllocPartFloats / per_split);
+  if (nsplit > fit) nsplit = fit;
+  if (!ensure_smem<attend_kernel<KT, D, G>>(S::smem_bytes(), device)) return TS_ERR_CUDA;
+  AttKArgs a = proto;
+  a.counters = reinterpret_cast<unsigned*>(dev.base);
+  a.part = reinterpret_cast<float*>(dev.base + kNoAllocHeadBytes);
+  if (!a.status) a.status = reinterpret_cast<int*>(dev.base + kNoAllocMaxBatch * kCounterSlots * sizeof(unsigned));
+  // the merge counters must start at zero
+  if (cudaMemsetAsync(dev.base, 0, (size_t)B * kCounterSlots * sizeof(unsigned), s) != cudaSuccess)
+    return TS_ERR_CUDA;
+  attend_kernel<KT, D, G><<<dim3(nsplit, HKV, B), S::THREADS, S::smem_bytes(), s>>>(a);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+}  // namespace ts
+
+extern "C" ts_status ts_sparse_attend_noalloc(int n_q_heads, int n_kv_heads, int head_dim, int kv_dtype,
+                                              const float* q, const void* k_pool, const void* v_pool,
+                                              int64_t num_pages, const int32_t* page_table,
+                                              int max_pages_per_seq, const int32_t* idx, int64_t idx_stride,
+                                              const int32_t* count, int B, float scale, float* out,
+                                              float* lse, int32_t* status, void* stream) {
+  using namespace ts;
+  if (!q || !k_pool || !v_pool || !page_table || !idx || !count || !out) return TS_ERR_INVALID_ARG;
+  if (n_q_heads < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads != 0 || num_pages < 1 ||
+      max_pages_per_seq < 1 || idx_stride < 1 || B < 1)
+    return TS_ERR_INVALID_ARG;
+  if (kv_dtype != TS_KV_F32 && kv_dtype != TS_KV_BF16) return TS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(k_pool) % 16 != 0 || reinterpret_cast<uintptr_t>(v_pool) % 16 != 0)
+    return TS_ERR_INVALID_ARG;
+  if (B > kNoAllocMaxBatch || n_kv_heads > kCounterSlots - 2) return TS_ERR_SCRATCH_LIMIT;
+  if ((int64_t)max_pages_per_seq * kPage > ((int64_t)1 << 30)) return TS_ERR_SHAPE;
+  int device = 0;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= kNoAllocMaxDevices) return TS_ERR_CUDA;
+  NoAllocDevice dev;
+  ts_status st = noalloc_setup(device, dev);
+  if (st != TS_OK) return st;
+  AttKArgs a;
+  a.q = q;
+  a.k_pool = static_cast<const unsigned char*>(k_pool);
+  a.v_pool = static_cast<const unsigned char*>(v_pool);
+  a.page_table = page_table;
+  a.pt_stride = max_pages_per_seq;
+  a.num_pages = num_pages;
+  a.max_tokens = max_pages_per_seq * kPage;
+  a.idx = idx;
+  a.idx_stride = idx_stride;
+  a.count = count;
+  a.H = n_q_heads;
+  a.HKV = n_kv_heads;
+  a.scale = scale == 0.f ? 1.f / sqrtf((float)head_dim) : scale;
+  a.out = out;
+  a.lse = lse;
+  a.part = nullptr;
+  a.counters = nullptr;
+  a.status = status;
+  const int G = n_q_heads / n_kv_heads;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+#define X(DT, T, D_, G_) \
+  if (kv_dtype == DT && head_dim == D_ && G == G_) return run_attend_noalloc<T, D_, G_>(a, B, n_kv_heads, device, dev, s);
+  TS_ATTEND_GEOMETRIES(X)
+#undef X
+  return TS_ERR_UNSUPPORTED;
+}
