@@ -190,6 +190,23 @@ def score_traffic():
     return None
 
 
+def step_traffic():
+    """Per-launch DRAM bytes of the persistent step kernel at 128K (miss step) from the
+    committed ncu summary, or None when absent or taken on another kernel revision."""
+    src = open(os.path.join(ROOT, "token_level_sparse_gb300", "csrc", "ts_step.cu"), "rb").read()
+    sha = hashlib.sha256(src).hexdigest()
+    prof = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(prof):
+        return None
+    for fn in sorted(os.listdir(prof)):
+        if fn.endswith(".md"):
+            m = re.search(r"step_traffic_bytes_per_launch_n128k:\s*([0-9.e+]+)\s+step_source_sha256:\s*([0-9a-f]{64})",
+                          open(os.path.join(prof, fn)).read())
+            if m and m.group(2) == sha:
+                return float(m.group(1))
+    return None
+
+
 class DecodeBench:
     """One workload on one GPU: buffers, a captured CUDA graph of one decode step
     (all layers), and the timed loop."""
@@ -356,10 +373,18 @@ def summarise(bench, rec, peak_gbs):
     ms = [r["ms"] for r in rec]
     total_ms = sum(ms)
     miss = [r for r in rec if r["any_miss"]]
-    score_ms = sum(r["prof"]["score"][0] for r in miss)
-    score_launches = sum(r["n_miss"] for r in miss)   # launches that scanned (one per missing layer)
-    scan_bytes = sum(r["scan"] for r in miss)
-    out = dict(steps=len(rec), ms_per_step=total_ms / len(rec), value=1000.0 * len(rec) / total_ms,
+    fused = rec and rec[0]["prof"].get("step", (0.0, 0))[1] > 0
+    if fused:
+        # one persistent kernel per (step, layer): its bytes are the scan plus the gather
+        score_ms = sum(r["prof"]["step"][0] for r in miss)
+        score_launches = sum(r["prof"]["step"][1] for r in miss)
+        scan_bytes = sum(r["scan"] + r["gather"] for r in miss)
+    else:
+        score_ms = sum(r["prof"]["score"][0] for r in miss)
+        score_launches = sum(r["n_miss"] for r in miss)   # launches that scanned (one per missing layer)
+        scan_bytes = sum(r["scan"] for r in miss)
+    out = {"fused": bool(fused)}
+    out.update(steps=len(rec), ms_per_step=total_ms / len(rec), value=1000.0 * len(rec) / total_ms,
                hit_rate=1.0 - sum(r["n_miss"] for r in rec) / (len(rec) * bench.sp.layers * bench.sp.batch))
     if miss and score_ms > 0:
         out["score_gbs"] = scan_bytes / (score_ms * 1e-3) / 1e9
@@ -555,9 +580,11 @@ def main(argv=None):
         return
     clocks = clk.summary()
     traffic = score_traffic()
+    kname = ("step_kernel (persistent: cache test, paged score, vote, select, attend; miss steps)"
+             if s.get("fused") else "score_logits_kernel (paged dot product + per-CTA normaliser)")
     roof = {"bound": "hbm", "achieved": s.get("score_gbs"), "peak": peak_gbs, "unit": "GB/s",
             "frac": (s["score_gbs"] / peak_gbs) if s.get("score_gbs") else None,
-            "traffic": traffic, "kernel": "score_logits_kernel (paged dot product + per-CTA normaliser)",
+            "traffic": traffic if not s.get("fused") else step_traffic(), "kernel": kname,
             "peak_source": f"{peak_src} hbm_gbs", "algorithmic_bytes_per_launch": s.get("scan_bytes_per_launch"),
             "us_per_launch": s.get("score_us_per_launch")}
     line = {

@@ -202,7 +202,8 @@ enum {
   TS_PROF_VOTE = 2,    /* head soft vote                            */
   TS_PROF_SELECT = 3,  /* radix selection, refresh and compaction   */
   TS_PROF_ATTEND = 4,  /* sparse attention + merge                  */
-  TS_PROF_N = 5
+  TS_PROF_STEP = 5,    /* the persistent whole-step kernel          */
+  TS_PROF_N = 6
 };
 typedef struct {
   double ms[TS_PROF_N];        /* summed device time per family */

@@ -49,10 +49,10 @@ class Config(ctypes.Structure):
 
 
 class Profile(ctypes.Structure):
-    _fields_ = [("ms", c_double * 5), ("launches", c_int64 * 5)]
+    _fields_ = [("ms", c_double * 6), ("launches", c_int64 * 6)]
 
 
-PROF_FAMILIES = ("check", "score", "vote", "select", "attend")
+PROF_FAMILIES = ("check", "score", "vote", "select", "attend", "step")
 
 
 class SelectParams(ctypes.Structure):

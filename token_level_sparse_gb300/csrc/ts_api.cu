@@ -35,6 +35,14 @@ void free_ctx_buffers(ts_ctx* c) {
   cudaFree(c->attn_part);
   cudaFree(c->vote);
   cudaFree(c->hit);
+  cudaFree(c->step_partials);
+  cudaFree(c->step_hist);
+  cudaFree(c->step_mass);
+  cudaFree(c->cand_n);
+  cudaFree(c->cands);
+  cudaFree(c->cta_cnt);
+  cudaFree(c->apart);
+  cudaFree(c->gsync);
 }
 
 float resolve_scale(const ts_ctx* ctx, float scale) {
@@ -105,8 +113,18 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   auto chk = [&](cudaError_t r) {
     if (e == cudaSuccess) e = r;
   };
+  const size_t NS = (size_t)ctx->num_sms;
+  ctx->logits_floats = (int64_t)(B * H * T + H * NS * 2 * kPage);
   chk(alloc(&ctx->status, 1));
-  chk(alloc(&ctx->logits, B * H * T));
+  chk(alloc(&ctx->logits, (size_t)ctx->logits_floats));
+  chk(alloc(&ctx->step_partials, B * NS * H));
+  chk(alloc(&ctx->step_hist, 3 * B * 2048));
+  chk(alloc(&ctx->step_mass, 3 * B * 2048));
+  chk(alloc(&ctx->cand_n, B));
+  chk(alloc(&ctx->cands, B * 2048));
+  chk(alloc(&ctx->cta_cnt, B * NS * 3));
+  chk(alloc(&ctx->apart, B * NS * H * (D + 2)));
+  chk(alloc(&ctx->gsync, 4));
   chk(alloc(&ctx->partials, B * ctx->score_max_chunks * H));
   chk(alloc(&ctx->stats, B * H));
   chk(alloc(&ctx->counters, B * kCounterSlots));
@@ -253,6 +271,35 @@ ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q
   const bool use_cache = cache != nullptr && params->theta <= 1.f;
   uint8_t* hbuf = hit ? hit : ctx->hit;
   ts_status st = TS_OK;
+  if (ctx->use_step && step_supported(ctx->cfg) && B <= 64) {
+    // one persistent cooperative kernel for the whole step
+    if (!use_cache && hit && cudaMemsetAsync(hit, 0, B, s) != cudaSuccess) return TS_ERR_CUDA;
+    StepCall sc{};
+    sc.phases = kPhaseScore | kPhaseSelect | kPhaseAttend | (use_cache ? kPhaseCheck : 0);
+    sc.B = B;
+    sc.q = q;
+    sc.k_pool = k_pool;
+    sc.v_pool = v_pool;
+    sc.page_table = page_table;
+    sc.seq_lens = seq_lens;
+    sc.scale = scale;
+    sc.theta = params->theta;
+    sc.hit_in = nullptr;
+    sc.hit_out = use_cache ? hbuf : nullptr;
+    sc.cache = cache;
+    sc.layer = layer;
+    sc.params = *params;
+    sc.vote = vote;
+    sc.vote_stride = vote_stride;
+    sc.idx = idx;
+    sc.idx_stride = idx_stride;
+    sc.count = count;
+    sc.out = out;
+    sc.lse = lse;
+    st = launch_step(ctx, sc, s);
+    if (st != TS_ERR_COOP_UNAVAILABLE) return st;
+    ctx->use_step = false;  // the multi-kernel path below from now on
+  }
   if (use_cache) {
     st = launch_cache_check(ctx, cache, layer, q, B, params->theta, hbuf, nullptr, s);
     if (st != TS_OK) return st;

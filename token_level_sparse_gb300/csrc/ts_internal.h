@@ -64,6 +64,18 @@ struct ts_ctx {
   float* vote = nullptr;                 // [max_batch][max_tokens] (decode step)
   uint8_t* hit = nullptr;                // [max_batch] (decode step)
   int64_t kernels = 0;           // kernel launches issued
+  // persistent decode-step kernel
+  int step_grid = 0;                     // CTAs of the cooperative launch (0: not yet sized)
+  int64_t logits_floats = 0;             // size of `logits` (also the step kernel's spill area)
+  float2* step_partials = nullptr;       // [max_batch][num_sms][H]
+  unsigned* step_hist = nullptr;         // [3][max_batch][2048]
+  unsigned long long* step_mass = nullptr;  // [3][max_batch][2048]
+  unsigned* cand_n = nullptr;            // [max_batch]
+  unsigned long long* cands = nullptr;   // [max_batch][2048]
+  int* cta_cnt = nullptr;                // [max_batch][num_sms][3]
+  float* apart = nullptr;                // [max_batch][num_sms][H][d + 2]
+  unsigned* gsync = nullptr;             // grid barrier state (4 words)
+  bool use_step = true;                  // the persistent kernel is available
   // kernel timing
   bool prof_on = false;
   int prof_used = 0;
@@ -126,6 +138,44 @@ struct AttendCall {
   float* lse;
 };
 
+struct StepCall {
+  int phases;            // TS_PHASE_* bits
+  int B;
+  const float* q;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  float scale;
+  float theta;
+  const uint8_t* hit_in;
+  uint8_t* hit_out;
+  ts_cache* cache;
+  int layer;
+  ts_select_params params;
+  float* vote;
+  int64_t vote_stride;
+  int32_t* idx;
+  int64_t idx_stride;
+  int32_t* count;
+  float* out;
+  float* lse;
+};
+constexpr int kPhaseCheck = 1, kPhaseScore = 2, kPhaseSelect = 4, kPhaseAttend = 8;
+
+// Head geometries with a compiled kernel: (kv type flag, element type, d, H_kv, G).
+#define TS_STEP_GEOMETRIES(X)             \
+  X(TS_KV_F32, float, 64, 4, 1)           \
+  X(TS_KV_F32, float, 64, 2, 4)           \
+  X(TS_KV_F32, float, 128, 8, 4)          \
+  X(TS_KV_BF16, __nv_bfloat16, 128, 8, 4) \
+  X(TS_KV_BF16, __nv_bfloat16, 128, 4, 7) \
+  X(TS_KV_BF16, __nv_bfloat16, 128, 8, 1) \
+  X(TS_KV_BF16, __nv_bfloat16, 64, 4, 2)  \
+  X(TS_KV_BF16, __nv_bfloat16, 128, 2, 8)
+
+bool step_supported(const ts_config& c);
+ts_status launch_step(ts_ctx* ctx, const StepCall& a, cudaStream_t s);
 bool score_supported(const ts_config& c);
 ts_status launch_score(ts_ctx* ctx, const ScoreCall& a, cudaStream_t s);
 ts_status launch_select(ts_ctx* ctx, const SelectCall& a, cudaStream_t s);
