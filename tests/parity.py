@@ -59,7 +59,7 @@ class GpuRunner:
     """Drives ts_decode_step (or the three separate calls) over a workload."""
 
     def __init__(self, wl: W.Workload, theta=None, cache=True, mode=None, top_p=None, k=None,
-                 n_sink=None, n_local=None, separate_calls=False):
+                 n_sink=None, n_local=None, separate_calls=False, multi_kernel=False):
         T = tsl()
         self.T = T
         self.wl = wl
@@ -74,8 +74,17 @@ class GpuRunner:
             theta=sp.theta if theta is None else theta)
         dev = wl.page_table.device
         B = sp.batch
-        self.ctx = T.Context(sp.n_q_heads, sp.n_kv_heads, sp.head_dim, kv_flag(T, sp), B,
-                             wl.page_table.shape[1], wl.num_pages)
+        import os
+        prev = os.environ.get("TOKENSELECT_MULTI_KERNEL")
+        os.environ["TOKENSELECT_MULTI_KERNEL"] = "1" if multi_kernel else "0"
+        try:
+            self.ctx = T.Context(sp.n_q_heads, sp.n_kv_heads, sp.head_dim, kv_flag(T, sp), B,
+                                 wl.page_table.shape[1], wl.num_pages)
+        finally:
+            if prev is None:
+                del os.environ["TOKENSELECT_MULTI_KERNEL"]
+            else:
+                os.environ["TOKENSELECT_MULTI_KERNEL"] = prev
         mt = self.ctx.max_tokens
         cap = self.params.k + self.params.n_sink + self.params.n_local if self.mode == "topk" else mt
         self.cache = self.ctx.cache(sp.layers, self.params.k if self.mode == "topk" else mt) if cache else None
@@ -230,10 +239,11 @@ class TrajectoryReport:
 
 
 def run_trajectory(wl, steps, layers=(0,), theta=None, mode=None, top_p=None, check_votes=True,
-                   separate_calls=False, **sel):
+                   separate_calls=False, multi_kernel=False, **sel):
     """Steps the GPU and the oracle together and checks every output."""
     sp = wl.spec
-    gpu = GpuRunner(wl, theta=theta, mode=mode, top_p=top_p, separate_calls=separate_calls, **sel)
+    gpu = GpuRunner(wl, theta=theta, mode=mode, top_p=top_p, separate_calls=separate_calls,
+                    multi_kernel=multi_kernel, **sel)
     ora = OracleRunner(wl, layers=list(layers), mode=mode, top_p=top_p, theta=theta, **sel)
     rep = TrajectoryReport()
     H = sp.n_q_heads

@@ -28,6 +28,18 @@ def test_tiny_fp32_trajectory_with_cache():
     assert rep.steps == 8
 
 
+@pytest.mark.parametrize("multi", [False, True])
+def test_llama_small_both_paths(multi):
+    sp = W.spec(1, n0=(9001,), steps=4, k=512, n_local=128)
+    _run(sp, 4, multi_kernel=multi)
+
+
+@pytest.mark.parametrize("multi", [False, True])
+def test_qwen_batched_small_both_paths(multi):
+    sp = W.spec(2, n0=(700, 5000, 3100, 40), n0_range=None, batch=4, steps=3, k=256, n_local=64)
+    _run(sp, 3, multi_kernel=multi)
+
+
 def test_tiny_fp32_separate_calls_all_miss():
     _run(W.spec(0), 4, separate_calls=True, theta=2.0)
 

@@ -1,6 +1,7 @@
 // C ABI of libtokenselect: argument validation, context and cache lifetime,
 // and the stream-ordered composition of one decode step.
 #include <cmath>
+#include <cstdio>
 #include <cstdlib>
 #include <new>
 
@@ -98,6 +99,8 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   ts_ctx* ctx = new (std::nothrow) ts_ctx();
   if (!ctx) return TS_ERR_CUDA;
   ctx->cfg = c;
+  // TOKENSELECT_MULTI_KERNEL=1 keeps ts_decode_step on the multi-kernel path (tests, comparisons)
+  if (const char* env = std::getenv("TOKENSELECT_MULTI_KERNEL")) ctx->use_step = !(env[0] == '1');
   if (cudaGetDevice(&ctx->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess) {
     delete ctx;
@@ -297,6 +300,7 @@ ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q
     sc.out = out;
     sc.lse = lse;
     st = launch_step(ctx, sc, s);
+    if (std::getenv("TS_DEBUG")) std::fprintf(stderr, "ts decode step: persistent kernel -> %s\n", ts_status_str(st));
     if (st != TS_ERR_COOP_UNAVAILABLE) return st;
     ctx->use_step = false;  // the multi-kernel path below from now on
   }

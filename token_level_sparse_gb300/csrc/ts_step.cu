@@ -26,6 +26,8 @@
 // the kernel records TS_ERR_TIMEOUT and returns.
 #include <cfloat>
 #include <cmath>
+#include <cstdio>
+#include <cstdlib>
 
 #include "ts_common.cuh"
 
@@ -61,8 +63,8 @@ struct StepShape {
   static constexpr int DPL = EPC * CPL;
   static constexpr int LPR = D / DPL;                     // lanes per K row in the scan
   static constexpr int RPW = 32 / LPR;                    // rows per warp step
-  static constexpr int NCW = cmin(16, HKV * P / RPW);     // consumer warps
-  static constexpr int NW = NCW + 1;                      // + the producer warp
+  static constexpr int NCW = cmin(16, HKV * P / RPW);     // warps (all consume; the last to finish a
+  static constexpr int NW = NCW;                          // stage refills it: no producer warp)
   static constexpr int THREADS = NW * 32;
   static constexpr int ROWS = P * HKV / NCW;              // rows of a stage per consumer warp
   static constexpr int ITERS = ROWS / RPW;
@@ -71,7 +73,8 @@ struct StepShape {
   static constexpr int NST = STAGE_BYTES <= 8192 ? 6 : (STAGE_BYTES <= 16384 ? 4 : (STAGE_BYTES <= 32768 ? 3 : 2));
   static constexpr int RING_BYTES = NST * STAGE_BYTES;
   // attention: a lane reads ACB bytes of a row; ALPT lanes per row
-  static constexpr int ACB = (G > 4 && D * (int)sizeof(KT) / 8 <= 32) ? 8 : 16;
+  // (8-byte lane chunks keep the per-lane softmax state small: 17 warps leave 96 registers)
+  static constexpr int ACB = (D * (int)sizeof(KT) / 8 <= 32) ? 8 : 16;
   static constexpr int ALPT = D * (int)sizeof(KT) / ACB;
   static constexpr int AEPC = ACB / (int)sizeof(KT);
   static constexpr int ATPW = 32 / ALPT;                  // tokens per warp step
@@ -248,6 +251,9 @@ struct Smem {
   int stage_tok[8][16];    // per ring stage: CTA-local first token of each page (-1: unused)
   int stage_nv[8][16];     // valid slots of each page
   int stage_b[8][16];      // its sequence
+  int stage_done[8];       // warps finished with the current use of each ring slot
+  int slot_last[8];        // the last ring use issued into each slot (-1: none)
+  int timed_out;
   int wsum[33];
   int flag;
   float red_f[3][32];
@@ -259,11 +265,11 @@ struct Smem {
 // --------------------------------------------------------------- the kernel
 
 template <typename KT, int D, int HKV, int G>
-__global__ void __maxnreg__(120) step_kernel(StepKArgs a) {
+__global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_kernel(StepKArgs a) {
   using S = StepShape<KT, D, HKV, G>;
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ Smem sm;
-  __shared__ __align__(8) uint64_t full[S::NST], empty[S::NST];
+  __shared__ __align__(8) uint64_t full[S::NST];
   __shared__ __align__(8) uint64_t abar;
 
   unsigned char* ring = dsm;
@@ -278,8 +284,10 @@ __global__ void __maxnreg__(120) step_kernel(StepKArgs a) {
   if (tid == 0) {
     for (int s = 0; s < S::NST; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], S::NCW);
+      sm.stage_done[s] = 0;
+      sm.slot_last[s] = -1;
     }
+    sm.timed_out = 0;
     mbar_init(&abar, 1);
     mbar_fence_init();
   }
@@ -432,59 +440,50 @@ __global__ void __maxnreg__(120) step_kernel(StepKArgs a) {
     const int nstages = (np + pps - 1) / pps;
     const int slab = hpw * S::P * S::ROW_BYTES;      // bytes of one page's heads of the wave
     int stage_seq = 0;                               // ring use counter across waves
+    // Issues ring use u = stage_seq + si (the pps pages si*pps.. of my range, the wave's
+    // heads of each) into slot u % NST: metadata first, then arrive.expect_tx, then the copies.
+    auto issue = [&](int u, int si, int g0) {
+      const int s = u % S::NST;
+      sm.slot_last[s] = u;
+      uint32_t bytes = 0;
+      int pages[16];
+      for (int j = 0; j < pps; ++j) {
+        const int gp = sm.p0 + si * pps + j;
+        sm.stage_tok[s][j] = -1;
+        sm.stage_nv[s][j] = 0;
+        sm.stage_b[s][j] = 0;
+        pages[j] = -1;
+        if (gp >= sm.p1) continue;
+        int seg = 0;
+        while (seg + 1 < sm.nseg && gp >= sm.seg_pend[seg]) ++seg;
+        const int b = sm.seg_b[seg];
+        const int lp = gp - sm.seq[b].pg0;
+        const int page = a.page_table[(size_t)b * a.pt_stride + lp];
+        sm.stage_tok[s][j] = (gp - sm.p0) * S::P;
+        sm.stage_b[s][j] = b;
+        if (page < 0 || (int64_t)page >= a.num_pages) {
+          set_error(a.status, TS_ERR_PAGE_OOB);
+          continue;
+        }
+        sm.stage_nv[s][j] = min(S::P, sm.seq[b].n - lp * S::P);
+        pages[j] = page;
+        bytes += (uint32_t)slab;
+      }
+      mbar_arrive_expect_tx(&full[s], bytes);
+      for (int j = 0; j < pps; ++j) {
+        if (pages[j] < 0) continue;
+        bulk_g2s(ring + (size_t)s * S::STAGE_BYTES + (size_t)j * slab,
+                 a.k_pool + ((size_t)pages[j] * HKV + g0) * S::P * S::ROW_BYTES, (uint32_t)slab, &full[s]);
+      }
+    };
     for (int wv = 0; wv < nwaves; ++wv) {
       const int g0 = wv * hpw;
-      if (warp == S::NCW) {
-        // ---- producer: one lane streams my pages, pps pages per stage
-        if (lane == 0) {
-          int seg = 0;
-          int issued = 0;
-          for (int si = 0; si < nstages; ++si) {
-            const int u = stage_seq + si;
-            const int s = u % S::NST;
-            if (u >= S::NST && !mbar_wait(&empty[s], ((u / S::NST) - 1) & 1)) {
-              set_error(a.status, TS_ERR_TIMEOUT);
-              break;
-            }
-            uint32_t bytes = 0;
-            int pages[16];
-            for (int j = 0; j < pps; ++j) {
-              const int gp = sm.p0 + si * pps + j;
-              sm.stage_tok[s][j] = -1;
-              sm.stage_nv[s][j] = 0;
-              sm.stage_b[s][j] = 0;
-              pages[j] = -1;
-              if (gp >= sm.p1) continue;
-              while (seg + 1 < sm.nseg && gp >= sm.seg_pend[seg]) ++seg;
-              const int b = sm.seg_b[seg];
-              const int lp = gp - sm.seq[b].pg0;
-              const int page = a.page_table[(size_t)b * a.pt_stride + lp];
-              sm.stage_tok[s][j] = (gp - sm.p0) * S::P;
-              sm.stage_b[s][j] = b;
-              if (page < 0 || (int64_t)page >= a.num_pages) {
-                set_error(a.status, TS_ERR_PAGE_OOB);
-                continue;
-              }
-              sm.stage_nv[s][j] = min(S::P, sm.seq[b].n - lp * S::P);
-              pages[j] = page;
-              bytes += (uint32_t)slab;
-            }
-            mbar_arrive_expect_tx(&full[s], bytes);
-            for (int j = 0; j < pps; ++j) {
-              if (pages[j] < 0) continue;
-              bulk_g2s(ring + (size_t)s * S::STAGE_BYTES + (size_t)j * slab,
-                       a.k_pool + ((size_t)pages[j] * HKV + g0) * S::P * S::ROW_BYTES, (uint32_t)slab, &full[s]);
-            }
-            ++issued;
-          }
-          // every copy lands before shared memory is reused
-          for (int si = max(0, issued - S::NST); si < issued; ++si) {
-            const int u = stage_seq + si;
-            if (!mbar_wait(&full[u % S::NST], (u / S::NST) & 1)) set_error(a.status, TS_ERR_TIMEOUT);
-          }
-        }
-      } else {
-        // ---- consumers: warp -> KV head g0 + gi, ROWS rows of that head in each stage
+      // the ring is idle between waves: fill it
+      if (tid == 0)
+        for (int si = 0; si < min(S::NST, nstages); ++si) issue(stage_seq + si, si, g0);
+      __syncthreads();
+      {
+        // ---- warp -> KV head g0 + gi, ROWS rows of that head in each stage
         const int wph = S::NCW / hpw;
         const int gi = warp / wph;
         const int row0 = (warp % wph) * S::ROWS;     // rows of one page: ROWS divides P or P divides ROWS
@@ -501,6 +500,7 @@ __global__ void __maxnreg__(120) step_kernel(StepKArgs a) {
           const int s = u % S::NST;
           if (!mbar_wait(&full[s], (u / S::NST) & 1)) {
             set_error(a.status, TS_ERR_TIMEOUT);
+            sm.timed_out = 1;
             break;
           }
           const KT* st = reinterpret_cast<const KT*>(ring + (size_t)s * S::STAGE_BYTES);
@@ -550,10 +550,22 @@ __global__ void __maxnreg__(120) step_kernel(StepKArgs a) {
               *eaddr(gi * G + which, tloc + slot) = slot < nv ? dot * a.scale : -INFINITY;
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[s]);
+          if (lane == 0) {
+            // the last warp done with this use of the slot refills it with use u + NST
+            if (atomicAdd(&sm.stage_done[s], 1) == S::NCW - 1) {
+              sm.stage_done[s] = 0;
+              if (si + S::NST < nstages) issue(u + S::NST, si + S::NST, g0);
+            }
+          }
         }
       }
       stage_seq += nstages;
+      __syncthreads();
+      if (sm.timed_out && tid == 0) {
+        // copies issued but never consumed must land before the ring is reused
+        for (int ss = 0; ss < S::NST; ++ss)
+          if (sm.slot_last[ss] >= 0) mbar_wait(&full[ss], (sm.slot_last[ss] / S::NST) & 1);
+      }
       __syncthreads();
 
       // ---- per (segment, wave head): max, exp in place, compensated sum -> partials
@@ -1253,17 +1265,37 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return TS_ERR_CUDA;
     static_bytes = (int)fa.sharedSizeBytes;
   }
-  const int dyn = (kSmemLimit - static_bytes - 128) / 128 * 128;
+  static int smem_avail = -1;      // shared memory one CTA of the SM may use in all
+  if (smem_avail < 0) {
+    int optin = 0, per_sm = 0, reserved = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, ctx->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, ctx->device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, ctx->device) != cudaSuccess)
+      return TS_ERR_CUDA;
+    smem_avail = min(min(optin, per_sm - reserved), kSmemLimit);
+    if (std::getenv("TS_DEBUG"))
+      std::fprintf(stderr, "ts step: smem optin %d, per SM %d, reserved/block %d\n", optin, per_sm, reserved);
+    // the whole unified L1/shared array as shared memory for this kernel
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+      return TS_ERR_CUDA;
+  }
+  const int dyn = (smem_avail - static_bytes - 1024) / 128 * 128;
   const int flag_cap = 8192;   // >= kMaxB * kMaxWaveHeads * 4 (vote weights alias it)
   static_assert(kMaxB * kMaxWaveHeads * 4 <= 8192, "weights fit the flag area");
   const int e_bytes = dyn - S::RING_BYTES - flag_cap;
   if (e_bytes < 16 * 1024) return TS_ERR_UNSUPPORTED;
-  if (!ensure_smem<step_kernel<KT, D, HKV, G>>((size_t)dyn, ctx->device)) return TS_ERR_CUDA;
+  if (!ensure_smem<step_kernel<KT, D, HKV, G>>((size_t)dyn, ctx->device)) {
+    if (std::getenv("TS_DEBUG")) std::fprintf(stderr, "ts step: smem attribute %d B refused\n", dyn);
+    return TS_ERR_CUDA;
+  }
+  const bool debug = std::getenv("TS_DEBUG") != nullptr;
   if (ctx->step_grid <= 0) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, S::THREADS, (size_t)dyn) != cudaSuccess ||
-        per_sm < 1)
-      return TS_ERR_COOP_UNAVAILABLE;
+    const cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, S::THREADS, (size_t)dyn);
+    if (debug)
+      std::fprintf(stderr, "ts step: static %d B, dynamic %d B, threads %d, blocks/SM %d (%s)\n", static_bytes, dyn,
+                   S::THREADS, per_sm, cudaGetErrorString(oe));
+    if (oe != cudaSuccess || per_sm < 1) return TS_ERR_COOP_UNAVAILABLE;
     ctx->step_grid = ctx->num_sms;
   }
   const ts_config& cfg = ctx->cfg;
@@ -1334,6 +1366,7 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   ctx->kernels += 1;
   ProfScope ps(ctx, TS_PROF_STEP, s);
   const cudaError_t e = cudaLaunchKernelEx(&lc, kern, a);
+  if (debug && e != cudaSuccess) std::fprintf(stderr, "ts step launch: %s\n", cudaGetErrorString(e));
   if (e == cudaErrorCooperativeLaunchTooLarge) return TS_ERR_COOP_UNAVAILABLE;
   return cuda_status(e);
 }
