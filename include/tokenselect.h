@@ -219,6 +219,15 @@ ts_status ts_profile_read(ts_ctx* ctx, ts_profile* out, int keep);
  * graph) since ts_create, counted on the host at each launch. */
 ts_status ts_kernel_count(ts_ctx* ctx, int64_t* out);
 
+/* Tracing: %globaltimer values (ns) at which CTA 0 of the last persistent
+ * decode-step kernel reached its phase boundaries (0: start, 1: set-up done,
+ * 2+3w / 3+3w / 4+3w: wave w scanned / partials written / barrier passed,
+ * 20: scoring done, 21: radix levels done, 22: candidates gathered,
+ * 23: selection done, 24: attention done, 25: last barrier passed,
+ * 26: outputs merged, 27: end; 0 where not reached). Synchronises `stream`,
+ * copies 32 values to out32 (host) and clears them. */
+ts_status ts_debug_phase_ns(ts_ctx* ctx, uint64_t* out32, void* stream);
+
 /* Library version, e.g. 100 for 0.1.0. */
 int ts_version(void);
 

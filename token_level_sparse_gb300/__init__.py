@@ -21,7 +21,7 @@ __all__ = [
     "ts_create", "ts_destroy", "ts_cache_create", "ts_cache_destroy", "ts_cache_reset",
     "ts_cache_check", "ts_score", "ts_select", "ts_sparse_attend", "ts_decode_step",
     "ts_get_status", "ts_status_str", "ts_version", "ts_profile_enable", "ts_profile_read",
-    "ts_kernel_count", "ts_sparse_attend_noalloc", "Context", "Cache", "Profile", "PROF_FAMILIES",
+    "ts_kernel_count", "ts_debug_phase_ns", "ts_sparse_attend_noalloc", "Context", "Cache", "Profile", "PROF_FAMILIES",
 ]
 
 TS_KV_F32, TS_KV_BF16 = 0, 1
@@ -84,6 +84,7 @@ _SIGS = {
     "ts_profile_enable": (c_int, [c_void_p, c_int]),
     "ts_profile_read": (c_int, [c_void_p, c_void_p, c_int]),
     "ts_kernel_count": (c_int, [c_void_p, POINTER(c_int64)]),
+    "ts_debug_phase_ns": (c_int, [c_void_p, c_void_p, c_void_p]),
     "ts_sparse_attend_noalloc": (c_int, [c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p, c_int64,
                                          c_void_p, c_int, c_void_p, c_int64, c_void_p, c_int, c_float,
                                          c_void_p, c_void_p, c_void_p, c_void_p]),
@@ -225,6 +226,13 @@ def ts_profile_read(ctx, keep: bool = False) -> dict:
     p = Profile()
     _check(library().ts_profile_read(ctx, ctypes.byref(p), 1 if keep else 0), "ts_profile_read")
     return {f: (p.ms[i], p.launches[i]) for i, f in enumerate(PROF_FAMILIES)}
+
+
+def ts_debug_phase_ns(ctx, stream=None) -> list:
+    """Phase-boundary times (ns) of CTA 0 in the last persistent step kernel."""
+    buf = (ctypes.c_uint64 * 32)()
+    _check(library().ts_debug_phase_ns(ctx, buf, _s(stream)), "ts_debug_phase_ns")
+    return list(buf)
 
 
 def ts_kernel_count(ctx) -> int:

@@ -1,6 +1,7 @@
 // C ABI of libtokenselect: argument validation, context and cache lifetime,
 // and the stream-ordered composition of one decode step.
 #include <cmath>
+#include <algorithm>
 #include <cstdio>
 #include <cstdlib>
 #include <new>
@@ -43,7 +44,9 @@ void free_ctx_buffers(ts_ctx* c) {
   cudaFree(c->cands);
   cudaFree(c->cta_cnt);
   cudaFree(c->apart);
+  cudaFree(c->step_wpart);
   cudaFree(c->gsync);
+  cudaFree(c->phase_ns);
 }
 
 float resolve_scale(const ts_ctx* ctx, float scale) {
@@ -117,6 +120,8 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
     if (e == cudaSuccess) e = r;
   };
   const size_t NS = (size_t)ctx->num_sms;
+  // [B][H][T] logits of the multi-kernel path; the persistent kernel keeps, per CTA, the
+  // logits of its page range: at most (B*T/16 + NS) pages, which this also covers
   ctx->logits_floats = (int64_t)(B * H * T + H * NS * 2 * kPage);
   chk(alloc(&ctx->status, 1));
   chk(alloc(&ctx->logits, (size_t)ctx->logits_floats));
@@ -127,7 +132,9 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   chk(alloc(&ctx->cands, B * 2048));
   chk(alloc(&ctx->cta_cnt, B * NS * 3));
   chk(alloc(&ctx->apart, B * NS * H * (D + 2)));
+  chk(alloc(&ctx->step_wpart, NS * B * kMaxScanWarps * kMaxScanG * 2));
   chk(alloc(&ctx->gsync, 4));
+  chk(alloc(&ctx->phase_ns, 32));
   chk(alloc(&ctx->partials, B * ctx->score_max_chunks * H));
   chk(alloc(&ctx->stats, B * H));
   chk(alloc(&ctx->counters, B * kCounterSlots));
@@ -143,6 +150,7 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   if (e == cudaSuccess) chk(cudaMemset(ctx->hist, 0, B * 2048 * sizeof(unsigned)));
   if (e == cudaSuccess) chk(cudaMemset(ctx->mass_hist, 0, B * 2048 * sizeof(unsigned long long)));
   if (e == cudaSuccess) chk(cudaMemset(ctx->hit, 0, B));
+  if (e == cudaSuccess) chk(cudaMemset(ctx->phase_ns, 0, 32 * sizeof(unsigned long long)));
   if (e == cudaSuccess) chk(cudaDeviceSynchronize());
   if (e != cudaSuccess) {
     free_ctx_buffers(ctx);
@@ -319,6 +327,14 @@ ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q
   if (st != TS_OK) return st;
   AttendCall ac{q, k_pool, v_pool, page_table, idx, idx_stride, count, B, scale, out, lse};
   return launch_attend(ctx, ac, s);
+}
+
+ts_status ts_debug_phase_ns(ts_ctx* ctx, uint64_t* out32, void* stream) {
+  if (!ctx || !out32) return TS_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return TS_ERR_CUDA;
+  if (cudaMemcpy(out32, ctx->phase_ns, 32 * sizeof(uint64_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return TS_ERR_CUDA;
+  return cudaMemset(ctx->phase_ns, 0, 32 * sizeof(uint64_t)) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 
 ts_status ts_kernel_count(ts_ctx* ctx, int64_t* out) {

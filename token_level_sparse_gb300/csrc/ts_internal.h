@@ -73,8 +73,10 @@ struct ts_ctx {
   unsigned* cand_n = nullptr;            // [max_batch]
   unsigned long long* cands = nullptr;   // [max_batch][2048]
   int* cta_cnt = nullptr;                // [max_batch][num_sms][3]
-  float* apart = nullptr;                // [max_batch][num_sms][H][d + 2]
+  float* apart = nullptr;                // [max_batch][num_sms][H][d] outputs, then [..][H] (max, sum)
+  float* step_wpart = nullptr;           // [num_sms][max_batch][16 warps][8 heads] (max, sum exp)
   unsigned* gsync = nullptr;             // grid barrier state (4 words)
+  unsigned long long* phase_ns = nullptr;  // [32] phase boundary times of the last step kernel
   bool use_step = true;                  // the persistent kernel is available
   // kernel timing
   bool prof_on = false;
@@ -96,6 +98,8 @@ namespace ts {
 
 // Counter slots per sequence: [0] score, [1] select, [2 .. 2+H_kv) attention.
 constexpr int kCounterSlots = 2 + 64;
+constexpr int kMaxScanWarps = 16;  // warps of the persistent step kernel's scan
+constexpr int kMaxScanG = 8;       // query heads per KV head the persistent kernel supports
 
 struct ScoreCall {
   const float* q;

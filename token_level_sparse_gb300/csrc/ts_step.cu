@@ -24,6 +24,7 @@
 //    bulk copy; per-CTA (max, sum, o) partials are merged after one barrier.
 // Grid barriers and mbarrier waits are bounded by %globaltimer; on time-out
 // the kernel records TS_ERR_TIMEOUT and returns.
+#include <algorithm>
 #include <cfloat>
 #include <cmath>
 #include <cstdio>
@@ -39,6 +40,11 @@ constexpr int kCandCap = 2048;     // candidates gathered per sequence
 constexpr int kBins = 2048;
 constexpr int kMaxRound = 128;     // attention tokens per gather round
 constexpr int kMaxWaveHeads = 32;  // query heads of one scan wave
+constexpr int kMaxG = kMaxScanG;   // query heads per KV head
+constexpr int kMaxPagesCta = 1024; // page ids of a CTA's range kept in shared memory
+constexpr int kMaxSlots = 12;      // ring slots (runtime count per launch)
+constexpr int64_t kLogitL2Budget = 48ll << 20;  // default bytes of logits one scan wave keeps in L2
+constexpr int kSelScratch = kBins * 12 + kCandCap * 8;  // CTA histogram and candidates while selecting
 constexpr float kFx = 1099511627776.0f;  // 2^40
 constexpr int kPhCheck = 1, kPhScore = 2, kPhSelect = 4, kPhAttend = 8;
 constexpr int kSmemLimit = 232448;  // bytes of shared memory per CTA on sm_103a
@@ -70,8 +76,7 @@ struct StepShape {
   static constexpr int ITERS = ROWS / RPW;
   static constexpr int ROW_BYTES = D * (int)sizeof(KT);
   static constexpr int STAGE_BYTES = HKV * P * ROW_BYTES; // H_kv (page, head) slabs of 16 rows
-  static constexpr int NST = STAGE_BYTES <= 8192 ? 6 : (STAGE_BYTES <= 16384 ? 4 : (STAGE_BYTES <= 32768 ? 3 : 2));
-  static constexpr int RING_BYTES = NST * STAGE_BYTES;
+  static constexpr int MIN_SLOTS = 2;
   // attention: a lane reads ACB bytes of a row; ALPT lanes per row
   // (8-byte lane chunks keep the per-lane softmax state small: 17 warps leave 96 registers)
   static constexpr int ACB = (D * (int)sizeof(KT) / 8 <= 32) ? 8 : 16;
@@ -83,8 +88,8 @@ struct StepShape {
   static_assert(NCW >= 1 && (P * HKV) % NCW == 0 && ROWS % RPW == 0 && ITERS >= 1, "scan warp split");
   static_assert(NCW % HKV == 0 && P % ROWS == 0 || ROWS % P == 0, "rows of a warp stay in one page");
   static_assert(32 % ALPT == 0 && GP <= ALPT, "attention lane split");
-  static_assert(RING_BYTES >= kBins * 12 + kCandCap * 8, "histograms and candidates alias the ring");
-  static_assert(G <= kMaxWaveHeads, "heads per KV head");
+  static_assert(G <= kMaxG, "heads per KV head");
+  static_assert(NCW <= kMaxScanWarps && NCW % HKV == 0, "scan warps split evenly over the KV heads");
 };
 
 struct GridSync {
@@ -130,12 +135,15 @@ struct StepKArgs {
   unsigned long long* cands;   // [B][kCandCap]  (key << 32 | ~index)
   int* cta_cnt;                // [B][nCTA][3]  cand-range selected, all selected, ties
   float* apart;                // [B][nCTA][H][D + 2]
-  float* spill;                // e-values past the shared-memory capacity
+  float* spill;                // per CTA: logits [tok][wave head]
+  float2* wpart;               // per CTA: [segment][scan warp][head] (max, sum exp) of a wave
   int64_t spill_floats;
+  int64_t l2_budget;           // bytes of logits one scan wave may keep in L2
   GridSync* gsync;
   int* status;
+  unsigned long long* phase_ns;  // CTA 0's %globaltimer at phase boundaries (debug)
   int dyn_bytes;               // dynamic shared memory of the launch
-  int e_cap;                   // floats of the shared e-buffer
+  int nslot;                   // ring slots of STAGE_BYTES each
   int flag_cap;                // bytes reserved at the tail for selection flags
 };
 
@@ -188,6 +196,20 @@ __device__ bool grid_sync(GridSync* gs, int* status) {
   return s_ok != 0;
 }
 
+// The value index that transpose_reduce<NV, LPR> leaves in `lane`.
+template <int NV, int LPR>
+__device__ __forceinline__ int reduce_slot(int lane) {
+  int base = 0, n = NV;
+#pragma unroll
+  for (int d = LPR / 2; d >= 1; d >>= 1) {
+    if (n > 1) {
+      n /= 2;
+      if (lane & d) base += n;
+    }
+  }
+  return base;
+}
+
 // Block-wide exclusive scan of one int per thread; total in *total.
 __device__ __forceinline__ int block_scan(int x, int* wsum, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -217,16 +239,6 @@ __device__ __forceinline__ int block_scan(int x, int* wsum, int& total) {
   return r;
 }
 
-// First index in the ascending list a[0, n) that is >= x.
-__device__ __forceinline__ int lower_bound_i(const int32_t* a, int n, int x) {
-  int l = 0, r = n;
-  while (l < r) {
-    const int m = (l + r) >> 1;
-    if (a[m] < x) l = m + 1; else r = m;
-  }
-  return l;
-}
-
 // ------------------------------------------------------------- shared state
 
 struct SeqState {        // per sequence, identical in every CTA
@@ -247,16 +259,22 @@ struct Smem {
   SeqState seq[kMaxB];
   int nseg;
   int seg_b[kMaxB], seg_lp0[kMaxB], seg_t0[kMaxB], seg_ntok[kMaxB], seg_pend[kMaxB];
-  int p0, p1, ppc, tok_stride, hpw, nwaves, tok_smem, spill_ok, ptot;
-  int stage_tok[8][16];    // per ring stage: CTA-local first token of each page (-1: unused)
-  int stage_nv[8][16];     // valid slots of each page
-  int stage_b[8][16];      // its sequence
-  int stage_done[8];       // warps finished with the current use of each ring slot
-  int slot_last[8];        // the last ring use issued into each slot (-1: none)
+  int p0, p1, ppc, tok_stride, hpw, nwaves, spill_ok, ptot, region;
+  int stage_tok[kMaxSlots][16];  // per ring slot: CTA-local first token of each page (-1: unused)
+  int stage_nv[kMaxSlots][16];   // valid slots of each page
+  int stage_b[kMaxSlots][16];    // its sequence
+  int stage_done[kMaxSlots];     // warps finished with the current use of each ring slot
+  int slot_last[kMaxSlots];      // the last ring use issued into each slot (-1: none)
+  int ct_lo[kMaxB], ct_hi[kMaxB];  // hit: the cached part inside [s_end, ls)
+  int pre_c[kMaxB], pre_a[kMaxB];  // selected tokens of the CTAs before mine (candidates, all)
+  int tot_c[kMaxB], tot_a[kMaxB];  // and of all CTAs
+  int tie_base[kMaxB];             // exact ties in the CTAs before mine, per segment
+  int my_pages[kMaxPagesCta];  // physical page ids of my range (first kMaxPagesCta pages)
   int timed_out;
   int wsum[33];
   int flag;
   float red_f[3][32];
+  int red_i[2][32];
   int toks[kMaxRound];
   int tval[kMaxRound];
   int my_seg_of[kMaxB];    // segment of sequence b in this CTA, or -1
@@ -264,32 +282,38 @@ struct Smem {
 
 // --------------------------------------------------------------- the kernel
 
+// CTA 0 records the time it reaches phase boundary i (0..31).
+#define TS_MARK(i)                                                     \
+  do {                                                                 \
+    if (c == 0 && tid == 0 && a.phase_ns) a.phase_ns[i] = globaltimer_ns(); \
+  } while (0)
+
 template <typename KT, int D, int HKV, int G>
 __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_kernel(StepKArgs a) {
   using S = StepShape<KT, D, HKV, G>;
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ Smem sm;
-  __shared__ __align__(8) uint64_t full[S::NST];
+  __shared__ __align__(8) uint64_t full[kMaxSlots];
   __shared__ __align__(8) uint64_t abar;
 
-  unsigned char* ring = dsm;
-  float* ebuf = reinterpret_cast<float*>(dsm + S::RING_BYTES);
-  uint8_t* selflag = dsm + a.dyn_bytes - a.flag_cap;       // selection flags of my tokens
-  float* wts = reinterpret_cast<float*>(selflag);          // vote weights [segment][wave head] while scoring
+  const int nslot = a.nslot;
+  unsigned char* ring = dsm;                                               // nslot x STAGE_BYTES of K
+  uint8_t* selflag = dsm + a.dyn_bytes - a.flag_cap;                       // selection flags of my tokens
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, nCTA = gridDim.x;
   const int B = a.B, H = a.H;
 
+  TS_MARK(0);
   if (tid == 0) {
-    for (int s = 0; s < S::NST; ++s) {
+    for (int s = 0; s < nslot; ++s) {
       mbar_init(&full[s], 1);
       sm.stage_done[s] = 0;
       sm.slot_last[s] = -1;
     }
-    sm.timed_out = 0;
     mbar_init(&abar, 1);
     mbar_fence_init();
+    sm.timed_out = 0;
   }
 
   // ------------------------------------------------ setup: lengths, cache test, partition
@@ -311,6 +335,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     }
     st.hit = (!(a.phases & kPhCheck) && a.hit_in) ? (a.hit_in[b] != 0) : 0;
     sm.my_seg_of[b] = -1;
+    sm.ct_lo[b] = 0;
+    sm.ct_hi[b] = 0;
   }
   __syncthreads();
   if (a.phases & kPhCheck) {
@@ -321,6 +347,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       const float* x = a.q + (size_t)b * HD;
       const float* y = a.cq + (size_t)b * HD;
       float xy = 0.f, xx = 0.f, yy = 0.f;
+#pragma unroll 8
       for (int i = tid; i < HD; i += blockDim.x) {
         const float u = x[i], v = __ldcg(y + i);
         xy = fmaf(u, v, xy);
@@ -349,6 +376,30 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       }
       __syncthreads();
     }
+  }
+  // a hit reuses the cached indices inside [s_end, ls): their bounds in the ascending
+  // list, by counting the entries below s_end and below ls with every thread
+  if (a.ct) {
+    for (int b = 0; b < B; ++b) {
+      if (!sm.seq[b].hit) continue;
+      const int32_t* ctb = a.ct + (size_t)b * a.cap;
+      const int cnt = a.filled[b] ? min(a.ct_count[b], a.cap) : 0;
+      const int se = sm.seq[b].s_end, ls = sm.seq[b].ls;
+      int below_s = 0, below_l = 0;
+#pragma unroll 4
+      for (int j = tid; j < cnt; j += blockDim.x) {
+        const int v = __ldcg(ctb + j);
+        below_s += v < se;
+        below_l += v < ls;
+      }
+      below_s = warp_sum_i(below_s);
+      below_l = warp_sum_i(below_l);
+      if (lane == 0 && (below_s | below_l)) {
+        atomicAdd(&sm.ct_lo[b], below_s);
+        atomicAdd(&sm.ct_hi[b], below_l);
+      }
+    }
+    __syncthreads();
   }
   if (tid == 0) {
     int pg = 0;
@@ -399,22 +450,32 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       ++ns;
     }
     sm.nseg = ns;
-    // scan waves: the largest power-of-two divisor hpw of H_kv whose e-values fit
+    // scan waves: the most KV heads per wave (a power-of-two divisor of H_kv) whose
+    // logits stay within the L2 budget
     int hpw = HKV;
-    while (hpw > 1 && ((int64_t)hpw * G * sm.tok_stride > a.e_cap || hpw * G > kMaxWaveHeads)) hpw >>= 1;
+    while (hpw > 1 && ((int64_t)ptot * S::P * hpw * G * 4 > a.l2_budget || hpw * G > kMaxWaveHeads)) hpw >>= 1;
     sm.hpw = hpw;
     sm.nwaves = HKV / hpw;
-    sm.tok_smem = min(sm.tok_stride, a.e_cap / (hpw * G));
-    sm.spill_ok = (int64_t)nCTA * hpw * G * (sm.tok_stride - sm.tok_smem) <= a.spill_floats &&
-                  sm.tok_stride <= a.flag_cap;
+    // my logits [tok_stride][hpw*G] in scratch
+    sm.region = ppc * hpw * G * S::P;
+    sm.spill_ok = (int64_t)nCTA * sm.region <= a.spill_floats && sm.tok_stride <= a.flag_cap &&
+                  hpw * G <= kMaxWaveHeads;
     sm.flag = 0;
   }
   __syncthreads();
   if (!sm.spill_ok) {
     if (c == 0 && tid == 0) set_error(a.status, TS_ERR_SHAPE);
-    return;  // uniform across CTAs: same inputs, same decision, before any barrier
+    return;  // the same decision in every CTA, before any grid barrier
   }
   if (c == 0 && tid < B && (a.phases & kPhCheck) && a.hit_out) a.hit_out[tid] = (uint8_t)sm.seq[tid].hit;
+  // page ids of my range, read once (ring refills and attention gathers need no global load)
+  for (int i = tid; i < min(sm.p1 - sm.p0, kMaxPagesCta); i += blockDim.x) {
+    const int gp = sm.p0 + i;
+    int sg = 0;
+    while (sg + 1 < sm.nseg && gp >= sm.seg_pend[sg]) ++sg;
+    const int b = sm.seg_b[sg];
+    sm.my_pages[i] = a.page_table[(size_t)b * a.pt_stride + (gp - sm.seq[b].pg0)];
+  }
   if (a.phases & kPhSelect) {
     // zero the selection histograms (first touched after a barrier)
     const size_t nh = (size_t)3 * B * kBins;
@@ -424,13 +485,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     }
     if (c == 0 && tid < B) a.cand_n[tid] = 0u;
   }
-
-  const int tstride = sm.tok_stride;
-  const int tsm = sm.tok_smem;
-  auto eaddr = [&](int hl, int t) -> float* {
-    return t < tsm ? ebuf + (size_t)hl * tsm + t
-                   : a.spill + ((size_t)c * (sm.hpw * G) + hl) * (size_t)(tstride - tsm) + (t - tsm);
-  };
+  __syncthreads();
+  TS_MARK(1);
 
   // ========================================================================= SCORE
   if ((a.phases & kPhScore) && sm.ptot > 0) {   // nothing to scan when every sequence hits
@@ -439,11 +495,15 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     const int np = sm.p1 - sm.p0;
     const int nstages = (np + pps - 1) / pps;
     const int slab = hpw * S::P * S::ROW_BYTES;      // bytes of one page's heads of the wave
+    const int tstride = sm.tok_stride;
+    float* eb = a.spill + (size_t)c * sm.region;     // my logits, token-major [tstride][HW]
+    float2* wp = a.wpart + (size_t)c * B * S::NCW * G;  // [segment][warp][head of the warp] (max, sum exp)
+    const uint64_t pol = l2_evict_first_policy();
     int stage_seq = 0;                               // ring use counter across waves
-    // Issues ring use u = stage_seq + si (the pps pages si*pps.. of my range, the wave's
-    // heads of each) into slot u % NST: metadata first, then arrive.expect_tx, then the copies.
+    // Issues ring use u (pages si*pps.. of my range, the wave's heads of each) into slot
+    // u % nslot: metadata first, then arrive.expect_tx, then the copies.
     auto issue = [&](int u, int si, int g0) {
-      const int s = u % S::NST;
+      const int s = u % nslot;
       sm.slot_last[s] = u;
       uint32_t bytes = 0;
       int pages[16];
@@ -458,7 +518,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         while (seg + 1 < sm.nseg && gp >= sm.seg_pend[seg]) ++seg;
         const int b = sm.seg_b[seg];
         const int lp = gp - sm.seq[b].pg0;
-        const int page = a.page_table[(size_t)b * a.pt_stride + lp];
+        const int page = (gp - sm.p0 < kMaxPagesCta) ? sm.my_pages[gp - sm.p0]
+                                                      : a.page_table[(size_t)b * a.pt_stride + lp];
         sm.stage_tok[s][j] = (gp - sm.p0) * S::P;
         sm.stage_b[s][j] = b;
         if (page < 0 || (int64_t)page >= a.num_pages) {
@@ -472,21 +533,19 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       mbar_arrive_expect_tx(&full[s], bytes);
       for (int j = 0; j < pps; ++j) {
         if (pages[j] < 0) continue;
-        bulk_g2s(ring + (size_t)s * S::STAGE_BYTES + (size_t)j * slab,
-                 a.k_pool + ((size_t)pages[j] * HKV + g0) * S::P * S::ROW_BYTES, (uint32_t)slab, &full[s]);
+        bulk_g2s_hint(ring + (size_t)s * S::STAGE_BYTES + (size_t)j * slab,
+                      a.k_pool + ((size_t)pages[j] * HKV + g0) * S::P * S::ROW_BYTES, (uint32_t)slab, &full[s], pol);
       }
     };
     for (int wv = 0; wv < nwaves; ++wv) {
       const int g0 = wv * hpw;
-      // the ring is idle between waves: fill it
-      if (tid == 0)
-        for (int si = 0; si < min(S::NST, nstages); ++si) issue(stage_seq + si, si, g0);
-      __syncthreads();
+      if (tid == 0)  // the ring is idle between waves: fill it
+        for (int si = 0; si < min(nslot, nstages); ++si) issue(stage_seq + si, si, g0);
       {
         // ---- warp -> KV head g0 + gi, ROWS rows of that head in each stage
         const int wph = S::NCW / hpw;
         const int gi = warp / wph;
-        const int row0 = (warp % wph) * S::ROWS;     // rows of one page: ROWS divides P or P divides ROWS
+        const int row0 = (warp % wph) * S::ROWS;     // ROWS divides P or P divides ROWS
         const int lrow = lane / S::LPR, lin = lane % S::LPR;
         float qr[S::GP][S::DPL];
 #pragma unroll
@@ -495,10 +554,22 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           for (int e = 0; e < S::DPL; ++e) qr[j][e] = 0.f;
         int qb = -1;                                 // sequence whose queries sit in qr
         const bool writer = (lin & (S::LPR / S::GP - 1)) == 0;
+        const int mywhich = reduce_slot<S::GP, S::LPR>(lane);   // the head this lane's sums belong to
+        // (max, sum exp) of this warp's rows of each of my segments, this wave's heads
+        int cur_sg = -1;
+        float run_m = -INFINITY;
+        KahanF run_z;
+        for (int i = lane; i < sm.nseg * G; i += 32)
+          wp[((size_t)(i / G) * S::NCW + warp) * G + (i % G)] = make_float2(-INFINITY, 0.f);
+        __syncwarp();
+        auto flush = [&](int sg) {
+          if (sg >= 0 && lrow == 0 && writer && mywhich < G)
+            wp[((size_t)sg * S::NCW + warp) * G + mywhich] = make_float2(run_m, run_z.s - run_z.c);
+        };
         for (int si = 0; si < nstages; ++si) {
           const int u = stage_seq + si;
-          const int s = u % S::NST;
-          if (!mbar_wait(&full[s], (u / S::NST) & 1)) {
+          const int s = u % nslot;
+          if (!mbar_wait(&full[s], (u / nslot) & 1)) {
             set_error(a.status, TS_ERR_TIMEOUT);
             sm.timed_out = 1;
             break;
@@ -508,7 +579,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           for (int it = 0; it < S::ITERS; ++it) {
             const int r = row0 + it * S::RPW + lrow;   // row among this head's pps*16 rows
             const int j = r / S::P, slot = r % S::P;   // all lanes of a step share the page j
-            const int tloc = sm.stage_tok[s][j];
+            const int tl = sm.stage_tok[s][j];
+            if (tl < 0) continue;                    // past my range (uniform in the warp)
             const int nv = sm.stage_nv[s][j];
             const int bq = sm.stage_b[s][j];
             if (bq != qb) {                          // new sequence: its queries of this KV head
@@ -522,6 +594,13 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
                     qr[jj][cc * S::EPC + e] = (jj < G) ? qh[(lin + cc * S::LPR) * S::EPC + e] : 0.f;
               }
               qb = bq;
+            }
+            const int sg = sm.my_seg_of[bq];
+            if (sg != cur_sg) {                      // new segment: its running statistics
+              flush(cur_sg);
+              cur_sg = sg;
+              run_m = -INFINITY;
+              run_z = KahanF();
             }
             const KT* rp = st + ((size_t)(j * hpw + gi) * S::P + slot) * D;
             float acc0[S::GP], acc1[S::GP];
@@ -546,48 +625,67 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
             for (int jj = 0; jj < S::GP; ++jj) v[jj] = acc0[jj] + acc1[jj];
             int which;
             const float dot = transpose_reduce<S::GP, S::LPR>(v, lane, which);
-            if (writer && which < G && tloc >= 0)
-              *eaddr(gi * G + which, tloc + slot) = slot < nv ? dot * a.scale : -INFINITY;
+            const float x = slot < nv ? dot * a.scale : -INFINITY;
+            if (writer && which < G) eb[(size_t)(tl + slot) * HW + gi * G + which] = x;
+            // running max and compensated sum of exp over the rows of this step (lanes of equal `which`)
+            float mi = x;
+#pragma unroll
+            for (int d = S::LPR; d < 32; d <<= 1) mi = fmaxf(mi, __shfl_xor_sync(kFull, mi, d));
+            const float mn = fmaxf(run_m, mi);
+            float ex = mn > -INFINITY ? expf(x - mn) : 0.f;
+#pragma unroll
+            for (int d = S::LPR; d < 32; d <<= 1) ex += __shfl_xor_sync(kFull, ex, d);
+            if (mn > run_m && run_m > -INFINITY) {
+              const float f = expf(run_m - mn);
+              run_z.s *= f;
+              run_z.c *= f;
+            }
+            run_z.add(ex);
+            run_m = mn;
           }
+          // the last warp done with this use of the slot refills it
           __syncwarp();
           if (lane == 0) {
-            // the last warp done with this use of the slot refills it with use u + NST
             if (atomicAdd(&sm.stage_done[s], 1) == S::NCW - 1) {
               sm.stage_done[s] = 0;
-              if (si + S::NST < nstages) issue(u + S::NST, si + S::NST, g0);
+              if (si + nslot < nstages) issue(u + nslot, si + nslot, g0);
             }
           }
         }
+        flush(cur_sg);
       }
       stage_seq += nstages;
       __syncthreads();
-      if (sm.timed_out && tid == 0) {
-        // copies issued but never consumed must land before the ring is reused
-        for (int ss = 0; ss < S::NST; ++ss)
-          if (sm.slot_last[ss] >= 0) mbar_wait(&full[ss], (sm.slot_last[ss] / S::NST) & 1);
-      }
-      __syncthreads();
-
-      // ---- per (segment, wave head): max, exp in place, compensated sum -> partials
-      for (int item = warp; item < sm.nseg * HW; item += S::NW) {
-        const int sg = item / HW, hl = item % HW;
-        const int t0 = sm.seg_t0[sg], nt = sm.seg_ntok[sg];
-        float m = -INFINITY;
-        for (int t = lane; t < nt; t += 32) m = fmaxf(m, *eaddr(hl, t0 + t));
-        m = warp_max(m);
-        KahanF z;
-        for (int t = lane; t < nt; t += 32) {
-          float* p = eaddr(hl, t0 + t);
-          const float e = (m > -INFINITY) ? expf(*p - m) : 0.f;
-          *p = e;
-          z.add(e);
+      if (sm.timed_out) {
+        if (tid == 0) {
+          // copies issued but never consumed land before the CTA leaves
+          for (int ss = 0; ss < nslot; ++ss)
+            if (sm.slot_last[ss] >= 0) mbar_wait(&full[ss], (sm.slot_last[ss] / nslot) & 1);
+          atomicExch(&a.gsync->abort, 1u);   // the others leave at their next barrier
         }
-        const double zs = warp_sum_f64((double)z.s - (double)z.c);
-        if (lane == 0) a.partials[((size_t)sm.seg_b[sg] * nCTA + c) * H + g0 * G + hl] = make_float2(m, (float)zs);
+        return;
       }
+      TS_MARK(2 + 3 * min(wv, 5));
+
+      // ---- per (segment, wave head): combine the warps' (max, sum exp) -> partials
+      {
+        const int wph = S::NCW / hpw;
+        for (int item = warp; item < sm.nseg * HW; item += S::NW) {
+          const int sg = item / HW, hl = item % HW;
+          const int gi = hl / G, w = hl % G;
+          float2 mz = make_float2(-INFINITY, 0.f);
+          if (lane < wph) mz = wp[((size_t)sg * S::NCW + gi * wph + lane) * G + w];
+          const float m = warp_max(mz.x);
+          const double z = warp_sum_f64((m > -INFINITY && mz.y > 0.f) ? (double)mz.y * (double)expf(mz.x - m) : 0.0);
+          if (lane == 0) a.partials[((size_t)sm.seg_b[sg] * nCTA + c) * H + g0 * G + hl] = make_float2(m, (float)z);
+        }
+      }
+      TS_MARK(3 + 3 * min(wv, 5));
       if (!grid_sync(a.gsync, a.status)) return;
+      TS_MARK(4 + 3 * min(wv, 5));
 
       // ---- each head's normaliser over the CTAs of the sequence, then my votes
+      float2* wz = reinterpret_cast<float2*>(ring);  // [segment][kMaxWaveHeads]: (max, 1 / sum)
       for (int item = warp; item < sm.nseg * HW; item += S::NW) {
         const int sg = item / HW, hl = item % HW;
         const SeqState& st = sm.seq[sm.seg_b[sg]];
@@ -596,23 +694,35 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         for (int cc = st.first_cta + lane; cc <= st.last_cta; cc += 32) M = fmaxf(M, __ldcg(pp + (size_t)cc * H).x);
         M = warp_max(M);
         KahanF kz;
-        for (int cc = st.first_cta + lane; cc <= st.last_cta; cc += 32) {
-          const float2 mz = __ldcg(pp + (size_t)cc * H);
-          if (mz.y > 0.f) kz.add(mz.y * expf(mz.x - M));
-        }
+        if (M > -INFINITY)
+          for (int cc = st.first_cta + lane; cc <= st.last_cta; cc += 32) {
+            const float2 mz = __ldcg(pp + (size_t)cc * H);
+            if (mz.y > 0.f) kz.add(mz.y * expf(mz.x - M));
+          }
         const double z = warp_sum_f64((double)kz.s - (double)kz.c);
-        if (lane == 0) {
-          const float mine = __ldcg(pp + (size_t)c * H).x;
-          wts[sg * kMaxWaveHeads + hl] = (mine > -INFINITY && z > 0.0) ? (float)((double)expf(mine - M) / z) : 0.f;
-        }
+        if (lane == 0)
+          wz[sg * kMaxWaveHeads + hl] = (M > -INFINITY && z > 0.0) ? make_float2(M, (float)(1.0 / z))
+                                                                   : make_float2(INFINITY, 0.f);
       }
       __syncthreads();
       for (int sg = 0; sg < sm.nseg; ++sg) {
         const int b = sm.seg_b[sg], t0 = sm.seg_t0[sg], nt = sm.seg_ntok[sg];
         float* vb = a.vote + (size_t)b * a.vote_stride + (size_t)sm.seg_lp0[sg] * S::P;
+        const float2* w = wz + sg * kMaxWaveHeads;
         for (int t = tid; t < nt; t += blockDim.x) {
+          const float* row = eb + (size_t)(t0 + t) * HW;
           KahanF acc;
-          for (int hl = 0; hl < HW; ++hl) acc.add(*eaddr(hl, t0 + t) * wts[sg * kMaxWaveHeads + hl]);
+          if ((HW & 3) == 0) {
+            for (int h4 = 0; h4 < HW; h4 += 4) {
+              const float4 x = *reinterpret_cast<const float4*>(row + h4);
+              acc.add(expf(x.x - w[h4].x) * w[h4].y);
+              acc.add(expf(x.y - w[h4 + 1].x) * w[h4 + 1].y);
+              acc.add(expf(x.z - w[h4 + 2].x) * w[h4 + 2].y);
+              acc.add(expf(x.w - w[h4 + 3].x) * w[h4 + 3].y);
+            }
+          } else {
+            for (int hl = 0; hl < HW; ++hl) acc.add(expf(row[hl] - w[hl].x) * w[hl].y);
+          }
           const float v = acc.s - acc.c;
           vb[t] = (wv == 0) ? v : vb[t] + v;
         }
@@ -621,14 +731,21 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     }
   }
 
+  TS_MARK(20);
   // ======================================================================== SELECT
   if (a.phases & kPhSelect) {
     if (!(a.phases & kPhScore) && sm.ptot > 0) {
       if (!grid_sync(a.gsync, a.status)) return;   // the histograms are zero everywhere
     }
+    // shared memory while selecting: this CTA's histogram (counts, masses), the gathered
+    // candidates, then the global histograms of a batch of sequences
     unsigned* sh = reinterpret_cast<unsigned*>(ring);
     unsigned long long* smh = reinterpret_cast<unsigned long long*>(ring + kBins * sizeof(unsigned));
     unsigned long long* scand = reinterpret_cast<unsigned long long*>(ring + kBins * 12);
+    unsigned char* bat = ring + kSelScratch;
+    const bool topp = a.mode == TS_SELECT_TOPP;
+    const int per_seq = kBins * (topp ? 12 : 4);
+    const int room = max(1, (a.dyn_bytes - a.flag_cap - kSelScratch) / per_seq);
     if (tid == 0) {
       for (int b = 0; b < B; ++b) {
         SeqState& st = sm.seq[b];
@@ -670,7 +787,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         if (st.done) continue;
         for (int i = tid; i < nbins; i += blockDim.x) {
           sh[i] = 0u;
-          if (a.mode == TS_SELECT_TOPP) smh[i] = 0ull;
+          if (topp) smh[i] = 0ull;
         }
         __syncthreads();
         const int tl0 = sm.seg_lp0[sg] * S::P;
@@ -682,93 +799,131 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           if ((key & st.mask) == st.prefix) {
             const int bin = (key >> shift) & (nbins - 1);
             atomicAdd(&sh[bin], 1u);
-            if (a.mode == TS_SELECT_TOPP) atomicAdd(&smh[bin], to_fx(v));
+            if (topp) atomicAdd(&smh[bin], to_fx(v));
           }
         }
         __syncthreads();
         for (int i = tid; i < nbins; i += blockDim.x) {
           if (sh[i]) {
             atomicAdd(&gh[(size_t)b * kBins + i], sh[i]);
-            if (a.mode == TS_SELECT_TOPP) atomicAdd(&gm[(size_t)b * kBins + i], smh[i]);
+            if (topp) atomicAdd(&gm[(size_t)b * kBins + i], smh[i]);
           }
         }
         __syncthreads();
       }
       if (!grid_sync(a.gsync, a.status)) return;
-      // every CTA: the crossing bin of every unresolved sequence, one warp each
-      for (int b = warp; b < B; b += S::NW) {
-        SeqState& st = sm.seq[b];
-        if (st.done) continue;
-        const int per = nbins / 32;
-        unsigned cnt = 0;
-        unsigned long long ms = 0;
-        for (int j = 0; j < per; ++j) {
-          const int bin = nbins - 1 - (lane * per + j);
-          cnt += __ldcg(&gh[(size_t)b * kBins + bin]);
-          if (a.mode == TS_SELECT_TOPP) ms += __ldcg(&gm[(size_t)b * kBins + bin]);
+      // every CTA finds the crossing bin of every unresolved sequence: the histograms of
+      // a batch of sequences are read into shared memory at once, then one warp each scans
+      for (int b0 = 0; b0 < B; b0 += room) {
+        const int nb = min(room, B - b0);
+        unsigned* bc = reinterpret_cast<unsigned*>(bat);                                  // [nb][nbins]
+        unsigned long long* bm = reinterpret_cast<unsigned long long*>(bat + (size_t)room * kBins * 4);
+#pragma unroll 4
+        for (int i = tid; i < nb * nbins; i += blockDim.x) {
+          const int bi = i / nbins, bin = i % nbins;
+          if (sm.seq[b0 + bi].done) continue;
+          bc[i] = __ldcg(&gh[(size_t)(b0 + bi) * kBins + bin]);
+          if (topp) bm[i] = __ldcg(&gm[(size_t)(b0 + bi) * kBins + bin]);
         }
-        unsigned ic = cnt;
-        unsigned long long im = ms;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-          const unsigned oc = __shfl_up_sync(kFull, ic, d);
-          const unsigned long long om = __shfl_up_sync(kFull, im, d);
-          if (lane >= d) {
-            ic += oc;
-            im += om;
-          }
-        }
-        const unsigned ec = ic - cnt;
-        const unsigned long long em = im - ms;
-        const unsigned need_c = (unsigned)st.k_rem;
-        const unsigned long long need_m = st.mass_rem;
-        const bool crosses = (a.mode == TS_SELECT_TOPK) ? (ec < need_c && ic >= need_c) : (em < need_m && im >= need_m);
-        const unsigned ballot = __ballot_sync(kFull, crosses);
-        if (ballot == 0u) {
-          if (lane == 0) {  // top-p whose fixed-point total falls short: the whole domain
-            st.all = 1;
-            st.done = 1;
-          }
-        } else if (lane == __ffs(ballot) - 1) {
-          unsigned cb = ec;
-          unsigned long long mb = em;
-          for (int j = 0; j < per; ++j) {
+        __syncthreads();
+        for (int bi = warp; bi < nb; bi += S::NW) {
+          SeqState& st = sm.seq[b0 + bi];
+          if (st.done) continue;
+          const unsigned* hc_ = bc + (size_t)bi * nbins;
+          const unsigned long long* hm_ = bm + (size_t)bi * nbins;
+          // lane L sums the bins nbins-1-(L*per + j), j < per (descending vote); the start is
+          // rotated by the lane so that the lanes hit different banks
+          const int per = nbins / 32;
+          unsigned cnt = 0;
+          unsigned long long ms = 0;
+          for (int jj = 0; jj < per; ++jj) {
+            const int j = (jj + lane) & (per - 1);
             const int bin = nbins - 1 - (lane * per + j);
-            const unsigned hc = __ldcg(&gh[(size_t)b * kBins + bin]);
-            const unsigned long long hm = (a.mode == TS_SELECT_TOPP) ? __ldcg(&gm[(size_t)b * kBins + bin]) : 0ull;
-            const bool here = (a.mode == TS_SELECT_TOPK) ? (cb + hc >= need_c) : (mb + hm >= need_m);
-            if (here) {
-              st.prefix |= (uint32_t)bin << shift;
-              st.mask |= (uint32_t)(nbins - 1) << shift;
-              st.n_gt += (int)cb;
-              if (a.mode == TS_SELECT_TOPK)
-                st.k_rem = (int)(need_c - cb);
-              else
-                st.mass_rem = need_m - mb;
-              if (hc <= (unsigned)kCandCap) {
-                st.cand = 1;
-                st.done = 1;
-              } else if (level == 2) {
-                st.tie_mode = 1;
-                st.done = 1;
-                if (a.mode == TS_SELECT_TOPK) {
-                  st.ties = st.k_rem;
-                } else {
-                  const unsigned long long tfx = to_fx(__uint_as_float(st.prefix));
-                  const unsigned long long t = tfx ? (st.mass_rem + tfx - 1) / tfx : (unsigned long long)hc;
-                  st.ties = (int)(t < hc ? t : hc);
+            cnt += hc_[bin];
+            if (topp) ms += hm_[bin];
+          }
+          unsigned ic = cnt;
+          unsigned long long im = ms;
+#pragma unroll
+          for (int d = 1; d < 32; d <<= 1) {
+            const unsigned oc = __shfl_up_sync(kFull, ic, d);
+            const unsigned long long om = __shfl_up_sync(kFull, im, d);
+            if (lane >= d) {
+              ic += oc;
+              im += om;
+            }
+          }
+          const unsigned need_c = (unsigned)st.k_rem;
+          const unsigned long long need_m = st.mass_rem;
+          const bool crosses = topp ? (im - ms < need_m && im >= need_m) : (ic - cnt < need_c && ic >= need_c);
+          const unsigned ballot = __ballot_sync(kFull, crosses);
+          if (ballot == 0u) {
+            if (lane == 0) {  // top-p whose fixed-point total falls short: the whole domain
+              st.all = 1;
+              st.done = 1;
+            }
+            continue;
+          }
+          const int L = __ffs(ballot) - 1;
+          unsigned cb = __shfl_sync(kFull, ic - cnt, L);
+          unsigned long long mb = __shfl_sync(kFull, im - ms, L);
+          // the crossing lane's bins, 32 at a time, by the whole warp
+          for (int j0 = 0; j0 < per; j0 += 32) {
+            const int j = j0 + lane;
+            const int bin = nbins - 1 - (L * per + j);
+            const bool in = j < per;
+            const unsigned hc = in ? hc_[bin] : 0u;
+            const unsigned long long hm = (in && topp) ? hm_[bin] : 0ull;
+            unsigned xc = hc;
+            unsigned long long xm = hm;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+              const unsigned oc = __shfl_up_sync(kFull, xc, d);
+              const unsigned long long om = __shfl_up_sync(kFull, xm, d);
+              if (lane >= d) {
+                xc += oc;
+                xm += om;
+              }
+            }
+            const bool here = in && (topp ? (mb + xm >= need_m) : (cb + xc >= need_c));
+            const unsigned hb = __ballot_sync(kFull, here);
+            if (hb) {
+              if (lane == __ffs(hb) - 1) {
+                const unsigned before_c = cb + xc - hc;
+                const unsigned long long before_m = mb + xm - hm;
+                st.prefix |= (uint32_t)bin << shift;
+                st.mask |= (uint32_t)(nbins - 1) << shift;
+                st.n_gt += (int)before_c;
+                if (topp)
+                  st.mass_rem = need_m - before_m;
+                else
+                  st.k_rem = (int)(need_c - before_c);
+                if (hc <= (unsigned)kCandCap) {
+                  st.cand = 1;
+                  st.done = 1;
+                } else if (level == 2) {
+                  st.tie_mode = 1;
+                  st.done = 1;
+                  if (!topp) {
+                    st.ties = st.k_rem;
+                  } else {
+                    const unsigned long long tfx = to_fx(__uint_as_float(st.prefix));
+                    const unsigned long long t = tfx ? (st.mass_rem + tfx - 1) / tfx : (unsigned long long)hc;
+                    st.ties = (int)(t < hc ? t : hc);
+                  }
                 }
               }
               break;
             }
-            cb += hc;
-            mb += hm;
+            cb += __shfl_sync(kFull, xc, 31);
+            mb += __shfl_sync(kFull, xm, 31);
           }
         }
+        __syncthreads();
       }
-      __syncthreads();
     }
 
+    TS_MARK(21);
     // ---- gather the crossing-bin tokens (candidates); per-CTA exact-tie counts
     int need_cand = 0, need_tie = 0;
     for (int b = 0; b < B; ++b) {
@@ -814,16 +969,28 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     if (need_cand || need_tie) {
       if (!grid_sync(a.gsync, a.status)) return;
     }
+    if (need_tie) {
+      // exact ties before mine, per segment, one warp each
+      for (int sg = warp; sg < sm.nseg; sg += S::NW) {
+        const int b = sm.seg_b[sg];
+        const SeqState& st = sm.seq[b];
+        int s = 0;
+        if (st.tie_mode)
+          for (int cc = st.first_cta + lane; cc < c; cc += 32) s += __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 3 + 2]);
+        s = warp_sum_i(s);
+        if (lane == 0) sm.tie_base[sg] = s;
+      }
+      __syncthreads();
+    }
 
+    TS_MARK(22);
     // ---- the selection flag of each of my tokens, and the counts for output positions
     for (int sg = 0; sg < sm.nseg; ++sg) {
       const int b = sm.seg_b[sg];
       const SeqState& st = sm.seq[b];
       const int tl0 = sm.seg_lp0[sg] * S::P, t0l = sm.seg_t0[sg], nt = sm.seg_ntok[sg];
       const float* vb = a.vote + (size_t)b * a.vote_stride;
-      int tie_base = 0;
-      if (st.tie_mode)
-        for (int cc = st.first_cta; cc < c; ++cc) tie_base += __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 3 + 2]);
+      int tie_base = st.tie_mode ? sm.tie_base[sg] : 0;
       const int m_cand = st.cand ? (int)min(__ldcg(&a.cand_n[b]), (unsigned)kCandCap) : 0;
       for (int j = tid; j < m_cand; j += blockDim.x) scand[j] = __ldcg(&a.cands[(size_t)b * kCandCap + j]);
       __syncthreads();
@@ -845,31 +1012,24 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
             else if (st.tie_mode) tie = true;
           }
         }
-        int tie_tot;
-        const int tr = block_scan(tie ? 1 : 0, sm.wsum, tie_tot);
-        if (tie) f = (tie_base + tr) < st.ties;
-        tie_base += tie_tot;
+        if (st.tie_mode) {
+          int tie_tot;
+          const int tr = block_scan(tie ? 1 : 0, sm.wsum, tie_tot);
+          if (tie) f = (tie_base + tr) < st.ties;
+          tie_base += tie_tot;
+        }
         // candidates: one warp ranks one candidate against the gathered list
         if (st.cand) {
           int nr;
           const int rr = block_scan(rank_me ? 1 : 0, sm.wsum, nr);
-          if (rank_me && rr < kMaxRound) {
-            sm.toks[rr] = i;
-            sm.tval[rr] = (int)key;
-          }
-          __syncthreads();
           for (int r0 = 0; r0 < nr; r0 += kMaxRound) {
             const int nrr = min(kMaxRound, nr - r0);
-            if (r0 > 0) {
-              // more than kMaxRound candidates in this chunk: refill the list
-              const int rrr = rr - r0;
-              __syncthreads();
-              if (rank_me && rrr >= 0 && rrr < kMaxRound) {
-                sm.toks[rrr] = i;
-                sm.tval[rrr] = (int)key;
-              }
-              __syncthreads();
+            const int rrr = rr - r0;
+            if (rank_me && rrr >= 0 && rrr < kMaxRound) {
+              sm.toks[rrr] = i;
+              sm.tval[rrr] = (int)key;
             }
+            __syncthreads();
             for (int q = warp; q < nrr; q += S::NW) {
               const int ii = sm.toks[q];
               const uint32_t kk = (uint32_t)sm.tval[q];
@@ -880,7 +1040,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
                 const unsigned long long y = scand[j];
                 if (y > me) {
                   ++above;
-                  if (a.mode == TS_SELECT_TOPP) cum += to_fx(__uint_as_float((uint32_t)(y >> 32)));
+                  if (topp) cum += to_fx(__uint_as_float((uint32_t)(y >> 32)));
                 }
               }
 #pragma unroll
@@ -889,7 +1049,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
                 cum += __shfl_xor_sync(kFull, cum, d);
               }
               if (lane == 0) {
-                const int sel = (a.mode == TS_SELECT_TOPK) ? (above < (unsigned)st.k_rem) : (cum < st.mass_rem);
+                const int sel = topp ? (cum < st.mass_rem) : (above < (unsigned)st.k_rem);
                 selflag[t0l + ii] = (uint8_t)sel;
               }
             }
@@ -902,21 +1062,33 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         n_sel_cand += f && t >= st.s_end && t < st.ls;
         __syncthreads();
       }
-      int tot_c, tot_a;
-      block_scan(n_sel_cand, sm.wsum, tot_c);
-      block_scan(n_sel_all, sm.wsum, tot_a);
-      if (tid == 0) {
-        a.cta_cnt[((size_t)b * nCTA + c) * 3 + 0] = tot_c;
-        a.cta_cnt[((size_t)b * nCTA + c) * 3 + 1] = tot_a;
+      n_sel_cand = warp_sum_i(n_sel_cand);
+      n_sel_all = warp_sum_i(n_sel_all);
+      if (lane == 0) {
+        sm.red_i[0][warp] = n_sel_cand;
+        sm.red_i[1][warp] = n_sel_all;
       }
+      __syncthreads();
+      if (tid == 0) {
+        int tc = 0, ta = 0;
+        for (int w = 0; w < S::NW; ++w) {
+          tc += sm.red_i[0][w];
+          ta += sm.red_i[1][w];
+        }
+        a.cta_cnt[((size_t)b * nCTA + c) * 3 + 0] = tc;
+        a.cta_cnt[((size_t)b * nCTA + c) * 3 + 1] = ta;
+      }
+      __syncthreads();
     }
-    __syncthreads();
   }
 
+  TS_MARK(23);
   // ======================================================================== ATTEND
   // My tokens per sequence: a round-robin share of the fixed ones (sinks and
   // window, the cached part of a hit, or the caller's index list) and my own
   // selected candidates; gathered by bulk copy; one partial per CTA and head.
+  float* ao = a.apart;                                                        // [B][nCTA][H][D]
+  float2* aml = reinterpret_cast<float2*>(a.apart + (size_t)B * nCTA * H * D); // [B][nCTA][H] (max, sum)
   if (a.phases & kPhAttend) {
     const bool given = !(a.phases & kPhSelect);
     const int stage_bytes = a.dyn_bytes - a.flag_cap;
@@ -939,9 +1111,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         nfix = st.s_end + (st.n - st.ls);
         if (st.hit && a.ct) {
           ctb = a.ct + (size_t)b * a.cap;
-          const int cnt = a.filled[b] ? a.ct_count[b] : 0;
-          ct_lo = lower_bound_i(ctb, cnt, st.s_end);
-          ct_hi = lower_bound_i(ctb, cnt, st.ls);
+          ct_lo = sm.ct_lo[b];
+          ct_hi = sm.ct_hi[b];
           nfix += ct_hi - ct_lo;
         }
       }
@@ -949,6 +1120,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       const int sgi = sm.my_seg_of[b];
       const bool own = !given && !st.hit && sgi >= 0;
       const int own_n = own ? sm.seg_ntok[sgi] : 0;
+      const int own_lp0 = own ? sm.seg_lp0[sgi] : 0, own_t0 = own ? sm.seg_t0[sgi] : 0;
       const int nfix_mine = c < nfix ? (nfix - c + nCTA - 1) / nCTA : 0;
       float qr[S::GP][S::AEPC];
       float m_[G], l_[G], o_[G][S::AEPC];
@@ -976,21 +1148,29 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           int t;
           if (given) t = gib[f];
           else if (f < st.s_end) t = f;
-          else if (f < st.s_end + nmid) t = ctb[ct_lo + (f - st.s_end)];
+          else if (f < st.s_end + nmid) t = __ldcg(ctb + ct_lo + (f - st.s_end));
           else t = st.ls + (f - st.s_end - nmid);
+          int page = -1;
+          if (t >= 0 && t < a.max_tokens) page = a.page_table[(size_t)b * a.pt_stride + t / S::P];
           sm.toks[i] = t;
+          sm.tval[i] = page;
         }
         fdone += nf;
         cnt = nf;
         while (own && opos < own_n && cnt < around) {
           // one chunk of blockDim own tokens; take as many selected ones as fit
           const int i = opos + tid;
-          const int t = sm.seg_lp0[sgi] * S::P + i;
-          const bool take = i < own_n && selflag[sm.seg_t0[sgi] + i] && t >= st.s_end && t < st.ls;
+          const int t = own_lp0 * S::P + i;
+          const bool take = i < own_n && selflag[own_t0 + i] && t >= st.s_end && t < st.ls;
           int tot;
           const int r = block_scan(take ? 1 : 0, sm.wsum, tot);
           const int room = around - cnt;
-          if (take && r < room) sm.toks[cnt + r] = t;
+          if (take && r < room) {
+            const int lpg = (own_t0 + i) / S::P;   // my page of the token
+            sm.toks[cnt + r] = t;
+            sm.tval[cnt + r] = lpg < kMaxPagesCta ? sm.my_pages[lpg]
+                                                  : a.page_table[(size_t)b * a.pt_stride + t / S::P];
+          }
           if (tot <= room) {
             opos += blockDim.x;
             cnt += tot;
@@ -1006,22 +1186,16 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         if (cnt == 0) break;                          // uniform: same counters in every thread
         // ---- gather K and V rows of every KV head
         if (tid == 0) mbar_arrive_expect_tx(&abar, (uint32_t)(cnt * S::TOKEN_BYTES));
-        for (int i = tid; i < cnt; i += blockDim.x) {
-          const int t = sm.toks[i];
-          int page = -1;
-          if (t >= 0 && t < a.max_tokens) page = a.page_table[(size_t)b * a.pt_stride + t / S::P];
-          const bool valid = page >= 0 && (int64_t)page < a.num_pages;
-          if (!valid) set_error(a.status, TS_ERR_PAGE_OOB);
-          sm.tval[i] = valid;
-        }
         __syncthreads();
         for (int i = tid; i < 2 * cnt * HKV; i += blockDim.x) {
           const int ti = i / (2 * HKV), rem = i % (2 * HKV), g = rem >> 1, isv = rem & 1;
           const int t = sm.toks[ti];
+          const int page = sm.tval[ti];
           size_t off = 0;
-          if (sm.tval[ti]) {
-            const int page = a.page_table[(size_t)b * a.pt_stride + t / S::P];
+          if (page >= 0 && (int64_t)page < a.num_pages) {
             off = (((size_t)page * HKV + g) * S::P + (t % S::P)) * S::ROW_BYTES;
+          } else if (i % (2 * HKV) == 0) {
+            set_error(a.status, TS_ERR_PAGE_OOB);
           }
           bulk_g2s((isv ? Vs : Ks) + ((size_t)ti * HKV + g) * D, (isv ? a.v_pool : a.k_pool) + off,
                    S::ROW_BYTES, &abar);
@@ -1077,7 +1251,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           }
           int which;
           const float red = transpose_reduce<S::GP, S::ALPT>(acc, lane, which);
-          const bool live = act && sm.tval[jj] != 0;
+          const bool live = act && sm.tval[jj] >= 0 && (int64_t)sm.tval[jj] < a.num_pages;
 #pragma unroll
           for (int h = 0; h < G; ++h) {
             const float dot = __shfl_sync(kFull, red, (lane & ~(S::ALPT - 1)) + h * (S::ALPT / S::GP));
@@ -1115,7 +1289,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         }
       }
       __syncthreads();
-      float* pb = a.apart + ((size_t)b * nCTA + c) * H * (D + 2);
+      float* pb = ao + ((size_t)b * nCTA + c) * H * D;
+      float2* pml = aml + ((size_t)b * nCTA + c) * H;
       for (int i = tid; i < HKV * G * D; i += blockDim.x) {
         const int hg = i / (G * D), rem = i % (G * D), h = rem / D, d = rem % D;
         float M = -INFINITY;
@@ -1132,53 +1307,124 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
             }
         }
         const int qh = hg * G + h;
-        pb[(size_t)qh * (D + 2) + d] = num;
-        if (d == 0) {
-          pb[(size_t)qh * (D + 2) + D] = M;
-          pb[(size_t)qh * (D + 2) + D + 1] = den;
-        }
+        pb[(size_t)qh * D + d] = num;
+        if (d == 0) pml[qh] = make_float2(M, den);
       }
       __syncthreads();
     }
   }
 
+  TS_MARK(24);
   // ============================================== outputs, after one more barrier
   if (!(a.phases & (kPhSelect | kPhAttend))) return;
   if (!grid_sync(a.gsync, a.status)) return;
+  TS_MARK(25);
   if (a.phases & kPhAttend) {
-    // merge the CTA partials: item = (sequence, query head, 32-dim slice)
-    const int nslice = D / 32;
-    for (int item = c * S::NW + warp; item < B * H * nslice; item += nCTA * S::NW) {
-      const int b = item / (H * nslice), rem = item % (H * nslice), h = rem / nslice, sl = rem % nslice;
-      const float* pp = a.apart + (size_t)b * nCTA * H * (D + 2) + (size_t)h * (D + 2);
-      float M = -INFINITY;
-      for (int cc = lane; cc < nCTA; cc += 32) M = fmaxf(M, __ldcg(pp + (size_t)cc * H * (D + 2) + D));
-      M = warp_max(M);
-      float num = 0.f, den = 0.f;
-      if (M > -INFINITY) {
-        for (int cc = 0; cc < nCTA; ++cc) {
-          const float* pc = pp + (size_t)cc * H * (D + 2);
-          const float mc = __ldcg(pc + D);
-          if (mc == -INFINITY) continue;
-          const float wgt = expf(mc - M);
-          num = fmaf(wgt, __ldcg(pc + sl * 32 + lane), num);
-          den = fmaf(wgt, __ldcg(pc + D + 1), den);
-        }
+    // merge the CTA partials of one (sequence, query head) per CTA pass: weights from
+    // the (max, sum) pairs, then the weighted rows with 16-byte loads, reduced in a
+    // fixed order
+    float* pw = reinterpret_cast<float*>(dsm);     // [nCTA] weights
+    float* pm = pw + nCTA;                         // [nCTA] maxima
+    float* pl = pm + nCTA;                         // [nCTA] sums
+    float4* racc = reinterpret_cast<float4*>(dsm + (((size_t)3 * nCTA * 4 + 15) & ~(size_t)15));  // [ngrp][D/4]
+    constexpr int ncol = D / 4;
+    const int ngrp = blockDim.x / ncol;
+    const int col = tid % ncol, grp = tid / ncol;
+    for (int item = c; item < B * H; item += nCTA) {
+      const int b = item / H, h = item % H;
+      const float2* mlp = aml + (size_t)b * nCTA * H + h;
+      for (int cc = tid; cc < nCTA; cc += blockDim.x) {
+        const float2 v = __ldcg(mlp + (size_t)cc * H);
+        pm[cc] = v.x;
+        pl[cc] = v.y;
       }
-      a.out[((size_t)b * H + h) * D + sl * 32 + lane] = den > 0.f ? num / den : 0.f;
-      if (a.lse && sl == 0 && lane == 0) a.lse[(size_t)b * H + h] = den > 0.f ? M + logf(den) : -INFINITY;
+      __syncthreads();
+      float M = -INFINITY;
+      for (int cc = lane; cc < nCTA; cc += 32) M = fmaxf(M, pm[cc]);
+      M = warp_max(M);                                       // every warp computes the same M
+      for (int cc = tid; cc < nCTA; cc += blockDim.x)
+        pw[cc] = (M > -INFINITY && pm[cc] > -INFINITY) ? expf(pm[cc] - M) : 0.f;
+      __syncthreads();
+      if (warp == 0) {
+        float den = 0.f;
+        for (int cc = lane; cc < nCTA; cc += 32) den = fmaf(pw[cc], pl[cc], den);
+        den = warp_sum(den);
+        if (lane == 0) sm.red_f[0][0] = den;
+      }
+      const float4* ob = reinterpret_cast<const float4*>(ao + ((size_t)b * nCTA * H + h) * D) + col;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (grp < ngrp) {
+        for (int cc = grp; cc < nCTA; cc += ngrp) {
+          const float w = pw[cc];
+          if (w != 0.f) {
+            const float4 v = __ldcg(ob + (size_t)cc * H * ncol);
+            acc.x = fmaf(w, v.x, acc.x);
+            acc.y = fmaf(w, v.y, acc.y);
+            acc.z = fmaf(w, v.z, acc.z);
+            acc.w = fmaf(w, v.w, acc.w);
+          }
+        }
+        racc[grp * ncol + col] = acc;
+      }
+      __syncthreads();
+      const float den = sm.red_f[0][0];
+      if (tid < ncol) {
+        float4 s = racc[tid];
+        for (int g = 1; g < ngrp; ++g) {
+          const float4 v = racc[g * ncol + tid];
+          s.x += v.x;
+          s.y += v.y;
+          s.z += v.z;
+          s.w += v.w;
+        }
+        const float inv = den > 0.f ? 1.f / den : 0.f;
+        float* o = a.out + ((size_t)b * H + h) * D + 4 * tid;   // the caller's buffer: 4-byte aligned only
+        o[0] = s.x * inv;
+        o[1] = s.y * inv;
+        o[2] = s.z * inv;
+        o[3] = s.w * inv;
+      }
+      if (a.lse && tid == 0) a.lse[(size_t)b * H + h] = den > 0.f ? M + logf(den) : -INFINITY;
+      __syncthreads();
     }
   }
+  TS_MARK(26);
   if (a.phases & kPhSelect) {
+    // counts of the CTAs before mine and of all CTAs, every sequence at once (warp per sequence)
+    for (int b = warp; b < B; b += S::NW) {
+      const SeqState& st = sm.seq[b];
+      int pc = 0, pa = 0, tc = 0, ta = 0;
+      if (!st.hit)
+        for (int cc = st.first_cta + lane; cc <= st.last_cta; cc += 32) {
+          const int xc = __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 3 + 0]);
+          const int xa = __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 3 + 1]);
+          if (cc < c) {
+            pc += xc;
+            pa += xa;
+          }
+          tc += xc;
+          ta += xa;
+        }
+      pc = warp_sum_i(pc);
+      pa = warp_sum_i(pa);
+      tc = warp_sum_i(tc);
+      ta = warp_sum_i(ta);
+      if (lane == 0) {
+        sm.pre_c[b] = pc;
+        sm.pre_a[b] = pa;
+        sm.tot_c[b] = tc;
+        sm.tot_a[b] = ta;
+      }
+    }
+    __syncthreads();
     // ascending index lists and Selection Cache entries
     for (int b = 0; b < B; ++b) {
       const SeqState& st = sm.seq[b];
       int32_t* ib = a.idx + (size_t)b * a.idx_stride;
       if (st.hit) {
         const int32_t* ctb = a.ct ? a.ct + (size_t)b * a.cap : nullptr;
-        const int cnt = (ctb && a.filled[b]) ? a.ct_count[b] : 0;
-        const int lo = ctb ? lower_bound_i(ctb, cnt, st.s_end) : 0;
-        const int mcount = ctb ? lower_bound_i(ctb, cnt, st.ls) - lo : 0;
+        const int lo = sm.ct_lo[b];
+        const int mcount = sm.ct_hi[b] - lo;
         const int total = st.s_end + mcount + (st.n - st.ls);
         if (total > a.idx_stride) {
           if (c == 0 && tid == 0) {
@@ -1191,24 +1437,15 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         for (int j = c * per + tid; j < min(total, (c + 1) * per); j += blockDim.x) {
           int v;
           if (j < st.s_end) v = j;
-          else if (j < st.s_end + mcount) v = ctb[lo + j - st.s_end];
+          else if (j < st.s_end + mcount) v = __ldcg(ctb + lo + j - st.s_end);
           else v = st.ls + (j - st.s_end - mcount);
           ib[j] = v;
         }
         if (c == 0 && tid == 0) a.count[b] = total;
         continue;
       }
-      int tot_c = 0, tot_a = 0, pre_c = 0, pre_a = 0;
-      for (int cc = st.first_cta; cc <= st.last_cta; ++cc) {
-        const int xc = __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 3 + 0]);
-        const int xa = __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 3 + 1]);
-        if (cc < c) {
-          pre_c += xc;
-          pre_a += xa;
-        }
-        tot_c += xc;
-        tot_a += xa;
-      }
+      const int tot_c = sm.tot_c[b], tot_a = sm.tot_a[b];
+      int pre_c = sm.pre_c[b], pre_a = sm.pre_a[b];
       const int total = st.s_end + tot_c + (st.n - st.ls);
       const bool fits = total <= a.idx_stride;
       const bool cfits = a.ct != nullptr && tot_a <= a.cap;
@@ -1251,6 +1488,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       }
     }
   }
+  TS_MARK(27);
 }
 
 // ------------------------------------------------------------------- launch
@@ -1280,10 +1518,13 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
       return TS_ERR_CUDA;
   }
   const int dyn = (smem_avail - static_bytes - 1024) / 128 * 128;
-  const int flag_cap = 8192;   // >= kMaxB * kMaxWaveHeads * 4 (vote weights alias it)
-  static_assert(kMaxB * kMaxWaveHeads * 4 <= 8192, "weights fit the flag area");
-  const int e_bytes = dyn - S::RING_BYTES - flag_cap;
-  if (e_bytes < 16 * 1024) return TS_ERR_UNSUPPORTED;
+  const int flag_cap = 8192;   // one byte per token of a CTA's range
+  // ring slots of one stage of K each; the selection scratch and one
+  // sequence's global histograms (with masses) alias the same space later
+  const int nslot = std::min(kMaxSlots, (dyn - flag_cap) / S::STAGE_BYTES);
+  if (nslot < S::MIN_SLOTS || dyn - flag_cap < kSelScratch + kBins * 12 ||
+      dyn - flag_cap < kMaxB * kMaxWaveHeads * 8)
+    return TS_ERR_UNSUPPORTED;
   if (!ensure_smem<step_kernel<KT, D, HKV, G>>((size_t)dyn, ctx->device)) {
     if (std::getenv("TS_DEBUG")) std::fprintf(stderr, "ts step: smem attribute %d B refused\n", dyn);
     return TS_ERR_CUDA;
@@ -1293,8 +1534,8 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
     int per_sm = 0;
     const cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, S::THREADS, (size_t)dyn);
     if (debug)
-      std::fprintf(stderr, "ts step: static %d B, dynamic %d B, threads %d, blocks/SM %d (%s)\n", static_bytes, dyn,
-                   S::THREADS, per_sm, cudaGetErrorString(oe));
+      std::fprintf(stderr, "ts step: static %d B, dynamic %d B, threads %d, ring slots %d, blocks/SM %d (%s)\n",
+                   static_bytes, dyn, S::THREADS, nslot, per_sm, cudaGetErrorString(oe));
     if (oe != cudaSuccess || per_sm < 1) return TS_ERR_COOP_UNAVAILABLE;
     ctx->step_grid = ctx->num_sms;
   }
@@ -1347,10 +1588,17 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   a.apart = ctx->apart;
   a.spill = ctx->logits;
   a.spill_floats = ctx->logits_floats;
+  a.wpart = reinterpret_cast<float2*>(ctx->step_wpart);
+  a.l2_budget = kLogitL2Budget;
+  if (const char* env = std::getenv("TOKENSELECT_L2_BUDGET_MB")) {
+    const long mb = std::strtol(env, nullptr, 10);
+    if (mb > 0) a.l2_budget = (int64_t)mb << 20;
+  }
   a.gsync = reinterpret_cast<GridSync*>(ctx->gsync);
   a.status = ctx->status;
+  a.phase_ns = ctx->phase_ns;
   a.dyn_bytes = dyn;
-  a.e_cap = e_bytes / 4;
+  a.nslot = nslot;
   a.flag_cap = flag_cap;
   if (cudaMemsetAsync(ctx->gsync, 0, sizeof(GridSync), s) != cudaSuccess) return TS_ERR_CUDA;
   cudaLaunchConfig_t lc = {};
