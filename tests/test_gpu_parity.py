@@ -40,6 +40,27 @@ def test_qwen_batched_small_both_paths(multi):
     _run(sp, 3, multi_kernel=multi)
 
 
+@pytest.mark.parametrize("scan", ["tensor", "cuda"])
+def test_llama_scan_paths(scan, monkeypatch):
+    # bf16 pages of 8 KV heads scan on the tensor cores unless TOKENSELECT_NO_TC=1
+    if scan == "cuda":
+        monkeypatch.setenv("TOKENSELECT_NO_TC", "1")
+    sp = W.spec(1, n0=(20011,), steps=3, k=1024, n_local=128)
+    _run(sp, 3)
+
+
+def test_llama_batched_two_sequences_per_cta():
+    # every CTA range meets at most two sequences: tensor-core scan with two query images
+    sp = W.spec(1, n0=(40000, 33001), n0_range=None, batch=2, steps=2, k=512, n_local=64)
+    _run(sp, 2, theta=2.0)
+
+
+def test_llama_batched_many_short_sequences():
+    # a CTA range meets three or more sequences: the CUDA-core scan takes over
+    sp = W.spec(1, n0=(300, 17, 2000, 45, 999, 5), n0_range=None, batch=6, steps=2, k=128, n_local=32)
+    _run(sp, 2, theta=2.0)
+
+
 def test_tiny_fp32_separate_calls_all_miss():
     _run(W.spec(0), 4, separate_calls=True, theta=2.0)
 

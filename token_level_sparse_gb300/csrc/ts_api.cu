@@ -132,7 +132,8 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   chk(alloc(&ctx->cands, B * 2048));
   chk(alloc(&ctx->cta_cnt, B * NS * 3));
   chk(alloc(&ctx->apart, B * NS * H * (D + 2)));
-  chk(alloc(&ctx->step_wpart, NS * B * kMaxScanWarps * kMaxScanG * 2));
+  // per CTA: [sequence][scan warp][head] pairs (CUDA-core scan) or [2][128 rows][head] (tensor-core scan)
+  chk(alloc(&ctx->step_wpart, NS * std::max<size_t>(B * kMaxScanWarps, 2 * 128) * kMaxScanG * 2));
   chk(alloc(&ctx->gsync, 4));
   chk(alloc(&ctx->phase_ns, 32));
   chk(alloc(&ctx->partials, B * ctx->score_max_chunks * H));

@@ -74,7 +74,13 @@ struct ts_ctx {
   unsigned long long* cands = nullptr;   // [max_batch][2048]
   int* cta_cnt = nullptr;                // [max_batch][num_sms][3]
   float* apart = nullptr;                // [max_batch][num_sms][H][d] outputs, then [..][H] (max, sum)
-  float* step_wpart = nullptr;           // [num_sms][max_batch][16 warps][8 heads] (max, sum exp)
+  struct KMap {                          // encoded TMA tensor maps of recent K pools
+    const void* pool = nullptr;
+    int64_t num_pages = 0;
+    alignas(64) unsigned char map[128];
+  } kmaps[8];
+  int kmap_next = 0;
+  float* step_wpart = nullptr;           // per SM: scan (max, sum exp) pairs, see the persistent kernel
   unsigned* gsync = nullptr;             // grid barrier state (4 words)
   unsigned long long* phase_ns = nullptr;  // [32] phase boundary times of the last step kernel
   bool use_step = true;                  // the persistent kernel is available

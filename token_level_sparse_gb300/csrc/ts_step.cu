@@ -29,8 +29,14 @@
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <type_traits>
 
 #include "ts_common.cuh"
+#include "ts_tc.cuh"
 
 namespace ts {
 namespace {
@@ -88,6 +94,18 @@ struct StepShape {
   static_assert(NCW >= 1 && (P * HKV) % NCW == 0 && ROWS % RPW == 0 && ITERS >= 1, "scan warp split");
   static_assert(NCW % HKV == 0 && P % ROWS == 0 || ROWS % P == 0, "rows of a warp stay in one page");
   static_assert(32 % ALPT == 0 && GP <= ALPT, "attention lane split");
+  // tensor-core scan (bf16 pages of 128 rows = H_kv x 16 tokens): one M = 128 tcgen05.mma
+  // tile per page against all query heads, each split into three bf16 terms
+  static constexpr bool TC = std::is_same<KT, __nv_bfloat16>::value && HKV * P == 128 && (D == 128 || D == 64) &&
+                             3 * HKV * G <= 256 && G <= 8;
+  static constexpr int TC_N = (3 * HKV * G + 15) / 16 * 16;           // B rows (q terms), multiple of 16
+  static constexpr int TC_HALVES = D / 64;                             // 128-byte swizzle rows per K row
+  static constexpr int TC_TILE = 128 * D * 2;                          // one page of K
+  static constexpr int TC_BIMG = TC_N * D * 2;                         // one sequence's query terms
+  static constexpr int TC_COLS = TC_N <= 32 ? 32 : (TC_N <= 64 ? 64 : (TC_N <= 128 ? 128 : 256));
+  static constexpr int TC_NLD = (6 * G + 7) / 8;                       // 8-column loads per epilogue warp
+  static_assert(!TC || (2 * TC_COLS <= 512 && 6 * G * 3 + 8 * TC_NLD <= TC_COLS && NW >= 8 && TC_HALVES >= 1 &&
+                        TC_BIMG % 1024 == 0 && TC_TILE % 1024 == 0), "tensor-core scan");
   static_assert(G <= kMaxG, "heads per KV head");
   static_assert(NCW <= kMaxScanWarps && NCW % HKV == 0, "scan warps split evenly over the KV heads");
 };
@@ -97,6 +115,9 @@ struct GridSync {
 };
 
 struct StepKArgs {
+  CUtensorMap tmap_k;          // K pool as [num_pages * H_kv * 16][d] bf16, box 64 x 128, 128-byte swizzle
+  int tc;                      // the tensor-core scan may run (map encoded, geometry supported)
+  int nslot_tc;                // its ring slots
   int phases;
   int B, H, max_tokens, pt_stride;
   int64_t num_pages;
@@ -269,6 +290,9 @@ struct Smem {
   int pre_c[kMaxB], pre_a[kMaxB];  // selected tokens of the CTAs before mine (candidates, all)
   int tot_c[kMaxB], tot_a[kMaxB];  // and of all CTAs
   int tie_base[kMaxB];             // exact ties in the CTAs before mine, per segment
+  int use_tc;                      // this launch scans with the tensor cores
+  uint32_t tmem;                   // TMEM base address of the accumulators
+  int acc_tl[2], acc_nv[2], acc_sg[2];  // per accumulator buffer: first token, valid rows, segment
   int my_pages[kMaxPagesCta];  // physical page ids of my range (first kMaxPagesCta pages)
   int timed_out;
   int wsum[33];
@@ -289,16 +313,22 @@ struct Smem {
   } while (0)
 
 template <typename KT, int D, int HKV, int G>
-__global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_kernel(StepKArgs a) {
+__global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_kernel(const __grid_constant__ StepKArgs a) {
   using S = StepShape<KT, D, HKV, G>;
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ Smem sm;
   __shared__ __align__(8) uint64_t full[kMaxSlots];
+  __shared__ __align__(8) uint64_t empty[kMaxSlots];  // tensor-core scan: ring slot read by its MMAs
+  __shared__ __align__(8) uint64_t accf[2], acce[2];   // accumulator buffer written / read out
+  __shared__ __align__(8) uint64_t drainb;            // every MMA issued has completed
   __shared__ __align__(8) uint64_t abar;
 
   const int nslot = a.nslot;
   unsigned char* ring = dsm;                                               // nslot x STAGE_BYTES of K
   uint8_t* selflag = dsm + a.dyn_bytes - a.flag_cap;                       // selection flags of my tokens
+  // tensor-core scan: 1024-aligned ring of pages, then the query-term images of two sequences
+  unsigned char* tcr = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~(uintptr_t)1023);
+  unsigned char* tcb = tcr + (size_t)a.nslot_tc * S::TC_TILE;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, nCTA = gridDim.x;
@@ -306,11 +336,17 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
 
   TS_MARK(0);
   if (tid == 0) {
-    for (int s = 0; s < nslot; ++s) {
+    for (int s = 0; s < kMaxSlots; ++s) {
       mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
       sm.stage_done[s] = 0;
       sm.slot_last[s] = -1;
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accf[i], 2);     // the MMAs' commit and the issuer's own arrive (metadata)
+      mbar_init(&acce[i], 128);   // every epilogue thread
+    }
+    mbar_init(&drainb, 1);
     mbar_init(&abar, 1);
     mbar_fence_init();
     sm.timed_out = 0;
@@ -450,10 +486,30 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       ++ns;
     }
     sm.nseg = ns;
+    // the tensor-core scan holds the query terms of two sequences: it runs when no CTA's page
+    // range meets three (a middle sequence inside one CTA whose neighbours both reach it)
+    int use_tc = 0;
+    if constexpr (S::TC) {
+      use_tc = a.tc && (a.phases & kPhScore) && H <= kMaxWaveHeads;
+      int prev = -1, prev2 = -1;
+      for (int b = 0; b < B && use_tc; ++b) {
+        const SeqState& st = sm.seq[b];
+        if (st.pg1 <= st.pg0) continue;
+        if (prev2 >= 0) {
+          const SeqState& m = sm.seq[prev];
+          if (m.first_cta == m.last_cta && sm.seq[prev2].last_cta == m.first_cta && st.first_cta == m.last_cta)
+            use_tc = 0;
+        }
+        prev2 = prev;
+        prev = b;
+      }
+    }
+    sm.use_tc = use_tc;
     // scan waves: the most KV heads per wave (a power-of-two divisor of H_kv) whose
-    // logits stay within the L2 budget
+    // logits stay within the L2 budget (the tensor-core scan takes every head at once)
     int hpw = HKV;
-    while (hpw > 1 && ((int64_t)ptot * S::P * hpw * G * 4 > a.l2_budget || hpw * G > kMaxWaveHeads)) hpw >>= 1;
+    while (!use_tc && hpw > 1 && ((int64_t)ptot * S::P * hpw * G * 4 > a.l2_budget || hpw * G > kMaxWaveHeads))
+      hpw >>= 1;
     sm.hpw = hpw;
     sm.nwaves = HKV / hpw;
     // my logits [tok_stride][hpw*G] in scratch
@@ -485,17 +541,281 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     }
     if (c == 0 && tid < B) a.cand_n[tid] = 0u;
   }
+  if constexpr (S::TC) {
+    if (sm.use_tc) {
+      // B operand of each of my (at most two) sequences: row n = 3 h + term holds that term of
+      // query head h, K-major in the 128-byte swizzle layout; rows past 3 H are zero
+      constexpr int CH = D / 8;                        // 16-byte chunks of a row
+      for (int i = tid; i < sm.nseg * S::TC_N * CH; i += blockDim.x) {
+        const int sg = i / (S::TC_N * CH), rem = i % (S::TC_N * CH);
+        const int n = rem / CH, ch = rem % CH;
+        const int h = n / 3, term = n % 3;
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (h < H) {
+          const float* qh = a.q + ((size_t)sm.seg_b[sg] * H + h) * D + ch * 8;
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = (uint32_t)__bfloat16_as_ushort(bf16_split_term(qh[2 * e], term)) |
+                   ((uint32_t)__bfloat16_as_ushort(bf16_split_term(qh[2 * e + 1], term)) << 16);
+        }
+        *reinterpret_cast<uint4*>(tcb + (size_t)sg * S::TC_BIMG + (ch / 8) * (S::TC_N * 128) +
+                                  sw128_offset(n, (ch % 8) * 8)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_proxy_async();
+    }
+  }
   __syncthreads();
   TS_MARK(1);
 
   // ========================================================================= SCORE
   if ((a.phases & kPhScore) && sm.ptot > 0) {   // nothing to scan when every sequence hits
+    // each head's normaliser over the CTAs of the sequence, then the votes of my tokens for
+    // heads [g0 G, g0 G + HW); eb holds my logits [token][HW]
+    auto vote_pass = [&](const float* eb, int g0, int HW, int wv) {
+      float2* wz = reinterpret_cast<float2*>(ring);  // [segment][kMaxWaveHeads]: (max, 1 / sum)
+      for (int item = warp; item < sm.nseg * HW; item += S::NW) {
+        const int sg = item / HW, hl = item % HW;
+        const SeqState& st = sm.seq[sm.seg_b[sg]];
+        const float2* pp = a.partials + (size_t)sm.seg_b[sg] * nCTA * H + g0 * G + hl;
+        float M = -INFINITY;
+        for (int cc = st.first_cta + lane; cc <= st.last_cta; cc += 32) M = fmaxf(M, __ldcg(pp + (size_t)cc * H).x);
+        M = warp_max(M);
+        KahanF kz;
+        if (M > -INFINITY)
+          for (int cc = st.first_cta + lane; cc <= st.last_cta; cc += 32) {
+            const float2 mz = __ldcg(pp + (size_t)cc * H);
+            if (mz.y > 0.f) kz.add(mz.y * expf(mz.x - M));
+          }
+        const double z = warp_sum_f64((double)kz.s - (double)kz.c);
+        if (lane == 0)
+          wz[sg * kMaxWaveHeads + hl] = (M > -INFINITY && z > 0.0) ? make_float2(M, (float)(1.0 / z))
+                                                                   : make_float2(INFINITY, 0.f);
+      }
+      __syncthreads();
+      for (int sg = 0; sg < sm.nseg; ++sg) {
+        const int b = sm.seg_b[sg], t0 = sm.seg_t0[sg], nt = sm.seg_ntok[sg];
+        float* vb = a.vote + (size_t)b * a.vote_stride + (size_t)sm.seg_lp0[sg] * S::P;
+        const float2* w = wz + sg * kMaxWaveHeads;
+        for (int t = tid; t < nt; t += blockDim.x) {
+          const float* row = eb + (size_t)(t0 + t) * HW;
+          KahanF acc;
+          if ((HW & 3) == 0) {
+            for (int h4 = 0; h4 < HW; h4 += 4) {
+              const float4 x = *reinterpret_cast<const float4*>(row + h4);
+              acc.add(expf(x.x - w[h4].x) * w[h4].y);
+              acc.add(expf(x.y - w[h4 + 1].x) * w[h4 + 1].y);
+              acc.add(expf(x.z - w[h4 + 2].x) * w[h4 + 2].y);
+              acc.add(expf(x.w - w[h4 + 3].x) * w[h4 + 3].y);
+            }
+          } else {
+            for (int hl = 0; hl < HW; ++hl) acc.add(expf(row[hl] - w[hl].x) * w[hl].y);
+          }
+          const float v = acc.s - acc.c;
+          vb[t] = (wv == 0) ? v : vb[t] + v;
+        }
+      }
+      __syncthreads();
+    };
+    bool scanned = false;
+    if constexpr (S::TC) {
+      if (sm.use_tc) {
+        scanned = true;
+        // ---- pages of my range through a ring of TMA tiles; one elected thread multiplies each
+        // page (128 rows = H_kv heads x 16 tokens) by the query terms of its sequence into a
+        // TMEM accumulator (two buffers); four warps read the accumulators out: logits to the
+        // scratch, running (max, sum exp) per row and head in registers
+        const int np = sm.p1 - sm.p0;
+        const int nsl = a.nslot_tc;
+        float* eb = a.spill + (size_t)c * sm.region;             // [tok_stride][H]
+        float2* wpt = a.wpart + (size_t)c * 2 * 128 * G;         // [segment < 2][row][head of the row]
+        if (warp == 2) {
+          tmem_alloc(&sm.tmem, 2 * S::TC_COLS);
+          tmem_relinquish();
+        }
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        const uint32_t tmem = sm.tmem;
+        if (warp == 0) {
+          if (lane == 0) {                                       // producer
+            const uint64_t pol = l2_evict_first_policy();
+            int sg = 0;
+            for (int u = 0; u < np; ++u) {
+              const int s = u % nsl;
+              if (u >= nsl && !mbar_wait(&empty[s], ((u / nsl) - 1) & 1)) {
+                set_error(a.status, TS_ERR_TIMEOUT);
+                sm.timed_out = 1;
+                break;
+              }
+              const int gp = sm.p0 + u;
+              while (sg + 1 < sm.nseg && gp >= sm.seg_pend[sg]) ++sg;
+              const int b = sm.seg_b[sg];
+              const int lp = gp - sm.seq[b].pg0;
+              const int page = u < kMaxPagesCta ? sm.my_pages[u] : a.page_table[(size_t)b * a.pt_stride + lp];
+              const bool valid = page >= 0 && (int64_t)page < a.num_pages;
+              sm.stage_tok[s][0] = u * S::P;
+              sm.stage_b[s][0] = b;
+              sm.stage_nv[s][0] = valid ? min(S::P, sm.seq[b].n - lp * S::P) : 0;
+              sm.slot_last[s] = u;
+              if (valid) {
+                mbar_arrive_expect_tx(&full[s], (uint32_t)S::TC_TILE);
+#pragma unroll
+                for (int h = 0; h < S::TC_HALVES; ++h)
+                  tma_load_2d(tcr + (size_t)s * S::TC_TILE + h * (S::TC_TILE / S::TC_HALVES), &a.tmap_k, h * 64,
+                              page * 128, &full[s], pol);
+              } else {
+                set_error(a.status, TS_ERR_PAGE_OOB);
+                mbar_arrive(&full[s]);
+              }
+            }
+          }
+        } else if (warp == 1) {
+          if (lane == 0) {                                       // MMA issuer
+            constexpr uint32_t idesc = idesc_bf16_f32(128, S::TC_N);
+            for (int u = 0; u < np; ++u) {
+              const int s = u % nsl, buf = u & 1;
+              if (!mbar_wait(&full[s], (u / nsl) & 1) || (u >= 2 && !mbar_wait(&acce[buf], ((u >> 1) - 1) & 1))) {
+                set_error(a.status, TS_ERR_TIMEOUT);
+                sm.timed_out = 1;
+                break;
+              }
+              tc_fence_after();
+              const int b = sm.stage_b[s][0], nv = sm.stage_nv[s][0];
+              const int sgi = sm.my_seg_of[b];
+              sm.acc_tl[buf] = sm.stage_tok[s][0];
+              sm.acc_nv[buf] = nv;
+              sm.acc_sg[buf] = sgi;
+              if (nv > 0) {
+                const uint32_t a0 = smem_addr(tcr + (size_t)s * S::TC_TILE);
+                const uint32_t b0 = smem_addr(tcb + (size_t)sgi * S::TC_BIMG);
+#pragma unroll
+                for (int h = 0; h < S::TC_HALVES; ++h)
+#pragma unroll
+                  for (int ks = 0; ks < 4; ++ks)
+                    umma_bf16(tmem + buf * S::TC_COLS, sdesc_sw128(a0 + h * (S::TC_TILE / S::TC_HALVES) + ks * 32),
+                              sdesc_sw128(b0 + h * (S::TC_N * 128) + ks * 32), idesc, (h | ks) != 0);
+              }
+              umma_commit(&empty[s]);      // the slot is free once its MMAs have read it
+              umma_commit(&accf[buf]);     // the accumulator is complete
+              mbar_arrive(&accf[buf]);     // and its metadata above is published
+            }
+            umma_commit(&drainb);
+          }
+        } else if (warp >= 4 && warp < 8) {                      // epilogue: thread = row (head g, slot t)
+          const int q4 = warp & 3, row = q4 * 32 + lane, g = row >> 4, t = row & 15;
+          const bool odd = (g & 1) != 0;                         // second KV head of the warp's columns
+          const uint32_t tq = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(6 * G * q4);
+          float run_m[G];
+          KahanF run_z[G];
+          int cur = -1;
+          auto flush = [&]() {
+            if (cur >= 0)
+#pragma unroll
+              for (int j = 0; j < G; ++j)
+                wpt[((size_t)cur * 128 + row) * G + j] = make_float2(run_m[j], run_z[j].s - run_z[j].c);
+          };
+          for (int u = 0; u < np; ++u) {
+            const int buf = u & 1;
+            if (!__all_sync(kFull, mbar_wait(&accf[buf], (u >> 1) & 1))) {
+              if (lane == 0) {
+                set_error(a.status, TS_ERR_TIMEOUT);
+                sm.timed_out = 1;
+              }
+              break;
+            }
+            tc_fence_after();
+            const int tl = sm.acc_tl[buf], nv = sm.acc_nv[buf], sgi = sm.acc_sg[buf];
+            float r[8 * S::TC_NLD];
+#pragma unroll
+            for (int i = 0; i < S::TC_NLD; ++i)
+              tmem_ld_x8(tq + buf * S::TC_COLS + 8 * i, *reinterpret_cast<float(*)[8]>(r + 8 * i));
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive(&acce[buf]);
+            if (sgi != cur) {
+              flush();
+              cur = sgi;
+#pragma unroll
+              for (int j = 0; j < G; ++j) {
+                run_m[j] = -INFINITY;
+                run_z[j] = KahanF();
+              }
+            }
+            float x[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+              const float hi = odd ? r[3 * G + 3 * j] : r[3 * j];
+              const float mid = odd ? r[3 * G + 3 * j + 1] : r[3 * j + 1];
+              const float lo = odd ? r[3 * G + 3 * j + 2] : r[3 * j + 2];
+              x[j] = t < nv ? ((lo + mid) + hi) * a.scale : -INFINITY;
+            }
+            float* dst = eb + (size_t)(tl + t) * H + g * G;
+            if constexpr (G == 4) {
+              *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < G; ++j) dst[j] = x[j];
+            }
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+              if (x[j] > run_m[j]) {
+                if (run_m[j] > -INFINITY) {
+                  const float f = expf(run_m[j] - x[j]);
+                  run_z[j].s *= f;
+                  run_z[j].c *= f;
+                }
+                run_z[j].add(1.f);
+                run_m[j] = x[j];
+              } else if (x[j] > -INFINITY) {
+                run_z[j].add(expf(x[j] - run_m[j]));
+              }
+            }
+          }
+          flush();
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 32 && !mbar_wait(&drainb, 0)) {               // every MMA issued has completed
+          set_error(a.status, TS_ERR_TIMEOUT);
+          sm.timed_out = 1;
+        }
+        __syncthreads();
+        if (tid == 0 && sm.timed_out) {
+          // copies issued but never consumed land before the CTA leaves
+          for (int ss = 0; ss < nsl; ++ss)
+            if (sm.slot_last[ss] >= 0) mbar_wait(&full[ss], (sm.slot_last[ss] / nsl) & 1);
+        }
+        __syncthreads();
+        if (warp == 2) {
+          tc_fence_after();
+          tmem_dealloc(tmem, 2 * S::TC_COLS);
+        }
+        if (sm.timed_out) {
+          if (tid == 0) atomicExch(&a.gsync->abort, 1u);   // the others leave at their next barrier
+          return;
+        }
+        TS_MARK(2);
+        // ---- per (segment, head): combine the 16 rows' (max, sum exp) -> partials
+        for (int item = warp; item < sm.nseg * H; item += S::NW) {
+          const int sg = item / H, h = item % H, g = h / G, j = h % G;
+          float2 mz = make_float2(-INFINITY, 0.f);
+          if (lane < 16) mz = wpt[((size_t)sg * 128 + g * 16 + lane) * G + j];
+          const float m = warp_max(mz.x);
+          const double z = warp_sum_f64((m > -INFINITY && mz.y > 0.f) ? (double)mz.y * (double)expf(mz.x - m) : 0.0);
+          if (lane == 0) a.partials[((size_t)sm.seg_b[sg] * nCTA + c) * H + h] = make_float2(m, (float)z);
+        }
+        TS_MARK(3);
+        if (!grid_sync(a.gsync, a.status)) return;
+        TS_MARK(4);
+        vote_pass(eb, 0, H, 0);
+      }
+    }
+    if (!scanned) {
     const int hpw = sm.hpw, HW = hpw * G, nwaves = sm.nwaves;
     const int pps = HKV / hpw;                       // pages per stage
     const int np = sm.p1 - sm.p0;
     const int nstages = (np + pps - 1) / pps;
     const int slab = hpw * S::P * S::ROW_BYTES;      // bytes of one page's heads of the wave
-    const int tstride = sm.tok_stride;
     float* eb = a.spill + (size_t)c * sm.region;     // my logits, token-major [tstride][HW]
     float2* wp = a.wpart + (size_t)c * B * S::NCW * G;  // [segment][warp][head of the warp] (max, sum exp)
     const uint64_t pol = l2_evict_first_policy();
@@ -684,50 +1004,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       if (!grid_sync(a.gsync, a.status)) return;
       TS_MARK(4 + 3 * min(wv, 5));
 
-      // ---- each head's normaliser over the CTAs of the sequence, then my votes
-      float2* wz = reinterpret_cast<float2*>(ring);  // [segment][kMaxWaveHeads]: (max, 1 / sum)
-      for (int item = warp; item < sm.nseg * HW; item += S::NW) {
-        const int sg = item / HW, hl = item % HW;
-        const SeqState& st = sm.seq[sm.seg_b[sg]];
-        const float2* pp = a.partials + (size_t)sm.seg_b[sg] * nCTA * H + g0 * G + hl;
-        float M = -INFINITY;
-        for (int cc = st.first_cta + lane; cc <= st.last_cta; cc += 32) M = fmaxf(M, __ldcg(pp + (size_t)cc * H).x);
-        M = warp_max(M);
-        KahanF kz;
-        if (M > -INFINITY)
-          for (int cc = st.first_cta + lane; cc <= st.last_cta; cc += 32) {
-            const float2 mz = __ldcg(pp + (size_t)cc * H);
-            if (mz.y > 0.f) kz.add(mz.y * expf(mz.x - M));
-          }
-        const double z = warp_sum_f64((double)kz.s - (double)kz.c);
-        if (lane == 0)
-          wz[sg * kMaxWaveHeads + hl] = (M > -INFINITY && z > 0.0) ? make_float2(M, (float)(1.0 / z))
-                                                                   : make_float2(INFINITY, 0.f);
-      }
-      __syncthreads();
-      for (int sg = 0; sg < sm.nseg; ++sg) {
-        const int b = sm.seg_b[sg], t0 = sm.seg_t0[sg], nt = sm.seg_ntok[sg];
-        float* vb = a.vote + (size_t)b * a.vote_stride + (size_t)sm.seg_lp0[sg] * S::P;
-        const float2* w = wz + sg * kMaxWaveHeads;
-        for (int t = tid; t < nt; t += blockDim.x) {
-          const float* row = eb + (size_t)(t0 + t) * HW;
-          KahanF acc;
-          if ((HW & 3) == 0) {
-            for (int h4 = 0; h4 < HW; h4 += 4) {
-              const float4 x = *reinterpret_cast<const float4*>(row + h4);
-              acc.add(expf(x.x - w[h4].x) * w[h4].y);
-              acc.add(expf(x.y - w[h4 + 1].x) * w[h4 + 1].y);
-              acc.add(expf(x.z - w[h4 + 2].x) * w[h4 + 2].y);
-              acc.add(expf(x.w - w[h4 + 3].x) * w[h4 + 3].y);
-            }
-          } else {
-            for (int hl = 0; hl < HW; ++hl) acc.add(expf(row[hl] - w[hl].x) * w[hl].y);
-          }
-          const float v = acc.s - acc.c;
-          vb[t] = (wv == 0) ? v : vb[t] + v;
-        }
-      }
-      __syncthreads();
+      vote_pass(eb, g0, HW, wv);
+    }
     }
   }
 
@@ -1493,6 +1771,33 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
 
 // ------------------------------------------------------------------- launch
 
+// Tensor map of a bf16 K pool seen as [num_pages * 128 rows][d]: boxes of 64 elements x 128 rows
+// (one page), 128-byte swizzle. The encoder comes from the driver through the runtime, so the
+// library needs no link against the driver library. False when it cannot be encoded.
+bool encode_kmap(CUtensorMap* map, const void* k_pool, int64_t num_pages, int d) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static bool looked = false;
+  if (!looked) {
+    looked = true;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  if (!encode || (reinterpret_cast<uintptr_t>(k_pool) & 15) != 0 || num_pages <= 0 ||
+      num_pages * 128 > (int64_t)0x7fffffff)
+    return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)num_pages * 128};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(k_pool), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename KT, int D, int HKV, int G>
 ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   using S = StepShape<KT, D, HKV, G>;
@@ -1599,6 +1904,34 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   a.phase_ns = ctx->phase_ns;
   a.dyn_bytes = dyn;
   a.nslot = nslot;
+  a.tc = 0;
+  a.nslot_tc = 0;
+  if constexpr (S::TC) {
+    // tensor-core scan: 1024-aligned ring of page tiles plus two query-term images
+    const int nslot_tc = std::min(kMaxSlots, (dyn - flag_cap - 1024 - 2 * S::TC_BIMG) / S::TC_TILE);
+    const char* no_tc_env = std::getenv("TOKENSELECT_NO_TC");   // =1: CUDA-core scan (comparisons, tests)
+    const bool no_tc = no_tc_env && no_tc_env[0] == '1';
+    if (!no_tc && nslot_tc >= 2 && (c.phases & kPhScore) && c.k_pool) {
+      auto& cache = ctx->kmaps;   // a few recent pools (one per layer in a decode loop)
+      int hitc = -1;
+      for (int i = 0; i < (int)(sizeof(cache) / sizeof(cache[0])); ++i)
+        if (cache[i].pool == c.k_pool && cache[i].num_pages == cfg.num_pages) hitc = i;
+      if (hitc < 0) {
+        hitc = ctx->kmap_next;
+        ctx->kmap_next = (ctx->kmap_next + 1) % (int)(sizeof(cache) / sizeof(cache[0]));
+        cache[hitc].pool = nullptr;
+        if (encode_kmap(reinterpret_cast<CUtensorMap*>(cache[hitc].map), c.k_pool, cfg.num_pages, D)) {
+          cache[hitc].pool = c.k_pool;
+          cache[hitc].num_pages = cfg.num_pages;
+        }
+      }
+      if (cache[hitc].pool == c.k_pool) {
+        std::memcpy(&a.tmap_k, cache[hitc].map, sizeof(CUtensorMap));
+        a.tc = 1;
+        a.nslot_tc = nslot_tc;
+      }
+    }
+  }
   a.flag_cap = flag_cap;
   if (cudaMemsetAsync(ctx->gsync, 0, sizeof(GridSync), s) != cudaSuccess) return TS_ERR_CUDA;
   cudaLaunchConfig_t lc = {};

@@ -133,4 +133,16 @@ __host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int k) {
   return (uint32_t)row * 128u + (uint32_t)((((k >> 3) ^ (row & 7)) << 4) + ((k & 7) << 1));
 }
 
+// Term `term` (0, 1, 2) of the three-term bf16 split of x: hi = bf16(x),
+// mid = bf16(x - hi), lo = bf16(x - hi - mid); hi + mid + lo equals x to
+// within 2^-27 relative, and each product with a bf16 value is exact in fp32.
+__device__ __forceinline__ __nv_bfloat16 bf16_split_term(float x, int term) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(x);
+  const float r1 = x - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(mid);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r2);
+  return term == 0 ? hi : (term == 1 ? mid : lo);
+}
+
 }  // namespace ts
