@@ -43,14 +43,14 @@ __global__ void __launch_bounds__(kCheckThreads)
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    double sxy = 0, sxx = 0, syy = 0;
+    KahanF sxy, sxx, syy;   // fp32: FP64 is a slow pipe here
     for (int w = 0; w < kCheckThreads / 32; ++w) {
-      sxy += red[0][w];
-      sxx += red[1][w];
-      syy += red[2][w];
+      sxy.add(red[0][w]);
+      sxx.add(red[1][w]);
+      syy.add(red[2][w]);
     }
-    const double den = sqrt(sxx) * sqrt(syy);
-    const float c = den > 0.0 ? (float)(sxy / den) : __int_as_float(0x7fc00000);
+    const float den = sqrtf(sxx.s - sxx.c) * sqrtf(syy.s - syy.c);
+    const float c = den > 0.f ? (sxy.s - sxy.c) / den : __int_as_float(0x7fc00000);
     hit[b] = (c >= theta) ? 1 : 0;  // NaN compares false: a miss
     if (cos_out) cos_out[b] = c;
   }

@@ -190,16 +190,33 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-__device__ __forceinline__ double warp_sum_f64(double x) {
+__device__ __forceinline__ int warp_sum_i(int x) {
 #pragma unroll
   for (int d = 16; d >= 1; d >>= 1) x += __shfl_xor_sync(kFull, x, d);
   return x;
 }
 
-__device__ __forceinline__ int warp_sum_i(int x) {
+// Error-free transformation of a sum (Knuth's TwoSum): s + e == a + b exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// Sum over the warp of the float pairs hi + lo, every level exact up to the low
+// parts (TwoSum on the high parts). Partners combine the same two values, so
+// every lane returns the same bits. FP64 is a slow pipe on this part; this keeps
+// near-double accuracy on the fp32 pipe.
+__device__ __forceinline__ float warp_sum_comp(float hi, float lo = 0.f) {
 #pragma unroll
-  for (int d = 16; d >= 1; d >>= 1) x += __shfl_xor_sync(kFull, x, d);
-  return x;
+  for (int d = 16; d >= 1; d >>= 1) {
+    const float oh = __shfl_xor_sync(kFull, hi, d), ol = __shfl_xor_sync(kFull, lo, d);
+    float s, e;
+    two_sum(hi, oh, s, e);
+    hi = s;
+    lo = (lo + ol) + e;
+  }
+  return hi + lo;
 }
 
 // Compensated (Kahan) accumulation in fp32.

@@ -237,8 +237,8 @@ __global__ void __launch_bounds__(ScoreShape<KT, D, HKV, G>::THREADS, 1)
       const float2 mz = __ldcg(pp + (size_t)c * H);
       if (mz.y > 0.f) kz.add(mz.y * expf(mz.x - M));
     }
-    const double z = warp_sum_f64((double)kz.s - (double)kz.c);
-    if (lane == 0) a.stats[(size_t)b * H + h] = make_float2(M, (float)(1.0 / z));
+    const float z = warp_sum_comp(kz.s, -kz.c);
+    if (lane == 0) a.stats[(size_t)b * H + h] = make_float2(M, 1.f / z);
   }
   if (tid == 0) a.counters[(size_t)b * kCounterSlots] = 0u;
 }

@@ -290,6 +290,7 @@ struct Smem {
   int pre_c[kMaxB], pre_a[kMaxB];  // selected tokens of the CTAs before mine (candidates, all)
   int tot_c[kMaxB], tot_a[kMaxB];  // and of all CTAs
   int tie_base[kMaxB];             // exact ties in the CTAs before mine, per segment
+  int filled[kMaxB], ctc[kMaxB];   // cache entry filled, its cached index count
   int use_tc;                      // this launch scans with the tensor cores
   uint32_t tmem;                   // TMEM base address of the accumulators
   int acc_tl[2], acc_nv[2], acc_sg[2];  // per accumulator buffer: first token, valid rows, segment
@@ -306,7 +307,10 @@ struct Smem {
 
 // --------------------------------------------------------------- the kernel
 
-// CTA 0 records the time it reaches phase boundary i (0..31).
+// CTA 0 records the time it reaches phase boundary i (0..31): 0 start, 1 set-up done,
+// 2 + 3 w / 3 + 3 w / 4 + 3 w scan wave w done / partials written / barrier passed,
+// 20 score done, 28 + l histogram level l built, 21 levels done, 22 candidates, 23 select
+// done, 24 attend done, 25 last barrier, 26 merged, 27 end.
 #define TS_MARK(i)                                                     \
   do {                                                                 \
     if (c == 0 && tid == 0 && a.phase_ns) a.phase_ns[i] = globaltimer_ns(); \
@@ -353,6 +357,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   }
 
   // ------------------------------------------------ setup: lengths, cache test, partition
+  // one round of independent loads per sequence: length, cache entry state
+  const bool have_cache = a.ct != nullptr && a.filled != nullptr;
   for (int b = tid; b < B; b += blockDim.x) {
     int n = a.seq_lens[b];
     if (n < 0 || n > a.max_tokens) {
@@ -373,70 +379,83 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     sm.my_seg_of[b] = -1;
     sm.ct_lo[b] = 0;
     sm.ct_hi[b] = 0;
+    sm.filled[b] = have_cache ? a.filled[b] : 0;
+    sm.ctc[b] = have_cache ? max(0, min(a.ct_count[b], a.cap)) : 0;
   }
   __syncthreads();
-  if (a.phases & kPhCheck) {
-    // Algorithm 1: hit iff the entry is filled and cos(q, C_Q) >= theta
+  TS_MARK(5);
+  // every filled entry in one pass without barriers: cos(q, C_Q) (Algorithm 1: hit iff
+  // cos >= theta) and, for the reuse on a hit, how many cached indices lie below s_end and
+  // below ls; per-warp partials in shared memory, summed in a fixed order below
+  {
+    float* cr = reinterpret_cast<float*>(dsm);                       // [B][3][NW]
+    int* cn = reinterpret_cast<int*>(cr + (size_t)B * 3 * S::NW);     // [B][2][NW]
+    const bool check = (a.phases & kPhCheck) != 0;
     const int HD = H * D;
     for (int b = 0; b < B; ++b) {
-      if (!a.filled[b]) continue;
-      const float* x = a.q + (size_t)b * HD;
-      const float* y = a.cq + (size_t)b * HD;
-      float xy = 0.f, xx = 0.f, yy = 0.f;
+      if (!sm.filled[b]) continue;
+      if (check) {
+        const float* x = a.q + (size_t)b * HD;
+        const float* y = a.cq + (size_t)b * HD;
+        float xy = 0.f, xx = 0.f, yy = 0.f;
 #pragma unroll 8
-      for (int i = tid; i < HD; i += blockDim.x) {
-        const float u = x[i], v = __ldcg(y + i);
-        xy = fmaf(u, v, xy);
-        xx = fmaf(u, u, xx);
-        yy = fmaf(v, v, yy);
-      }
-      xy = warp_sum(xy);
-      xx = warp_sum(xx);
-      yy = warp_sum(yy);
-      if (lane == 0) {
-        sm.red_f[0][warp] = xy;
-        sm.red_f[1][warp] = xx;
-        sm.red_f[2][warp] = yy;
-      }
-      __syncthreads();
-      if (tid == 0) {
-        double sxy = 0, sxx = 0, syy = 0;
-        for (int w = 0; w < S::NW; ++w) {
-          sxy += sm.red_f[0][w];
-          sxx += sm.red_f[1][w];
-          syy += sm.red_f[2][w];
+        for (int i = tid; i < HD; i += blockDim.x) {
+          const float u = x[i], v = y[i];
+          xy = fmaf(u, v, xy);
+          xx = fmaf(u, u, xx);
+          yy = fmaf(v, v, yy);
         }
-        const double den = sqrt(sxx) * sqrt(syy);
-        const float cs = den > 0.0 ? (float)(sxy / den) : __int_as_float(0x7fc00000);
-        sm.seq[b].hit = (cs >= a.theta) ? 1 : 0;
+        xy = warp_sum(xy);
+        xx = warp_sum(xx);
+        yy = warp_sum(yy);
+        TS_MARK(12);
+        if (lane == 0) {
+          cr[(b * 3 + 0) * S::NW + warp] = xy;
+          cr[(b * 3 + 1) * S::NW + warp] = xx;
+          cr[(b * 3 + 2) * S::NW + warp] = yy;
+        }
       }
-      __syncthreads();
-    }
-  }
-  // a hit reuses the cached indices inside [s_end, ls): their bounds in the ascending
-  // list, by counting the entries below s_end and below ls with every thread
-  if (a.ct) {
-    for (int b = 0; b < B; ++b) {
-      if (!sm.seq[b].hit) continue;
       const int32_t* ctb = a.ct + (size_t)b * a.cap;
-      const int cnt = a.filled[b] ? min(a.ct_count[b], a.cap) : 0;
       const int se = sm.seq[b].s_end, ls = sm.seq[b].ls;
       int below_s = 0, below_l = 0;
 #pragma unroll 4
-      for (int j = tid; j < cnt; j += blockDim.x) {
-        const int v = __ldcg(ctb + j);
+      for (int j = tid; j < sm.ctc[b]; j += blockDim.x) {
+        const int v = ctb[j];
         below_s += v < se;
         below_l += v < ls;
       }
       below_s = warp_sum_i(below_s);
       below_l = warp_sum_i(below_l);
-      if (lane == 0 && (below_s | below_l)) {
-        atomicAdd(&sm.ct_lo[b], below_s);
-        atomicAdd(&sm.ct_hi[b], below_l);
+      if (lane == 0) {
+        cn[(b * 2 + 0) * S::NW + warp] = below_s;
+        cn[(b * 2 + 1) * S::NW + warp] = below_l;
       }
     }
     __syncthreads();
+    for (int b = tid; b < B; b += blockDim.x) {
+      if (!sm.filled[b]) continue;
+      if (check) {
+        KahanF sxy, sxx, syy;                                         // fp32: FP64 is a slow pipe here
+        for (int w = 0; w < S::NW; ++w) {
+          sxy.add(cr[(b * 3 + 0) * S::NW + w]);
+          sxx.add(cr[(b * 3 + 1) * S::NW + w]);
+          syy.add(cr[(b * 3 + 2) * S::NW + w]);
+        }
+        const float den = sqrtf(sxx.s - sxx.c) * sqrtf(syy.s - syy.c);
+        const float cs = den > 0.f ? (sxy.s - sxy.c) / den : __int_as_float(0x7fc00000);
+        sm.seq[b].hit = (cs >= a.theta) ? 1 : 0;
+      }
+      int lo = 0, hi = 0;
+      for (int w = 0; w < S::NW; ++w) {
+        lo += cn[(b * 2 + 0) * S::NW + w];
+        hi += cn[(b * 2 + 1) * S::NW + w];
+      }
+      sm.ct_lo[b] = lo;
+      sm.ct_hi[b] = hi;
+    }
+    __syncthreads();
   }
+  TS_MARK(6);
   if (tid == 0) {
     int pg = 0;
     for (int b = 0; b < B; ++b) {
@@ -523,6 +542,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     if (c == 0 && tid == 0) set_error(a.status, TS_ERR_SHAPE);
     return;  // the same decision in every CTA, before any grid barrier
   }
+  TS_MARK(7);
   if (c == 0 && tid < B && (a.phases & kPhCheck) && a.hit_out) a.hit_out[tid] = (uint8_t)sm.seq[tid].hit;
   // page ids of my range, read once (ring refills and attention gathers need no global load)
   for (int i = tid; i < min(sm.p1 - sm.p0, kMaxPagesCta); i += blockDim.x) {
@@ -546,20 +566,37 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       // B operand of each of my (at most two) sequences: row n = 3 h + term holds that term of
       // query head h, K-major in the 128-byte swizzle layout; rows past 3 H are zero
       constexpr int CH = D / 8;                        // 16-byte chunks of a row
-      for (int i = tid; i < sm.nseg * S::TC_N * CH; i += blockDim.x) {
-        const int sg = i / (S::TC_N * CH), rem = i % (S::TC_N * CH);
-        const int n = rem / CH, ch = rem % CH;
-        const int h = n / 3, term = n % 3;
-        uint32_t w[4] = {0u, 0u, 0u, 0u};
-        if (h < H) {
-          const float* qh = a.q + ((size_t)sm.seg_b[sg] * H + h) * D + ch * 8;
+      const int total = sm.nseg * S::TC_N * CH;
+      for (int i0 = tid; i0 < total; i0 += 2 * blockDim.x) {   // two chunks' loads in flight
+        float4 qv[2][2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int i = i0 + k * blockDim.x;
+          const int sg = i / (S::TC_N * CH), rem = i % (S::TC_N * CH);
+          const int n = rem / CH, ch = rem % CH, h = n / 3;
+          qv[k][0] = qv[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (i < total && h < H) {
+            const float4* qh = reinterpret_cast<const float4*>(a.q + ((size_t)sm.seg_b[sg] * H + h) * D + ch * 8);
+            qv[k][0] = qh[0];
+            qv[k][1] = qh[1];
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int i = i0 + k * blockDim.x;
+          if (i >= total) continue;
+          const int sg = i / (S::TC_N * CH), rem = i % (S::TC_N * CH);
+          const int n = rem / CH, ch = rem % CH, term = n % 3;
+          const float e8[8] = {qv[k][0].x, qv[k][0].y, qv[k][0].z, qv[k][0].w,
+                               qv[k][1].x, qv[k][1].y, qv[k][1].z, qv[k][1].w};
+          uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            w[e] = (uint32_t)__bfloat16_as_ushort(bf16_split_term(qh[2 * e], term)) |
-                   ((uint32_t)__bfloat16_as_ushort(bf16_split_term(qh[2 * e + 1], term)) << 16);
+            w[e] = (uint32_t)__bfloat16_as_ushort(bf16_split_term(e8[2 * e], term)) |
+                   ((uint32_t)__bfloat16_as_ushort(bf16_split_term(e8[2 * e + 1], term)) << 16);
+          *reinterpret_cast<uint4*>(tcb + (size_t)sg * S::TC_BIMG + (ch / 8) * (S::TC_N * 128) +
+                                    sw128_offset(n, (ch % 8) * 8)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        *reinterpret_cast<uint4*>(tcb + (size_t)sg * S::TC_BIMG + (ch / 8) * (S::TC_N * 128) +
-                                  sw128_offset(n, (ch % 8) * 8)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       fence_proxy_async();
     }
@@ -572,46 +609,80 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     // each head's normaliser over the CTAs of the sequence, then the votes of my tokens for
     // heads [g0 G, g0 G + HW); eb holds my logits [token][HW]
     auto vote_pass = [&](const float* eb, int g0, int HW, int wv) {
-      float2* wz = reinterpret_cast<float2*>(ring);  // [segment][kMaxWaveHeads]: (max, 1 / sum)
-      for (int item = warp; item < sm.nseg * HW; item += S::NW) {
-        const int sg = item / HW, hl = item % HW;
+      float2* wz = reinterpret_cast<float2*>(ring);                // [segment][kMaxWaveHeads]: (max, 1 / sum)
+      float2* pc = wz + kMaxB * kMaxWaveHeads;                     // one segment's partials [head][cta]
+      for (int sg = 0; sg < sm.nseg; ++sg) {
         const SeqState& st = sm.seq[sm.seg_b[sg]];
-        const float2* pp = a.partials + (size_t)sm.seg_b[sg] * nCTA * H + g0 * G + hl;
-        float M = -INFINITY;
-        for (int cc = st.first_cta + lane; cc <= st.last_cta; cc += 32) M = fmaxf(M, __ldcg(pp + (size_t)cc * H).x);
-        M = warp_max(M);
-        KahanF kz;
-        if (M > -INFINITY)
-          for (int cc = st.first_cta + lane; cc <= st.last_cta; cc += 32) {
-            const float2 mz = __ldcg(pp + (size_t)cc * H);
-            if (mz.y > 0.f) kz.add(mz.y * expf(mz.x - M));
+        const int ncta = st.last_cta - st.first_cta + 1;
+        const int pstr = ncta | 1;                                 // odd row stride: lanes on distinct banks
+        const float2* pp = a.partials + ((size_t)sm.seg_b[sg] * nCTA + st.first_cta) * H + g0 * G;
+        for (int i0 = tid; i0 < ncta * HW; i0 += 4 * blockDim.x) {   // 4 loads in flight per thread
+          float2 v[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int i = i0 + k * blockDim.x;
+            if (i < ncta * HW) v[k] = __ldcg(pp + (size_t)(i / HW) * H + (i % HW));
           }
-        const double z = warp_sum_f64((double)kz.s - (double)kz.c);
-        if (lane == 0)
-          wz[sg * kMaxWaveHeads + hl] = (M > -INFINITY && z > 0.0) ? make_float2(M, (float)(1.0 / z))
-                                                                   : make_float2(INFINITY, 0.f);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int i = i0 + k * blockDim.x;
+            if (i < ncta * HW) pc[(i % HW) * pstr + i / HW] = v[k];
+          }
+        }
+        __syncthreads();
+        TS_MARK(13);
+        for (int hl = warp; hl < HW; hl += S::NW) {
+          float M = -INFINITY;
+          for (int cc = lane; cc < ncta; cc += 32) M = fmaxf(M, pc[hl * pstr + cc].x);
+          M = warp_max(M);
+          KahanF kz;
+          if (M > -INFINITY)
+            for (int cc = lane; cc < ncta; cc += 32) {
+              const float2 mz = pc[hl * pstr + cc];
+              if (mz.y > 0.f) kz.add(mz.y * expf(mz.x - M));
+            }
+          const float z = warp_sum_comp(kz.s, -kz.c);
+          if (lane == 0)
+            wz[sg * kMaxWaveHeads + hl] = (M > -INFINITY && z > 0.f) ? make_float2(M, 1.f / z)
+                                                                     : make_float2(INFINITY, 0.f);
+        }
+        __syncthreads();
+        TS_MARK(14);
       }
-      __syncthreads();
+      // v_i (+)= sum over the wave's heads of exp(l - M) / Z, compensated; a token's row is
+      // loaded whole before the sum
       for (int sg = 0; sg < sm.nseg; ++sg) {
         const int b = sm.seg_b[sg], t0 = sm.seg_t0[sg], nt = sm.seg_ntok[sg];
         float* vb = a.vote + (size_t)b * a.vote_stride + (size_t)sm.seg_lp0[sg] * S::P;
         const float2* w = wz + sg * kMaxWaveHeads;
-        for (int t = tid; t < nt; t += blockDim.x) {
-          const float* row = eb + (size_t)(t0 + t) * HW;
-          KahanF acc;
-          if ((HW & 3) == 0) {
-            for (int h4 = 0; h4 < HW; h4 += 4) {
-              const float4 x = *reinterpret_cast<const float4*>(row + h4);
-              acc.add(expf(x.x - w[h4].x) * w[h4].y);
-              acc.add(expf(x.y - w[h4 + 1].x) * w[h4 + 1].y);
-              acc.add(expf(x.z - w[h4 + 2].x) * w[h4 + 2].y);
-              acc.add(expf(x.w - w[h4 + 3].x) * w[h4 + 3].y);
-            }
-          } else {
-            for (int hl = 0; hl < HW; ++hl) acc.add(expf(row[hl] - w[hl].x) * w[hl].y);
+        if ((HW & 3) == 0) {
+          for (int t = tid; t < nt; t += blockDim.x) {
+            const float4* row = reinterpret_cast<const float4*>(eb + (size_t)(t0 + t) * HW);
+            float4 x[kMaxWaveHeads / 4];
+#pragma unroll
+            for (int q = 0; q < kMaxWaveHeads / 4; ++q)
+              if (4 * q < HW) x[q] = row[q];
+            KahanF acc;
+#pragma unroll
+            for (int q = 0; q < kMaxWaveHeads / 4; ++q)
+              if (4 * q < HW) {
+                const float2 w0 = w[4 * q], w1 = w[4 * q + 1], w2 = w[4 * q + 2], w3 = w[4 * q + 3];
+                acc.add(expf(x[q].x - w0.x) * w0.y);
+                acc.add(expf(x[q].y - w1.x) * w1.y);
+                acc.add(expf(x[q].z - w2.x) * w2.y);
+                acc.add(expf(x[q].w - w3.x) * w3.y);
+              }
+            const float v = acc.s - acc.c;
+            vb[t] = (wv == 0) ? v : vb[t] + v;
           }
-          const float v = acc.s - acc.c;
-          vb[t] = (wv == 0) ? v : vb[t] + v;
+        } else {
+          for (int t = tid; t < nt; t += blockDim.x) {
+            const float* row = eb + (size_t)(t0 + t) * HW;
+            KahanF acc;
+            for (int hl = 0; hl < HW; ++hl) acc.add(expf(row[hl] - w[hl].x) * w[hl].y);
+            const float v = acc.s - acc.c;
+            vb[t] = (wv == 0) ? v : vb[t] + v;
+          }
         }
       }
       __syncthreads();
@@ -801,8 +872,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           float2 mz = make_float2(-INFINITY, 0.f);
           if (lane < 16) mz = wpt[((size_t)sg * 128 + g * 16 + lane) * G + j];
           const float m = warp_max(mz.x);
-          const double z = warp_sum_f64((m > -INFINITY && mz.y > 0.f) ? (double)mz.y * (double)expf(mz.x - m) : 0.0);
-          if (lane == 0) a.partials[((size_t)sm.seg_b[sg] * nCTA + c) * H + h] = make_float2(m, (float)z);
+          const float z = warp_sum_comp((m > -INFINITY && mz.y > 0.f) ? mz.y * expf(mz.x - m) : 0.f);
+          if (lane == 0) a.partials[((size_t)sm.seg_b[sg] * nCTA + c) * H + h] = make_float2(m, z);
         }
         TS_MARK(3);
         if (!grid_sync(a.gsync, a.status)) return;
@@ -996,8 +1067,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           float2 mz = make_float2(-INFINITY, 0.f);
           if (lane < wph) mz = wp[((size_t)sg * S::NCW + gi * wph + lane) * G + w];
           const float m = warp_max(mz.x);
-          const double z = warp_sum_f64((m > -INFINITY && mz.y > 0.f) ? (double)mz.y * (double)expf(mz.x - m) : 0.0);
-          if (lane == 0) a.partials[((size_t)sm.seg_b[sg] * nCTA + c) * H + g0 * G + hl] = make_float2(m, (float)z);
+          const float z = warp_sum_comp((m > -INFINITY && mz.y > 0.f) ? mz.y * expf(mz.x - m) : 0.f);
+          if (lane == 0) a.partials[((size_t)sm.seg_b[sg] * nCTA + c) * H + g0 * G + hl] = make_float2(m, z);
         }
       }
       TS_MARK(3 + 3 * min(wv, 5));
@@ -1089,6 +1160,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         }
         __syncthreads();
       }
+      TS_MARK(28 + level);
       if (!grid_sync(a.gsync, a.status)) return;
       // every CTA finds the crossing bin of every unresolved sequence: the histograms of
       // a batch of sequences are read into shared memory at once, then one warp each scans
@@ -1435,6 +1507,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         }
         fdone += nf;
         cnt = nf;
+        TS_MARK(8);
         while (own && opos < own_n && cnt < around) {
           // one chunk of blockDim own tokens; take as many selected ones as fit
           const int i = opos + tid;
@@ -1461,6 +1534,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           }
           __syncthreads();
         }
+        TS_MARK(9);
         if (cnt == 0) break;                          // uniform: same counters in every thread
         // ---- gather K and V rows of every KV head
         if (tid == 0) mbar_arrive_expect_tx(&abar, (uint32_t)(cnt * S::TOKEN_BYTES));
@@ -1481,6 +1555,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         const bool landed = mbar_wait(&abar, aphase);
         aphase ^= 1u;
         ok = __syncthreads_and(landed) != 0;
+        TS_MARK(10);
         if (!ok) {
           if (tid == 0) {
             set_error(a.status, TS_ERR_TIMEOUT);
@@ -1489,14 +1564,11 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           __syncthreads();
           break;
         }
-        // ---- online softmax: warp -> KV head hw, tokens strided over that head's warps
-        for (int j0 = wslot * S::ATPW; j0 < cnt; j0 += wph * S::ATPW) {
-          const int j = j0 + tslot;
-          const bool act = j < cnt;
-          const int jj = act ? j : 0;
-          const KT* kr = Ks + ((size_t)jj * HKV + hw) * D + lt * S::AEPC;
-          const KT* vr = Vs + ((size_t)jj * HKV + hw) * D + lt * S::AEPC;
-          float kf[S::AEPC], vf[S::AEPC];
+        // ---- online softmax: warp -> KV head hw, tokens strided over that head's warps, two
+        // tokens per step (independent dot products, one rescale)
+        auto load_row = [&](int j, float (&kf)[S::AEPC], float (&vf)[S::AEPC]) {
+          const KT* kr = Ks + ((size_t)j * HKV + hw) * D + lt * S::AEPC;
+          const KT* vr = Vs + ((size_t)j * HKV + hw) * D + lt * S::AEPC;
           if constexpr (S::ACB == 16) {
             KV<KT>::unpack(lds128(kr), kf);
             KV<KT>::unpack(lds128(vr), vf);
@@ -1519,28 +1591,45 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
               vf[1] = __uint_as_float(v2.y);
             }
           }
-          float acc[S::GP];
+        };
+        const int jstep = wph * S::ATPW;
+        for (int j0 = wslot * S::ATPW; j0 < cnt; j0 += 2 * jstep) {
+          const int ja = j0 + tslot, jb = ja + jstep;
+          const bool la = ja < cnt && sm.tval[ja] >= 0 && (int64_t)sm.tval[ja] < a.num_pages;
+          const bool lb = jb < cnt && sm.tval[jb] >= 0 && (int64_t)sm.tval[jb] < a.num_pages;
+          float ka[S::AEPC], va[S::AEPC], kb[S::AEPC], vb_[S::AEPC];
+          load_row(ja < cnt ? ja : 0, ka, va);
+          load_row(jb < cnt ? jb : 0, kb, vb_);
+          float acca[S::GP], accb[S::GP];
 #pragma unroll
           for (int h = 0; h < S::GP; ++h) {
-            float x = 0.f;
+            float x = 0.f, y = 0.f;
 #pragma unroll
-            for (int e = 0; e < S::AEPC; ++e) x = fmaf(qr[h][e], kf[e], x);
-            acc[h] = x;
+            for (int e = 0; e < S::AEPC; ++e) {
+              x = fmaf(qr[h][e], ka[e], x);
+              y = fmaf(qr[h][e], kb[e], y);
+            }
+            acca[h] = x;
+            accb[h] = y;
           }
           int which;
-          const float red = transpose_reduce<S::GP, S::ALPT>(acc, lane, which);
-          const bool live = act && sm.tval[jj] >= 0 && (int64_t)sm.tval[jj] < a.num_pages;
+          const float reda = transpose_reduce<S::GP, S::ALPT>(acca, lane, which);
+          const float redb = transpose_reduce<S::GP, S::ALPT>(accb, lane, which);
 #pragma unroll
           for (int h = 0; h < G; ++h) {
-            const float dot = __shfl_sync(kFull, red, (lane & ~(S::ALPT - 1)) + h * (S::ALPT / S::GP));
-            if (live) {
-              const float sc = dot * a.scale;
-              const float mn = fmaxf(m_[h], sc);
-              const float corr = expf(m_[h] - mn);
-              const float p = expf(sc - mn);
-              l_[h] = l_[h] * corr + p;
+            const int src = (lane & ~(S::ALPT - 1)) + h * (S::ALPT / S::GP);
+            // every lane shuffles (the halves of a warp may hold different tokens), then selects
+            const float da = __shfl_sync(kFull, reda, src), db = __shfl_sync(kFull, redb, src);
+            const float sa = la ? da * a.scale : -INFINITY;
+            const float sb = lb ? db * a.scale : -INFINITY;
+            const float mn = fmaxf(m_[h], fmaxf(sa, sb));
+            if (mn > -INFINITY) {
+              const float corr = m_[h] > -INFINITY ? expf(m_[h] - mn) : 0.f;
+              const float pa = la ? expf(sa - mn) : 0.f;
+              const float pb = lb ? expf(sb - mn) : 0.f;
+              l_[h] = fmaf(l_[h], corr, pa + pb);
 #pragma unroll
-              for (int e = 0; e < S::AEPC; ++e) o_[h][e] = fmaf(p, vf[e], o_[h][e] * corr);
+              for (int e = 0; e < S::AEPC; ++e) o_[h][e] = fmaf(pb, vb_[e], fmaf(pa, va[e], o_[h][e] * corr));
               m_[h] = mn;
             }
           }
@@ -1551,6 +1640,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         if (tid == 0) atomicExch(&a.gsync->abort, 1u);   // the others leave the last barrier
         return;
       }
+      TS_MARK(11);
       // ---- this CTA's partial of every query head: merge all warps' token slots
       float* mg = reinterpret_cast<float*>(dsm);      // [NW*ATPW][G][D], then m and l
       const int slots = S::NW * S::ATPW;
@@ -1827,8 +1917,9 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   // ring slots of one stage of K each; the selection scratch and one
   // sequence's global histograms (with masses) alias the same space later
   const int nslot = std::min(kMaxSlots, (dyn - flag_cap) / S::STAGE_BYTES);
+  // (the vote pass keeps (max, 1/sum) per segment and head plus one segment's CTA partials)
   if (nslot < S::MIN_SLOTS || dyn - flag_cap < kSelScratch + kBins * 12 ||
-      dyn - flag_cap < kMaxB * kMaxWaveHeads * 8)
+      dyn - flag_cap < (kMaxB + ctx->num_sms + 1) * kMaxWaveHeads * 8)
     return TS_ERR_UNSUPPORTED;
   if (!ensure_smem<step_kernel<KT, D, HKV, G>>((size_t)dyn, ctx->device)) {
     if (std::getenv("TS_DEBUG")) std::fprintf(stderr, "ts step: smem attribute %d B refused\n", dyn);
@@ -1911,7 +2002,7 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
     const int nslot_tc = std::min(kMaxSlots, (dyn - flag_cap - 1024 - 2 * S::TC_BIMG) / S::TC_TILE);
     const char* no_tc_env = std::getenv("TOKENSELECT_NO_TC");   // =1: CUDA-core scan (comparisons, tests)
     const bool no_tc = no_tc_env && no_tc_env[0] == '1';
-    if (!no_tc && nslot_tc >= 2 && (c.phases & kPhScore) && c.k_pool) {
+    if (!no_tc && nslot_tc >= 2 && (c.phases & kPhScore) && c.k_pool && (reinterpret_cast<uintptr_t>(c.q) & 15) == 0) {
       auto& cache = ctx->kmaps;   // a few recent pools (one per layer in a decode loop)
       int hitc = -1;
       for (int i = 0; i < (int)(sizeof(cache) / sizeof(cache[0])); ++i)
