@@ -47,6 +47,7 @@ constexpr int kBins = 2048;
 constexpr int kMaxRound = 128;     // attention tokens per gather round
 constexpr int kMaxWaveHeads = 32;  // query heads of one scan wave
 constexpr int kMaxG = kMaxScanG;   // query heads per KV head
+constexpr int kMaxAttH = 64;       // query heads of the attention phase
 constexpr int kMaxPagesCta = 1024; // page ids of a CTA's range kept in shared memory
 constexpr int kMaxSlots = 12;      // ring slots (runtime count per launch)
 constexpr int64_t kLogitL2Budget = 48ll << 20;  // default bytes of logits one scan wave keeps in L2
@@ -63,6 +64,28 @@ constexpr int cpow2(int x) {
 constexpr int cmin(int a, int b) { return a < b ? a : b; }
 
 __device__ __forceinline__ unsigned long long to_fx(float v) { return __float2ull_rz(v * kFx); }
+
+// N consecutive K or V elements (fp32 or bf16) from shared memory as floats; the address is
+// aligned to N elements.
+template <typename KT, int N>
+__device__ __forceinline__ void load_elems(const KT* p, float (&f)[N]) {
+  if constexpr (sizeof(KT) == 4 && N == 4) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+  } else if constexpr (sizeof(KT) == 4 && N == 2) {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    f[0] = v.x; f[1] = v.y;
+  } else if constexpr (sizeof(KT) == 2 && N == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xffff0000u);
+    f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xffff0000u);
+  } else if constexpr (sizeof(KT) == 2 && N == 2) {
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+    f[0] = __uint_as_float(v << 16); f[1] = __uint_as_float(v & 0xffff0000u);
+  } else {
+    static_assert(N == 4 || N == 2, "load_elems width");
+  }
+}
 
 // ------------------------------------------------------------------ shapes
 
@@ -83,17 +106,11 @@ struct StepShape {
   static constexpr int ROW_BYTES = D * (int)sizeof(KT);
   static constexpr int STAGE_BYTES = HKV * P * ROW_BYTES; // H_kv (page, head) slabs of 16 rows
   static constexpr int MIN_SLOTS = 2;
-  // attention: a lane reads ACB bytes of a row; ALPT lanes per row
-  // (8-byte lane chunks keep the per-lane softmax state small: 17 warps leave 96 registers)
-  static constexpr int ACB = (D * (int)sizeof(KT) / 8 <= 32) ? 8 : 16;
-  static constexpr int ALPT = D * (int)sizeof(KT) / ACB;
-  static constexpr int AEPC = ACB / (int)sizeof(KT);
-  static constexpr int ATPW = 32 / ALPT;                  // tokens per warp step
   static constexpr int TOKEN_BYTES = 2 * HKV * ROW_BYTES; // K and V rows of every KV head
   static_assert(D % DPL == 0 && 32 % LPR == 0 && GP <= LPR, "scan lane split");
   static_assert(NCW >= 1 && (P * HKV) % NCW == 0 && ROWS % RPW == 0 && ITERS >= 1, "scan warp split");
   static_assert(NCW % HKV == 0 && P % ROWS == 0 || ROWS % P == 0, "rows of a warp stay in one page");
-  static_assert(32 % ALPT == 0 && GP <= ALPT, "attention lane split");
+  static_assert(GP <= 32, "attention reduction");
   // tensor-core scan (bf16 pages of 128 rows = H_kv x 16 tokens): one M = 128 tcgen05.mma
   // tile per page against all query heads, each split into three bf16 terms
   static constexpr bool TC = std::is_same<KT, __nv_bfloat16>::value && HKV * P == 128 && (D == 128 || D == 64) &&
@@ -291,6 +308,7 @@ struct Smem {
   int tot_c[kMaxB], tot_a[kMaxB];  // and of all CTAs
   int tie_base[kMaxB];             // exact ties in the CTAs before mine, per segment
   int filled[kMaxB], ctc[kMaxB];   // cache entry filled, its cached index count
+  float att_m[kMaxAttH], att_l[kMaxAttH], att_c[kMaxAttH];  // attention: running max, sum, round correction
   int use_tc;                      // this launch scans with the tensor cores
   uint32_t tmem;                   // TMEM base address of the accumulators
   int acc_tl[2], acc_nv[2], acc_sg[2];  // per accumulator buffer: first token, valid rows, segment
@@ -1440,16 +1458,22 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   float* ao = a.apart;                                                        // [B][nCTA][H][D]
   float2* aml = reinterpret_cast<float2*>(a.apart + (size_t)B * nCTA * H * D); // [B][nCTA][H] (max, sum)
   if (a.phases & kPhAttend) {
+    // Per gather round: (1) one warp per (token, KV head) pair writes the G scores to shared
+    // memory, (2) one warp per query head takes the round's max, turns scores into weights
+    // against a running (max, sum) and keeps the correction of earlier rounds, (3) each thread
+    // owns float4 slices of the output and adds the weighted V rows. The CTA's partial per
+    // head (o, max, sum) goes to scratch for the merge after the last barrier.
+    constexpr int HQ = HKV * G, EPL = D / 32, D4 = D / 4, NGRP = HQ * D4;
+    constexpr int NG = (NGRP + S::THREADS - 1) / S::THREADS;
+    static_assert(HQ <= kMaxAttH && D % 32 == 0, "attention layout");
     const bool given = !(a.phases & kPhSelect);
-    const int stage_bytes = a.dyn_bytes - a.flag_cap;
-    const int around = min(kMaxRound, stage_bytes / S::TOKEN_BYTES);
+    const int stage_bytes = a.dyn_bytes - a.flag_cap - HQ * D * 4;
+    const int around = min(kMaxRound, stage_bytes / (S::TOKEN_BYTES + HQ * 4));
     KT* Ks = reinterpret_cast<KT*>(dsm);
     KT* Vs = Ks + (size_t)around * HKV * D;
+    float* Ps = reinterpret_cast<float*>(Vs + (size_t)around * HKV * D);   // [around][HQ] scores, weights
+    float* Qs = Ps + (size_t)around * HQ;                                  // [HQ][D] this sequence's queries
     uint32_t aphase = 0;
-    const int hw = warp % HKV;                         // warp -> KV head
-    const int wslot = warp / HKV;
-    const int wph = (S::NW - hw + HKV - 1) / HKV;      // warps on head hw
-    const int lt = lane % S::ALPT, tslot = lane / S::ALPT;
     for (int b = 0; b < B; ++b) {
       const SeqState& st = sm.seq[b];
       const int32_t* gib = a.idx + (size_t)b * a.idx_stride;
@@ -1472,23 +1496,26 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       const int own_n = own ? sm.seg_ntok[sgi] : 0;
       const int own_lp0 = own ? sm.seg_lp0[sgi] : 0, own_t0 = own ? sm.seg_t0[sgi] : 0;
       const int nfix_mine = c < nfix ? (nfix - c + nCTA - 1) / nCTA : 0;
-      float qr[S::GP][S::AEPC];
-      float m_[G], l_[G], o_[G][S::AEPC];
+      for (int i0 = tid; i0 < HQ * D; i0 += 8 * blockDim.x) {   // eight loads in flight per thread
+        float qv[8];
 #pragma unroll
-      for (int j = 0; j < G; ++j) {
-        m_[j] = -INFINITY;
-        l_[j] = 0.f;
+        for (int k = 0; k < 8; ++k)
+          if (i0 + k * (int)blockDim.x < HQ * D) qv[k] = a.q[(size_t)b * HQ * D + i0 + k * blockDim.x];
 #pragma unroll
-        for (int e = 0; e < S::AEPC; ++e) o_[j][e] = 0.f;
+        for (int k = 0; k < 8; ++k)
+          if (i0 + k * (int)blockDim.x < HQ * D) Qs[i0 + k * blockDim.x] = qv[k];
       }
+      if (tid < HQ) {
+        sm.att_m[tid] = -INFINITY;
+        sm.att_l[tid] = 0.f;
+      }
+      float4 o[NG];
 #pragma unroll
-      for (int j = 0; j < S::GP; ++j)
-#pragma unroll
-        for (int e = 0; e < S::AEPC; ++e)
-          qr[j][e] = (j < G) ? a.q[((size_t)b * H + hw * G + j) * D + lt * S::AEPC + e] : 0.f;
+      for (int k = 0; k < NG; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       int fdone = 0;     // fixed tokens of mine already taken
       int opos = 0;      // next own token (segment-local) to examine
       bool ok = true;
+      __syncthreads();
       while (true) {
         // ---- this round's tokens: fixed share first, then own selected ones
         int cnt = 0;
@@ -1507,7 +1534,6 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         }
         fdone += nf;
         cnt = nf;
-        TS_MARK(8);
         while (own && opos < own_n && cnt < around) {
           // one chunk of blockDim own tokens; take as many selected ones as fit
           const int i = opos + tid;
@@ -1564,74 +1590,68 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           __syncthreads();
           break;
         }
-        // ---- online softmax: warp -> KV head hw, tokens strided over that head's warps, two
-        // tokens per step (independent dot products, one rescale)
-        auto load_row = [&](int j, float (&kf)[S::AEPC], float (&vf)[S::AEPC]) {
-          const KT* kr = Ks + ((size_t)j * HKV + hw) * D + lt * S::AEPC;
-          const KT* vr = Vs + ((size_t)j * HKV + hw) * D + lt * S::AEPC;
-          if constexpr (S::ACB == 16) {
-            KV<KT>::unpack(lds128(kr), kf);
-            KV<KT>::unpack(lds128(vr), vf);
-          } else {
-            const uint2 k2 = *reinterpret_cast<const uint2*>(kr);
-            const uint2 v2 = *reinterpret_cast<const uint2*>(vr);
-            if constexpr (sizeof(KT) == 2) {
-              kf[0] = __uint_as_float(k2.x << 16);
-              kf[1] = __uint_as_float(k2.x & 0xffff0000u);
-              kf[2] = __uint_as_float(k2.y << 16);
-              kf[3] = __uint_as_float(k2.y & 0xffff0000u);
-              vf[0] = __uint_as_float(v2.x << 16);
-              vf[1] = __uint_as_float(v2.x & 0xffff0000u);
-              vf[2] = __uint_as_float(v2.y << 16);
-              vf[3] = __uint_as_float(v2.y & 0xffff0000u);
-            } else {
-              kf[0] = __uint_as_float(k2.x);
-              kf[1] = __uint_as_float(k2.y);
-              vf[0] = __uint_as_float(v2.x);
-              vf[1] = __uint_as_float(v2.y);
-            }
-          }
-        };
-        const int jstep = wph * S::ATPW;
-        for (int j0 = wslot * S::ATPW; j0 < cnt; j0 += 2 * jstep) {
-          const int ja = j0 + tslot, jb = ja + jstep;
-          const bool la = ja < cnt && sm.tval[ja] >= 0 && (int64_t)sm.tval[ja] < a.num_pages;
-          const bool lb = jb < cnt && sm.tval[jb] >= 0 && (int64_t)sm.tval[jb] < a.num_pages;
-          float ka[S::AEPC], va[S::AEPC], kb[S::AEPC], vb_[S::AEPC];
-          load_row(ja < cnt ? ja : 0, ka, va);
-          load_row(jb < cnt ? jb : 0, kb, vb_);
-          float acca[S::GP], accb[S::GP];
+        // ---- (1) scores: warp per (token, KV head); lane holds EPL dims, the G dot products
+        // are reduced across the warp so that lane `which` ends with head `which`
+        for (int p = warp; p < cnt * HKV; p += S::NW) {
+          const int j = p / HKV, g = p % HKV;
+          float kf[EPL];
+          load_elems<KT, EPL>(Ks + ((size_t)j * HKV + g) * D + lane * EPL, kf);
+          float acc[S::GP];
 #pragma unroll
           for (int h = 0; h < S::GP; ++h) {
-            float x = 0.f, y = 0.f;
+            float x = 0.f;
+            if (h < G) {
+              const float* qh = Qs + (size_t)(g * G + h) * D + lane * EPL;
 #pragma unroll
-            for (int e = 0; e < S::AEPC; ++e) {
-              x = fmaf(qr[h][e], ka[e], x);
-              y = fmaf(qr[h][e], kb[e], y);
+              for (int e = 0; e < EPL; ++e) x = fmaf(qh[e], kf[e], x);
             }
-            acca[h] = x;
-            accb[h] = y;
+            acc[h] = x;
           }
           int which;
-          const float reda = transpose_reduce<S::GP, S::ALPT>(acca, lane, which);
-          const float redb = transpose_reduce<S::GP, S::ALPT>(accb, lane, which);
+          const float dot = transpose_reduce<S::GP, 32>(acc, lane, which);
+          const bool live = sm.tval[j] >= 0 && (int64_t)sm.tval[j] < a.num_pages;
+          if ((lane & (32 / S::GP - 1)) == 0 && which < G) Ps[j * HQ + g * G + which] = live ? dot * a.scale : -INFINITY;
+        }
+        __syncthreads();
+        // ---- (2) weights: warp per query head
+        for (int h = warp; h < HQ; h += S::NW) {
+          float mr = -INFINITY;
+          for (int t = lane; t < cnt; t += 32) mr = fmaxf(mr, Ps[t * HQ + h]);
+          mr = warp_max(mr);
+          const float mo = sm.att_m[h], mn = fmaxf(mo, mr);
+          float sum = 0.f;
+          for (int t = lane; t < cnt; t += 32) {
+            const float w = mn > -INFINITY ? expf(Ps[t * HQ + h] - mn) : 0.f;
+            Ps[t * HQ + h] = w;
+            sum += w;
+          }
+          sum = warp_sum_comp(sum);
+          if (lane == 0) {
+            const float corr = mo > -INFINITY ? expf(mo - mn) : 0.f;
+            sm.att_c[h] = corr;
+            sm.att_l[h] = fmaf(sm.att_l[h], corr, sum);
+            sm.att_m[h] = mn;
+          }
+        }
+        __syncthreads();
+        // ---- (3) outputs: thread -> float4 slices (head, 4 dims)
 #pragma unroll
-          for (int h = 0; h < G; ++h) {
-            const int src = (lane & ~(S::ALPT - 1)) + h * (S::ALPT / S::GP);
-            // every lane shuffles (the halves of a warp may hold different tokens), then selects
-            const float da = __shfl_sync(kFull, reda, src), db = __shfl_sync(kFull, redb, src);
-            const float sa = la ? da * a.scale : -INFINITY;
-            const float sb = lb ? db * a.scale : -INFINITY;
-            const float mn = fmaxf(m_[h], fmaxf(sa, sb));
-            if (mn > -INFINITY) {
-              const float corr = m_[h] > -INFINITY ? expf(m_[h] - mn) : 0.f;
-              const float pa = la ? expf(sa - mn) : 0.f;
-              const float pb = lb ? expf(sb - mn) : 0.f;
-              l_[h] = fmaf(l_[h], corr, pa + pb);
-#pragma unroll
-              for (int e = 0; e < S::AEPC; ++e) o_[h][e] = fmaf(pb, vb_[e], fmaf(pa, va[e], o_[h][e] * corr));
-              m_[h] = mn;
+        for (int k = 0; k < NG; ++k) {
+          const int qd = tid + k * S::THREADS;
+          if (qd < NGRP) {
+            const int h = qd / D4, d4 = qd % D4, g = h / G;
+            const float corr = sm.att_c[h];
+            float4 acc = make_float4(o[k].x * corr, o[k].y * corr, o[k].z * corr, o[k].w * corr);
+            for (int t = 0; t < cnt; ++t) {
+              const float w = Ps[t * HQ + h];
+              float vf[4];
+              load_elems<KT, 4>(Vs + ((size_t)t * HKV + g) * D + d4 * 4, vf);
+              acc.x = fmaf(w, vf[0], acc.x);
+              acc.y = fmaf(w, vf[1], acc.y);
+              acc.z = fmaf(w, vf[2], acc.z);
+              acc.w = fmaf(w, vf[3], acc.w);
             }
+            o[k] = acc;
           }
         }
         __syncthreads();
@@ -1641,43 +1661,15 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         return;
       }
       TS_MARK(11);
-      // ---- this CTA's partial of every query head: merge all warps' token slots
-      float* mg = reinterpret_cast<float*>(dsm);      // [NW*ATPW][G][D], then m and l
-      const int slots = S::NW * S::ATPW;
-      float* mm = mg + (size_t)slots * G * D;
-      float* ml = mm + slots * G;
-      const int myslot = warp * S::ATPW + tslot;
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int e = 0; e < S::AEPC; ++e) mg[((size_t)myslot * G + h) * D + lt * S::AEPC + e] = o_[h][e];
-        if (lt == 0) {
-          mm[myslot * G + h] = m_[h];
-          ml[myslot * G + h] = l_[h];
-        }
-      }
-      __syncthreads();
+      // ---- this CTA's partial of every query head
       float* pb = ao + ((size_t)b * nCTA + c) * H * D;
       float2* pml = aml + ((size_t)b * nCTA + c) * H;
-      for (int i = tid; i < HKV * G * D; i += blockDim.x) {
-        const int hg = i / (G * D), rem = i % (G * D), h = rem / D, d = rem % D;
-        float M = -INFINITY;
-        for (int w = hg; w < S::NW; w += HKV)
-          for (int ts = 0; ts < S::ATPW; ++ts) M = fmaxf(M, mm[(w * S::ATPW + ts) * G + h]);
-        float num = 0.f, den = 0.f;
-        if (M > -INFINITY) {
-          for (int w = hg; w < S::NW; w += HKV)
-            for (int ts = 0; ts < S::ATPW; ++ts) {
-              const int sl = w * S::ATPW + ts;
-              const float wgt = expf(mm[sl * G + h] - M);
-              num = fmaf(wgt, mg[((size_t)sl * G + h) * D + d], num);
-              den = fmaf(wgt, ml[sl * G + h], den);
-            }
-        }
-        const int qh = hg * G + h;
-        pb[(size_t)qh * D + d] = num;
-        if (d == 0) pml[qh] = make_float2(M, den);
+#pragma unroll
+      for (int k = 0; k < NG; ++k) {
+        const int qd = tid + k * S::THREADS;
+        if (qd < NGRP) reinterpret_cast<float4*>(pb)[qd] = o[k];
       }
+      if (tid < HQ) pml[tid] = make_float2(sm.att_m[tid], sm.att_l[tid]);
       __syncthreads();
     }
   }
