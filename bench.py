@@ -49,6 +49,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-baseline-only", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--case", choices=sorted(CASES),
                    help="run --steps decode steps of one workload and exit (for ncu captures; no timing)")
+    p.add_argument("--phases", action="store_true",
+                   help="with --case: print CTA 0's phase timestamps of each step (persistent kernel)")
     return p.parse_args(argv)
 
 
@@ -67,9 +69,31 @@ def case_main(args):
     if sp.mode == "topp":
         raise SystemExit("the top-p workload has no graph bench yet")
     b = DecodeBench(sp, "cuda:0", theta=theta)
-    b.run(args.steps, 0, flush=False)
+    if args.phases:
+        for i in range(args.steps):
+            b.run(1, 0, flush=True, start=i)
+            print_phases(b, i)
+    else:
+        b.run(args.steps, 0, flush=False)
     torch.cuda.synchronize()
     print(f"case {args.case}: {args.steps} steps, kernels per step {b.kernels_per_step}")
+
+
+# phase boundaries the persistent kernel records (CTA 0, %globaltimer) when it ends a phase
+PHASES = {0: "start", 1: "setup", 5: "lengths", 6: "cache-test", 7: "partition", 2: "scanned",
+          3: "stats", 4: "scan-barrier", 13: "vote-partials", 14: "vote-norm", 20: "votes",
+          28: "hist0", 29: "hist1", 30: "hist2", 21: "levels", 22: "candidates", 23: "flags",
+          10: "gathered", 9: "rounds", 11: "attended", 24: "partials", 25: "last-barrier",
+          26: "merged", 27: "end"}
+
+
+def print_phases(b, step):
+    """One line: microseconds since kernel start at each recorded phase boundary (last layer)."""
+    ph = b.T.ts_debug_phase_ns(b.ctx.handle)
+    t0 = ph[0]
+    pts = sorted((v - t0, i) for i, v in enumerate(ph) if v and i in PHASES and v >= t0)
+    hit = bool(b.hit[b.sp.layers - 1][0])
+    print(f"step {step} hit={hit}: " + " ".join(f"{PHASES[i]} {dt / 1000:.1f}" for dt, i in pts))
 
 
 # ------------------------------------------------------------ distributed
@@ -190,11 +214,21 @@ def score_traffic():
     return None
 
 
+STEP_SOURCES = ("ts_step.cu", "ts_tc.cuh", "ts_common.cuh", "ts_internal.h")
+
+
+def step_source_sha256() -> str:
+    """Digest of the sources the persistent step kernel is compiled from."""
+    h = hashlib.sha256()
+    for fn in STEP_SOURCES:
+        h.update(open(os.path.join(ROOT, "token_level_sparse_gb300", "csrc", fn), "rb").read())
+    return h.hexdigest()
+
+
 def step_traffic():
     """Per-launch DRAM bytes of the persistent step kernel at 128K (miss step) from the
     committed ncu summary, or None when absent or taken on another kernel revision."""
-    src = open(os.path.join(ROOT, "token_level_sparse_gb300", "csrc", "ts_step.cu"), "rb").read()
-    sha = hashlib.sha256(src).hexdigest()
+    sha = step_source_sha256()
     prof = os.path.join(ROOT, "profiles")
     if not os.path.isdir(prof):
         return None
@@ -280,8 +314,9 @@ class DecodeBench:
         gather = sum(int(c) * row * 2 for c in counts)
         return scan, gather
 
-    def run(self, steps, warmup, flush=True):
-        """Runs warmup + steps graph replays; returns per-step device times and kernel times."""
+    def run(self, steps, warmup, flush=True, start=0):
+        """Runs warmup + steps graph replays (trajectory steps from `start`); returns per-step
+        device times and kernel times."""
         torch, T = self.torch, self.T
         if self.graph is None:
             self.capture()
@@ -289,7 +324,7 @@ class DecodeBench:
         rec = []
         L, B = self.sp.layers, self.sp.batch
         for i in range(warmup + steps):
-            t = i % self.sp.steps
+            t = (start + i) % self.sp.steps
             if t == 0:
                 self.cache.reset()
             self._stage(t)

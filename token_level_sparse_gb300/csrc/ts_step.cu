@@ -325,10 +325,12 @@ struct Smem {
 
 // --------------------------------------------------------------- the kernel
 
-// CTA 0 records the time it reaches phase boundary i (0..31): 0 start, 1 set-up done,
-// 2 + 3 w / 3 + 3 w / 4 + 3 w scan wave w done / partials written / barrier passed,
-// 20 score done, 28 + l histogram level l built, 21 levels done, 22 candidates, 23 select
-// done, 24 attend done, 25 last barrier, 26 merged, 27 end.
+// CTA 0 records the time it reaches phase boundary i (0..31), for diagnosis: 0 start, 5 lengths
+// read, 6 cache test, 7 partition, 1 set-up done; scan wave w: 2 + 3 w scanned, 3 + 3 w
+// statistics, 4 + 3 w barrier passed; 13 / 14 vote partials / normalisers, 20 votes done;
+// 28 + l histogram level l built, 21 levels, 22 candidates, 23 flags; 10 last gather landed,
+// 9 last round list built, 11 attended, 24 partials written, 25 last barrier, 26 merged, 27
+// end. (The marks of waves past the first share slots 5..19 with the others.)
 #define TS_MARK(i)                                                     \
   do {                                                                 \
     if (c == 0 && tid == 0 && a.phase_ns) a.phase_ns[i] = globaltimer_ns(); \
@@ -426,7 +428,6 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         xy = warp_sum(xy);
         xx = warp_sum(xx);
         yy = warp_sum(yy);
-        TS_MARK(12);
         if (lane == 0) {
           cr[(b * 3 + 0) * S::NW + warp] = xy;
           cr[(b * 3 + 1) * S::NW + warp] = xx;
