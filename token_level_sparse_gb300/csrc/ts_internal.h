@@ -73,7 +73,7 @@ struct ts_ctx {
   unsigned* cand_n = nullptr;            // [max_batch]
   unsigned long long* cands = nullptr;   // [max_batch][2048]
   int* cta_cnt = nullptr;                // [max_batch][num_sms][3]
-  float* apart = nullptr;                // [max_batch][num_sms][H][d] outputs, then [..][H] (max, sum)
+  float* apart = nullptr;                // attention partials: o [B][H][num_sms][d], (max, sum) [B][H][even]
   struct KMap {                          // encoded TMA tensor maps of recent K pools
     const void* pool = nullptr;
     int64_t num_pages = 0;
@@ -105,6 +105,7 @@ namespace ts {
 // Counter slots per sequence: [0] score, [1] select, [2 .. 2+H_kv) attention.
 constexpr int kCounterSlots = 2 + 64;
 constexpr int kMaxScanWarps = 16;  // warps of the persistent step kernel's scan
+constexpr int kStepHistPerSeq = 16384 + 128 + 2048 + 64;  // persistent kernel radix histogram bins per sequence
 constexpr int kMaxScanG = 8;       // query heads per KV head the persistent kernel supports
 
 struct ScoreCall {

@@ -43,7 +43,6 @@ namespace {
 
 constexpr int kMaxB = 64;          // sequences per call (= most segments one CTA can touch)
 constexpr int kCandCap = 2048;     // candidates gathered per sequence
-constexpr int kBins = 2048;
 constexpr int kMaxRound = 128;     // attention tokens per gather round
 constexpr int kMaxWaveHeads = 32;  // query heads of one scan wave
 constexpr int kMaxG = kMaxScanG;   // query heads per KV head
@@ -51,7 +50,17 @@ constexpr int kMaxAttH = 64;       // query heads of the attention phase
 constexpr int kMaxPagesCta = 1024; // page ids of a CTA's range kept in shared memory
 constexpr int kMaxSlots = 12;      // ring slots (runtime count per launch)
 constexpr int64_t kLogitL2Budget = 48ll << 20;  // default bytes of logits one scan wave keeps in L2
-constexpr int kSelScratch = kBins * 12 + kCandCap * 8;  // CTA histogram and candidates while selecting
+// radix levels over the vote bits (votes are >= +0, bit 31 is always 0): bits 30..17, 16..6,
+// 5..0. The first level is fine enough that its crossing bin usually holds few enough tokens
+// to gather them as candidates at once (the votes of long sequences lie close together).
+__host__ __device__ constexpr int lvl_shift(int l) { return l == 0 ? 17 : (l == 1 ? 6 : 0); }
+__host__ __device__ constexpr int lvl_bins(int l) { return l == 0 ? 16384 : (l == 1 ? 2048 : 64); }
+// per sequence: level 0 fine [16384], its coarse sums [128] (fine bins 128 c .. 128 c + 127),
+// level 1 [2048], level 2 [64]
+constexpr int kCoarseOff = 16384;
+__host__ __device__ constexpr int lvl_off(int l) { return l == 0 ? 0 : (l == 1 ? 16384 + 128 : 16384 + 128 + 2048); }
+constexpr int kHistPerSeq = kStepHistPerSeq;            // 16384 + 128 + 2048 + 64
+static_assert(lvl_off(2) + lvl_bins(2) == kHistPerSeq, "histogram layout");
 constexpr float kFx = 1099511627776.0f;  // 2^40
 constexpr int kPhCheck = 1, kPhScore = 2, kPhSelect = 4, kPhAttend = 8;
 constexpr int kSmemLimit = 232448;  // bytes of shared memory per CTA on sm_103a
@@ -111,6 +120,7 @@ struct StepShape {
   static_assert(NCW >= 1 && (P * HKV) % NCW == 0 && ROWS % RPW == 0 && ITERS >= 1, "scan warp split");
   static_assert(NCW % HKV == 0 && P % ROWS == 0 || ROWS % P == 0, "rows of a warp stay in one page");
   static_assert(GP <= 32, "attention reduction");
+  static_assert((HKV * G) % 2 == 0, "rows of H (max, sum) pairs are whole 16-byte blocks");
   // tensor-core scan (bf16 pages of 128 rows = H_kv x 16 tokens): one M = 128 tcgen05.mma
   // tile per page against all query heads, each split into three bf16 terms
   static constexpr bool TC = std::is_same<KT, __nv_bfloat16>::value && HKV * P == 128 && (D == 128 || D == 64) &&
@@ -167,8 +177,8 @@ struct StepKArgs {
   float* lse;
   // scratch
   float2* partials;            // [B][nCTA][H]
-  unsigned* hist;              // [3][B][kBins]
-  unsigned long long* mass;    // [3][B][kBins]
+  unsigned* hist;              // [B][kHistPerSeq]: level l at lvl_off(l)
+  unsigned long long* mass;    // [B][kHistPerSeq]
   unsigned* cand_n;            // [B]
   unsigned long long* cands;   // [B][kCandCap]  (key << 32 | ~index)
   int* cta_cnt;                // [B][nCTA][3]  cand-range selected, all selected, ties
@@ -199,7 +209,7 @@ __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
 
 // All CTAs of the cooperative grid meet here. False after a time-out or an
 // abort raised by another CTA; the caller then returns.
-__device__ bool grid_sync(GridSync* gs, int* status) {
+__device__ __noinline__ bool grid_sync(GridSync* gs, int* status) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -249,7 +259,7 @@ __device__ __forceinline__ int reduce_slot(int lane) {
 }
 
 // Block-wide exclusive scan of one int per thread; total in *total.
-__device__ __forceinline__ int block_scan(int x, int* wsum, int& total) {
+__device__ __noinline__ int block_scan(int x, int* wsum, int& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   int inc = x;
 #pragma unroll
@@ -274,6 +284,85 @@ __device__ __forceinline__ int block_scan(int x, int* wsum, int& total) {
   const int r = wsum[warp] + inc - x;
   total = wsum[32];
   __syncthreads();
+  return r;
+}
+
+// The crossing bin of a histogram scan.
+struct Cross {
+  int bin;                       // bin index, -1 when the total falls short
+  unsigned before_c;             // count of everything above it (including the start count)
+  unsigned long long before_m;   // fixed-point mass of everything above it
+  unsigned hc;                   // its own count
+};
+
+// One warp scans a histogram in shared memory from its highest bin down, starting from the
+// count c0 and mass m0 of everything above the histogram's range, and returns the first bin
+// where the cumulative count reaches need_c (top-k) or the cumulative mass reaches need_m
+// (top-p). nbins is a power of two >= 32. Every lane returns the same result.
+__device__ __noinline__ Cross find_crossing(const unsigned* hc_, const unsigned long long* hm_, int nbins, bool topp,
+                                            unsigned c0, unsigned long long m0, unsigned need_c,
+                                            unsigned long long need_m) {
+  const int lane = threadIdx.x & 31;
+  // lane L sums the bins nbins-1-(L*per + j), j < per (descending vote); the start is rotated
+  // by the lane so that the lanes hit different banks
+  const int per = nbins / 32;
+  unsigned cnt = 0;
+  unsigned long long ms = 0;
+  for (int jj = 0; jj < per; ++jj) {
+    const int j = (jj + lane) & (per - 1);
+    const int bin = nbins - 1 - (lane * per + j);
+    cnt += hc_[bin];
+    if (topp) ms += hm_[bin];
+  }
+  unsigned ic = cnt;
+  unsigned long long im = ms;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const unsigned oc = __shfl_up_sync(kFull, ic, d);
+    const unsigned long long om = __shfl_up_sync(kFull, im, d);
+    if (lane >= d) {
+      ic += oc;
+      im += om;
+    }
+  }
+  const bool crosses = topp ? (m0 + im - ms < need_m && m0 + im >= need_m) : (c0 + ic - cnt < need_c && c0 + ic >= need_c);
+  const unsigned ballot = __ballot_sync(kFull, crosses);
+  Cross r{-1, 0u, 0ull, 0u};
+  if (ballot == 0u) return r;
+  const int L = __ffs(ballot) - 1;
+  unsigned cb = c0 + __shfl_sync(kFull, ic - cnt, L);
+  unsigned long long mb = m0 + __shfl_sync(kFull, im - ms, L);
+  // the crossing lane's bins, 32 at a time, by the whole warp
+  for (int j0 = 0; j0 < per; j0 += 32) {
+    const int j = j0 + lane;
+    const int bin = nbins - 1 - (L * per + j);
+    const bool in = j < per;
+    const unsigned hc = in ? hc_[bin] : 0u;
+    const unsigned long long hm = (in && topp) ? hm_[bin] : 0ull;
+    unsigned xc = hc;
+    unsigned long long xm = hm;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const unsigned oc = __shfl_up_sync(kFull, xc, d);
+      const unsigned long long om = __shfl_up_sync(kFull, xm, d);
+      if (lane >= d) {
+        xc += oc;
+        xm += om;
+      }
+    }
+    const bool here = in && (topp ? (mb + xm >= need_m) : (cb + xc >= need_c));
+    const unsigned hb = __ballot_sync(kFull, here);
+    if (hb) {
+      const int f = __ffs(hb) - 1;
+      r.bin = __shfl_sync(kFull, bin, f);
+      r.before_c = __shfl_sync(kFull, cb + xc - hc, f);
+      r.before_m = __shfl_sync(kFull, mb + xm - hm, f);
+      r.hc = __shfl_sync(kFull, hc, f);
+      return r;
+    }
+    cb += __shfl_sync(kFull, xc, 31);
+    mb += __shfl_sync(kFull, xm, 31);
+  }
   return r;
 }
 
@@ -308,6 +397,9 @@ struct Smem {
   int tot_c[kMaxB], tot_a[kMaxB];  // and of all CTAs
   int tie_base[kMaxB];             // exact ties in the CTAs before mine, per segment
   int filled[kMaxB], ctc[kMaxB];   // cache entry filled, its cached index count
+  int x_bin[kMaxB];                // selection: crossing coarse bin of level 0, and the
+  unsigned x_c[kMaxB];             // count and mass above it
+  unsigned long long x_m[kMaxB];
   float att_m[kMaxAttH], att_l[kMaxAttH], att_c[kMaxAttH];  // attention: running max, sum, round correction
   int use_tc;                      // this launch scans with the tensor cores
   uint32_t tmem;                   // TMEM base address of the accumulators
@@ -346,6 +438,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   __shared__ __align__(8) uint64_t accf[2], acce[2];   // accumulator buffer written / read out
   __shared__ __align__(8) uint64_t drainb;            // every MMA issued has completed
   __shared__ __align__(8) uint64_t abar;
+  __shared__ __align__(8) uint64_t xbar;              // bulk copies of partials (vote, merge)
 
   const int nslot = a.nslot;
   unsigned char* ring = dsm;                                               // nslot x STAGE_BYTES of K
@@ -357,6 +450,22 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, nCTA = gridDim.x;
   const int B = a.B, H = a.H;
+  // Whole-CTA fetch of up to two contiguous global blocks (written by other CTAs before a grid
+  // barrier) into shared memory by bulk copy; false (and a recorded time-out) if they do not land.
+  uint32_t xph = 0;
+  auto bulk_fetch = [&](void* d0, const void* s0, uint32_t n0, void* d1, const void* s1, uint32_t n1) -> bool {
+    if (tid == 0) {
+      fence_proxy_async_global();
+      mbar_arrive_expect_tx(&xbar, n0 + n1);
+      bulk_g2s(d0, s0, n0, &xbar);
+      if (n1) bulk_g2s(d1, s1, n1, &xbar);
+    }
+    const bool landed = mbar_wait(&xbar, xph);
+    xph ^= 1u;
+    const bool ok = __syncthreads_and(landed) != 0;
+    if (!ok && tid == 0) set_error(a.status, TS_ERR_TIMEOUT);
+    return ok;
+  };
 
   TS_MARK(0);
   if (tid == 0) {
@@ -372,6 +481,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     }
     mbar_init(&drainb, 1);
     mbar_init(&abar, 1);
+    mbar_init(&xbar, 1);
     mbar_fence_init();
     sm.timed_out = 0;
   }
@@ -379,6 +489,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   // ------------------------------------------------ setup: lengths, cache test, partition
   // one round of independent loads per sequence: length, cache entry state
   const bool have_cache = a.ct != nullptr && a.filled != nullptr;
+  #pragma unroll 1
   for (int b = tid; b < B; b += blockDim.x) {
     int n = a.seq_lens[b];
     if (n < 0 || n > a.max_tokens) {
@@ -412,6 +523,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     int* cn = reinterpret_cast<int*>(cr + (size_t)B * 3 * S::NW);     // [B][2][NW]
     const bool check = (a.phases & kPhCheck) != 0;
     const int HD = H * D;
+    #pragma unroll 1
     for (int b = 0; b < B; ++b) {
       if (!sm.filled[b]) continue;
       if (check) {
@@ -451,6 +563,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       }
     }
     __syncthreads();
+    #pragma unroll 1
     for (int b = tid; b < B; b += blockDim.x) {
       if (!sm.filled[b]) continue;
       if (check) {
@@ -477,6 +590,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   TS_MARK(6);
   if (tid == 0) {
     int pg = 0;
+    #pragma unroll 1
     for (int b = 0; b < B; ++b) {
       SeqState& st = sm.seq[b];
       st.pg0 = pg;
@@ -500,6 +614,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     sm.p0 = min(ptot, c * ppc);
     sm.p1 = min(ptot, sm.p0 + ppc);
     sm.tok_stride = ppc * S::P;
+    #pragma unroll 1
     for (int b = 0; b < B; ++b) {
       SeqState& st = sm.seq[b];
       if (st.pg1 > st.pg0) {
@@ -511,6 +626,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       }
     }
     int ns = 0;
+    #pragma unroll 1
     for (int b = 0; b < B; ++b) {
       const SeqState& st = sm.seq[b];
       const int lo = max(st.pg0, sm.p0), hi = min(st.pg1, sm.p1);
@@ -530,6 +646,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     if constexpr (S::TC) {
       use_tc = a.tc && (a.phases & kPhScore) && H <= kMaxWaveHeads;
       int prev = -1, prev2 = -1;
+      #pragma unroll 1
       for (int b = 0; b < B && use_tc; ++b) {
         const SeqState& st = sm.seq[b];
         if (st.pg1 <= st.pg0) continue;
@@ -564,6 +681,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   TS_MARK(7);
   if (c == 0 && tid < B && (a.phases & kPhCheck) && a.hit_out) a.hit_out[tid] = (uint8_t)sm.seq[tid].hit;
   // page ids of my range, read once (ring refills and attention gathers need no global load)
+  #pragma unroll 1
   for (int i = tid; i < min(sm.p1 - sm.p0, kMaxPagesCta); i += blockDim.x) {
     const int gp = sm.p0 + i;
     int sg = 0;
@@ -573,7 +691,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   }
   if (a.phases & kPhSelect) {
     // zero the selection histograms (first touched after a barrier)
-    const size_t nh = (size_t)3 * B * kBins;
+    const size_t nh = (size_t)B * kHistPerSeq;
+    #pragma unroll 1
     for (size_t i = (size_t)c * blockDim.x + tid; i < nh; i += (size_t)nCTA * blockDim.x) {
       a.hist[i] = 0u;
       if (a.mode == TS_SELECT_TOPP) a.mass[i] = 0ull;
@@ -586,6 +705,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       // query head h, K-major in the 128-byte swizzle layout; rows past 3 H are zero
       constexpr int CH = D / 8;                        // 16-byte chunks of a row
       const int total = sm.nseg * S::TC_N * CH;
+      #pragma unroll 1
       for (int i0 = tid; i0 < total; i0 += 2 * blockDim.x) {   // two chunks' loads in flight
         float4 qv[2][2];
 #pragma unroll
@@ -627,42 +747,47 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   if ((a.phases & kPhScore) && sm.ptot > 0) {   // nothing to scan when every sequence hits
     // each head's normaliser over the CTAs of the sequence, then the votes of my tokens for
     // heads [g0 G, g0 G + HW); eb holds my logits [token][HW]
-    auto vote_pass = [&](const float* eb, int g0, int HW, int wv) {
+    auto vote_pass = [&](const float* eb, int g0, int HW, int wv) -> bool {
       float2* wz = reinterpret_cast<float2*>(ring);                // [segment][kMaxWaveHeads]: (max, 1 / sum)
-      float2* pc = wz + kMaxB * kMaxWaveHeads;                     // one segment's partials [head][cta]
+      float2* pcs = wz + kMaxB * kMaxWaveHeads;                    // one segment's partials [cta][H]
+      #pragma unroll 1
       for (int sg = 0; sg < sm.nseg; ++sg) {
         const SeqState& st = sm.seq[sm.seg_b[sg]];
         const int ncta = st.last_cta - st.first_cta + 1;
-        const int pstr = ncta | 1;                                 // odd row stride: lanes on distinct banks
-        const float2* pp = a.partials + ((size_t)sm.seg_b[sg] * nCTA + st.first_cta) * H + g0 * G;
-        for (int i0 = tid; i0 < ncta * HW; i0 += 4 * blockDim.x) {   // 4 loads in flight per thread
-          float2 v[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int i = i0 + k * blockDim.x;
-            if (i < ncta * HW) v[k] = __ldcg(pp + (size_t)(i / HW) * H + (i % HW));
-          }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int i = i0 + k * blockDim.x;
-            if (i < ncta * HW) pc[(i % HW) * pstr + i / HW] = v[k];
-          }
+        float* rmx = reinterpret_cast<float*>(pcs + (size_t)ncta * H);   // [NW][32] per-slice maxima
+        float* rz = rmx + S::NW * 32;                                    // [NW][32] per-slice sums
+        if (!bulk_fetch(pcs, a.partials + ((size_t)sm.seg_b[sg] * nCTA + st.first_cta) * H,
+                        (uint32_t)(ncta * H * sizeof(float2)), nullptr, nullptr, 0u)) {
+          if (tid == 0) atomicExch(&a.gsync->abort, 1u);
+          return false;
         }
-        __syncthreads();
         TS_MARK(13);
-        for (int hl = warp; hl < HW; hl += S::NW) {
-          float M = -INFINITY;
-          for (int cc = lane; cc < ncta; cc += 32) M = fmaxf(M, pc[hl * pstr + cc].x);
-          M = warp_max(M);
-          KahanF kz;
-          if (M > -INFINITY)
-            for (int cc = lane; cc < ncta; cc += 32) {
-              const float2 mz = pc[hl * pstr + cc];
-              if (mz.y > 0.f) kz.add(mz.y * expf(mz.x - M));
-            }
-          const float z = warp_sum_comp(kz.s, -kz.c);
-          if (lane == 0)
-            wz[sg * kMaxWaveHeads + hl] = (M > -INFINITY && z > 0.f) ? make_float2(M, 1.f / z)
+        // lane = head of the wave, warp = a slice of the CTAs: conflict-free rows of H pairs
+        const int per = (ncta + S::NW - 1) / S::NW;
+        const int c0 = min(ncta, warp * per), c1 = min(ncta, c0 + per);
+        const bool lh = lane < HW;
+        float m = -INFINITY;
+        if (lh)
+          #pragma unroll 1
+          for (int cc = c0; cc < c1; ++cc) m = fmaxf(m, pcs[cc * H + g0 * G + lane].x);
+        rmx[warp * 32 + lane] = m;
+        __syncthreads();
+        float M = -INFINITY;
+        for (int w = 0; w < S::NW; ++w) M = fmaxf(M, rmx[w * 32 + lane]);
+        KahanF kz;
+        if (lh && M > -INFINITY)
+          #pragma unroll 1
+          for (int cc = c0; cc < c1; ++cc) {
+            const float2 mz = pcs[cc * H + g0 * G + lane];
+            if (mz.y > 0.f) kz.add(mz.y * expf(mz.x - M));
+          }
+        rz[warp * 32 + lane] = kz.s - kz.c;
+        __syncthreads();
+        if (warp == 0 && lh) {
+          KahanF z;
+          for (int w = 0; w < S::NW; ++w) z.add(rz[w * 32 + lane]);
+          const float Z = z.s - z.c;
+          wz[sg * kMaxWaveHeads + lane] = (M > -INFINITY && Z > 0.f) ? make_float2(M, 1.f / Z)
                                                                      : make_float2(INFINITY, 0.f);
         }
         __syncthreads();
@@ -670,34 +795,47 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       }
       // v_i (+)= sum over the wave's heads of exp(l - M) / Z, compensated; a token's row is
       // loaded whole before the sum
+      #pragma unroll 1
       for (int sg = 0; sg < sm.nseg; ++sg) {
         const int b = sm.seg_b[sg], t0 = sm.seg_t0[sg], nt = sm.seg_ntok[sg];
         float* vb = a.vote + (size_t)b * a.vote_stride + (size_t)sm.seg_lp0[sg] * S::P;
         const float2* w = wz + sg * kMaxWaveHeads;
         if ((HW & 3) == 0) {
+          #pragma unroll 1
           for (int t = tid; t < nt; t += blockDim.x) {
             const float4* row = reinterpret_cast<const float4*>(eb + (size_t)(t0 + t) * HW);
             float4 x[kMaxWaveHeads / 4];
 #pragma unroll
             for (int q = 0; q < kMaxWaveHeads / 4; ++q)
               if (4 * q < HW) x[q] = row[q];
-            KahanF acc;
+            // the wave's terms in registers, summed as a pairwise tree (error a few ulp; no
+            // serial compensation chain)
+            float e[kMaxWaveHeads];
 #pragma unroll
-            for (int q = 0; q < kMaxWaveHeads / 4; ++q)
-              if (4 * q < HW) {
-                const float2 w0 = w[4 * q], w1 = w[4 * q + 1], w2 = w[4 * q + 2], w3 = w[4 * q + 3];
-                acc.add(expf(x[q].x - w0.x) * w0.y);
-                acc.add(expf(x[q].y - w1.x) * w1.y);
-                acc.add(expf(x[q].z - w2.x) * w2.y);
-                acc.add(expf(x[q].w - w3.x) * w3.y);
-              }
+            for (int q = 0; q < kMaxWaveHeads / 4; ++q) {
+              const bool in = 4 * q < HW;
+              const float2 w0 = w[in ? 4 * q : 0], w1 = w[in ? 4 * q + 1 : 0], w2 = w[in ? 4 * q + 2 : 0],
+                           w3 = w[in ? 4 * q + 3 : 0];
+              e[4 * q] = in ? expf(x[q].x - w0.x) * w0.y : 0.f;
+              e[4 * q + 1] = in ? expf(x[q].y - w1.x) * w1.y : 0.f;
+              e[4 * q + 2] = in ? expf(x[q].z - w2.x) * w2.y : 0.f;
+              e[4 * q + 3] = in ? expf(x[q].w - w3.x) * w3.y : 0.f;
+            }
+#pragma unroll
+            for (int half = kMaxWaveHeads / 2; half >= 1; half >>= 1)
+#pragma unroll
+              for (int i = 0; i < half; ++i) e[i] += e[i + half];
+            KahanF acc;
+            acc.add(e[0]);
             const float v = acc.s - acc.c;
             vb[t] = (wv == 0) ? v : vb[t] + v;
           }
         } else {
+          #pragma unroll 1
           for (int t = tid; t < nt; t += blockDim.x) {
             const float* row = eb + (size_t)(t0 + t) * HW;
             KahanF acc;
+            #pragma unroll 1
             for (int hl = 0; hl < HW; ++hl) acc.add(expf(row[hl] - w[hl].x) * w[hl].y);
             const float v = acc.s - acc.c;
             vb[t] = (wv == 0) ? v : vb[t] + v;
@@ -705,6 +843,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         }
       }
       __syncthreads();
+      return true;
     };
     bool scanned = false;
     if constexpr (S::TC) {
@@ -886,6 +1025,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         }
         TS_MARK(2);
         // ---- per (segment, head): combine the 16 rows' (max, sum exp) -> partials
+        #pragma unroll 1
         for (int item = warp; item < sm.nseg * H; item += S::NW) {
           const int sg = item / H, h = item % H, g = h / G, j = h % G;
           float2 mz = make_float2(-INFINITY, 0.f);
@@ -894,10 +1034,11 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           const float z = warp_sum_comp((m > -INFINITY && mz.y > 0.f) ? mz.y * expf(mz.x - m) : 0.f);
           if (lane == 0) a.partials[((size_t)sm.seg_b[sg] * nCTA + c) * H + h] = make_float2(m, z);
         }
+        fence_proxy_async_global();
         TS_MARK(3);
         if (!grid_sync(a.gsync, a.status)) return;
         TS_MARK(4);
-        vote_pass(eb, 0, H, 0);
+        if (!vote_pass(eb, 0, H, 0)) return;
       }
     }
     if (!scanned) {
@@ -1090,11 +1231,12 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           if (lane == 0) a.partials[((size_t)sm.seg_b[sg] * nCTA + c) * H + g0 * G + hl] = make_float2(m, z);
         }
       }
+      fence_proxy_async_global();
       TS_MARK(3 + 3 * min(wv, 5));
       if (!grid_sync(a.gsync, a.status)) return;
       TS_MARK(4 + 3 * min(wv, 5));
 
-      vote_pass(eb, g0, HW, wv);
+      if (!vote_pass(eb, g0, HW, wv)) return;
     }
     }
   }
@@ -1105,16 +1247,16 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     if (!(a.phases & kPhScore) && sm.ptot > 0) {
       if (!grid_sync(a.gsync, a.status)) return;   // the histograms are zero everywhere
     }
-    // shared memory while selecting: this CTA's histogram (counts, masses), the gathered
-    // candidates, then the global histograms of a batch of sequences
+    // shared memory while selecting, one use after another: this CTA's histogram (counts,
+    // then masses at a fixed offset); after the barrier, the global histograms of a batch of
+    // sequences; later the gathered candidates
     unsigned* sh = reinterpret_cast<unsigned*>(ring);
-    unsigned long long* smh = reinterpret_cast<unsigned long long*>(ring + kBins * sizeof(unsigned));
-    unsigned long long* scand = reinterpret_cast<unsigned long long*>(ring + kBins * 12);
-    unsigned char* bat = ring + kSelScratch;
+    unsigned long long* smh = reinterpret_cast<unsigned long long*>(ring + lvl_bins(0) * sizeof(unsigned));
+    unsigned long long* scand = reinterpret_cast<unsigned long long*>(ring);
+    unsigned char* bat = ring;
     const bool topp = a.mode == TS_SELECT_TOPP;
-    const int per_seq = kBins * (topp ? 12 : 4);
-    const int room = max(1, (a.dyn_bytes - a.flag_cap - kSelScratch) / per_seq);
     if (tid == 0) {
+      #pragma unroll 1
       for (int b = 0; b < B; ++b) {
         SeqState& st = sm.seq[b];
         const int len = st.hi - st.lo;
@@ -1137,30 +1279,38 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       }
     }
     __syncthreads();
+#pragma unroll 1   // one copy of the level code: it runs once per level and is fetched cold
     for (int level = 0; level < 3; ++level) {
       if (tid == 0) {
         int any = 0;
+        #pragma unroll 1
         for (int b = 0; b < B; ++b) any |= !sm.seq[b].done;
         sm.flag = any;
       }
       __syncthreads();
       if (!sm.flag) break;                     // identical in every CTA
-      const int shift = level == 0 ? 21 : (level == 1 ? 10 : 0);
-      const int nbins = level == 2 ? 1024 : kBins;
-      unsigned* gh = a.hist + (size_t)level * B * kBins;
-      unsigned long long* gm = a.mass + (size_t)level * B * kBins;
+      const int shift = lvl_shift(level), nbins = lvl_bins(level);
+      unsigned* gh = a.hist + lvl_off(level);                  // + b * kHistPerSeq
+      unsigned long long* gm = a.mass + lvl_off(level);
+      const int room = max(1, (a.dyn_bytes - a.flag_cap) / (nbins * (topp ? 12 : 4)));
+      #pragma unroll 1
       for (int sg = 0; sg < sm.nseg; ++sg) {
         const int b = sm.seg_b[sg];
         const SeqState& st = sm.seq[b];
         if (st.done) continue;
-        for (int i = tid; i < nbins; i += blockDim.x) {
-          sh[i] = 0u;
-          if (topp) smh[i] = 0ull;
+        #pragma unroll 1
+        for (int i = tid; i < nbins / 4; i += blockDim.x) {
+          reinterpret_cast<uint4*>(sh)[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (topp) {
+            reinterpret_cast<uint4*>(smh)[2 * i] = make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4*>(smh)[2 * i + 1] = make_uint4(0u, 0u, 0u, 0u);
+          }
         }
         __syncthreads();
         const int tl0 = sm.seg_lp0[sg] * S::P;
         const int lo = max(st.lo, tl0), hi = min(st.hi, tl0 + sm.seg_ntok[sg]);
         const float* vb = a.vote + (size_t)b * a.vote_stride;
+        #pragma unroll 4
         for (int t = lo + tid; t < hi; t += blockDim.x) {
           const float v = __ldcg(vb + t);
           const uint32_t key = __float_as_uint(v);
@@ -1171,134 +1321,183 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           }
         }
         __syncthreads();
+        #pragma unroll 1
         for (int i = tid; i < nbins; i += blockDim.x) {
           if (sh[i]) {
-            atomicAdd(&gh[(size_t)b * kBins + i], sh[i]);
-            if (topp) atomicAdd(&gm[(size_t)b * kBins + i], smh[i]);
+            atomicAdd(&gh[(size_t)b * kHistPerSeq + i], sh[i]);
+            if (topp) atomicAdd(&gm[(size_t)b * kHistPerSeq + i], smh[i]);
+          }
+        }
+        if (level == 0) {
+          // coarse sums of 128 fine bins, one warp each, added once per CTA
+          #pragma unroll 1
+          for (int cbn = warp; cbn < 128; cbn += S::NW) {
+            const uint4 v = reinterpret_cast<const uint4*>(sh + cbn * 128)[lane];
+            const unsigned scn = __reduce_add_sync(kFull, v.x + v.y + v.z + v.w);
+            unsigned long long smm = 0ull;
+            if (topp) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) smm += smh[cbn * 128 + lane * 4 + j];
+#pragma unroll
+              for (int d = 16; d >= 1; d >>= 1) smm += __shfl_xor_sync(kFull, smm, d);
+            }
+            if (lane == 0 && scn) {
+              atomicAdd(&a.hist[(size_t)b * kHistPerSeq + kCoarseOff + cbn], scn);
+              if (topp) atomicAdd(&a.mass[(size_t)b * kHistPerSeq + kCoarseOff + cbn], smm);
+            }
           }
         }
         __syncthreads();
       }
+      fence_proxy_async_global();   // the histograms are read back by bulk copy
       TS_MARK(28 + level);
       if (!grid_sync(a.gsync, a.status)) return;
-      // every CTA finds the crossing bin of every unresolved sequence: the histograms of
-      // a batch of sequences are read into shared memory at once, then one warp each scans
-      for (int b0 = 0; b0 < B; b0 += room) {
-        const int nb = min(room, B - b0);
-        unsigned* bc = reinterpret_cast<unsigned*>(bat);                                  // [nb][nbins]
-        unsigned long long* bm = reinterpret_cast<unsigned long long*>(bat + (size_t)room * kBins * 4);
-#pragma unroll 4
-        for (int i = tid; i < nb * nbins; i += blockDim.x) {
-          const int bi = i / nbins, bin = i % nbins;
-          if (sm.seq[b0 + bi].done) continue;
-          bc[i] = __ldcg(&gh[(size_t)(b0 + bi) * kBins + bin]);
-          if (topp) bm[i] = __ldcg(&gm[(size_t)(b0 + bi) * kBins + bin]);
+      // every CTA finds the crossing bin of every unresolved sequence from shared copies of
+      // the global histograms (bulk copies); level 0 in two steps: its 128 coarse bins, then
+      // the 128 fine bins of the crossing coarse bin
+      auto apply = [&](SeqState& st, int bin, const Cross& r) {   // lane 0 of the scanning warp
+        st.prefix |= (uint32_t)bin << shift;
+        st.mask |= (uint32_t)(nbins - 1) << shift;
+        st.n_gt += (int)r.before_c;
+        if (topp)
+          st.mass_rem = st.mass_rem - r.before_m;
+        else
+          st.k_rem = st.k_rem - (int)r.before_c;
+        if (r.hc <= (unsigned)kCandCap) {
+          st.cand = 1;
+          st.done = 1;
+        } else if (level == 2) {
+          st.tie_mode = 1;
+          st.done = 1;
+          if (!topp) {
+            st.ties = st.k_rem;
+          } else {
+            const unsigned long long tfx = to_fx(__uint_as_float(st.prefix));
+            const unsigned long long t = tfx ? (st.mass_rem + tfx - 1) / tfx : (unsigned long long)r.hc;
+            st.ties = (int)(t < r.hc ? t : r.hc);
+          }
         }
-        __syncthreads();
-        for (int bi = warp; bi < nb; bi += S::NW) {
-          SeqState& st = sm.seq[b0 + bi];
+      };
+      // whole CTA: one bulk-copy transaction of a 128-bin block (counts, masses) per unresolved
+      // sequence, at block offset off(b) of its histogram
+      auto fetch128 = [&](unsigned* dc, unsigned long long* dm, auto off) -> bool {
+        if (tid == 0) {
+          uint32_t bytes = 0;
+          #pragma unroll 1
+          for (int b = 0; b < B; ++b)
+            if (!sm.seq[b].done) bytes += topp ? 128u * 12u : 128u * 4u;
+          fence_proxy_async_global();
+          mbar_arrive_expect_tx(&xbar, bytes);
+          #pragma unroll 1
+          for (int b = 0; b < B; ++b) {
+            if (sm.seq[b].done) continue;
+            bulk_g2s(dc + b * 128, a.hist + (size_t)b * kHistPerSeq + off(b), 512u, &xbar);
+            if (topp) bulk_g2s(dm + b * 128, a.mass + (size_t)b * kHistPerSeq + off(b), 1024u, &xbar);
+          }
+        }
+        const bool landed = mbar_wait(&xbar, xph);
+        xph ^= 1u;
+        if (__syncthreads_and(landed)) return true;
+        if (tid == 0) {
+          set_error(a.status, TS_ERR_TIMEOUT);
+          atomicExch(&a.gsync->abort, 1u);
+        }
+        return false;
+      };
+      if (level == 0) {
+        unsigned* cc_ = reinterpret_cast<unsigned*>(bat);                                   // [B][128]
+        unsigned long long* cm_ = reinterpret_cast<unsigned long long*>(bat + (size_t)B * 512);
+        if (!fetch128(cc_, cm_, [](int) { return kCoarseOff; })) return;
+        #pragma unroll 1
+        for (int b = warp; b < B; b += S::NW) {
+          SeqState& st = sm.seq[b];
           if (st.done) continue;
-          const unsigned* hc_ = bc + (size_t)bi * nbins;
-          const unsigned long long* hm_ = bm + (size_t)bi * nbins;
-          // lane L sums the bins nbins-1-(L*per + j), j < per (descending vote); the start is
-          // rotated by the lane so that the lanes hit different banks
-          const int per = nbins / 32;
-          unsigned cnt = 0;
-          unsigned long long ms = 0;
-          for (int jj = 0; jj < per; ++jj) {
-            const int j = (jj + lane) & (per - 1);
-            const int bin = nbins - 1 - (lane * per + j);
-            cnt += hc_[bin];
-            if (topp) ms += hm_[bin];
-          }
-          unsigned ic = cnt;
-          unsigned long long im = ms;
-#pragma unroll
-          for (int d = 1; d < 32; d <<= 1) {
-            const unsigned oc = __shfl_up_sync(kFull, ic, d);
-            const unsigned long long om = __shfl_up_sync(kFull, im, d);
-            if (lane >= d) {
-              ic += oc;
-              im += om;
-            }
-          }
-          const unsigned need_c = (unsigned)st.k_rem;
-          const unsigned long long need_m = st.mass_rem;
-          const bool crosses = topp ? (im - ms < need_m && im >= need_m) : (ic - cnt < need_c && ic >= need_c);
-          const unsigned ballot = __ballot_sync(kFull, crosses);
-          if (ballot == 0u) {
-            if (lane == 0) {  // top-p whose fixed-point total falls short: the whole domain
+          const Cross r = find_crossing(cc_ + b * 128, cm_ + b * 128, 128, topp, 0u, 0ull, (unsigned)st.k_rem,
+                                        st.mass_rem);
+          if (lane == 0) {
+            if (r.bin < 0) {        // top-p whose fixed-point total falls short: the whole domain
               st.all = 1;
               st.done = 1;
+            } else {
+              sm.x_bin[b] = r.bin;
+              sm.x_c[b] = r.before_c;
+              sm.x_m[b] = r.before_m;
             }
-            continue;
-          }
-          const int L = __ffs(ballot) - 1;
-          unsigned cb = __shfl_sync(kFull, ic - cnt, L);
-          unsigned long long mb = __shfl_sync(kFull, im - ms, L);
-          // the crossing lane's bins, 32 at a time, by the whole warp
-          for (int j0 = 0; j0 < per; j0 += 32) {
-            const int j = j0 + lane;
-            const int bin = nbins - 1 - (L * per + j);
-            const bool in = j < per;
-            const unsigned hc = in ? hc_[bin] : 0u;
-            const unsigned long long hm = (in && topp) ? hm_[bin] : 0ull;
-            unsigned xc = hc;
-            unsigned long long xm = hm;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-              const unsigned oc = __shfl_up_sync(kFull, xc, d);
-              const unsigned long long om = __shfl_up_sync(kFull, xm, d);
-              if (lane >= d) {
-                xc += oc;
-                xm += om;
-              }
-            }
-            const bool here = in && (topp ? (mb + xm >= need_m) : (cb + xc >= need_c));
-            const unsigned hb = __ballot_sync(kFull, here);
-            if (hb) {
-              if (lane == __ffs(hb) - 1) {
-                const unsigned before_c = cb + xc - hc;
-                const unsigned long long before_m = mb + xm - hm;
-                st.prefix |= (uint32_t)bin << shift;
-                st.mask |= (uint32_t)(nbins - 1) << shift;
-                st.n_gt += (int)before_c;
-                if (topp)
-                  st.mass_rem = need_m - before_m;
-                else
-                  st.k_rem = (int)(need_c - before_c);
-                if (hc <= (unsigned)kCandCap) {
-                  st.cand = 1;
-                  st.done = 1;
-                } else if (level == 2) {
-                  st.tie_mode = 1;
-                  st.done = 1;
-                  if (!topp) {
-                    st.ties = st.k_rem;
-                  } else {
-                    const unsigned long long tfx = to_fx(__uint_as_float(st.prefix));
-                    const unsigned long long t = tfx ? (st.mass_rem + tfx - 1) / tfx : (unsigned long long)hc;
-                    st.ties = (int)(t < hc ? t : hc);
-                  }
-                }
-              }
-              break;
-            }
-            cb += __shfl_sync(kFull, xc, 31);
-            mb += __shfl_sync(kFull, xm, 31);
           }
         }
         __syncthreads();
+        if (!fetch128(cc_, cm_, [&](int b) { return sm.x_bin[b] * 128; })) return;
+        #pragma unroll 1
+        for (int b = warp; b < B; b += S::NW) {
+          SeqState& st = sm.seq[b];
+          if (st.done) continue;
+          const Cross r = find_crossing(cc_ + b * 128, cm_ + b * 128, 128, topp, sm.x_c[b], sm.x_m[b],
+                                        (unsigned)st.k_rem, st.mass_rem);
+          if (lane == 0 && r.bin >= 0) apply(st, sm.x_bin[b] * 128 + r.bin, r);
+        }
+        __syncthreads();
+      } else {
+        const int room = max(1, (a.dyn_bytes - a.flag_cap) / (nbins * (topp ? 12 : 4)));
+        #pragma unroll 1
+        for (int b0 = 0; b0 < B; b0 += room) {
+          const int nb = min(room, B - b0);
+          unsigned* bc = reinterpret_cast<unsigned*>(bat);                                  // [nb][nbins]
+          unsigned long long* bm = reinterpret_cast<unsigned long long*>(bat + (size_t)room * nbins * 4);
+          if (tid == 0) {
+            uint32_t bytes = 0;
+            #pragma unroll 1
+            for (int bi = 0; bi < nb; ++bi)
+              if (!sm.seq[b0 + bi].done) bytes += (uint32_t)nbins * (topp ? 12u : 4u);
+            fence_proxy_async_global();
+            mbar_arrive_expect_tx(&xbar, bytes);
+            #pragma unroll 1
+            for (int bi = 0; bi < nb; ++bi) {
+              if (sm.seq[b0 + bi].done) continue;
+              bulk_g2s(bc + (size_t)bi * nbins, gh + (size_t)(b0 + bi) * kHistPerSeq, (uint32_t)nbins * 4u, &xbar);
+              if (topp)
+                bulk_g2s(bm + (size_t)bi * nbins, gm + (size_t)(b0 + bi) * kHistPerSeq, (uint32_t)nbins * 8u, &xbar);
+            }
+          }
+          {
+            const bool landed = mbar_wait(&xbar, xph);
+            xph ^= 1u;
+            if (!__syncthreads_and(landed)) {
+              if (tid == 0) {
+                set_error(a.status, TS_ERR_TIMEOUT);
+                atomicExch(&a.gsync->abort, 1u);
+              }
+              return;
+            }
+          }
+          #pragma unroll 1
+          for (int bi = warp; bi < nb; bi += S::NW) {
+            SeqState& st = sm.seq[b0 + bi];
+            if (st.done) continue;
+            const Cross r = find_crossing(bc + (size_t)bi * nbins, bm + (size_t)bi * nbins, nbins, topp, 0u, 0ull,
+                                          (unsigned)st.k_rem, st.mass_rem);
+            if (lane == 0) {
+              if (r.bin < 0) {
+                st.all = 1;
+                st.done = 1;
+              } else {
+                apply(st, r.bin, r);
+              }
+            }
+          }
+          __syncthreads();
+        }
       }
     }
 
     TS_MARK(21);
     // ---- gather the crossing-bin tokens (candidates); per-CTA exact-tie counts
     int need_cand = 0, need_tie = 0;
+    #pragma unroll 1
     for (int b = 0; b < B; ++b) {
       need_cand |= sm.seq[b].cand;
       need_tie |= sm.seq[b].tie_mode;
     }
+    #pragma unroll 1
     for (int sg = 0; sg < sm.nseg; ++sg) {
       const int b = sm.seg_b[sg];
       const SeqState& st = sm.seq[b];
@@ -1307,6 +1506,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       const int lo = max(st.lo, tl0), hi = min(st.hi, tl0 + sm.seg_ntok[sg]);
       const float* vb = a.vote + (size_t)b * a.vote_stride;
       int n_eq = 0;
+      #pragma unroll 2
       for (int t0 = lo; t0 < hi; t0 += blockDim.x) {
         const int t = t0 + tid;
         bool is = false;
@@ -1340,11 +1540,13 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     }
     if (need_tie) {
       // exact ties before mine, per segment, one warp each
+      #pragma unroll 1
       for (int sg = warp; sg < sm.nseg; sg += S::NW) {
         const int b = sm.seg_b[sg];
         const SeqState& st = sm.seq[b];
         int s = 0;
         if (st.tie_mode)
+          #pragma unroll 1
           for (int cc = st.first_cta + lane; cc < c; cc += 32) s += __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 3 + 2]);
         s = warp_sum_i(s);
         if (lane == 0) sm.tie_base[sg] = s;
@@ -1354,6 +1556,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
 
     TS_MARK(22);
     // ---- the selection flag of each of my tokens, and the counts for output positions
+    #pragma unroll 1
     for (int sg = 0; sg < sm.nseg; ++sg) {
       const int b = sm.seg_b[sg];
       const SeqState& st = sm.seq[b];
@@ -1361,9 +1564,11 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       const float* vb = a.vote + (size_t)b * a.vote_stride;
       int tie_base = st.tie_mode ? sm.tie_base[sg] : 0;
       const int m_cand = st.cand ? (int)min(__ldcg(&a.cand_n[b]), (unsigned)kCandCap) : 0;
+      #pragma unroll 4
       for (int j = tid; j < m_cand; j += blockDim.x) scand[j] = __ldcg(&a.cands[(size_t)b * kCandCap + j]);
       __syncthreads();
       int n_sel_cand = 0, n_sel_all = 0;
+      #pragma unroll 1
       for (int base = 0; base < nt; base += blockDim.x) {
         const int i = base + tid;
         const int t = tl0 + i;
@@ -1391,6 +1596,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         if (st.cand) {
           int nr;
           const int rr = block_scan(rank_me ? 1 : 0, sm.wsum, nr);
+          #pragma unroll 1
           for (int r0 = 0; r0 < nr; r0 += kMaxRound) {
             const int nrr = min(kMaxRound, nr - r0);
             const int rrr = rr - r0;
@@ -1399,12 +1605,14 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
               sm.tval[rrr] = (int)key;
             }
             __syncthreads();
+            #pragma unroll 1
             for (int q = warp; q < nrr; q += S::NW) {
               const int ii = sm.toks[q];
               const uint32_t kk = (uint32_t)sm.tval[q];
               const unsigned long long me = ((unsigned long long)kk << 32) | (0xffffffffu - (uint32_t)(tl0 + ii));
               unsigned above = 0;
               unsigned long long cum = 0;
+              #pragma unroll 1
               for (int j = lane; j < m_cand; j += 32) {
                 const unsigned long long y = scand[j];
                 if (y > me) {
@@ -1456,8 +1664,11 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   // My tokens per sequence: a round-robin share of the fixed ones (sinks and
   // window, the cached part of a hit, or the caller's index list) and my own
   // selected candidates; gathered by bulk copy; one partial per CTA and head.
-  float* ao = a.apart;                                                        // [B][nCTA][H][D]
-  float2* aml = reinterpret_cast<float2*>(a.apart + (size_t)B * nCTA * H * D); // [B][nCTA][H] (max, sum)
+  // attention partials, each (sequence, head) contiguous for one bulk copy in the merge:
+  // o [B][H][nCTA][D], then (max, sum) [B][H][nCTAp] (nCTAp even: 16-byte blocks)
+  const int nCTAp = (nCTA + 1) & ~1;
+  float* ao = a.apart;
+  float2* aml = reinterpret_cast<float2*>(a.apart + (size_t)B * H * nCTA * D);
   if (a.phases & kPhAttend) {
     // Per gather round: (1) one warp per (token, KV head) pair writes the G scores to shared
     // memory, (2) one warp per query head takes the round's max, turns scores into weights
@@ -1475,6 +1686,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     float* Ps = reinterpret_cast<float*>(Vs + (size_t)around * HKV * D);   // [around][HQ] scores, weights
     float* Qs = Ps + (size_t)around * HQ;                                  // [HQ][D] this sequence's queries
     uint32_t aphase = 0;
+    #pragma unroll 1
     for (int b = 0; b < B; ++b) {
       const SeqState& st = sm.seq[b];
       const int32_t* gib = a.idx + (size_t)b * a.idx_stride;
@@ -1497,6 +1709,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       const int own_n = own ? sm.seg_ntok[sgi] : 0;
       const int own_lp0 = own ? sm.seg_lp0[sgi] : 0, own_t0 = own ? sm.seg_t0[sgi] : 0;
       const int nfix_mine = c < nfix ? (nfix - c + nCTA - 1) / nCTA : 0;
+      #pragma unroll 1
       for (int i0 = tid; i0 < HQ * D; i0 += 8 * blockDim.x) {   // eight loads in flight per thread
         float qv[8];
 #pragma unroll
@@ -1521,6 +1734,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         // ---- this round's tokens: fixed share first, then own selected ones
         int cnt = 0;
         const int nf = min(around, nfix_mine - fdone);
+        #pragma unroll 1
         for (int i = tid; i < nf; i += blockDim.x) {
           const int f = c + (fdone + i) * nCTA;
           int t;
@@ -1566,6 +1780,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         // ---- gather K and V rows of every KV head
         if (tid == 0) mbar_arrive_expect_tx(&abar, (uint32_t)(cnt * S::TOKEN_BYTES));
         __syncthreads();
+        #pragma unroll 1
         for (int i = tid; i < 2 * cnt * HKV; i += blockDim.x) {
           const int ti = i / (2 * HKV), rem = i % (2 * HKV), g = rem >> 1, isv = rem & 1;
           const int t = sm.toks[ti];
@@ -1593,6 +1808,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         }
         // ---- (1) scores: warp per (token, KV head); lane holds EPL dims, the G dot products
         // are reduced across the warp so that lane `which` ends with head `which`
+        #pragma unroll 1
         for (int p = warp; p < cnt * HKV; p += S::NW) {
           const int j = p / HKV, g = p % HKV;
           float kf[EPL];
@@ -1615,12 +1831,15 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         }
         __syncthreads();
         // ---- (2) weights: warp per query head
+        #pragma unroll 1
         for (int h = warp; h < HQ; h += S::NW) {
           float mr = -INFINITY;
+          #pragma unroll 1
           for (int t = lane; t < cnt; t += 32) mr = fmaxf(mr, Ps[t * HQ + h]);
           mr = warp_max(mr);
           const float mo = sm.att_m[h], mn = fmaxf(mo, mr);
           float sum = 0.f;
+          #pragma unroll 1
           for (int t = lane; t < cnt; t += 32) {
             const float w = mn > -INFINITY ? expf(Ps[t * HQ + h] - mn) : 0.f;
             Ps[t * HQ + h] = w;
@@ -1643,6 +1862,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
             const int h = qd / D4, d4 = qd % D4, g = h / G;
             const float corr = sm.att_c[h];
             float4 acc = make_float4(o[k].x * corr, o[k].y * corr, o[k].z * corr, o[k].w * corr);
+            #pragma unroll 1
             for (int t = 0; t < cnt; ++t) {
               const float w = Ps[t * HQ + h];
               float vf[4];
@@ -1662,15 +1882,17 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         return;
       }
       TS_MARK(11);
-      // ---- this CTA's partial of every query head
-      float* pb = ao + ((size_t)b * nCTA + c) * H * D;
-      float2* pml = aml + ((size_t)b * nCTA + c) * H;
+      // ---- this CTA's partial of every query head (read back by bulk copy after the barrier)
 #pragma unroll
       for (int k = 0; k < NG; ++k) {
         const int qd = tid + k * S::THREADS;
-        if (qd < NGRP) reinterpret_cast<float4*>(pb)[qd] = o[k];
+        if (qd < NGRP) {
+          const int h = qd / D4, d4 = qd % D4;
+          reinterpret_cast<float4*>(ao + (((size_t)b * H + h) * nCTA + c) * D)[d4] = o[k];
+        }
       }
-      if (tid < HQ) pml[tid] = make_float2(sm.att_m[tid], sm.att_l[tid]);
+      if (tid < HQ) aml[((size_t)b * H + tid) * nCTAp + c] = make_float2(sm.att_m[tid], sm.att_l[tid]);
+      fence_proxy_async_global();
       __syncthreads();
     }
   }
@@ -1681,44 +1903,47 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   if (!grid_sync(a.gsync, a.status)) return;
   TS_MARK(25);
   if (a.phases & kPhAttend) {
-    // merge the CTA partials of one (sequence, query head) per CTA pass: weights from
-    // the (max, sum) pairs, then the weighted rows with 16-byte loads, reduced in a
+    // merge the CTA partials of one (sequence, query head) per CTA pass: the item's rows and
+    // (max, sum) pairs arrive by bulk copy, then weights, then the weighted rows reduced in a
     // fixed order
-    float* pw = reinterpret_cast<float*>(dsm);     // [nCTA] weights
-    float* pm = pw + nCTA;                         // [nCTA] maxima
-    float* pl = pm + nCTA;                         // [nCTA] sums
-    float4* racc = reinterpret_cast<float4*>(dsm + (((size_t)3 * nCTA * 4 + 15) & ~(size_t)15));  // [ngrp][D/4]
+    float* po = reinterpret_cast<float*>(dsm);                          // [nCTA][D]
+    float2* pml = reinterpret_cast<float2*>(po + (size_t)nCTA * D);     // [nCTAp]
+    float* pw = reinterpret_cast<float*>(pml + nCTAp);                  // [nCTA] weights
+    float4* racc = reinterpret_cast<float4*>(dsm + (((size_t)nCTA * D * 4 + (size_t)nCTAp * 8 + (size_t)nCTA * 4 + 15) &
+                                                     ~(size_t)15));     // [ngrp][D/4]
     constexpr int ncol = D / 4;
     const int ngrp = blockDim.x / ncol;
     const int col = tid % ncol, grp = tid / ncol;
+    #pragma unroll 1
     for (int item = c; item < B * H; item += nCTA) {
       const int b = item / H, h = item % H;
-      const float2* mlp = aml + (size_t)b * nCTA * H + h;
-      for (int cc = tid; cc < nCTA; cc += blockDim.x) {
-        const float2 v = __ldcg(mlp + (size_t)cc * H);
-        pm[cc] = v.x;
-        pl[cc] = v.y;
+      if (!bulk_fetch(po, ao + ((size_t)b * H + h) * nCTA * D, (uint32_t)(nCTA * D * 4), pml,
+                      aml + ((size_t)b * H + h) * nCTAp, (uint32_t)(nCTAp * 8))) {
+        if (tid == 0) atomicExch(&a.gsync->abort, 1u);
+        return;
       }
-      __syncthreads();
       float M = -INFINITY;
-      for (int cc = lane; cc < nCTA; cc += 32) M = fmaxf(M, pm[cc]);
+      #pragma unroll 1
+      for (int cc = lane; cc < nCTA; cc += 32) M = fmaxf(M, pml[cc].x);
       M = warp_max(M);                                       // every warp computes the same M
+      #pragma unroll 1
       for (int cc = tid; cc < nCTA; cc += blockDim.x)
-        pw[cc] = (M > -INFINITY && pm[cc] > -INFINITY) ? expf(pm[cc] - M) : 0.f;
+        pw[cc] = (M > -INFINITY && pml[cc].x > -INFINITY) ? expf(pml[cc].x - M) : 0.f;
       __syncthreads();
       if (warp == 0) {
         float den = 0.f;
-        for (int cc = lane; cc < nCTA; cc += 32) den = fmaf(pw[cc], pl[cc], den);
+        #pragma unroll 1
+        for (int cc = lane; cc < nCTA; cc += 32) den = fmaf(pw[cc], pml[cc].y, den);
         den = warp_sum(den);
         if (lane == 0) sm.red_f[0][0] = den;
       }
-      const float4* ob = reinterpret_cast<const float4*>(ao + ((size_t)b * nCTA * H + h) * D) + col;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       if (grp < ngrp) {
+        #pragma unroll 1
         for (int cc = grp; cc < nCTA; cc += ngrp) {
           const float w = pw[cc];
           if (w != 0.f) {
-            const float4 v = __ldcg(ob + (size_t)cc * H * ncol);
+            const float4 v = reinterpret_cast<const float4*>(po + (size_t)cc * D)[col];
             acc.x = fmaf(w, v.x, acc.x);
             acc.y = fmaf(w, v.y, acc.y);
             acc.z = fmaf(w, v.z, acc.z);
@@ -1730,20 +1955,20 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       __syncthreads();
       const float den = sm.red_f[0][0];
       if (tid < ncol) {
-        float4 s = racc[tid];
+        float4 s4 = racc[tid];
         for (int g = 1; g < ngrp; ++g) {
           const float4 v = racc[g * ncol + tid];
-          s.x += v.x;
-          s.y += v.y;
-          s.z += v.z;
-          s.w += v.w;
+          s4.x += v.x;
+          s4.y += v.y;
+          s4.z += v.z;
+          s4.w += v.w;
         }
         const float inv = den > 0.f ? 1.f / den : 0.f;
         float* o = a.out + ((size_t)b * H + h) * D + 4 * tid;   // the caller's buffer: 4-byte aligned only
-        o[0] = s.x * inv;
-        o[1] = s.y * inv;
-        o[2] = s.z * inv;
-        o[3] = s.w * inv;
+        o[0] = s4.x * inv;
+        o[1] = s4.y * inv;
+        o[2] = s4.z * inv;
+        o[3] = s4.w * inv;
       }
       if (a.lse && tid == 0) a.lse[(size_t)b * H + h] = den > 0.f ? M + logf(den) : -INFINITY;
       __syncthreads();
@@ -1752,10 +1977,12 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   TS_MARK(26);
   if (a.phases & kPhSelect) {
     // counts of the CTAs before mine and of all CTAs, every sequence at once (warp per sequence)
+    #pragma unroll 1
     for (int b = warp; b < B; b += S::NW) {
       const SeqState& st = sm.seq[b];
       int pc = 0, pa = 0, tc = 0, ta = 0;
       if (!st.hit)
+        #pragma unroll 8
         for (int cc = st.first_cta + lane; cc <= st.last_cta; cc += 32) {
           const int xc = __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 3 + 0]);
           const int xa = __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 3 + 1]);
@@ -1779,6 +2006,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     }
     __syncthreads();
     // ascending index lists and Selection Cache entries
+    #pragma unroll 1
     for (int b = 0; b < B; ++b) {
       const SeqState& st = sm.seq[b];
       int32_t* ib = a.idx + (size_t)b * a.idx_stride;
@@ -1795,6 +2023,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           continue;
         }
         const int per = (total + nCTA - 1) / nCTA;
+        #pragma unroll 1
         for (int j = c * per + tid; j < min(total, (c + 1) * per); j += blockDim.x) {
           int v;
           if (j < st.s_end) v = j;
@@ -1821,12 +2050,15 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       }
       if (c == 0) {
         if (fits) {
+          #pragma unroll 1
           for (int j = tid; j < st.s_end; j += blockDim.x) ib[j] = j;
+          #pragma unroll 1
           for (int j = tid; j < st.n - st.ls; j += blockDim.x) ib[st.s_end + tot_c + j] = st.ls + j;
         }
         if (a.cq) {
           const float* qb = a.q + (size_t)b * H * D;
           float* cqb = a.cq + (size_t)b * H * D;
+          #pragma unroll 8
           for (int j = tid; j < H * D; j += blockDim.x) cqb[j] = qb[j];
         }
       }
@@ -1834,6 +2066,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       if (sgi < 0) continue;
       const int tl0 = sm.seg_lp0[sgi] * S::P, nt = sm.seg_ntok[sgi], t0l = sm.seg_t0[sgi];
       int32_t* ctb = cfits ? a.ct + (size_t)b * a.cap : nullptr;
+      #pragma unroll 1
       for (int base = 0; base < nt; base += blockDim.x) {
         const int i = base + tid;
         const int t = tl0 + i;
@@ -1910,9 +2143,12 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   // ring slots of one stage of K each; the selection scratch and one
   // sequence's global histograms (with masses) alias the same space later
   const int nslot = std::min(kMaxSlots, (dyn - flag_cap) / S::STAGE_BYTES);
-  // (the vote pass keeps (max, 1/sum) per segment and head plus one segment's CTA partials)
-  if (nslot < S::MIN_SLOTS || dyn - flag_cap < kSelScratch + kBins * 12 ||
-      dyn - flag_cap < (kMaxB + ctx->num_sms + 1) * kMaxWaveHeads * 8)
+  // (the vote pass keeps (max, 1/sum) per segment and head, one segment's CTA partials and
+  // per-warp reductions; the merge one (sequence, head)'s CTA rows)
+  if (nslot < S::MIN_SLOTS || dyn - flag_cap < lvl_bins(0) * 12 || dyn - flag_cap < kCandCap * 8 ||
+      dyn - flag_cap < kMaxB * 128 * 12 ||
+      dyn - flag_cap < kMaxB * kMaxWaveHeads * 8 + ctx->num_sms * ctx->cfg.n_q_heads * 8 + 2 * 16 * 32 * 4 ||
+      dyn < ctx->num_sms * (D * 4 + 8 + 4) + 8 + 16 + S::THREADS * 16)   // the merge's rows, pairs, weights
     return TS_ERR_UNSUPPORTED;
   if (!ensure_smem<step_kernel<KT, D, HKV, G>>((size_t)dyn, ctx->device)) {
     if (std::getenv("TS_DEBUG")) std::fprintf(stderr, "ts step: smem attribute %d B refused\n", dyn);

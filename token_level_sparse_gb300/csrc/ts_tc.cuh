@@ -42,6 +42,12 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders generic-proxy global writes (made visible by a barrier) before this
+// thread's later async-proxy reads of them (bulk copies), and vice versa.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- TMEM
 
 // One full warp: allocates ncols columns (a power of two >= 32) and writes
