@@ -83,7 +83,7 @@ def case_main(args):
 PHASES = {0: "start", 1: "setup", 5: "lengths", 6: "cache-test", 7: "partition", 2: "scanned",
           3: "stats", 4: "scan-barrier", 13: "vote-partials", 14: "vote-norm", 20: "votes",
           28: "hist0", 29: "hist1", 30: "hist2", 21: "levels", 22: "candidates", 23: "flags",
-          10: "gathered", 9: "rounds", 11: "attended", 24: "partials", 25: "last-barrier",
+          10: "gathered", 15: "att-scores", 16: "att-weights", 9: "rounds", 11: "attended", 24: "partials", 25: "last-barrier",
           26: "merged", 27: "end"}
 
 

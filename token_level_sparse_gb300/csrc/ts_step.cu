@@ -119,6 +119,7 @@ struct StepShape {
   static_assert(D % DPL == 0 && 32 % LPR == 0 && GP <= LPR, "scan lane split");
   static_assert(NCW >= 1 && (P * HKV) % NCW == 0 && ROWS % RPW == 0 && ITERS >= 1, "scan warp split");
   static_assert(NCW % HKV == 0 && P % ROWS == 0 || ROWS % P == 0, "rows of a warp stay in one page");
+  static_assert(NW % HKV == 0, "attention scores: whole warps per KV head");
   static_assert(GP <= 32, "attention reduction");
   static_assert((HKV * G) % 2 == 0, "rows of H (max, sum) pairs are whole 16-byte blocks");
   // tensor-core scan (bf16 pages of 128 rows = H_kv x 16 tokens): one M = 128 tcgen05.mma
@@ -428,6 +429,210 @@ struct Smem {
     if (c == 0 && tid == 0 && a.phase_ns) a.phase_ns[i] = globaltimer_ns(); \
   } while (0)
 
+// One wave of the CUDA-core scan (geometries and launches without the tensor-core scan): the
+// wave's KV heads of my pages stream through the ring of 1-D bulk copies, every warp holds the
+// G queries of one KV head in registers, writes logits and keeps per-warp (max, sum exp);
+// then the per (segment, head) partials. Out of line so that its register pressure stays
+// here. False after a time-out (the abort word is raised).
+template <typename KT, int D, int HKV, int G>
+__device__ __noinline__ bool cuda_scan_wave(const StepKArgs& a, Smem& sm, unsigned char* ring, uint64_t* full, int wv,
+                                             int& stage_seq) {
+  using S = StepShape<KT, D, HKV, G>;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x, nCTA = gridDim.x;
+  const int B = a.B, H = a.H;
+  const int nslot = a.nslot;
+  const int hpw = sm.hpw, HW = hpw * G, nwaves = sm.nwaves;
+  const int pps = HKV / hpw;                       // pages per stage
+  const int np = sm.p1 - sm.p0;
+  const int nstages = (np + pps - 1) / pps;
+  const int slab = hpw * S::P * S::ROW_BYTES;      // bytes of one page's heads of the wave
+  float* eb = a.spill + (size_t)c * sm.region;     // my logits, token-major [tstride][HW]
+  float2* wp = a.wpart + (size_t)c * B * S::NCW * G;  // [segment][warp][head of the warp] (max, sum exp)
+  const uint64_t pol = l2_evict_first_policy();
+  // Issues ring use u (pages si*pps.. of my range, the wave's heads of each) into slot
+  // u % nslot: metadata first, then arrive.expect_tx, then the copies.
+  auto issue = [&](int u, int si, int g0) {
+    const int s = u % nslot;
+    sm.slot_last[s] = u;
+    uint32_t bytes = 0;
+    int pages[16];
+    for (int j = 0; j < pps; ++j) {
+      const int gp = sm.p0 + si * pps + j;
+      sm.stage_tok[s][j] = -1;
+      sm.stage_nv[s][j] = 0;
+      sm.stage_b[s][j] = 0;
+      pages[j] = -1;
+      if (gp >= sm.p1) continue;
+      int seg = 0;
+      while (seg + 1 < sm.nseg && gp >= sm.seg_pend[seg]) ++seg;
+      const int b = sm.seg_b[seg];
+      const int lp = gp - sm.seq[b].pg0;
+      const int page = (gp - sm.p0 < kMaxPagesCta) ? sm.my_pages[gp - sm.p0]
+                                                    : a.page_table[(size_t)b * a.pt_stride + lp];
+      sm.stage_tok[s][j] = (gp - sm.p0) * S::P;
+      sm.stage_b[s][j] = b;
+      if (page < 0 || (int64_t)page >= a.num_pages) {
+        set_error(a.status, TS_ERR_PAGE_OOB);
+        continue;
+      }
+      sm.stage_nv[s][j] = min(S::P, sm.seq[b].n - lp * S::P);
+      pages[j] = page;
+      bytes += (uint32_t)slab;
+    }
+    mbar_arrive_expect_tx(&full[s], bytes);
+    for (int j = 0; j < pps; ++j) {
+      if (pages[j] < 0) continue;
+      bulk_g2s_hint(ring + (size_t)s * S::STAGE_BYTES + (size_t)j * slab,
+                    a.k_pool + ((size_t)pages[j] * HKV + g0) * S::P * S::ROW_BYTES, (uint32_t)slab, &full[s], pol);
+    }
+  };
+  const int g0 = wv * hpw;
+  if (tid == 0)  // the ring is idle between waves: fill it
+    for (int si = 0; si < min(nslot, nstages); ++si) issue(stage_seq + si, si, g0);
+  {
+    // ---- warp -> KV head g0 + gi, ROWS rows of that head in each stage
+    const int wph = S::NCW / hpw;
+    const int gi = warp / wph;
+    const int row0 = (warp % wph) * S::ROWS;     // ROWS divides P or P divides ROWS
+    const int lrow = lane / S::LPR, lin = lane % S::LPR;
+    float qr[S::GP][S::DPL];
+#pragma unroll
+    for (int j = 0; j < S::GP; ++j)
+#pragma unroll
+      for (int e = 0; e < S::DPL; ++e) qr[j][e] = 0.f;
+    int qb = -1;                                 // sequence whose queries sit in qr
+    const bool writer = (lin & (S::LPR / S::GP - 1)) == 0;
+    const int mywhich = reduce_slot<S::GP, S::LPR>(lane);   // the head this lane's sums belong to
+    // (max, sum exp) of this warp's rows of each of my segments, this wave's heads
+    int cur_sg = -1;
+    float run_m = -INFINITY;
+    KahanF run_z;
+    for (int i = lane; i < sm.nseg * G; i += 32)
+      wp[((size_t)(i / G) * S::NCW + warp) * G + (i % G)] = make_float2(-INFINITY, 0.f);
+    __syncwarp();
+    auto flush = [&](int sg) {
+      if (sg >= 0 && lrow == 0 && writer && mywhich < G)
+        wp[((size_t)sg * S::NCW + warp) * G + mywhich] = make_float2(run_m, run_z.s - run_z.c);
+    };
+    for (int si = 0; si < nstages; ++si) {
+      const int u = stage_seq + si;
+      const int s = u % nslot;
+      if (!mbar_wait(&full[s], (u / nslot) & 1)) {
+        set_error(a.status, TS_ERR_TIMEOUT);
+        sm.timed_out = 1;
+        break;
+      }
+      const KT* st = reinterpret_cast<const KT*>(ring + (size_t)s * S::STAGE_BYTES);
+#pragma unroll
+      for (int it = 0; it < S::ITERS; ++it) {
+        const int r = row0 + it * S::RPW + lrow;   // row among this head's pps*16 rows
+        const int j = r / S::P, slot = r % S::P;   // all lanes of a step share the page j
+        const int tl = sm.stage_tok[s][j];
+        if (tl < 0) continue;                    // past my range (uniform in the warp)
+        const int nv = sm.stage_nv[s][j];
+        const int bq = sm.stage_b[s][j];
+        if (bq != qb) {                          // new sequence: its queries of this KV head
+#pragma unroll
+          for (int jj = 0; jj < S::GP; ++jj) {
+            const float* qh = a.q + ((size_t)bq * H + (g0 + gi) * G + jj) * D;
+#pragma unroll
+            for (int cc = 0; cc < S::CPL; ++cc)
+#pragma unroll
+              for (int e = 0; e < S::EPC; ++e)
+                qr[jj][cc * S::EPC + e] = (jj < G) ? qh[(lin + cc * S::LPR) * S::EPC + e] : 0.f;
+          }
+          qb = bq;
+        }
+        const int sg = sm.my_seg_of[bq];
+        if (sg != cur_sg) {                      // new segment: its running statistics
+          flush(cur_sg);
+          cur_sg = sg;
+          run_m = -INFINITY;
+          run_z = KahanF();
+        }
+        const KT* rp = st + ((size_t)(j * hpw + gi) * S::P + slot) * D;
+        float acc0[S::GP], acc1[S::GP];
+#pragma unroll
+        for (int jj = 0; jj < S::GP; ++jj) acc0[jj] = acc1[jj] = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < S::CPL; ++cc) {
+          float kf[S::EPC];
+          KV<KT>::unpack(lds128(rp + (lin + cc * S::LPR) * S::EPC), kf);
+#pragma unroll
+          for (int jj = 0; jj < S::GP; ++jj)
+#pragma unroll
+            for (int e = 0; e < S::EPC; ++e) {
+              if ((S::CPL == 2 ? cc : (e & 1)) == 0)
+                acc0[jj] = fmaf(qr[jj][cc * S::EPC + e], kf[e], acc0[jj]);
+              else
+                acc1[jj] = fmaf(qr[jj][cc * S::EPC + e], kf[e], acc1[jj]);
+            }
+        }
+        float v[S::GP];
+#pragma unroll
+        for (int jj = 0; jj < S::GP; ++jj) v[jj] = acc0[jj] + acc1[jj];
+        int which;
+        const float dot = transpose_reduce<S::GP, S::LPR>(v, lane, which);
+        const float x = slot < nv ? dot * a.scale : -INFINITY;
+        if (writer && which < G) eb[(size_t)(tl + slot) * HW + gi * G + which] = x;
+        // running max and compensated sum of exp over the rows of this step (lanes of equal `which`)
+        float mi = x;
+#pragma unroll
+        for (int d = S::LPR; d < 32; d <<= 1) mi = fmaxf(mi, __shfl_xor_sync(kFull, mi, d));
+        const float mn = fmaxf(run_m, mi);
+        float ex = mn > -INFINITY ? expf(x - mn) : 0.f;
+#pragma unroll
+        for (int d = S::LPR; d < 32; d <<= 1) ex += __shfl_xor_sync(kFull, ex, d);
+        if (mn > run_m && run_m > -INFINITY) {
+          const float f = expf(run_m - mn);
+          run_z.s *= f;
+          run_z.c *= f;
+        }
+        run_z.add(ex);
+        run_m = mn;
+      }
+      // the last warp done with this use of the slot refills it
+      __syncwarp();
+      if (lane == 0) {
+        if (atomicAdd(&sm.stage_done[s], 1) == S::NCW - 1) {
+          sm.stage_done[s] = 0;
+          if (si + nslot < nstages) issue(u + nslot, si + nslot, g0);
+        }
+      }
+    }
+    flush(cur_sg);
+  }
+  stage_seq += nstages;
+  __syncthreads();
+  if (sm.timed_out) {
+    if (tid == 0) {
+      // copies issued but never consumed land before the CTA leaves
+      for (int ss = 0; ss < nslot; ++ss)
+        if (sm.slot_last[ss] >= 0) mbar_wait(&full[ss], (sm.slot_last[ss] / nslot) & 1);
+      atomicExch(&a.gsync->abort, 1u);   // the others leave at their next barrier
+    }
+    return false;
+  }
+  TS_MARK(2 + 3 * min(wv, 5));
+
+  // ---- per (segment, wave head): combine the warps' (max, sum exp) -> partials
+  {
+    const int wph = S::NCW / hpw;
+    for (int item = warp; item < sm.nseg * HW; item += S::NW) {
+      const int sg = item / HW, hl = item % HW;
+      const int gi = hl / G, w = hl % G;
+      float2 mz = make_float2(-INFINITY, 0.f);
+      if (lane < wph) mz = wp[((size_t)sg * S::NCW + gi * wph + lane) * G + w];
+      const float m = warp_max(mz.x);
+      const float z = warp_sum_comp((m > -INFINITY && mz.y > 0.f) ? mz.y * expf(mz.x - m) : 0.f);
+      if (lane == 0) a.partials[((size_t)sm.seg_b[sg] * nCTA + c) * H + g0 * G + hl] = make_float2(m, z);
+    }
+  }
+  return true;
+}
+
+
 template <typename KT, int D, int HKV, int G>
 __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_kernel(const __grid_constant__ StepKArgs a) {
   using S = StepShape<KT, D, HKV, G>;
@@ -523,12 +728,55 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     int* cn = reinterpret_cast<int*>(cr + (size_t)B * 3 * S::NW);     // [B][2][NW]
     const bool check = (a.phases & kPhCheck) != 0;
     const int HD = H * D;
+    // few sequences: q, C_Q and the used part of C_T of every filled entry arrive in shared
+    // memory in one bulk-copy transaction (one round trip instead of one per operand)
+    const int cap16 = (a.cap + 8 + 3) & ~3;   // ints per staged C_T: the entries plus alignment slack, 16-byte rows
+    const size_t per_b = (size_t)(2 * HD + cap16) * 4;
+    unsigned char* stg = dsm + (((size_t)B * 5 * S::NW * 4 + 15) & ~(size_t)15);
+    const bool staged = have_cache && B * per_b + (stg - dsm) <= (size_t)(a.dyn_bytes - a.flag_cap) &&
+                        (reinterpret_cast<uintptr_t>(a.q) & 15) == 0 && (HD * 4) % 16 == 0;
+    if (staged) {
+      if (tid == 0) {
+        uint32_t bytes = 0;
+        for (int b = 0; b < B; ++b) {
+          if (!sm.filled[b]) continue;
+          const uintptr_t c0 = reinterpret_cast<uintptr_t>(a.ct + (size_t)b * a.cap);
+          const uintptr_t c1 = reinterpret_cast<uintptr_t>(a.ct + (size_t)b * a.cap + sm.ctc[b]);
+          const uint32_t ctbytes = (uint32_t)(((c1 + 15) & ~(uintptr_t)15) - (c0 & ~(uintptr_t)15));
+          bytes += (check ? 2u * HD * 4u : 0u) + ctbytes;
+        }
+        fence_proxy_async_global();
+        mbar_arrive_expect_tx(&xbar, bytes);
+        for (int b = 0; b < B; ++b) {
+          if (!sm.filled[b]) continue;
+          unsigned char* d = stg + b * per_b;
+          if (check) {
+            bulk_g2s(d, a.q + (size_t)b * HD, (uint32_t)HD * 4u, &xbar);
+            bulk_g2s(d + HD * 4, a.cq + (size_t)b * HD, (uint32_t)HD * 4u, &xbar);
+          }
+          const uintptr_t c0 = reinterpret_cast<uintptr_t>(a.ct + (size_t)b * a.cap);
+          const uintptr_t c1 = reinterpret_cast<uintptr_t>(a.ct + (size_t)b * a.cap + sm.ctc[b]);
+          const uint32_t ctbytes = (uint32_t)(((c1 + 15) & ~(uintptr_t)15) - (c0 & ~(uintptr_t)15));
+          if (ctbytes) bulk_g2s(d + 2 * HD * 4, reinterpret_cast<const void*>(c0 & ~(uintptr_t)15), ctbytes, &xbar);
+        }
+      }
+      const bool landed = mbar_wait(&xbar, xph);
+      xph ^= 1u;
+      if (!__syncthreads_and(landed)) {
+        if (tid == 0) {
+          set_error(a.status, TS_ERR_TIMEOUT);
+          atomicExch(&a.gsync->abort, 1u);   // the others leave at their first barrier
+        }
+        return;
+      }
+    }
     #pragma unroll 1
     for (int b = 0; b < B; ++b) {
       if (!sm.filled[b]) continue;
+      const unsigned char* sb = stg + b * per_b;
       if (check) {
-        const float* x = a.q + (size_t)b * HD;
-        const float* y = a.cq + (size_t)b * HD;
+        const float* x = staged ? reinterpret_cast<const float*>(sb) : a.q + (size_t)b * HD;
+        const float* y = staged ? reinterpret_cast<const float*>(sb + HD * 4) : a.cq + (size_t)b * HD;
         float xy = 0.f, xx = 0.f, yy = 0.f;
 #pragma unroll 8
         for (int i = tid; i < HD; i += blockDim.x) {
@@ -546,7 +794,9 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           cr[(b * 3 + 2) * S::NW + warp] = yy;
         }
       }
-      const int32_t* ctb = a.ct + (size_t)b * a.cap;
+      const int32_t* ctb = staged ? reinterpret_cast<const int32_t*>(sb + 2 * HD * 4) +
+                                        ((reinterpret_cast<uintptr_t>(a.ct + (size_t)b * a.cap) & 15) >> 2)
+                                  : a.ct + (size_t)b * a.cap;
       const int se = sm.seq[b].s_end, ls = sm.seq[b].ls;
       int below_s = 0, below_l = 0;
 #pragma unroll 4
@@ -793,42 +1043,40 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         __syncthreads();
         TS_MARK(14);
       }
-      // v_i (+)= sum over the wave's heads of exp(l - M) / Z, compensated; a token's row is
-      // loaded whole before the sum
+      // v_i (+)= sum over the wave's heads of exp(l - M) / Z
       #pragma unroll 1
       for (int sg = 0; sg < sm.nseg; ++sg) {
         const int b = sm.seg_b[sg], t0 = sm.seg_t0[sg], nt = sm.seg_ntok[sg];
         float* vb = a.vote + (size_t)b * a.vote_stride + (size_t)sm.seg_lp0[sg] * S::P;
         const float2* w = wz + sg * kMaxWaveHeads;
-        if ((HW & 3) == 0) {
+        const int lpt = HW / 4;                       // lanes per token row, one float4 (4 heads) each
+        if ((HW & 3) == 0 && HW <= 32 && (32 % lpt) == 0) {
+          // warp-cooperative and coalesced: a load instruction covers 32 / lpt whole rows; each
+          // lane forms its 4 terms, then the lpt lanes of a row add theirs (xor tree)
+          const int tpi = 32 / lpt, rl = lane / lpt, qd = lane % lpt;
+          const float2 w0 = w[4 * qd], w1 = w[4 * qd + 1], w2 = w[4 * qd + 2], w3 = w[4 * qd + 3];
           #pragma unroll 1
-          for (int t = tid; t < nt; t += blockDim.x) {
-            const float4* row = reinterpret_cast<const float4*>(eb + (size_t)(t0 + t) * HW);
-            float4 x[kMaxWaveHeads / 4];
+          for (int tw = warp * 8 * tpi; tw < nt; tw += S::NW * 8 * tpi) {
+            float part[8];
 #pragma unroll
-            for (int q = 0; q < kMaxWaveHeads / 4; ++q)
-              if (4 * q < HW) x[q] = row[q];
-            // the wave's terms in registers, summed as a pairwise tree (error a few ulp; no
-            // serial compensation chain)
-            float e[kMaxWaveHeads];
-#pragma unroll
-            for (int q = 0; q < kMaxWaveHeads / 4; ++q) {
-              const bool in = 4 * q < HW;
-              const float2 w0 = w[in ? 4 * q : 0], w1 = w[in ? 4 * q + 1 : 0], w2 = w[in ? 4 * q + 2 : 0],
-                           w3 = w[in ? 4 * q + 3 : 0];
-              e[4 * q] = in ? expf(x[q].x - w0.x) * w0.y : 0.f;
-              e[4 * q + 1] = in ? expf(x[q].y - w1.x) * w1.y : 0.f;
-              e[4 * q + 2] = in ? expf(x[q].z - w2.x) * w2.y : 0.f;
-              e[4 * q + 3] = in ? expf(x[q].w - w3.x) * w3.y : 0.f;
+            for (int k = 0; k < 8; ++k) {
+              const int t = tw + k * tpi + rl;
+              float4 xv = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+              if (t < nt) xv = reinterpret_cast<const float4*>(eb + (size_t)(t0 + t) * HW)[qd];
+              part[k] = (expf(xv.x - w0.x) * w0.y + expf(xv.y - w1.x) * w1.y) +
+                        (expf(xv.z - w2.x) * w2.y + expf(xv.w - w3.x) * w3.y);
             }
+            #pragma unroll 1
+            for (int d = lpt / 2; d >= 1; d >>= 1)
 #pragma unroll
-            for (int half = kMaxWaveHeads / 2; half >= 1; half >>= 1)
+              for (int k = 0; k < 8; ++k) part[k] += __shfl_xor_sync(kFull, part[k], d);
+            if (qd == 0) {
 #pragma unroll
-              for (int i = 0; i < half; ++i) e[i] += e[i + half];
-            KahanF acc;
-            acc.add(e[0]);
-            const float v = acc.s - acc.c;
-            vb[t] = (wv == 0) ? v : vb[t] + v;
+              for (int k = 0; k < 8; ++k) {
+                const int t = tw + k * tpi + rl;
+                if (t < nt) vb[t] = (wv == 0) ? part[k] : vb[t] + part[k];
+              }
+            }
           }
         } else {
           #pragma unroll 1
@@ -1042,202 +1290,18 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       }
     }
     if (!scanned) {
-    const int hpw = sm.hpw, HW = hpw * G, nwaves = sm.nwaves;
-    const int pps = HKV / hpw;                       // pages per stage
-    const int np = sm.p1 - sm.p0;
-    const int nstages = (np + pps - 1) / pps;
-    const int slab = hpw * S::P * S::ROW_BYTES;      // bytes of one page's heads of the wave
-    float* eb = a.spill + (size_t)c * sm.region;     // my logits, token-major [tstride][HW]
-    float2* wp = a.wpart + (size_t)c * B * S::NCW * G;  // [segment][warp][head of the warp] (max, sum exp)
-    const uint64_t pol = l2_evict_first_policy();
-    int stage_seq = 0;                               // ring use counter across waves
-    // Issues ring use u (pages si*pps.. of my range, the wave's heads of each) into slot
-    // u % nslot: metadata first, then arrive.expect_tx, then the copies.
-    auto issue = [&](int u, int si, int g0) {
-      const int s = u % nslot;
-      sm.slot_last[s] = u;
-      uint32_t bytes = 0;
-      int pages[16];
-      for (int j = 0; j < pps; ++j) {
-        const int gp = sm.p0 + si * pps + j;
-        sm.stage_tok[s][j] = -1;
-        sm.stage_nv[s][j] = 0;
-        sm.stage_b[s][j] = 0;
-        pages[j] = -1;
-        if (gp >= sm.p1) continue;
-        int seg = 0;
-        while (seg + 1 < sm.nseg && gp >= sm.seg_pend[seg]) ++seg;
-        const int b = sm.seg_b[seg];
-        const int lp = gp - sm.seq[b].pg0;
-        const int page = (gp - sm.p0 < kMaxPagesCta) ? sm.my_pages[gp - sm.p0]
-                                                      : a.page_table[(size_t)b * a.pt_stride + lp];
-        sm.stage_tok[s][j] = (gp - sm.p0) * S::P;
-        sm.stage_b[s][j] = b;
-        if (page < 0 || (int64_t)page >= a.num_pages) {
-          set_error(a.status, TS_ERR_PAGE_OOB);
-          continue;
-        }
-        sm.stage_nv[s][j] = min(S::P, sm.seq[b].n - lp * S::P);
-        pages[j] = page;
-        bytes += (uint32_t)slab;
+      const int hpw = sm.hpw, HW = hpw * G, nwaves = sm.nwaves;
+      float* eb = a.spill + (size_t)c * sm.region;   // my logits, token-major [tstride][HW]
+      int stage_seq = 0;                             // ring use counter across waves
+      for (int wv = 0; wv < nwaves; ++wv) {
+        const int g0 = wv * hpw;
+        if (!cuda_scan_wave<KT, D, HKV, G>(a, sm, ring, full, wv, stage_seq)) return;
+        fence_proxy_async_global();
+        TS_MARK(3 + 3 * min(wv, 5));
+        if (!grid_sync(a.gsync, a.status)) return;
+        TS_MARK(4 + 3 * min(wv, 5));
+        if (!vote_pass(eb, g0, HW, wv)) return;
       }
-      mbar_arrive_expect_tx(&full[s], bytes);
-      for (int j = 0; j < pps; ++j) {
-        if (pages[j] < 0) continue;
-        bulk_g2s_hint(ring + (size_t)s * S::STAGE_BYTES + (size_t)j * slab,
-                      a.k_pool + ((size_t)pages[j] * HKV + g0) * S::P * S::ROW_BYTES, (uint32_t)slab, &full[s], pol);
-      }
-    };
-    for (int wv = 0; wv < nwaves; ++wv) {
-      const int g0 = wv * hpw;
-      if (tid == 0)  // the ring is idle between waves: fill it
-        for (int si = 0; si < min(nslot, nstages); ++si) issue(stage_seq + si, si, g0);
-      {
-        // ---- warp -> KV head g0 + gi, ROWS rows of that head in each stage
-        const int wph = S::NCW / hpw;
-        const int gi = warp / wph;
-        const int row0 = (warp % wph) * S::ROWS;     // ROWS divides P or P divides ROWS
-        const int lrow = lane / S::LPR, lin = lane % S::LPR;
-        float qr[S::GP][S::DPL];
-#pragma unroll
-        for (int j = 0; j < S::GP; ++j)
-#pragma unroll
-          for (int e = 0; e < S::DPL; ++e) qr[j][e] = 0.f;
-        int qb = -1;                                 // sequence whose queries sit in qr
-        const bool writer = (lin & (S::LPR / S::GP - 1)) == 0;
-        const int mywhich = reduce_slot<S::GP, S::LPR>(lane);   // the head this lane's sums belong to
-        // (max, sum exp) of this warp's rows of each of my segments, this wave's heads
-        int cur_sg = -1;
-        float run_m = -INFINITY;
-        KahanF run_z;
-        for (int i = lane; i < sm.nseg * G; i += 32)
-          wp[((size_t)(i / G) * S::NCW + warp) * G + (i % G)] = make_float2(-INFINITY, 0.f);
-        __syncwarp();
-        auto flush = [&](int sg) {
-          if (sg >= 0 && lrow == 0 && writer && mywhich < G)
-            wp[((size_t)sg * S::NCW + warp) * G + mywhich] = make_float2(run_m, run_z.s - run_z.c);
-        };
-        for (int si = 0; si < nstages; ++si) {
-          const int u = stage_seq + si;
-          const int s = u % nslot;
-          if (!mbar_wait(&full[s], (u / nslot) & 1)) {
-            set_error(a.status, TS_ERR_TIMEOUT);
-            sm.timed_out = 1;
-            break;
-          }
-          const KT* st = reinterpret_cast<const KT*>(ring + (size_t)s * S::STAGE_BYTES);
-#pragma unroll
-          for (int it = 0; it < S::ITERS; ++it) {
-            const int r = row0 + it * S::RPW + lrow;   // row among this head's pps*16 rows
-            const int j = r / S::P, slot = r % S::P;   // all lanes of a step share the page j
-            const int tl = sm.stage_tok[s][j];
-            if (tl < 0) continue;                    // past my range (uniform in the warp)
-            const int nv = sm.stage_nv[s][j];
-            const int bq = sm.stage_b[s][j];
-            if (bq != qb) {                          // new sequence: its queries of this KV head
-#pragma unroll
-              for (int jj = 0; jj < S::GP; ++jj) {
-                const float* qh = a.q + ((size_t)bq * H + (g0 + gi) * G + jj) * D;
-#pragma unroll
-                for (int cc = 0; cc < S::CPL; ++cc)
-#pragma unroll
-                  for (int e = 0; e < S::EPC; ++e)
-                    qr[jj][cc * S::EPC + e] = (jj < G) ? qh[(lin + cc * S::LPR) * S::EPC + e] : 0.f;
-              }
-              qb = bq;
-            }
-            const int sg = sm.my_seg_of[bq];
-            if (sg != cur_sg) {                      // new segment: its running statistics
-              flush(cur_sg);
-              cur_sg = sg;
-              run_m = -INFINITY;
-              run_z = KahanF();
-            }
-            const KT* rp = st + ((size_t)(j * hpw + gi) * S::P + slot) * D;
-            float acc0[S::GP], acc1[S::GP];
-#pragma unroll
-            for (int jj = 0; jj < S::GP; ++jj) acc0[jj] = acc1[jj] = 0.f;
-#pragma unroll
-            for (int cc = 0; cc < S::CPL; ++cc) {
-              float kf[S::EPC];
-              KV<KT>::unpack(lds128(rp + (lin + cc * S::LPR) * S::EPC), kf);
-#pragma unroll
-              for (int jj = 0; jj < S::GP; ++jj)
-#pragma unroll
-                for (int e = 0; e < S::EPC; ++e) {
-                  if ((S::CPL == 2 ? cc : (e & 1)) == 0)
-                    acc0[jj] = fmaf(qr[jj][cc * S::EPC + e], kf[e], acc0[jj]);
-                  else
-                    acc1[jj] = fmaf(qr[jj][cc * S::EPC + e], kf[e], acc1[jj]);
-                }
-            }
-            float v[S::GP];
-#pragma unroll
-            for (int jj = 0; jj < S::GP; ++jj) v[jj] = acc0[jj] + acc1[jj];
-            int which;
-            const float dot = transpose_reduce<S::GP, S::LPR>(v, lane, which);
-            const float x = slot < nv ? dot * a.scale : -INFINITY;
-            if (writer && which < G) eb[(size_t)(tl + slot) * HW + gi * G + which] = x;
-            // running max and compensated sum of exp over the rows of this step (lanes of equal `which`)
-            float mi = x;
-#pragma unroll
-            for (int d = S::LPR; d < 32; d <<= 1) mi = fmaxf(mi, __shfl_xor_sync(kFull, mi, d));
-            const float mn = fmaxf(run_m, mi);
-            float ex = mn > -INFINITY ? expf(x - mn) : 0.f;
-#pragma unroll
-            for (int d = S::LPR; d < 32; d <<= 1) ex += __shfl_xor_sync(kFull, ex, d);
-            if (mn > run_m && run_m > -INFINITY) {
-              const float f = expf(run_m - mn);
-              run_z.s *= f;
-              run_z.c *= f;
-            }
-            run_z.add(ex);
-            run_m = mn;
-          }
-          // the last warp done with this use of the slot refills it
-          __syncwarp();
-          if (lane == 0) {
-            if (atomicAdd(&sm.stage_done[s], 1) == S::NCW - 1) {
-              sm.stage_done[s] = 0;
-              if (si + nslot < nstages) issue(u + nslot, si + nslot, g0);
-            }
-          }
-        }
-        flush(cur_sg);
-      }
-      stage_seq += nstages;
-      __syncthreads();
-      if (sm.timed_out) {
-        if (tid == 0) {
-          // copies issued but never consumed land before the CTA leaves
-          for (int ss = 0; ss < nslot; ++ss)
-            if (sm.slot_last[ss] >= 0) mbar_wait(&full[ss], (sm.slot_last[ss] / nslot) & 1);
-          atomicExch(&a.gsync->abort, 1u);   // the others leave at their next barrier
-        }
-        return;
-      }
-      TS_MARK(2 + 3 * min(wv, 5));
-
-      // ---- per (segment, wave head): combine the warps' (max, sum exp) -> partials
-      {
-        const int wph = S::NCW / hpw;
-        for (int item = warp; item < sm.nseg * HW; item += S::NW) {
-          const int sg = item / HW, hl = item % HW;
-          const int gi = hl / G, w = hl % G;
-          float2 mz = make_float2(-INFINITY, 0.f);
-          if (lane < wph) mz = wp[((size_t)sg * S::NCW + gi * wph + lane) * G + w];
-          const float m = warp_max(mz.x);
-          const float z = warp_sum_comp((m > -INFINITY && mz.y > 0.f) ? mz.y * expf(mz.x - m) : 0.f);
-          if (lane == 0) a.partials[((size_t)sm.seg_b[sg] * nCTA + c) * H + g0 * G + hl] = make_float2(m, z);
-        }
-      }
-      fence_proxy_async_global();
-      TS_MARK(3 + 3 * min(wv, 5));
-      if (!grid_sync(a.gsync, a.status)) return;
-      TS_MARK(4 + 3 * min(wv, 5));
-
-      if (!vote_pass(eb, g0, HW, wv)) return;
-    }
     }
   }
 
@@ -1314,11 +1378,13 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         for (int t = lo + tid; t < hi; t += blockDim.x) {
           const float v = __ldcg(vb + t);
           const uint32_t key = __float_as_uint(v);
-          if ((key & st.mask) == st.prefix) {
-            const int bin = (key >> shift) & (nbins - 1);
-            atomicAdd(&sh[bin], 1u);
-            if (topp) atomicAdd(&smh[bin], to_fx(v));
-          }
+          const bool in = (key & st.mask) == st.prefix;
+          const int bin = in ? (int)((key >> shift) & (nbins - 1)) : -1;
+          // lanes with the same bin add once (the votes of a sequence crowd into few bins)
+          const unsigned peers = __match_any_sync(__activemask(), bin);
+          const int leader = __ffs(peers) - 1;
+          if (in && lane == leader) atomicAdd(&sh[bin], (unsigned)__popc(peers));
+          if (topp && in) atomicAdd(&smh[bin], to_fx(v));
         }
         __syncthreads();
         #pragma unroll 1
@@ -1679,12 +1745,15 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     constexpr int NG = (NGRP + S::THREADS - 1) / S::THREADS;
     static_assert(HQ <= kMaxAttH && D % 32 == 0, "attention layout");
     const bool given = !(a.phases & kPhSelect);
-    const int stage_bytes = a.dyn_bytes - a.flag_cap - HQ * D * 4;
-    const int around = min(kMaxRound, stage_bytes / (S::TOKEN_BYTES + HQ * 4));
+    const int stage_bytes = a.dyn_bytes - a.flag_cap;
+    const int around = min(kMaxRound, (stage_bytes - HQ * 4) / (S::TOKEN_BYTES + HQ * 4));
     KT* Ks = reinterpret_cast<KT*>(dsm);
     KT* Vs = Ks + (size_t)around * HKV * D;
-    float* Ps = reinterpret_cast<float*>(Vs + (size_t)around * HKV * D);   // [around][HQ] scores, weights
-    float* Qs = Ps + (size_t)around * HQ;                                  // [HQ][D] this sequence's queries
+    float* Ps = reinterpret_cast<float*>(Vs + (size_t)around * HKV * D);   // [HQ][ldp] scores, weights
+    const int ldp = around | 1;                        // odd row stride: a warp's column reads hit distinct banks
+    // scores: warp -> one KV head (NW is a multiple of H_kv), its G queries in registers
+    constexpr int NWG = S::NW / HKV;
+    const int gw = warp % HKV, wsl = warp / HKV;
     uint32_t aphase = 0;
     #pragma unroll 1
     for (int b = 0; b < B; ++b) {
@@ -1709,16 +1778,12 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       const int own_n = own ? sm.seg_ntok[sgi] : 0;
       const int own_lp0 = own ? sm.seg_lp0[sgi] : 0, own_t0 = own ? sm.seg_t0[sgi] : 0;
       const int nfix_mine = c < nfix ? (nfix - c + nCTA - 1) / nCTA : 0;
-      #pragma unroll 1
-      for (int i0 = tid; i0 < HQ * D; i0 += 8 * blockDim.x) {   // eight loads in flight per thread
-        float qv[8];
+      float qreg[S::GP][EPL];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (i0 + k * (int)blockDim.x < HQ * D) qv[k] = a.q[(size_t)b * HQ * D + i0 + k * blockDim.x];
+      for (int h = 0; h < S::GP; ++h)
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          if (i0 + k * (int)blockDim.x < HQ * D) Qs[i0 + k * blockDim.x] = qv[k];
-      }
+        for (int e = 0; e < EPL; ++e)
+          qreg[h][e] = h < G ? a.q[((size_t)b * HQ + gw * G + h) * D + lane * EPL + e] : 0.f;
       if (tid < HQ) {
         sm.att_m[tid] = -INFINITY;
         sm.att_l[tid] = 0.f;
@@ -1806,43 +1871,40 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           __syncthreads();
           break;
         }
-        // ---- (1) scores: warp per (token, KV head); lane holds EPL dims, the G dot products
-        // are reduced across the warp so that lane `which` ends with head `which`
-        #pragma unroll 1
-        for (int p = warp; p < cnt * HKV; p += S::NW) {
-          const int j = p / HKV, g = p % HKV;
+        // ---- (1) scores: warp -> (its KV head, tokens wsl, wsl + NWG, ...); lane holds EPL dims,
+        // the G dot products are reduced across the warp so that lane `which` ends with head `which`
+#pragma unroll 2
+        for (int j = wsl; j < cnt; j += NWG) {
           float kf[EPL];
-          load_elems<KT, EPL>(Ks + ((size_t)j * HKV + g) * D + lane * EPL, kf);
+          load_elems<KT, EPL>(Ks + ((size_t)j * HKV + gw) * D + lane * EPL, kf);
           float acc[S::GP];
 #pragma unroll
           for (int h = 0; h < S::GP; ++h) {
             float x = 0.f;
-            if (h < G) {
-              const float* qh = Qs + (size_t)(g * G + h) * D + lane * EPL;
 #pragma unroll
-              for (int e = 0; e < EPL; ++e) x = fmaf(qh[e], kf[e], x);
-            }
+            for (int e = 0; e < EPL; ++e) x = fmaf(qreg[h][e], kf[e], x);
             acc[h] = x;
           }
           int which;
           const float dot = transpose_reduce<S::GP, 32>(acc, lane, which);
           const bool live = sm.tval[j] >= 0 && (int64_t)sm.tval[j] < a.num_pages;
-          if ((lane & (32 / S::GP - 1)) == 0 && which < G) Ps[j * HQ + g * G + which] = live ? dot * a.scale : -INFINITY;
+          if ((lane & (32 / S::GP - 1)) == 0 && which < G) Ps[(gw * G + which) * ldp + j] = live ? dot * a.scale : -INFINITY;
         }
         __syncthreads();
+        TS_MARK(15);
         // ---- (2) weights: warp per query head
         #pragma unroll 1
         for (int h = warp; h < HQ; h += S::NW) {
           float mr = -INFINITY;
           #pragma unroll 1
-          for (int t = lane; t < cnt; t += 32) mr = fmaxf(mr, Ps[t * HQ + h]);
+          for (int t = lane; t < cnt; t += 32) mr = fmaxf(mr, Ps[h * ldp + t]);
           mr = warp_max(mr);
           const float mo = sm.att_m[h], mn = fmaxf(mo, mr);
           float sum = 0.f;
           #pragma unroll 1
           for (int t = lane; t < cnt; t += 32) {
-            const float w = mn > -INFINITY ? expf(Ps[t * HQ + h] - mn) : 0.f;
-            Ps[t * HQ + h] = w;
+            const float w = mn > -INFINITY ? expf(Ps[h * ldp + t] - mn) : 0.f;
+            Ps[h * ldp + t] = w;
             sum += w;
           }
           sum = warp_sum_comp(sum);
@@ -1854,6 +1916,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           }
         }
         __syncthreads();
+        TS_MARK(16);
         // ---- (3) outputs: thread -> float4 slices (head, 4 dims)
 #pragma unroll
         for (int k = 0; k < NG; ++k) {
@@ -1864,7 +1927,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
             float4 acc = make_float4(o[k].x * corr, o[k].y * corr, o[k].z * corr, o[k].w * corr);
             #pragma unroll 1
             for (int t = 0; t < cnt; ++t) {
-              const float w = Ps[t * HQ + h];
+              const float w = Ps[h * ldp + t];
               float vf[4];
               load_elems<KT, 4>(Vs + ((size_t)t * HKV + g) * D + d4 * 4, vf);
               acc.x = fmaf(w, vf[0], acc.x);
