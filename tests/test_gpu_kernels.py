@@ -252,3 +252,37 @@ def test_multi_kernel_path_launch_count(monkeypatch):
                     idx, cnt, out)
     assert ctx.status() == 0
     assert T.ts_kernel_count(ctx.handle) - k0 >= 8
+
+
+def test_misaligned_query_takes_the_cuda_core_scan_with_the_same_result():
+    # a caller query that is only 4-byte aligned: no tensor-core scan and no staged cache test;
+    # selection and output agree with the aligned query (tensor-core scan)
+    T = tsl()
+    sp = W.spec(1, n0=(12001,), steps=1, k=512, n_local=64)
+    wl = W.generate(sp, DEV)
+    H, Hkv, d = sp.n_q_heads, sp.n_kv_heads, sp.head_dim
+    n = int(wl.n0[0])
+    ctx = T.Context(H, Hkv, d, T.TS_KV_BF16, 1, wl.page_table.shape[1], wl.num_pages)
+    seq = torch.tensor([n], dtype=torch.int32, device=DEV)
+    q = wl.q[0][0].contiguous()
+    qbuf = torch.zeros(q.numel() + 1, dtype=torch.float32, device=DEV)
+    qbuf[1:] = q.reshape(-1)
+    q_odd = qbuf[1:].view(1, H, d)
+    assert q_odd.data_ptr() % 16 != 0
+    res = []
+    for qq in (q, q_odd):
+        idx = torch.full((1, n), -1, dtype=torch.int32, device=DEV)
+        cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+        out = torch.zeros(1, H, d, device=DEV)
+        vote = torch.zeros(1, ctx.max_tokens, device=DEV)
+        ctx.decode_step(qq, wl.k_pool[0], wl.v_pool[0], wl.page_table, seq, T.params(k=512, n_local=64, theta=2.0),
+                        idx, cnt, out, vote=vote)
+        assert ctx.status() == 0
+        res.append((idx[0, :int(cnt[0])].cpu().numpy(), out.cpu(), vote[0, :n].cpu()))
+    (ia, oa, va), (ib, ob, vb) = res
+    rel = ((va.double() - vb.double()).abs() / va.double().abs().clamp_min(1e-30)).max().item()
+    assert rel < 1e-5, rel
+    if np.array_equal(ia, ib):
+        assert (oa - ob).abs().max().item() <= ATTN_REL * max(1.0, oa.abs().max().item())
+    else:   # a token within the vote tolerance of the k-th may swap
+        assert len(ia) == len(ib) and len(np.setxor1d(ia, ib)) <= 4

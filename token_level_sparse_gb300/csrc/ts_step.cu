@@ -398,6 +398,7 @@ struct Smem {
   int tot_c[kMaxB], tot_a[kMaxB];  // and of all CTAs
   int tie_base[kMaxB];             // exact ties in the CTAs before mine, per segment
   int filled[kMaxB], ctc[kMaxB];   // cache entry filled, its cached index count
+  int qst[kMaxB];                  // byte offset of sequence b's query staged in dynamic shared memory, or -1
   int x_bin[kMaxB];                // selection: crossing coarse bin of level 0, and the
   unsigned x_c[kMaxB];             // count and mass above it
   unsigned long long x_m[kMaxB];
@@ -716,6 +717,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     sm.ct_lo[b] = 0;
     sm.ct_hi[b] = 0;
     sm.filled[b] = have_cache ? a.filled[b] : 0;
+    sm.qst[b] = -1;
     sm.ctc[b] = have_cache ? max(0, min(a.ct_count[b], a.cap)) : 0;
   }
   __syncthreads();
@@ -751,6 +753,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           if (!sm.filled[b]) continue;
           unsigned char* d = stg + b * per_b;
           if (check) {
+            sm.qst[b] = (int)(d - dsm);
             bulk_g2s(d, a.q + (size_t)b * HD, (uint32_t)HD * 4u, &xbar);
             bulk_g2s(d + HD * 4, a.cq + (size_t)b * HD, (uint32_t)HD * 4u, &xbar);
           }
@@ -965,7 +968,12 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           const int n = rem / CH, ch = rem % CH, h = n / 3;
           qv[k][0] = qv[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (i < total && h < H) {
-            const float4* qh = reinterpret_cast<const float4*>(a.q + ((size_t)sm.seg_b[sg] * H + h) * D + ch * 8);
+            const int b = sm.seg_b[sg], off = sm.qst[b];
+            // the query staged by the cache test, when it lies below the image region
+            const float* qb = (off >= 0 && off + H * D * 4 <= (int)(tcb - dsm))
+                                  ? reinterpret_cast<const float*>(dsm + off)
+                                  : a.q + (size_t)b * H * D;
+            const float4* qh = reinterpret_cast<const float4*>(qb + (size_t)h * D + ch * 8);
             qv[k][0] = qh[0];
             qv[k][1] = qh[1];
           }
@@ -2111,18 +2119,20 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           a.filled[b] = cfits ? 1 : 0;
         }
       }
-      if (c == 0) {
+      {
+        // sinks and window, and the new C_Q, spread over every CTA (grid-stride)
+        const int gs = nCTA * blockDim.x, gi = c * blockDim.x + tid;
         if (fits) {
           #pragma unroll 1
-          for (int j = tid; j < st.s_end; j += blockDim.x) ib[j] = j;
+          for (int j = gi; j < st.s_end; j += gs) ib[j] = j;
           #pragma unroll 1
-          for (int j = tid; j < st.n - st.ls; j += blockDim.x) ib[st.s_end + tot_c + j] = st.ls + j;
+          for (int j = gi; j < st.n - st.ls; j += gs) ib[st.s_end + tot_c + j] = st.ls + j;
         }
         if (a.cq) {
           const float* qb = a.q + (size_t)b * H * D;
           float* cqb = a.cq + (size_t)b * H * D;
-          #pragma unroll 8
-          for (int j = tid; j < H * D; j += blockDim.x) cqb[j] = qb[j];
+          #pragma unroll 1
+          for (int j = gi; j < H * D; j += gs) cqb[j] = qb[j];
         }
       }
       const int sgi = sm.my_seg_of[b];
