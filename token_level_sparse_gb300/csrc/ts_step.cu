@@ -47,6 +47,7 @@ constexpr int kMaxRound = 128;     // attention tokens per gather round
 constexpr int kMaxWaveHeads = 32;  // query heads of one scan wave
 constexpr int kMaxG = kMaxScanG;   // query heads per KV head
 constexpr int kMaxAttH = 64;       // query heads of the attention phase
+constexpr int kPreFix = 512;       // fixed attention tokens of a CTA resolved at set-up
 constexpr int kMaxPagesCta = 1024; // page ids of a CTA's range kept in shared memory
 constexpr int kMaxSlots = 12;      // ring slots (runtime count per launch)
 constexpr int64_t kLogitL2Budget = 48ll << 20;  // default bytes of logits one scan wave keeps in L2
@@ -399,6 +400,9 @@ struct Smem {
   int tie_base[kMaxB];             // exact ties in the CTAs before mine, per segment
   int filled[kMaxB], ctc[kMaxB];   // cache entry filled, its cached index count
   int qst[kMaxB];                  // byte offset of sequence b's query staged in dynamic shared memory, or -1
+  int ctst[kMaxB];                 // byte offset of its first staged cached index, or -1
+  int pf_ok, pf_off[kMaxB + 1];    // attention: my fixed tokens of every sequence prefetched at set-up
+  int pf_t[kPreFix], pf_p[kPreFix];  // their indices and page ids
   int x_bin[kMaxB];                // selection: crossing coarse bin of level 0, and the
   unsigned x_c[kMaxB];             // count and mass above it
   unsigned long long x_m[kMaxB];
@@ -718,6 +722,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     sm.ct_hi[b] = 0;
     sm.filled[b] = have_cache ? a.filled[b] : 0;
     sm.qst[b] = -1;
+    sm.ctst[b] = -1;
     sm.ctc[b] = have_cache ? max(0, min(a.ct_count[b], a.cap)) : 0;
   }
   __syncthreads();
@@ -761,6 +766,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           const uintptr_t c1 = reinterpret_cast<uintptr_t>(a.ct + (size_t)b * a.cap + sm.ctc[b]);
           const uint32_t ctbytes = (uint32_t)(((c1 + 15) & ~(uintptr_t)15) - (c0 & ~(uintptr_t)15));
           if (ctbytes) bulk_g2s(d + 2 * HD * 4, reinterpret_cast<const void*>(c0 & ~(uintptr_t)15), ctbytes, &xbar);
+          sm.ctst[b] = (int)(d + 2 * HD * 4 - dsm) + (int)(c0 & 15);
         }
       }
       const bool landed = mbar_wait(&xbar, xph);
@@ -925,6 +931,17 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     sm.spill_ok = (int64_t)nCTA * sm.region <= a.spill_floats && sm.tok_stride <= a.flag_cap &&
                   hpw * G <= kMaxWaveHeads;
     sm.flag = 0;
+    // attention: how many fixed tokens (round-robin share) of every sequence are mine
+    int tot = 0;
+    for (int b = 0; b < B; ++b) {
+      const SeqState& st = sm.seq[b];
+      int nfix = st.s_end + (st.n - st.ls);
+      if (st.hit && a.ct) nfix += sm.ct_hi[b] - sm.ct_lo[b];
+      sm.pf_off[b] = tot;
+      tot += c < nfix ? (nfix - c + nCTA - 1) / nCTA : 0;
+    }
+    sm.pf_off[B] = tot;
+    sm.pf_ok = (a.phases & kPhAttend) && (a.phases & kPhSelect) && tot <= kPreFix;
   }
   __syncthreads();
   if (!sm.spill_ok) {
@@ -933,7 +950,9 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   }
   TS_MARK(7);
   if (c == 0 && tid < B && (a.phases & kPhCheck) && a.hit_out) a.hit_out[tid] = (uint8_t)sm.seq[tid].hit;
-  // page ids of my range, read once (ring refills and attention gathers need no global load)
+  // page ids of my range, read once (ring refills and attention gathers need no global load),
+  // and in the same pass my share of every sequence's fixed attention tokens -- sinks and
+  // window, plus the cached indices on a hit -- with their page ids
   #pragma unroll 1
   for (int i = tid; i < min(sm.p1 - sm.p0, kMaxPagesCta); i += blockDim.x) {
     const int gp = sm.p0 + i;
@@ -941,6 +960,27 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     while (sg + 1 < sm.nseg && gp >= sm.seg_pend[sg]) ++sg;
     const int b = sm.seg_b[sg];
     sm.my_pages[i] = a.page_table[(size_t)b * a.pt_stride + (gp - sm.seq[b].pg0)];
+  }
+  if (sm.pf_ok) {
+    #pragma unroll 1
+    for (int i = tid; i < sm.pf_off[B]; i += blockDim.x) {
+      int b = 0;
+      while (b + 1 < B && sm.pf_off[b + 1] <= i) ++b;
+      const SeqState& st = sm.seq[b];
+      const int f = c + (i - sm.pf_off[b]) * nCTA;
+      const int nmid = (st.hit && a.ct) ? sm.ct_hi[b] - sm.ct_lo[b] : 0;
+      int t;
+      if (f < st.s_end) {
+        t = f;
+      } else if (f < st.s_end + nmid) {
+        const int j = sm.ct_lo[b] + (f - st.s_end);
+        t = sm.ctst[b] >= 0 ? reinterpret_cast<const int32_t*>(dsm + sm.ctst[b])[j] : a.ct[(size_t)b * a.cap + j];
+      } else {
+        t = st.ls + (f - st.s_end - nmid);
+      }
+      sm.pf_t[i] = t;
+      sm.pf_p[i] = (t >= 0 && t < a.max_tokens) ? a.page_table[(size_t)b * a.pt_stride + t / S::P] : -1;
+    }
   }
   if (a.phases & kPhSelect) {
     // zero the selection histograms (first touched after a barrier)
@@ -1802,26 +1842,54 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       int fdone = 0;     // fixed tokens of mine already taken
       int opos = 0;      // next own token (segment-local) to examine
       bool ok = true;
+      // bulk copies of the K and V rows of every KV head of list entries [j0, j1)
+      auto gather_rows = [&](int j0, int j1) {
+        #pragma unroll 1
+        for (int i = tid; i < 2 * (j1 - j0) * HKV; i += blockDim.x) {
+          const int ti = j0 + i / (2 * HKV), rem = i % (2 * HKV), g = rem >> 1, isv = rem & 1;
+          const int t = sm.toks[ti];
+          const int page = sm.tval[ti];
+          size_t off = 0;
+          if (page >= 0 && (int64_t)page < a.num_pages) {
+            off = (((size_t)page * HKV + g) * S::P + (t % S::P)) * S::ROW_BYTES;
+          } else if (rem == 0) {
+            set_error(a.status, TS_ERR_PAGE_OOB);
+          }
+          bulk_g2s((isv ? Vs : Ks) + ((size_t)ti * HKV + g) * D, (isv ? a.v_pool : a.k_pool) + off,
+                   S::ROW_BYTES, &abar);
+        }
+      };
       __syncthreads();
       while (true) {
         // ---- this round's tokens: fixed share first, then own selected ones
         int cnt = 0;
         const int nf = min(around, nfix_mine - fdone);
+        const bool pf = !given && sm.pf_ok;
         #pragma unroll 1
         for (int i = tid; i < nf; i += blockDim.x) {
-          const int f = c + (fdone + i) * nCTA;
-          int t;
-          if (given) t = gib[f];
-          else if (f < st.s_end) t = f;
-          else if (f < st.s_end + nmid) t = __ldcg(ctb + ct_lo + (f - st.s_end));
-          else t = st.ls + (f - st.s_end - nmid);
-          int page = -1;
-          if (t >= 0 && t < a.max_tokens) page = a.page_table[(size_t)b * a.pt_stride + t / S::P];
+          int t, page = -1;
+          if (pf) {
+            t = sm.pf_t[sm.pf_off[b] + fdone + i];
+            page = sm.pf_p[sm.pf_off[b] + fdone + i];
+          } else {
+            const int f = c + (fdone + i) * nCTA;
+            if (given) t = gib[f];
+            else if (f < st.s_end) t = f;
+            else if (f < st.s_end + nmid) t = __ldcg(ctb + ct_lo + (f - st.s_end));
+            else t = st.ls + (f - st.s_end - nmid);
+            if (t >= 0 && t < a.max_tokens) page = a.page_table[(size_t)b * a.pt_stride + t / S::P];
+          }
           sm.toks[i] = t;
           sm.tval[i] = page;
         }
         fdone += nf;
         cnt = nf;
+        // the fixed tokens' rows start moving now; the own selected ones are listed meanwhile
+        if (nf > 0) {
+          if (tid == 0) mbar_expect_tx(&abar, (uint32_t)(nf * S::TOKEN_BYTES));
+          __syncthreads();
+          gather_rows(0, nf);
+        }
         while (own && opos < own_n && cnt < around) {
           // one chunk of blockDim own tokens; take as many selected ones as fit
           const int i = opos + tid;
@@ -1850,23 +1918,10 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         }
         TS_MARK(9);
         if (cnt == 0) break;                          // uniform: same counters in every thread
-        // ---- gather K and V rows of every KV head
-        if (tid == 0) mbar_arrive_expect_tx(&abar, (uint32_t)(cnt * S::TOKEN_BYTES));
+        // ---- the own tokens' rows; the phase completes with this arrive and every row
+        if (tid == 0) mbar_arrive_expect_tx(&abar, (uint32_t)((cnt - nf) * S::TOKEN_BYTES));
         __syncthreads();
-        #pragma unroll 1
-        for (int i = tid; i < 2 * cnt * HKV; i += blockDim.x) {
-          const int ti = i / (2 * HKV), rem = i % (2 * HKV), g = rem >> 1, isv = rem & 1;
-          const int t = sm.toks[ti];
-          const int page = sm.tval[ti];
-          size_t off = 0;
-          if (page >= 0 && (int64_t)page < a.num_pages) {
-            off = (((size_t)page * HKV + g) * S::P + (t % S::P)) * S::ROW_BYTES;
-          } else if (i % (2 * HKV) == 0) {
-            set_error(a.status, TS_ERR_PAGE_OOB);
-          }
-          bulk_g2s((isv ? Vs : Ks) + ((size_t)ti * HKV + g) * D, (isv ? a.v_pool : a.k_pool) + off,
-                   S::ROW_BYTES, &abar);
-        }
+        gather_rows(nf, cnt);
         const bool landed = mbar_wait(&abar, aphase);
         aphase ^= 1u;
         ok = __syncthreads_and(landed) != 0;
