@@ -286,3 +286,47 @@ def test_misaligned_query_takes_the_cuda_core_scan_with_the_same_result():
         assert (oa - ob).abs().max().item() <= ATTN_REL * max(1.0, oa.abs().max().item())
     else:   # a token within the vote tolerance of the k-th may swap
         assert len(ia) == len(ib) and len(np.setxor1d(ia, ib)) <= 4
+
+
+@pytest.mark.parametrize("ntie", [1500, 3000])
+def test_step_kernel_exact_vote_ties_go_to_the_lower_index(ntie):
+    # ntie tokens get the K rows of the highest-vote token: their votes are equal bit for bit
+    # and straddle the k-th place (1500: candidates ranked with ties; 3000: more tied tokens
+    # than candidates, the last radix level's tie mode). The selection must equal the top-k
+    # of the kernel's own votes with ties to the lower index (integer work: exact).
+    T = tsl()
+    k, s, w = 1024, 4, 64
+    sp = W.spec(1, n0=(20011,), steps=1, k=k, n_local=w)
+    wl = W.generate(sp, DEV)
+    H, Hkv, d, P = sp.n_q_heads, sp.n_kv_heads, sp.head_dim, sp.page_size
+    n = int(wl.n0[0])
+    seq = torch.tensor([n], dtype=torch.int32, device=DEV)
+    q = wl.q[0][0].contiguous()
+    prm = T.params(k=k, n_sink=s, n_local=w, theta=2.0)
+
+    def step():
+        ctx = T.Context(H, Hkv, d, T.TS_KV_BF16, 1, wl.page_table.shape[1], wl.num_pages)
+        idx = torch.full((1, n), -1, dtype=torch.int32, device=DEV)
+        cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+        out = torch.zeros(1, H, d, device=DEV)
+        vote = torch.zeros(1, ctx.max_tokens, device=DEV)
+        ctx.decode_step(q, wl.k_pool[0], wl.v_pool[0], wl.page_table, seq, prm, idx, cnt, out, vote=vote)
+        assert ctx.status() == 0
+        return idx[0, :int(cnt[0])].cpu().numpy(), vote[0, :n].cpu()
+
+    _, v0 = step()
+    src = int(torch.argmax(v0[s:n - w]).item()) + s
+    t0 = 6000
+    toks = torch.arange(t0, t0 + ntie, device=DEV)
+    pages = wl.page_table[0, (toks // P).long()].long()
+    sp_ = wl.page_table[0, src // P].long()
+    kp = wl.k_pool[0]
+    kp[pages, :, (toks % P).long(), :] = kp[sp_, :, src % P, :].unsqueeze(0)
+    got, v = step()
+    tied = v[t0:t0 + ntie]
+    assert bool((tied == tied[0]).all()), "identical keys must give identical votes"
+    want, _ = O.select_topk(v.double().numpy(), n, k, s, w)
+    assert np.array_equal(got, want)
+    # the cut fell inside the tied group: some of it selected, the rest not, lower indices first
+    chosen = np.intersect1d(got, np.arange(t0, t0 + ntie))
+    assert 0 < len(chosen) < ntie and np.array_equal(chosen, np.arange(t0, t0 + len(chosen)))
