@@ -1041,6 +1041,34 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   __syncthreads();
   TS_MARK(1);
 
+  // which sequences need no selection (hits, empty domains, k <= 0, everything fits, top-p 1):
+  // decided before the scan so that the vote pass can build the first histogram level
+  if (a.phases & kPhSelect) {
+    if (tid == 0) {
+      #pragma unroll 1
+      for (int b = 0; b < B; ++b) {
+        SeqState& st = sm.seq[b];
+        const int len = st.hi - st.lo;
+        if (st.hit || len <= 0) {
+          st.done = 1;
+          st.all = !st.hit && len > 0;
+        } else if (a.mode == TS_SELECT_TOPK) {
+          if (a.k <= 0) {
+            st.done = 1;
+            st.prefix = 0xffffffffu;     // above every finite vote: nothing selected
+            st.mask = 0xffffffffu;
+          } else if (len <= a.k) {
+            st.done = 1;
+            st.all = 1;
+          }
+        } else if (a.take_all_topp) {
+          st.done = 1;
+          st.all = 1;
+        }
+      }
+    }
+    __syncthreads();
+  }
   // ========================================================================= SCORE
   if ((a.phases & kPhScore) && sm.ptot > 0) {   // nothing to scan when every sequence hits
     // each head's normaliser over the CTAs of the sequence, then the votes of my tokens for
@@ -1367,29 +1395,6 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     unsigned long long* scand = reinterpret_cast<unsigned long long*>(ring);
     unsigned char* bat = ring;
     const bool topp = a.mode == TS_SELECT_TOPP;
-    if (tid == 0) {
-      #pragma unroll 1
-      for (int b = 0; b < B; ++b) {
-        SeqState& st = sm.seq[b];
-        const int len = st.hi - st.lo;
-        if (st.hit || len <= 0) {
-          st.done = 1;
-          st.all = !st.hit && len > 0;
-        } else if (a.mode == TS_SELECT_TOPK) {
-          if (a.k <= 0) {
-            st.done = 1;
-            st.prefix = 0xffffffffu;     // above every finite vote: nothing selected
-            st.mask = 0xffffffffu;
-          } else if (len <= a.k) {
-            st.done = 1;
-            st.all = 1;
-          }
-        } else if (a.take_all_topp) {
-          st.done = 1;
-          st.all = 1;
-        }
-      }
-    }
     __syncthreads();
 #pragma unroll 1   // one copy of the level code: it runs once per level and is fetched cold
     for (int level = 0; level < 3; ++level) {
@@ -1436,10 +1441,17 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         }
         __syncthreads();
         #pragma unroll 1
-        for (int i = tid; i < nbins; i += blockDim.x) {
-          if (sh[i]) {
-            atomicAdd(&gh[(size_t)b * kHistPerSeq + i], sh[i]);
-            if (topp) atomicAdd(&gm[(size_t)b * kHistPerSeq + i], smh[i]);
+        for (int i4 = tid; i4 < nbins / 4; i4 += blockDim.x) {
+          const uint4 cv = reinterpret_cast<const uint4*>(sh)[i4];
+          if (cv.x | cv.y | cv.z | cv.w) {
+            const unsigned c4[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (c4[j]) {
+                atomicAdd(&gh[(size_t)b * kHistPerSeq + 4 * i4 + j], c4[j]);
+                if (topp) atomicAdd(&gm[(size_t)b * kHistPerSeq + 4 * i4 + j], smh[4 * i4 + j]);
+              }
+            }
           }
         }
         if (level == 0) {
