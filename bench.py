@@ -66,8 +66,6 @@ def case_main(args):
     import workloads as W
     cfg, theta = CASES[args.case]
     sp = W.spec(3, layers=1) if cfg == "3x1" else W.spec(cfg)
-    if sp.mode == "topp":
-        raise SystemExit("the top-p workload has no graph bench yet")
     b = DecodeBench(sp, "cuda:0", theta=theta)
     if args.phases:
         for i in range(args.steps):
@@ -260,9 +258,12 @@ class DecodeBench:
         B, L, H, d = sp.batch, sp.layers, sp.n_q_heads, sp.head_dim
         self.ctx = T.Context(H, sp.n_kv_heads, d, T.TS_KV_BF16 if sp.kv_dtype == "bf16" else T.TS_KV_F32, B,
                              wl.page_table.shape[1], wl.num_pages)
-        self.cache = self.ctx.cache(L, sp.k)
-        self.params = T.params(k=sp.k, n_sink=sp.n_sink, n_local=sp.n_local, theta=theta)
-        cap = sp.k + sp.n_sink + sp.n_local
+        topp = sp.mode == "topp"
+        # top-p keeps a data-dependent count, up to every cached token
+        cap = self.ctx.max_tokens if topp else sp.k + sp.n_sink + sp.n_local
+        self.cache = self.ctx.cache(L, self.ctx.max_tokens if topp else sp.k)
+        self.params = T.params(mode=T.TS_SELECT_TOPP if topp else T.TS_SELECT_TOPK, k=sp.k, top_p=sp.top_p,
+                               n_sink=sp.n_sink, n_local=sp.n_local, theta=theta)
         z = dict(device=device)
         self.q_buf = [torch.zeros(B, H, d, **z) for _ in range(L)]
         self.seq_buf = torch.zeros(B, dtype=torch.int32, **z)
@@ -600,6 +601,15 @@ def main(argv=None):
                                               "miss_step_gbs") if k in s2}
             del b2
         torch.cuda.empty_cache()
+        sp4 = W.spec(4)
+        for name, theta in (("topp_b4_n256k_theta0.9", sp4.theta), ("topp_b4_n256k_miss_only", 2.0)):
+            b4 = DecodeBench(sp4, dev, theta=theta, seed_offset=rank)
+            s4 = summarise(b4, b4.run(sp4.steps, 3, flush=False), peak_gbs)
+            extras[name] = {k: s4[k] for k in ("value", "ms_per_step", "hit_rate", "step_gbs", "score_gbs",
+                                              "miss_step_gbs", "score_us_per_launch") if k in s4}
+            extras[name]["top_p"] = sp4.top_p
+            del b4
+            torch.cuda.empty_cache()
         sp3 = W.spec(3)
         for name, theta in (("n1m_theta0.9", sp3.theta), ("n1m_miss_only", 2.0)):
             b3 = DecodeBench(sp3, dev, theta=theta, seed_offset=rank)

@@ -289,6 +289,26 @@ __device__ __noinline__ int block_scan(int x, int* wsum, int& total) {
   return r;
 }
 
+// The number of entries below x1 and below x2 in the ascending list a[0, n) (global or shared
+// memory: generic loads), by one warp (32-ary narrowing with ballots; four rounds for a quarter
+// of a million entries), so that several lists are searched at once by different warps.
+__device__ __noinline__ void warp_lower_bound2(const int32_t* a, int n, int x1, int x2, int& r1, int& r2) {
+  const int lane = threadIdx.x & 31;
+  int lo1 = 0, hi1 = n, lo2 = 0, hi2 = n;
+  while (hi1 - lo1 > 32 || hi2 - lo2 > 32) {   // warp-uniform
+    const int st1 = (hi1 - lo1 + 31) / 32, st2 = (hi2 - lo2 + 31) / 32;
+    const int p1 = lo1 + lane * st1, p2 = lo2 + lane * st2;
+    const int c1 = __popc(__ballot_sync(kFull, p1 < hi1 && a[p1] < x1));
+    const int c2 = __popc(__ballot_sync(kFull, p2 < hi2 && a[p2] < x2));
+    if (c1 > 0) lo1 = lo1 + (c1 - 1) * st1 + 1;
+    hi1 = min(hi1, lo1 + st1);
+    if (c2 > 0) lo2 = lo2 + (c2 - 1) * st2 + 1;
+    hi2 = min(hi2, lo2 + st2);
+  }
+  r1 = lo1 + __popc(__ballot_sync(kFull, lo1 + lane < hi1 && a[lo1 + lane] < x1));
+  r2 = lo2 + __popc(__ballot_sync(kFull, lo2 + lane < hi2 && a[lo2 + lane] < x2));
+}
+
 // The crossing bin of a histogram scan.
 struct Cross {
   int bin;                       // bin index, -1 when the total falls short
@@ -738,10 +758,12 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     // few sequences: q, C_Q and the used part of C_T of every filled entry arrive in shared
     // memory in one bulk-copy transaction (one round trip instead of one per operand)
     const int cap16 = (a.cap + 8 + 3) & ~3;   // ints per staged C_T: the entries plus alignment slack, 16-byte rows
-    const size_t per_b = (size_t)(2 * HD + cap16) * 4;
     unsigned char* stg = dsm + (((size_t)B * 5 * S::NW * 4 + 15) & ~(size_t)15);
-    const bool staged = have_cache && B * per_b + (stg - dsm) <= (size_t)(a.dyn_bytes - a.flag_cap) &&
-                        (reinterpret_cast<uintptr_t>(a.q) & 15) == 0 && (HD * 4) % 16 == 0;
+    const size_t room_b = (size_t)(a.dyn_bytes - a.flag_cap) - (size_t)(stg - dsm);
+    const bool stage_ct = (size_t)B * (2 * HD + cap16) * 4 <= room_b;     // C_T too (top-k sizes)
+    const size_t per_b = (size_t)(2 * HD + (stage_ct ? cap16 : 0)) * 4;
+    const bool staged = have_cache && B * per_b <= room_b && (reinterpret_cast<uintptr_t>(a.q) & 15) == 0 &&
+                        (HD * 4) % 16 == 0;
     if (staged) {
       if (tid == 0) {
         uint32_t bytes = 0;
@@ -749,7 +771,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           if (!sm.filled[b]) continue;
           const uintptr_t c0 = reinterpret_cast<uintptr_t>(a.ct + (size_t)b * a.cap);
           const uintptr_t c1 = reinterpret_cast<uintptr_t>(a.ct + (size_t)b * a.cap + sm.ctc[b]);
-          const uint32_t ctbytes = (uint32_t)(((c1 + 15) & ~(uintptr_t)15) - (c0 & ~(uintptr_t)15));
+          const uint32_t ctbytes = stage_ct ? (uint32_t)(((c1 + 15) & ~(uintptr_t)15) - (c0 & ~(uintptr_t)15)) : 0u;
           bytes += (check ? 2u * HD * 4u : 0u) + ctbytes;
         }
         fence_proxy_async_global();
@@ -762,11 +784,13 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
             bulk_g2s(d, a.q + (size_t)b * HD, (uint32_t)HD * 4u, &xbar);
             bulk_g2s(d + HD * 4, a.cq + (size_t)b * HD, (uint32_t)HD * 4u, &xbar);
           }
-          const uintptr_t c0 = reinterpret_cast<uintptr_t>(a.ct + (size_t)b * a.cap);
-          const uintptr_t c1 = reinterpret_cast<uintptr_t>(a.ct + (size_t)b * a.cap + sm.ctc[b]);
-          const uint32_t ctbytes = (uint32_t)(((c1 + 15) & ~(uintptr_t)15) - (c0 & ~(uintptr_t)15));
-          if (ctbytes) bulk_g2s(d + 2 * HD * 4, reinterpret_cast<const void*>(c0 & ~(uintptr_t)15), ctbytes, &xbar);
-          sm.ctst[b] = (int)(d + 2 * HD * 4 - dsm) + (int)(c0 & 15);
+          if (stage_ct) {
+            const uintptr_t c0 = reinterpret_cast<uintptr_t>(a.ct + (size_t)b * a.cap);
+            const uintptr_t c1 = reinterpret_cast<uintptr_t>(a.ct + (size_t)b * a.cap + sm.ctc[b]);
+            const uint32_t ctbytes = (uint32_t)(((c1 + 15) & ~(uintptr_t)15) - (c0 & ~(uintptr_t)15));
+            if (ctbytes) bulk_g2s(d + 2 * HD * 4, reinterpret_cast<const void*>(c0 & ~(uintptr_t)15), ctbytes, &xbar);
+            sm.ctst[b] = (int)(d + 2 * HD * 4 - dsm) + (int)(c0 & 15);
+          }
         }
       }
       const bool landed = mbar_wait(&xbar, xph);
@@ -803,22 +827,41 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           cr[(b * 3 + 2) * S::NW + warp] = yy;
         }
       }
-      const int32_t* ctb = staged ? reinterpret_cast<const int32_t*>(sb + 2 * HD * 4) +
-                                        ((reinterpret_cast<uintptr_t>(a.ct + (size_t)b * a.cap) & 15) >> 2)
-                                  : a.ct + (size_t)b * a.cap;
+      const int32_t* ctb = sm.ctst[b] >= 0 ? reinterpret_cast<const int32_t*>(dsm + sm.ctst[b])
+                                           : a.ct + (size_t)b * a.cap;
       const int se = sm.seq[b].s_end, ls = sm.seq[b].ls;
       int below_s = 0, below_l = 0;
+      if (sm.ctc[b] > 4096) {
+        // long lists (top-p selections) are searched below, one warp per sequence
+      } else {
 #pragma unroll 4
-      for (int j = tid; j < sm.ctc[b]; j += blockDim.x) {
-        const int v = ctb[j];
-        below_s += v < se;
-        below_l += v < ls;
+        for (int j = tid; j < sm.ctc[b]; j += blockDim.x) {
+          const int v = ctb[j];
+          below_s += v < se;
+          below_l += v < ls;
+        }
+        below_s = warp_sum_i(below_s);
+        below_l = warp_sum_i(below_l);
+        if (lane == 0) {
+          cn[(b * 2 + 0) * S::NW + warp] = below_s;
+          cn[(b * 2 + 1) * S::NW + warp] = below_l;
+        }
       }
-      below_s = warp_sum_i(below_s);
-      below_l = warp_sum_i(below_l);
+    }
+    // long cached lists: entries below s_end and ls by a 32-ary search, one warp per sequence
+    #pragma unroll 1
+    for (int b = warp; b < B; b += S::NW) {
+      if (!sm.filled[b] || sm.ctc[b] <= 4096) continue;
+      const int32_t* ctb = sm.ctst[b] >= 0 ? reinterpret_cast<const int32_t*>(dsm + sm.ctst[b])
+                                           : a.ct + (size_t)b * a.cap;
+      int r1, r2;
+      warp_lower_bound2(ctb, sm.ctc[b], sm.seq[b].s_end, sm.seq[b].ls, r1, r2);
       if (lane == 0) {
-        cn[(b * 2 + 0) * S::NW + warp] = below_s;
-        cn[(b * 2 + 1) * S::NW + warp] = below_l;
+        #pragma unroll 1
+        for (int w = 0; w < S::NW; ++w) {
+          cn[(b * 2 + 0) * S::NW + w] = w == 0 ? r1 : 0;
+          cn[(b * 2 + 1) * S::NW + w] = w == 0 ? r2 : 0;
+        }
       }
     }
     __syncthreads();
