@@ -40,17 +40,24 @@ def test_qwen_batched_small_both_paths(multi):
     _run(sp, 3, multi_kernel=multi)
 
 
-@pytest.mark.parametrize("scan", ["tensor", "cuda"])
+@pytest.mark.parametrize("scan", ["tensor", "tensor-claim", "cuda"])
 def test_llama_scan_paths(scan, monkeypatch):
-    # bf16 pages of 8 KV heads scan on the tensor cores unless TOKENSELECT_NO_TC=1
+    # bf16 pages of 8 KV heads scan on the tensor cores unless TOKENSELECT_NO_TC=1; with
+    # TOKENSELECT_SCAN_CLAIM=1 the CTAs claim pages from a shared counter
     if scan == "cuda":
         monkeypatch.setenv("TOKENSELECT_NO_TC", "1")
+    if scan == "tensor-claim":
+        monkeypatch.setenv("TOKENSELECT_SCAN_CLAIM", "1")
     sp = W.spec(1, n0=(20011,), steps=3, k=1024, n_local=128)
     _run(sp, 3)
 
 
-def test_llama_batched_two_sequences_per_cta():
-    # every CTA range meets at most two sequences: tensor-core scan with two query images
+@pytest.mark.parametrize("claim", [False, True])
+def test_llama_batched_two_sequences_per_cta(claim, monkeypatch):
+    # two sequences: every CTA range meets at most two of them (or, claiming pages, every CTA
+    # holds both query images and takes pages of either)
+    if claim:
+        monkeypatch.setenv("TOKENSELECT_SCAN_CLAIM", "1")
     sp = W.spec(1, n0=(40000, 33001), n0_range=None, batch=2, steps=2, k=512, n_local=64)
     _run(sp, 2, theta=2.0)
 

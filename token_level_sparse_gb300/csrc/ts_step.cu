@@ -49,6 +49,7 @@ constexpr int kMaxG = kMaxScanG;   // query heads per KV head
 constexpr int kMaxAttH = 64;       // query heads of the attention phase
 constexpr int kPreFix = 512;       // fixed attention tokens of a CTA resolved at set-up
 constexpr int kMaxPagesCta = 1024; // page ids of a CTA's range kept in shared memory
+constexpr int kScanClaim = 2;      // pages per claim of a shared tensor-core scan
 constexpr int kMaxSlots = 12;      // ring slots (runtime count per launch)
 constexpr int64_t kLogitL2Budget = 48ll << 20;  // default bytes of logits one scan wave keeps in L2
 // radix levels over the vote bits (votes are >= +0, bit 31 is always 0): bits 30..17, 16..6,
@@ -140,13 +141,17 @@ struct StepShape {
 };
 
 struct GridSync {
-  unsigned count, gen, abort, pad;
+  unsigned count;   // barrier arrivals since the launch
+  unsigned abort;
+  unsigned claim;   // next page chunk of a shared tensor-core scan
+  unsigned pad;
 };
 
 struct StepKArgs {
   CUtensorMap tmap_k;          // K pool as [num_pages * H_kv * 16][d] bf16, box 64 x 128, 128-byte swizzle
   int tc;                      // the tensor-core scan may run (map encoded, geometry supported)
   int nslot_tc;                // its ring slots
+  int scan_dyn;                // it may share pages out by claims when at most two sequences scan
   int phases;
   int B, H, max_tokens, pt_stride;
   int64_t num_pages;
@@ -209,23 +214,25 @@ __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// All CTAs of the cooperative grid meet here. False after a time-out or an
-// abort raised by another CTA; the caller then returns.
-__device__ __noinline__ bool grid_sync(GridSync* gs, int* status) {
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// All CTAs of the cooperative grid meet here. The arrival counter only grows
+// (zeroed before each launch): barrier e of the launch is passed once it
+// reaches (e + 1) x grid size, so the last CTA to arrive releases the others
+// with its own increment. *epoch (shared memory, thread 0 only) counts this
+// CTA's barriers. False after a time-out or an abort raised by another CTA;
+// the caller then returns.
+__device__ __noinline__ bool grid_sync(GridSync* gs, int* status, unsigned* epoch) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    const unsigned gen0 = ld_acquire(&gs->gen);
-    __threadfence();
-    const unsigned arrived = atomicAdd(&gs->count, 1u) + 1u;
-    if (arrived == gridDim.x) {
-      atomicExch(&gs->count, 0u);
-      __threadfence();
-      st_release(&gs->gen, gen0 + 1u);
-    } else {
+    const unsigned target = (*epoch + 1u) * gridDim.x;
+    *epoch += 1u;
+    fence_acq_rel_gpu();                      // the CTA's writes (ordered by the CTA barrier) first
+    if (atomicAdd(&gs->count, 1u) + 1u < target) {
       const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire(&gs->gen) == gen0) {
+      while (ld_acquire(&gs->count) < target) {
         if (ld_acquire(&gs->abort)) {
           ok = 0;
           break;
@@ -236,10 +243,10 @@ __device__ __noinline__ bool grid_sync(GridSync* gs, int* status) {
           ok = 0;
           break;
         }
-        __nanosleep(64);
+        __nanosleep(32);
       }
     }
-    __threadfence();
+    fence_acq_rel_gpu();                      // then everything the others wrote before arriving
     s_ok = ok;
   }
   __syncthreads();
@@ -428,10 +435,14 @@ struct Smem {
   unsigned long long x_m[kMaxB];
   float att_m[kMaxAttH], att_l[kMaxAttH], att_c[kMaxAttH];  // attention: running max, sum, round correction
   int use_tc;                      // this launch scans with the tensor cores
+  int scan_dyn;                    // its pages are claimed from a shared counter, not partitioned
+  int tc_nimg, tc_seq[2];          // query images of the scan and the sequence of each
+  int tc_img_of[kMaxB];            // image of sequence b, or -1
   uint32_t tmem;                   // TMEM base address of the accumulators
   int acc_tl[2], acc_nv[2], acc_sg[2];  // per accumulator buffer: first token, valid rows, segment
   int my_pages[kMaxPagesCta];  // physical page ids of my range (first kMaxPagesCta pages)
   int timed_out;
+  unsigned gepoch;                 // grid barriers passed (thread 0)
   int wsum[33];
   int flag;
   float red_f[3][32];
@@ -669,6 +680,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   __shared__ __align__(8) uint64_t drainb;            // every MMA issued has completed
   __shared__ __align__(8) uint64_t abar;
   __shared__ __align__(8) uint64_t xbar;              // bulk copies of partials (vote, merge)
+  __shared__ __align__(8) uint64_t vbar[2];           // chunks of my logits for the votes
 
   const int nslot = a.nslot;
   unsigned char* ring = dsm;                                               // nslot x STAGE_BYTES of K
@@ -699,12 +711,14 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
 
   TS_MARK(0);
   if (tid == 0) {
+    #pragma unroll 1
     for (int s = 0; s < kMaxSlots; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
       sm.stage_done[s] = 0;
       sm.slot_last[s] = -1;
     }
+    #pragma unroll 1
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accf[i], 2);     // the MMAs' commit and the issuer's own arrive (metadata)
       mbar_init(&acce[i], 128);   // every epilogue thread
@@ -712,8 +726,11 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     mbar_init(&drainb, 1);
     mbar_init(&abar, 1);
     mbar_init(&xbar, 1);
+    mbar_init(&vbar[0], 1);
+    mbar_init(&vbar[1], 1);
     mbar_fence_init();
     sm.timed_out = 0;
+    sm.gepoch = 0u;
   }
 
   // ------------------------------------------------ setup: lengths, cache test, partition
@@ -738,6 +755,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     }
     st.hit = (!(a.phases & kPhCheck) && a.hit_in) ? (a.hit_in[b] != 0) : 0;
     sm.my_seg_of[b] = -1;
+    sm.tc_img_of[b] = -1;
     sm.ct_lo[b] = 0;
     sm.ct_hi[b] = 0;
     sm.filled[b] = have_cache ? a.filled[b] : 0;
@@ -767,6 +785,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     if (staged) {
       if (tid == 0) {
         uint32_t bytes = 0;
+        #pragma unroll 1
         for (int b = 0; b < B; ++b) {
           if (!sm.filled[b]) continue;
           const uintptr_t c0 = reinterpret_cast<uintptr_t>(a.ct + (size_t)b * a.cap);
@@ -776,6 +795,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         }
         fence_proxy_async_global();
         mbar_arrive_expect_tx(&xbar, bytes);
+        #pragma unroll 1
         for (int b = 0; b < B; ++b) {
           if (!sm.filled[b]) continue;
           unsigned char* d = stg + b * per_b;
@@ -811,7 +831,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         const float* x = staged ? reinterpret_cast<const float*>(sb) : a.q + (size_t)b * HD;
         const float* y = staged ? reinterpret_cast<const float*>(sb + HD * 4) : a.cq + (size_t)b * HD;
         float xy = 0.f, xx = 0.f, yy = 0.f;
-#pragma unroll 8
+#pragma unroll 2
         for (int i = tid; i < HD; i += blockDim.x) {
           const float u = x[i], v = y[i];
           xy = fmaf(u, v, xy);
@@ -834,7 +854,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       if (sm.ctc[b] > 4096) {
         // long lists (top-p selections) are searched below, one warp per sequence
       } else {
-#pragma unroll 4
+#pragma unroll 1
         for (int j = tid; j < sm.ctc[b]; j += blockDim.x) {
           const int v = ctb[j];
           below_s += v < se;
@@ -870,6 +890,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       if (!sm.filled[b]) continue;
       if (check) {
         KahanF sxy, sxx, syy;                                         // fp32: FP64 is a slow pipe here
+        #pragma unroll 1
         for (int w = 0; w < S::NW; ++w) {
           sxy.add(cr[(b * 3 + 0) * S::NW + w]);
           sxx.add(cr[(b * 3 + 1) * S::NW + w]);
@@ -880,6 +901,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         sm.seq[b].hit = (cs >= a.theta) ? 1 : 0;
       }
       int lo = 0, hi = 0;
+      #pragma unroll 1
       for (int w = 0; w < S::NW; ++w) {
         lo += cn[(b * 2 + 0) * S::NW + w];
         hi += cn[(b * 2 + 1) * S::NW + w];
@@ -962,6 +984,23 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       }
     }
     sm.use_tc = use_tc;
+    // with at most two sequences to scan every CTA holds both query images, and the pages are
+    // claimed in chunks from a counter so that CTAs with more bandwidth take more of them;
+    // otherwise each CTA scans its own range with the images of its segments
+    int nsc = 0;
+    #pragma unroll 1
+    for (int b = 0; b < B; ++b) nsc += sm.seq[b].pg1 > sm.seq[b].pg0;
+    sm.scan_dyn = use_tc && a.scan_dyn && nsc <= 2;
+    sm.tc_nimg = 0;
+    if (use_tc) {
+      #pragma unroll 1
+      for (int b = 0; b < B; ++b) {
+        const bool mine = sm.scan_dyn ? sm.seq[b].pg1 > sm.seq[b].pg0 : sm.my_seg_of[b] >= 0;
+        if (!mine) continue;
+        sm.tc_img_of[b] = sm.tc_nimg;
+        sm.tc_seq[sm.tc_nimg++] = b;
+      }
+    }
     // scan waves: the most KV heads per wave (a power-of-two divisor of H_kv) whose
     // logits stay within the L2 budget (the tensor-core scan takes every head at once)
     int hpw = HKV;
@@ -976,6 +1015,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     sm.flag = 0;
     // attention: how many fixed tokens (round-robin share) of every sequence are mine
     int tot = 0;
+    #pragma unroll 1
     for (int b = 0; b < B; ++b) {
       const SeqState& st = sm.seq[b];
       int nfix = st.s_end + (st.n - st.ls);
@@ -992,55 +1032,63 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
     return;  // the same decision in every CTA, before any grid barrier
   }
   TS_MARK(7);
-  if (c == 0 && tid < B && (a.phases & kPhCheck) && a.hit_out) a.hit_out[tid] = (uint8_t)sm.seq[tid].hit;
-  // page ids of my range, read once (ring refills and attention gathers need no global load),
-  // and in the same pass my share of every sequence's fixed attention tokens -- sinks and
-  // window, plus the cached indices on a hit -- with their page ids
-  #pragma unroll 1
-  for (int i = tid; i < min(sm.p1 - sm.p0, kMaxPagesCta); i += blockDim.x) {
-    const int gp = sm.p0 + i;
-    int sg = 0;
-    while (sg + 1 < sm.nseg && gp >= sm.seg_pend[sg]) ++sg;
-    const int b = sm.seg_b[sg];
-    sm.my_pages[i] = a.page_table[(size_t)b * a.pt_stride + (gp - sm.seq[b].pg0)];
-  }
-  if (sm.pf_ok) {
+  // the tensor-core scan runs this launch: warps 8.. finish the set-up while the pages stream
+  const bool tc_scan = S::TC && sm.use_tc && (a.phases & kPhScore) && sm.ptot > 0;
+  // set-up needed only after the scan
+  auto late_setup = [&](int ltid, int lth) {
+    // page ids of my range, read once (ring refills and attention gathers need no global load),
+    // and in the same pass my share of every sequence's fixed attention tokens -- sinks and
+    // window, plus the cached indices on a hit -- with their page ids
     #pragma unroll 1
-    for (int i = tid; i < sm.pf_off[B]; i += blockDim.x) {
-      int b = 0;
-      while (b + 1 < B && sm.pf_off[b + 1] <= i) ++b;
-      const SeqState& st = sm.seq[b];
-      const int f = c + (i - sm.pf_off[b]) * nCTA;
-      const int nmid = (st.hit && a.ct) ? sm.ct_hi[b] - sm.ct_lo[b] : 0;
-      int t;
-      if (f < st.s_end) {
-        t = f;
-      } else if (f < st.s_end + nmid) {
-        const int j = sm.ct_lo[b] + (f - st.s_end);
-        t = sm.ctst[b] >= 0 ? reinterpret_cast<const int32_t*>(dsm + sm.ctst[b])[j] : a.ct[(size_t)b * a.cap + j];
-      } else {
-        t = st.ls + (f - st.s_end - nmid);
+    for (int i = ltid; i < min(sm.p1 - sm.p0, kMaxPagesCta); i += lth) {
+      const int gp = sm.p0 + i;
+      int sg = 0;
+      while (sg + 1 < sm.nseg && gp >= sm.seg_pend[sg]) ++sg;
+      const int b = sm.seg_b[sg];
+      sm.my_pages[i] = a.page_table[(size_t)b * a.pt_stride + (gp - sm.seq[b].pg0)];
+    }
+    if (sm.pf_ok) {
+      #pragma unroll 1
+      for (int i = ltid; i < sm.pf_off[B]; i += lth) {
+        int b = 0;
+        while (b + 1 < B && sm.pf_off[b + 1] <= i) ++b;
+        const SeqState& st = sm.seq[b];
+        const int f = c + (i - sm.pf_off[b]) * nCTA;
+        const int nmid = (st.hit && a.ct) ? sm.ct_hi[b] - sm.ct_lo[b] : 0;
+        int t;
+        if (f < st.s_end) {
+          t = f;
+        } else if (f < st.s_end + nmid) {
+          const int j = sm.ct_lo[b] + (f - st.s_end);
+          // (the staged copy lies in the ring, which the producer may be filling)
+          t = (!tc_scan && sm.ctst[b] >= 0) ? reinterpret_cast<const int32_t*>(dsm + sm.ctst[b])[j]
+                                            : a.ct[(size_t)b * a.cap + j];
+        } else {
+          t = st.ls + (f - st.s_end - nmid);
+        }
+        sm.pf_t[i] = t;
+        sm.pf_p[i] = (t >= 0 && t < a.max_tokens) ? a.page_table[(size_t)b * a.pt_stride + t / S::P] : -1;
       }
-      sm.pf_t[i] = t;
-      sm.pf_p[i] = (t >= 0 && t < a.max_tokens) ? a.page_table[(size_t)b * a.pt_stride + t / S::P] : -1;
     }
-  }
-  if (a.phases & kPhSelect) {
-    // zero the selection histograms (first touched after a barrier)
-    const size_t nh = (size_t)B * kHistPerSeq;
-    #pragma unroll 1
-    for (size_t i = (size_t)c * blockDim.x + tid; i < nh; i += (size_t)nCTA * blockDim.x) {
-      a.hist[i] = 0u;
-      if (a.mode == TS_SELECT_TOPP) a.mass[i] = 0ull;
+    if (a.phases & kPhSelect) {
+      // zero the selection histograms (first touched after a barrier)
+      const size_t nh = (size_t)B * kHistPerSeq;
+      #pragma unroll 1
+      for (size_t i = (size_t)c * lth + ltid; i < nh; i += (size_t)nCTA * lth) {
+        a.hist[i] = 0u;
+        if (a.mode == TS_SELECT_TOPP) a.mass[i] = 0ull;
+      }
+      if (c == 0 && ltid < B) a.cand_n[ltid] = 0u;
     }
-    if (c == 0 && tid < B) a.cand_n[tid] = 0u;
-  }
+  };
+  if (c == 0 && tid < B && (a.phases & kPhCheck) && a.hit_out) a.hit_out[tid] = (uint8_t)sm.seq[tid].hit;
+  if (!tc_scan) late_setup(tid, (int)blockDim.x);
   if constexpr (S::TC) {
     if (sm.use_tc) {
       // B operand of each of my (at most two) sequences: row n = 3 h + term holds that term of
       // query head h, K-major in the 128-byte swizzle layout; rows past 3 H are zero
       constexpr int CH = D / 8;                        // 16-byte chunks of a row
-      const int total = sm.nseg * S::TC_N * CH;
+      const int total = sm.tc_nimg * S::TC_N * CH;
       #pragma unroll 1
       for (int i0 = tid; i0 < total; i0 += 2 * blockDim.x) {   // two chunks' loads in flight
         float4 qv[2][2];
@@ -1051,7 +1099,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           const int n = rem / CH, ch = rem % CH, h = n / 3;
           qv[k][0] = qv[k][1] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (i < total && h < H) {
-            const int b = sm.seg_b[sg], off = sm.qst[b];
+            const int b = sm.tc_seq[sg], off = sm.qst[b];
             // the query staged by the cache test, when it lies below the image region
             const float* qb = (off >= 0 && off + H * D * 4 <= (int)(tcb - dsm))
                                   ? reinterpret_cast<const float*>(dsm + off)
@@ -1114,18 +1162,40 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   }
   // ========================================================================= SCORE
   if ((a.phases & kPhScore) && sm.ptot > 0) {   // nothing to scan when every sequence hits
+    // my logits [row = token of my range][HW] pass through shared memory past the vote scratch
+    // in chunks of whole rows by bulk copy, two buffers when the range does not fit at once
+    const size_t vsb = ((size_t)kMaxB * kMaxWaveHeads * 8 + (size_t)nCTA * H * 8 + S::NW * 32 * 8 + 15) &
+                       ~(size_t)15;
+    float* vbuf = reinterpret_cast<float*>(ring + vsb);
+    const int vrows = (sm.p1 - sm.p0) * S::P;
+    uint32_t vph = 0u;                                             // phase bit of each chunk buffer
+    auto chunk_rows = [&](int HW) -> int {
+      const int fit = (int)(((size_t)(a.dyn_bytes - a.flag_cap) - vsb) / ((size_t)HW * 4));
+      return vrows <= fit ? vrows : max(16, (fit / 2) & ~15);
+    };
+    auto issue_chunk = [&](const float* eb, int k, int HW, int crow) {   // thread 0
+      const uint32_t bytes = (uint32_t)min(crow, vrows - k * crow) * (uint32_t)HW * 4u;
+      const unsigned char* src = reinterpret_cast<const unsigned char*>(eb + (size_t)k * crow * HW);
+      unsigned char* dst = reinterpret_cast<unsigned char*>(vbuf + (size_t)(k & 1) * crow * HW);
+      fence_proxy_async_global();
+      mbar_arrive_expect_tx(&vbar[k & 1], bytes);
+      #pragma unroll 1
+      for (uint32_t o = 0; o < bytes; o += 32768u) bulk_g2s(dst + o, src + o, min(32768u, bytes - o), &vbar[k & 1]);
+    };
     // each head's normaliser over the CTAs of the sequence, then the votes of my tokens for
-    // heads [g0 G, g0 G + HW); eb holds my logits [token][HW]
-    auto vote_pass = [&](const float* eb, int g0, int HW, int wv) -> bool {
+    // heads [g0 G, g0 G + HW); eb holds my logits [row][HW], of which the first `pre` chunks
+    // are already on their way
+    auto vote_pass = [&](const float* eb, int g0, int HW, int wv, int pre) -> bool {
       float2* wz = reinterpret_cast<float2*>(ring);                // [segment][kMaxWaveHeads]: (max, 1 / sum)
       float2* pcs = wz + kMaxB * kMaxWaveHeads;                    // one segment's partials [cta][H]
       #pragma unroll 1
       for (int sg = 0; sg < sm.nseg; ++sg) {
         const SeqState& st = sm.seq[sm.seg_b[sg]];
-        const int ncta = st.last_cta - st.first_cta + 1;
+        // a shared scan leaves partials of every sequence in every CTA
+        const int fc = sm.scan_dyn ? 0 : st.first_cta, ncta = sm.scan_dyn ? nCTA : st.last_cta - st.first_cta + 1;
         float* rmx = reinterpret_cast<float*>(pcs + (size_t)ncta * H);   // [NW][32] per-slice maxima
         float* rz = rmx + S::NW * 32;                                    // [NW][32] per-slice sums
-        if (!bulk_fetch(pcs, a.partials + ((size_t)sm.seg_b[sg] * nCTA + st.first_cta) * H,
+        if (!bulk_fetch(pcs, a.partials + ((size_t)sm.seg_b[sg] * nCTA + fc) * H,
                         (uint32_t)(ncta * H * sizeof(float2)), nullptr, nullptr, 0u)) {
           if (tid == 0) atomicExch(&a.gsync->abort, 1u);
           return false;
@@ -1142,6 +1212,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         rmx[warp * 32 + lane] = m;
         __syncthreads();
         float M = -INFINITY;
+        #pragma unroll 1
         for (int w = 0; w < S::NW; ++w) M = fmaxf(M, rmx[w * 32 + lane]);
         KahanF kz;
         if (lh && M > -INFINITY)
@@ -1154,6 +1225,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         __syncthreads();
         if (warp == 0 && lh) {
           KahanF z;
+          #pragma unroll 1
           for (int w = 0; w < S::NW; ++w) z.add(rz[w * 32 + lane]);
           const float Z = z.s - z.c;
           wz[sg * kMaxWaveHeads + lane] = (M > -INFINITY && Z > 0.f) ? make_float2(M, 1.f / Z)
@@ -1162,52 +1234,79 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         __syncthreads();
         TS_MARK(14);
       }
-      // v_i (+)= sum over the wave's heads of exp(l - M) / Z
+      // v_i (+)= sum over the wave's heads of exp(l - M) / Z, chunk by chunk
+      const int crow = chunk_rows(HW), nch = (vrows + crow - 1) / crow;
+      if (tid == 0)
+        #pragma unroll 1
+        for (int k = pre; k < min(nch, 2); ++k) issue_chunk(eb, k, HW, crow);
+      const int q4 = HW >> 2;
+      int lpt = 1;                                  // lanes per row, one float4 (4 heads) each
+      while (lpt < q4) lpt <<= 1;
+      const bool coop = (HW & 3) == 0 && lpt <= 32;
+      const int tpi = 32 / lpt, rl = lane / lpt, qd = lane % lpt;
       #pragma unroll 1
-      for (int sg = 0; sg < sm.nseg; ++sg) {
-        const int b = sm.seg_b[sg], t0 = sm.seg_t0[sg], nt = sm.seg_ntok[sg];
-        float* vb = a.vote + (size_t)b * a.vote_stride + (size_t)sm.seg_lp0[sg] * S::P;
-        const float2* w = wz + sg * kMaxWaveHeads;
-        const int lpt = HW / 4;                       // lanes per token row, one float4 (4 heads) each
-        if ((HW & 3) == 0 && HW <= 32 && (32 % lpt) == 0) {
-          // warp-cooperative and coalesced: a load instruction covers 32 / lpt whole rows; each
-          // lane forms its 4 terms, then the lpt lanes of a row add theirs (xor tree)
-          const int tpi = 32 / lpt, rl = lane / lpt, qd = lane % lpt;
-          const float2 w0 = w[4 * qd], w1 = w[4 * qd + 1], w2 = w[4 * qd + 2], w3 = w[4 * qd + 3];
-          #pragma unroll 1
-          for (int tw = warp * 8 * tpi; tw < nt; tw += S::NW * 8 * tpi) {
-            float part[8];
+      for (int k = 0; k < nch; ++k) {
+        const bool landed = mbar_wait(&vbar[k & 1], (vph >> (k & 1)) & 1u);
+        vph ^= 1u << (k & 1);
+        if (!__syncthreads_and(landed)) {
+          if (tid == 0) {
+            set_error(a.status, TS_ERR_TIMEOUT);
+            atomicExch(&a.gsync->abort, 1u);
+            if (k + 1 < nch) mbar_wait(&vbar[(k + 1) & 1], (vph >> ((k + 1) & 1)) & 1u);   // in flight
+          }
+          return false;
+        }
+        const int r0 = k * crow, r1 = min(vrows, r0 + crow);
+        const float* cb = vbuf + (size_t)(k & 1) * crow * HW;   // row r at cb + (r - r0) HW
+        #pragma unroll 1
+        for (int sg = 0; sg < sm.nseg; ++sg) {
+          const int b = sm.seg_b[sg], t0 = sm.seg_t0[sg];
+          const int lo = max(t0, r0), hi = min(t0 + sm.seg_ntok[sg], r1);   // rows of the segment here
+          if (hi <= lo) continue;
+          float* vb = a.vote + (size_t)b * a.vote_stride + (size_t)sm.seg_lp0[sg] * S::P;   // row t0 + i -> i
+          const float2* w = wz + sg * kMaxWaveHeads;
+          if (coop) {
+            // warp-cooperative: a load instruction covers 32 / lpt whole rows; each lane forms its 4
+            // terms, then the lpt lanes of a row add theirs (xor tree)
+            float2 wl[4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int t = tw + k * tpi + rl;
-              float4 xv = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-              if (t < nt) xv = reinterpret_cast<const float4*>(eb + (size_t)(t0 + t) * HW)[qd];
-              part[k] = (expf(xv.x - w0.x) * w0.y + expf(xv.y - w1.x) * w1.y) +
-                        (expf(xv.z - w2.x) * w2.y + expf(xv.w - w3.x) * w3.y);
-            }
+            for (int i = 0; i < 4; ++i) wl[i] = qd < q4 ? w[4 * qd + i] : make_float2(INFINITY, 0.f);
             #pragma unroll 1
-            for (int d = lpt / 2; d >= 1; d >>= 1)
+            for (int rw = lo + warp * 2 * tpi; rw < hi; rw += S::NW * 2 * tpi) {
+              float part[2];
 #pragma unroll
-              for (int k = 0; k < 8; ++k) part[k] += __shfl_xor_sync(kFull, part[k], d);
-            if (qd == 0) {
+              for (int u = 0; u < 2; ++u) {
+                const int r = rw + u * tpi + rl;
+                float4 xv = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                if (r < hi && qd < q4) xv = reinterpret_cast<const float4*>(cb + (size_t)(r - r0) * HW)[qd];
+                part[u] = (expf(xv.x - wl[0].x) * wl[0].y + expf(xv.y - wl[1].x) * wl[1].y) +
+                          (expf(xv.z - wl[2].x) * wl[2].y + expf(xv.w - wl[3].x) * wl[3].y);
+              }
+              #pragma unroll 1
+              for (int d = lpt / 2; d >= 1; d >>= 1) {
+                part[0] += __shfl_xor_sync(kFull, part[0], d);
+                part[1] += __shfl_xor_sync(kFull, part[1], d);
+              }
 #pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                const int t = tw + k * tpi + rl;
-                if (t < nt) vb[t] = (wv == 0) ? part[k] : vb[t] + part[k];
+              for (int u = 0; u < 2; ++u) {
+                const int r = rw + u * tpi + rl;
+                if (qd == 0 && r < hi) vb[r - t0] = (wv == 0) ? part[u] : vb[r - t0] + part[u];
               }
             }
-          }
-        } else {
-          #pragma unroll 1
-          for (int t = tid; t < nt; t += blockDim.x) {
-            const float* row = eb + (size_t)(t0 + t) * HW;
-            KahanF acc;
+          } else {
             #pragma unroll 1
-            for (int hl = 0; hl < HW; ++hl) acc.add(expf(row[hl] - w[hl].x) * w[hl].y);
-            const float v = acc.s - acc.c;
-            vb[t] = (wv == 0) ? v : vb[t] + v;
+            for (int r = lo + tid; r < hi; r += blockDim.x) {
+              const float* row = cb + (size_t)(r - r0) * HW;
+              KahanF acc;
+              #pragma unroll 1
+              for (int hl = 0; hl < HW; ++hl) acc.add(expf(row[hl] - w[hl].x) * w[hl].y);
+              const float v = acc.s - acc.c;
+              vb[r - t0] = (wv == 0) ? v : vb[r - t0] + v;
+            }
           }
         }
+        __syncthreads();                            // buffer k & 1 is free again
+        if (tid == 0 && k + 2 < nch) issue_chunk(eb, k + 2, HW, crow);
       }
       __syncthreads();
       return true;
@@ -1220,10 +1319,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         // page (128 rows = H_kv heads x 16 tokens) by the query terms of its sequence into a
         // TMEM accumulator (two buffers); four warps read the accumulators out: logits to the
         // scratch, running (max, sum exp) per row and head in registers
-        const int np = sm.p1 - sm.p0;
         const int nsl = a.nslot_tc;
         float* eb = a.spill + (size_t)c * sm.region;             // [tok_stride][H]
-        float2* wpt = a.wpart + (size_t)c * 2 * 128 * G;         // [segment < 2][row][head of the row]
         if (warp == 2) {
           tmem_alloc(&sm.tmem, 2 * S::TC_COLS);
           tmem_relinquish();
@@ -1235,27 +1332,20 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         if (warp == 0) {
           if (lane == 0) {                                       // producer
             const uint64_t pol = l2_evict_first_policy();
-            int sg = 0;
-            for (int u = 0; u < np; ++u) {
+            int u = 0;                                           // ring uses so far
+            // page gp (of sequence b, physical page) into the next ring slot; false after a time-out
+            auto put = [&](int gp, int b, int page) -> bool {
               const int s = u % nsl;
-              if (u >= nsl && !mbar_wait(&empty[s], ((u / nsl) - 1) & 1)) {
-                set_error(a.status, TS_ERR_TIMEOUT);
-                sm.timed_out = 1;
-                break;
-              }
-              const int gp = sm.p0 + u;
-              while (sg + 1 < sm.nseg && gp >= sm.seg_pend[sg]) ++sg;
-              const int b = sm.seg_b[sg];
+              if (u >= nsl && !mbar_wait(&empty[s], ((u / nsl) - 1) & 1)) return false;
               const int lp = gp - sm.seq[b].pg0;
-              const int page = u < kMaxPagesCta ? sm.my_pages[u] : a.page_table[(size_t)b * a.pt_stride + lp];
               const bool valid = page >= 0 && (int64_t)page < a.num_pages;
-              sm.stage_tok[s][0] = u * S::P;
+              sm.stage_tok[s][0] = gp * S::P;
               sm.stage_b[s][0] = b;
               sm.stage_nv[s][0] = valid ? min(S::P, sm.seq[b].n - lp * S::P) : 0;
               sm.slot_last[s] = u;
               if (valid) {
                 mbar_arrive_expect_tx(&full[s], (uint32_t)S::TC_TILE);
-#pragma unroll
+      #pragma unroll
                 for (int h = 0; h < S::TC_HALVES; ++h)
                   tma_load_2d(tcr + (size_t)s * S::TC_TILE + h * (S::TC_TILE / S::TC_HALVES), &a.tmap_k, h * 64,
                               page * 128, &full[s], pol);
@@ -1263,12 +1353,101 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
                 set_error(a.status, TS_ERR_PAGE_OOB);
                 mbar_arrive(&full[s]);
               }
+              ++u;
+              return true;
+            };
+            bool ok = true;
+            if (sm.scan_dyn) {
+              // chunks of kScanClaim pages, claimed two ahead; the page ids of the next chunk load
+              // while the ring takes the current one
+              const int b0 = sm.tc_seq[0], b1 = sm.tc_nimg > 1 ? sm.tc_seq[1] : b0;
+              const int split = sm.tc_nimg > 1 ? sm.seq[b1].pg0 : sm.ptot;
+              auto load_ids = [&](int g0, int (&pid)[kScanClaim]) {
+#pragma unroll
+                for (int j = 0; j < kScanClaim; ++j) {
+                  const int gp = g0 + j, b = gp >= split ? b1 : b0;
+                  pid[j] = gp < sm.ptot ? a.page_table[(size_t)b * a.pt_stride + (gp - sm.seq[b].pg0)] : -1;
+                }
+              };
+              int c1 = (int)atomicAdd(&a.gsync->claim, 1u) * kScanClaim, p1[kScanClaim];
+              load_ids(c1, p1);
+              int c2 = (int)atomicAdd(&a.gsync->claim, 1u) * kScanClaim;
+              #pragma unroll 1
+              while (ok && c1 < sm.ptot) {
+                const int cur = c1;
+                int pid[kScanClaim];
+#pragma unroll
+                for (int j = 0; j < kScanClaim; ++j) pid[j] = p1[j];
+                c1 = c2;
+                load_ids(c1, p1);
+                c2 = (int)atomicAdd(&a.gsync->claim, 1u) * kScanClaim;
+                #pragma unroll 1   // one copy of put; pid (loaded a chunk ago) picked by selects
+                for (int j = 0; j < kScanClaim; ++j) {
+                  int pj = pid[0];
+#pragma unroll
+                  for (int k = 1; k < kScanClaim; ++k)
+                    if (j == k) pj = pid[k];
+                  if (ok && cur + j < sm.ptot) ok = put(cur + j, cur + j >= split ? b1 : b0, pj);
+                }
+              }
+            } else {
+              // my range, eight pages at a time; the next eight page ids load while the ring takes
+              // the current ones (warps 8.. fill my_pages meanwhile)
+              int sg = 0;
+              auto load_ids = [&](int g0, int (&pid)[8], int (&pb)[8]) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const int gp = g0 + j;
+                  while (sg + 1 < sm.nseg && gp >= sm.seg_pend[sg]) ++sg;
+                  pb[j] = sm.seg_b[sg];
+                  pid[j] = gp < sm.p1 ? a.page_table[(size_t)pb[j] * a.pt_stride + (gp - sm.seq[pb[j]].pg0)] : -1;
+                }
+              };
+              int np_[8], nb_[8];
+              load_ids(sm.p0, np_, nb_);
+              #pragma unroll 1
+              for (int gp0 = sm.p0; ok && gp0 < sm.p1; gp0 += 8) {
+                int pid[8], pb[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  pid[j] = np_[j];
+                  pb[j] = nb_[j];
+                }
+                if (gp0 + 8 < sm.p1) load_ids(gp0 + 8, np_, nb_);
+                #pragma unroll 1   // one copy of put; pid (loaded eight pages ago) picked by selects
+                for (int j = 0; j < 8; ++j) {
+                  int pj = pid[0], bj = pb[0];
+#pragma unroll
+                  for (int k = 1; k < 8; ++k)
+                    if (j == k) {
+                      pj = pid[k];
+                      bj = pb[k];
+                    }
+                  if (ok && gp0 + j < sm.p1) ok = put(gp0 + j, bj, pj);
+                }
+              }
+            }
+            if (ok) {                                            // end of the stream: a slot with no page
+              const int s = u % nsl;
+              if (u >= nsl && !mbar_wait(&empty[s], ((u / nsl) - 1) & 1)) {
+                ok = false;
+              } else {
+                sm.stage_nv[s][0] = -1;
+                mbar_arrive(&full[s]);
+              }
+            }
+            if (!ok) {
+              set_error(a.status, TS_ERR_TIMEOUT);
+              sm.timed_out = 1;
             }
           }
+        } else if (warp >= 8) {
+          late_setup(tid - 256, (int)blockDim.x - 256);
         } else if (warp == 1) {
           if (lane == 0) {                                       // MMA issuer
             constexpr uint32_t idesc = idesc_bf16_f32(128, S::TC_N);
-            for (int u = 0; u < np; ++u) {
+            #pragma unroll 1
+            for (int u = 0;; ++u) {
               const int s = u % nsl, buf = u & 1;
               if (!mbar_wait(&full[s], (u / nsl) & 1) || (u >= 2 && !mbar_wait(&acce[buf], ((u >> 1) - 1) & 1))) {
                 set_error(a.status, TS_ERR_TIMEOUT);
@@ -1276,10 +1455,15 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
                 break;
               }
               tc_fence_after();
-              const int b = sm.stage_b[s][0], nv = sm.stage_nv[s][0];
-              const int sgi = sm.my_seg_of[b];
-              sm.acc_tl[buf] = sm.stage_tok[s][0];
+              const int nv = sm.stage_nv[s][0];
               sm.acc_nv[buf] = nv;
+              if (nv < 0) {                // end of the stream, forwarded to the epilogue
+                umma_commit(&accf[buf]);
+                mbar_arrive(&accf[buf]);
+                break;
+              }
+              const int sgi = sm.tc_img_of[sm.stage_b[s][0]];
+              sm.acc_tl[buf] = sm.stage_tok[s][0];
               sm.acc_sg[buf] = sgi;
               if (nv > 0) {
                 const uint32_t a0 = smem_addr(tcr + (size_t)s * S::TC_TILE);
@@ -1304,13 +1488,36 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           float run_m[G];
           KahanF run_z[G];
           int cur = -1;
-          auto flush = [&]() {
-            if (cur >= 0)
+          // the partials of (image, head): the 16 rows of KV head g are 16 lanes of this warp; images
+          // this CTA never meets stay (-inf, 0)
+          float2* pt = a.partials + (size_t)c * H + g * G;        // + sequence * nCTA * H + j
+          if (t == 0)
+            #pragma unroll 1
+            for (int im = 0; im < sm.tc_nimg; ++im)
 #pragma unroll
-              for (int j = 0; j < G; ++j)
-                wpt[((size_t)cur * 128 + row) * G + j] = make_float2(run_m[j], run_z[j].s - run_z[j].c);
+              for (int j = 0; j < G; ++j) pt[(size_t)sm.tc_seq[im] * nCTA * H + j] = make_float2(-INFINITY, 0.f);
+          auto flush = [&]() {                                   // whole warp (cur is uniform)
+            if (cur < 0) return;
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+              float m = run_m[j];
+#pragma unroll
+              for (int d = 8; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, d));
+              const float rz = run_z[j].s - run_z[j].c;
+              float z = (m > -INFINITY && rz > 0.f) ? rz * expf(run_m[j] - m) : 0.f, zl = 0.f;
+#pragma unroll
+              for (int d = 8; d >= 1; d >>= 1) {                // compensated sum over the 16 lanes
+                const float oh = __shfl_xor_sync(kFull, z, d), ol = __shfl_xor_sync(kFull, zl, d);
+                float sum, err;
+                two_sum(z, oh, sum, err);
+                z = sum;
+                zl = (zl + ol) + err;
+              }
+              if (t == 0) pt[(size_t)sm.tc_seq[cur] * nCTA * H + j] = make_float2(m, z + zl);
+            }
           };
-          for (int u = 0; u < np; ++u) {
+          #pragma unroll 1
+          for (int u = 0;; ++u) {
             const int buf = u & 1;
             if (!__all_sync(kFull, mbar_wait(&accf[buf], (u >> 1) & 1))) {
               if (lane == 0) {
@@ -1320,7 +1527,9 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
               break;
             }
             tc_fence_after();
-            const int tl = sm.acc_tl[buf], nv = sm.acc_nv[buf], sgi = sm.acc_sg[buf];
+            const int nv = sm.acc_nv[buf];
+            if (nv < 0) break;
+            const int tl = sm.acc_tl[buf], sgi = sm.acc_sg[buf];
             float r[8 * S::TC_NLD];
 #pragma unroll
             for (int i = 0; i < S::TC_NLD; ++i)
@@ -1345,7 +1554,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
               const float lo = odd ? r[3 * G + 3 * j + 2] : r[3 * j + 2];
               x[j] = t < nv ? ((lo + mid) + hi) * a.scale : -INFINITY;
             }
-            float* dst = eb + (size_t)(tl + t) * H + g * G;
+            float* dst = a.spill + (size_t)(tl + t) * H + g * G;
             if constexpr (G == 4) {
               *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
             } else {
@@ -1378,6 +1587,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         __syncthreads();
         if (tid == 0 && sm.timed_out) {
           // copies issued but never consumed land before the CTA leaves
+          #pragma unroll 1
           for (int ss = 0; ss < nsl; ++ss)
             if (sm.slot_last[ss] >= 0) mbar_wait(&full[ss], (sm.slot_last[ss] / nsl) & 1);
         }
@@ -1391,35 +1601,36 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           return;
         }
         TS_MARK(2);
-        // ---- per (segment, head): combine the 16 rows' (max, sum exp) -> partials
-        #pragma unroll 1
-        for (int item = warp; item < sm.nseg * H; item += S::NW) {
-          const int sg = item / H, h = item % H, g = h / G, j = h % G;
-          float2 mz = make_float2(-INFINITY, 0.f);
-          if (lane < 16) mz = wpt[((size_t)sg * 128 + g * 16 + lane) * G + j];
-          const float m = warp_max(mz.x);
-          const float z = warp_sum_comp((m > -INFINITY && mz.y > 0.f) ? mz.y * expf(mz.x - m) : 0.f);
-          if (lane == 0) a.partials[((size_t)sm.seg_b[sg] * nCTA + c) * H + h] = make_float2(m, z);
-        }
         fence_proxy_async_global();
+        // the first chunk of my logits (all written by this CTA) comes back into shared memory
+        // while the other CTAs finish their scans
+        const int pre = (!sm.scan_dyn && vrows > 0) ? 1 : 0;
+        if (pre) {
+          __syncthreads();                                       // after every writer's proxy fence
+          if (tid == 0) issue_chunk(eb, 0, H, chunk_rows(H));
+        }
         TS_MARK(3);
-        if (!grid_sync(a.gsync, a.status)) return;
+        if (!grid_sync(a.gsync, a.status, &sm.gepoch)) {
+          if (tid == 0 && pre) mbar_wait(&vbar[0], 0u);         // lands before the CTA leaves
+          return;
+        }
         TS_MARK(4);
-        if (!vote_pass(eb, 0, H, 0)) return;
+        if (!vote_pass(eb, 0, H, 0, pre)) return;
       }
     }
     if (!scanned) {
       const int hpw = sm.hpw, HW = hpw * G, nwaves = sm.nwaves;
       float* eb = a.spill + (size_t)c * sm.region;   // my logits, token-major [tstride][HW]
       int stage_seq = 0;                             // ring use counter across waves
+      #pragma unroll 1
       for (int wv = 0; wv < nwaves; ++wv) {
         const int g0 = wv * hpw;
         if (!cuda_scan_wave<KT, D, HKV, G>(a, sm, ring, full, wv, stage_seq)) return;
         fence_proxy_async_global();
         TS_MARK(3 + 3 * min(wv, 5));
-        if (!grid_sync(a.gsync, a.status)) return;
+        if (!grid_sync(a.gsync, a.status, &sm.gepoch)) return;
         TS_MARK(4 + 3 * min(wv, 5));
-        if (!vote_pass(eb, g0, HW, wv)) return;
+        if (!vote_pass(eb, g0, HW, wv, 0)) return;
       }
     }
   }
@@ -1428,7 +1639,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   // ======================================================================== SELECT
   if (a.phases & kPhSelect) {
     if (!(a.phases & kPhScore) && sm.ptot > 0) {
-      if (!grid_sync(a.gsync, a.status)) return;   // the histograms are zero everywhere
+      if (!grid_sync(a.gsync, a.status, &sm.gepoch)) return;   // the histograms are zero everywhere
     }
     // shared memory while selecting, one use after another: this CTA's histogram (counts,
     // then masses at a fixed offset); after the barrier, the global histograms of a batch of
@@ -1470,7 +1681,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         const int tl0 = sm.seg_lp0[sg] * S::P;
         const int lo = max(st.lo, tl0), hi = min(st.hi, tl0 + sm.seg_ntok[sg]);
         const float* vb = a.vote + (size_t)b * a.vote_stride;
-        #pragma unroll 4
+        #pragma unroll 2
         for (int t = lo + tid; t < hi; t += blockDim.x) {
           const float v = __ldcg(vb + t);
           const uint32_t key = __float_as_uint(v);
@@ -1520,7 +1731,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       }
       fence_proxy_async_global();   // the histograms are read back by bulk copy
       TS_MARK(28 + level);
-      if (!grid_sync(a.gsync, a.status)) return;
+      if (!grid_sync(a.gsync, a.status, &sm.gepoch)) return;
       // every CTA finds the crossing bin of every unresolved sequence from shared copies of
       // the global histograms (bulk copies); level 0 in two steps: its 128 coarse bins, then
       // the 128 fine bins of the crossing coarse bin
@@ -1675,7 +1886,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       const int lo = max(st.lo, tl0), hi = min(st.hi, tl0 + sm.seg_ntok[sg]);
       const float* vb = a.vote + (size_t)b * a.vote_stride;
       int n_eq = 0;
-      #pragma unroll 2
+      #pragma unroll 1
       for (int t0 = lo; t0 < hi; t0 += blockDim.x) {
         const int t = t0 + tid;
         bool is = false;
@@ -1705,7 +1916,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       }
     }
     if (need_cand || need_tie) {
-      if (!grid_sync(a.gsync, a.status)) return;
+      if (!grid_sync(a.gsync, a.status, &sm.gepoch)) return;
     }
     if (need_tie) {
       // exact ties before mine, per segment, one warp each
@@ -1817,6 +2028,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       __syncthreads();
       if (tid == 0) {
         int tc = 0, ta = 0;
+        #pragma unroll 1
         for (int w = 0; w < S::NW; ++w) {
           tc += sm.red_i[0][w];
           ta += sm.red_i[1][w];
@@ -2081,7 +2293,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   TS_MARK(24);
   // ============================================== outputs, after one more barrier
   if (!(a.phases & (kPhSelect | kPhAttend))) return;
-  if (!grid_sync(a.gsync, a.status)) return;
+  if (!grid_sync(a.gsync, a.status, &sm.gepoch)) return;
   TS_MARK(25);
   if (a.phases & kPhAttend) {
     // merge the CTA partials of one (sequence, query head) per CTA pass: the item's rows and
@@ -2137,6 +2349,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       const float den = sm.red_f[0][0];
       if (tid < ncol) {
         float4 s4 = racc[tid];
+        #pragma unroll 1
         for (int g = 1; g < ngrp; ++g) {
           const float4 v = racc[g * ncol + tid];
           s4.x += v.x;
@@ -2330,7 +2543,8 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   // per-warp reductions; the merge one (sequence, head)'s CTA rows)
   if (nslot < S::MIN_SLOTS || dyn - flag_cap < lvl_bins(0) * 12 || dyn - flag_cap < kCandCap * 8 ||
       dyn - flag_cap < kMaxB * 128 * 12 ||
-      dyn - flag_cap < kMaxB * kMaxWaveHeads * 8 + ctx->num_sms * ctx->cfg.n_q_heads * 8 + 2 * 16 * 32 * 4 ||
+      dyn - flag_cap < kMaxB * kMaxWaveHeads * 8 + ctx->num_sms * ctx->cfg.n_q_heads * 8 + 2 * 16 * 32 * 4 + 16 +
+                           2 * 16 * kMaxWaveHeads * 4 ||   // vote scratch, then two chunks of 16 logit rows
       dyn < ctx->num_sms * (D * 4 + 8 + 4) + 8 + 16 + S::THREADS * 16)   // the merge's rows, pairs, weights
     return TS_ERR_UNSUPPORTED;
   if (!ensure_smem<step_kernel<KT, D, HKV, G>>((size_t)dyn, ctx->device)) {
@@ -2409,6 +2623,7 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   a.nslot = nslot;
   a.tc = 0;
   a.nslot_tc = 0;
+  a.scan_dyn = 0;
   if constexpr (S::TC) {
     // tensor-core scan: 1024-aligned ring of page tiles plus two query-term images
     const int nslot_tc = std::min(kMaxSlots, (dyn - flag_cap - 1024 - 2 * S::TC_BIMG) / S::TC_TILE);
@@ -2432,6 +2647,11 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
         std::memcpy(&a.tmap_k, cache[hitc].map, sizeof(CUtensorMap));
         a.tc = 1;
         a.nslot_tc = nslot_tc;
+        // =1: CTAs claim pages of one or two scanned sequences from a shared counter instead of
+        // each scanning its own range. Faster where bandwidth differs between SMs, but which
+        // CTA sums which pages then varies, so repeated runs may differ in the last bits.
+        const char* cl_env = std::getenv("TOKENSELECT_SCAN_CLAIM");
+        a.scan_dyn = cl_env && cl_env[0] == '1';
       }
     }
   }
