@@ -73,7 +73,7 @@ struct ts_ctx {
   unsigned* cand_n = nullptr;            // [max_batch]
   unsigned long long* cands = nullptr;   // [max_batch][2048]
   int* cta_cnt = nullptr;                // [max_batch][num_sms][3]
-  float* apart = nullptr;                // attention partials: o [B][H][num_sms][d], (max, sum) [B][H][even]
+  float* apart = nullptr;                // attention partials: o [B][H][parts][num_sms][d / parts], (max, sum) [B][H][even]
   struct KMap {                          // encoded TMA tensor maps of recent K pools
     const void* pool = nullptr;
     int64_t num_pages = 0;

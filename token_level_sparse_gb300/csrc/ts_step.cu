@@ -161,6 +161,7 @@ struct StepKArgs {
   const int32_t* page_table;
   const int32_t* seq_lens;
   float scale;
+  float scale_l2;              // scale x log2(e): the scan keeps its logits in base-2 units (exp2)
   float theta;
   const uint8_t* hit_in;
   uint8_t* hit_out;
@@ -610,18 +611,18 @@ __device__ __noinline__ bool cuda_scan_wave(const StepKArgs& a, Smem& sm, unsign
         for (int jj = 0; jj < S::GP; ++jj) v[jj] = acc0[jj] + acc1[jj];
         int which;
         const float dot = transpose_reduce<S::GP, S::LPR>(v, lane, which);
-        const float x = slot < nv ? dot * a.scale : -INFINITY;
+        const float x = slot < nv ? dot * a.scale_l2 : -INFINITY;
         if (writer && which < G) eb[(size_t)(tl + slot) * HW + gi * G + which] = x;
         // running max and compensated sum of exp over the rows of this step (lanes of equal `which`)
         float mi = x;
 #pragma unroll
         for (int d = S::LPR; d < 32; d <<= 1) mi = fmaxf(mi, __shfl_xor_sync(kFull, mi, d));
         const float mn = fmaxf(run_m, mi);
-        float ex = mn > -INFINITY ? expf(x - mn) : 0.f;
+        float ex = mn > -INFINITY ? exp2f(x - mn) : 0.f;
 #pragma unroll
         for (int d = S::LPR; d < 32; d <<= 1) ex += __shfl_xor_sync(kFull, ex, d);
         if (mn > run_m && run_m > -INFINITY) {
-          const float f = expf(run_m - mn);
+          const float f = exp2f(run_m - mn);
           run_z.s *= f;
           run_z.c *= f;
         }
@@ -661,7 +662,7 @@ __device__ __noinline__ bool cuda_scan_wave(const StepKArgs& a, Smem& sm, unsign
       float2 mz = make_float2(-INFINITY, 0.f);
       if (lane < wph) mz = wp[((size_t)sg * S::NCW + gi * wph + lane) * G + w];
       const float m = warp_max(mz.x);
-      const float z = warp_sum_comp((m > -INFINITY && mz.y > 0.f) ? mz.y * expf(mz.x - m) : 0.f);
+      const float z = warp_sum_comp((m > -INFINITY && mz.y > 0.f) ? mz.y * exp2f(mz.x - m) : 0.f);
       if (lane == 0) a.partials[((size_t)sm.seg_b[sg] * nCTA + c) * H + g0 * G + hl] = make_float2(m, z);
     }
   }
@@ -1219,7 +1220,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           #pragma unroll 1
           for (int cc = c0; cc < c1; ++cc) {
             const float2 mz = pcs[cc * H + g0 * G + lane];
-            if (mz.y > 0.f) kz.add(mz.y * expf(mz.x - M));
+            if (mz.y > 0.f) kz.add(mz.y * exp2f(mz.x - M));
           }
         rz[warp * 32 + lane] = kz.s - kz.c;
         __syncthreads();
@@ -1234,7 +1235,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         __syncthreads();
         TS_MARK(14);
       }
-      // v_i (+)= sum over the wave's heads of exp(l - M) / Z, chunk by chunk
+      // v_i (+)= sum over the wave's heads of 2^(l - M) / Z (base-2 logits: exp(l - M) in natural
+      // units), chunk by chunk
       const int crow = chunk_rows(HW), nch = (vrows + crow - 1) / crow;
       if (tid == 0)
         #pragma unroll 1
@@ -1279,8 +1281,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
                 const int r = rw + u * tpi + rl;
                 float4 xv = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
                 if (r < hi && qd < q4) xv = reinterpret_cast<const float4*>(cb + (size_t)(r - r0) * HW)[qd];
-                part[u] = (expf(xv.x - wl[0].x) * wl[0].y + expf(xv.y - wl[1].x) * wl[1].y) +
-                          (expf(xv.z - wl[2].x) * wl[2].y + expf(xv.w - wl[3].x) * wl[3].y);
+                part[u] = (exp2f(xv.x - wl[0].x) * wl[0].y + exp2f(xv.y - wl[1].x) * wl[1].y) +
+                          (exp2f(xv.z - wl[2].x) * wl[2].y + exp2f(xv.w - wl[3].x) * wl[3].y);
               }
               #pragma unroll 1
               for (int d = lpt / 2; d >= 1; d >>= 1) {
@@ -1299,7 +1301,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
               const float* row = cb + (size_t)(r - r0) * HW;
               KahanF acc;
               #pragma unroll 1
-              for (int hl = 0; hl < HW; ++hl) acc.add(expf(row[hl] - w[hl].x) * w[hl].y);
+              for (int hl = 0; hl < HW; ++hl) acc.add(exp2f(row[hl] - w[hl].x) * w[hl].y);
               const float v = acc.s - acc.c;
               vb[r - t0] = (wv == 0) ? v : vb[r - t0] + v;
             }
@@ -1504,7 +1506,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
 #pragma unroll
               for (int d = 8; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, d));
               const float rz = run_z[j].s - run_z[j].c;
-              float z = (m > -INFINITY && rz > 0.f) ? rz * expf(run_m[j] - m) : 0.f, zl = 0.f;
+              float z = (m > -INFINITY && rz > 0.f) ? rz * exp2f(run_m[j] - m) : 0.f, zl = 0.f;
 #pragma unroll
               for (int d = 8; d >= 1; d >>= 1) {                // compensated sum over the 16 lanes
                 const float oh = __shfl_xor_sync(kFull, z, d), ol = __shfl_xor_sync(kFull, zl, d);
@@ -1552,7 +1554,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
               const float hi = odd ? r[3 * G + 3 * j] : r[3 * j];
               const float mid = odd ? r[3 * G + 3 * j + 1] : r[3 * j + 1];
               const float lo = odd ? r[3 * G + 3 * j + 2] : r[3 * j + 2];
-              x[j] = t < nv ? ((lo + mid) + hi) * a.scale : -INFINITY;
+              x[j] = t < nv ? ((lo + mid) + hi) * a.scale_l2 : -INFINITY;
             }
             float* dst = a.spill + (size_t)(tl + t) * H + g * G;
             if constexpr (G == 4) {
@@ -1565,14 +1567,14 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
             for (int j = 0; j < G; ++j) {
               if (x[j] > run_m[j]) {
                 if (run_m[j] > -INFINITY) {
-                  const float f = expf(run_m[j] - x[j]);
+                  const float f = exp2f(run_m[j] - x[j]);
                   run_z[j].s *= f;
                   run_z[j].c *= f;
                 }
                 run_z[j].add(1.f);
                 run_m[j] = x[j];
               } else if (x[j] > -INFINITY) {
-                run_z[j].add(expf(x[j] - run_m[j]));
+                run_z[j].add(exp2f(x[j] - run_m[j]));
               }
             }
           }
@@ -2045,9 +2047,14 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   // My tokens per sequence: a round-robin share of the fixed ones (sinks and
   // window, the cached part of a hit, or the caller's index list) and my own
   // selected candidates; gathered by bulk copy; one partial per CTA and head.
-  // attention partials, each (sequence, head) contiguous for one bulk copy in the merge:
-  // o [B][H][nCTA][D], then (max, sum) [B][H][nCTAp] (nCTAp even: 16-byte blocks)
+  // attention partials, each (sequence, head, part of the d columns) contiguous for one bulk copy
+  // in the merge: o [B][H][dq][nCTA][D / dq], then (max, sum) [B][H][nCTAp] (nCTAp even: 16-byte
+  // blocks); the columns split into dq parts (a power of two, D / dq >= 32) so that the merge
+  // has about one item per CTA
   const int nCTAp = (nCTA + 1) & ~1;
+  int dq = 1;
+  while (2 * dq * 32 <= D && B * H * 2 * dq <= nCTA) dq *= 2;
+  const int Dq = D / dq;
   float* ao = a.apart;
   float2* aml = reinterpret_cast<float2*>(a.apart + (size_t)B * H * nCTA * D);
   if (a.phases & kPhAttend) {
@@ -2280,8 +2287,8 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
       for (int k = 0; k < NG; ++k) {
         const int qd = tid + k * S::THREADS;
         if (qd < NGRP) {
-          const int h = qd / D4, d4 = qd % D4;
-          reinterpret_cast<float4*>(ao + (((size_t)b * H + h) * nCTA + c) * D)[d4] = o[k];
+          const int h = qd / D4, d4 = qd % D4, qq = d4 / (Dq / 4);
+          reinterpret_cast<float4*>(ao + ((((size_t)b * H + h) * dq + qq) * nCTA + c) * Dq)[d4 % (Dq / 4)] = o[k];
         }
       }
       if (tid < HQ) aml[((size_t)b * H + tid) * nCTAp + c] = make_float2(sm.att_m[tid], sm.att_l[tid]);
@@ -2296,22 +2303,22 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   if (!grid_sync(a.gsync, a.status, &sm.gepoch)) return;
   TS_MARK(25);
   if (a.phases & kPhAttend) {
-    // merge the CTA partials of one (sequence, query head) per CTA pass: the item's rows and
-    // (max, sum) pairs arrive by bulk copy, then weights, then the weighted rows reduced in a
-    // fixed order
-    float* po = reinterpret_cast<float*>(dsm);                          // [nCTA][D]
-    float2* pml = reinterpret_cast<float2*>(po + (size_t)nCTA * D);     // [nCTAp]
+    // merge the CTA partials of one (sequence, query head, column part) per CTA pass: the item's
+    // rows and (max, sum) pairs arrive by bulk copy, then weights, then the weighted rows reduced
+    // in a fixed order
+    float* po = reinterpret_cast<float*>(dsm);                          // [nCTA][Dq]
+    float2* pml = reinterpret_cast<float2*>(po + (size_t)nCTA * Dq);    // [nCTAp]
     float* pw = reinterpret_cast<float*>(pml + nCTAp);                  // [nCTA] weights
-    float4* racc = reinterpret_cast<float4*>(dsm + (((size_t)nCTA * D * 4 + (size_t)nCTAp * 8 + (size_t)nCTA * 4 + 15) &
-                                                     ~(size_t)15));     // [ngrp][D/4]
-    constexpr int ncol = D / 4;
-    const int ngrp = blockDim.x / ncol;
+    float4* racc = reinterpret_cast<float4*>(dsm + (((size_t)nCTA * Dq * 4 + (size_t)nCTAp * 8 + (size_t)nCTA * 4 + 15) &
+                                                     ~(size_t)15));     // [ngrp][Dq/4]
+    const int ncol = Dq / 4;
+    const int ngrp = min((int)blockDim.x / ncol, 16);
     const int col = tid % ncol, grp = tid / ncol;
     #pragma unroll 1
-    for (int item = c; item < B * H; item += nCTA) {
-      const int b = item / H, h = item % H;
-      if (!bulk_fetch(po, ao + ((size_t)b * H + h) * nCTA * D, (uint32_t)(nCTA * D * 4), pml,
-                      aml + ((size_t)b * H + h) * nCTAp, (uint32_t)(nCTAp * 8))) {
+    for (int item = c; item < B * H * dq; item += nCTA) {
+      const int bh = item / dq, qq = item % dq, b = bh / H, h = bh % H;
+      if (!bulk_fetch(po, ao + ((size_t)bh * dq + qq) * nCTA * Dq, (uint32_t)(nCTA * Dq * 4), pml,
+                      aml + (size_t)bh * nCTAp, (uint32_t)(nCTAp * 8))) {
         if (tid == 0) atomicExch(&a.gsync->abort, 1u);
         return;
       }
@@ -2336,7 +2343,7 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
         for (int cc = grp; cc < nCTA; cc += ngrp) {
           const float w = pw[cc];
           if (w != 0.f) {
-            const float4 v = reinterpret_cast<const float4*>(po + (size_t)cc * D)[col];
+            const float4 v = reinterpret_cast<const float4*>(po + (size_t)cc * Dq)[col];
             acc.x = fmaf(w, v.x, acc.x);
             acc.y = fmaf(w, v.y, acc.y);
             acc.z = fmaf(w, v.z, acc.z);
@@ -2358,13 +2365,13 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
           s4.w += v.w;
         }
         const float inv = den > 0.f ? 1.f / den : 0.f;
-        float* o = a.out + ((size_t)b * H + h) * D + 4 * tid;   // the caller's buffer: 4-byte aligned only
+        float* o = a.out + ((size_t)b * H + h) * D + qq * Dq + 4 * tid;   // the caller's buffer: 4-byte aligned only
         o[0] = s4.x * inv;
         o[1] = s4.y * inv;
         o[2] = s4.z * inv;
         o[3] = s4.w * inv;
       }
-      if (a.lse && tid == 0) a.lse[(size_t)b * H + h] = den > 0.f ? M + logf(den) : -INFINITY;
+      if (a.lse && tid == 0 && qq == 0) a.lse[(size_t)b * H + h] = den > 0.f ? M + logf(den) : -INFINITY;
       __syncthreads();
     }
   }
@@ -2575,6 +2582,7 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   a.page_table = c.page_table;
   a.seq_lens = c.seq_lens;
   a.scale = c.scale;
+  a.scale_l2 = (float)((double)c.scale * 1.4426950408889634);
   a.theta = c.theta;
   a.hit_in = c.hit_in;
   a.hit_out = c.hit_out;
