@@ -135,6 +135,7 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   // per CTA: [sequence][scan warp][head] pairs (CUDA-core scan) or [2][128 rows][head] (tensor-core scan)
   chk(alloc(&ctx->step_wpart, NS * std::max<size_t>(B * kMaxScanWarps, 2 * 128) * kMaxScanG * 2));
   chk(alloc(&ctx->gsync, 4));
+  if (e == cudaSuccess) chk(cudaMemset(ctx->gsync, 0, 4 * sizeof(unsigned)));   // then kept zero by each launch
   chk(alloc(&ctx->phase_ns, 32));
   chk(alloc(&ctx->partials, B * ctx->score_max_chunks * H));
   chk(alloc(&ctx->stats, B * H));

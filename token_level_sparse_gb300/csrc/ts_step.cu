@@ -144,7 +144,7 @@ struct GridSync {
   unsigned count;   // barrier arrivals since the launch
   unsigned abort;
   unsigned claim;   // next page chunk of a shared tensor-core scan
-  unsigned pad;
+  unsigned exits;   // CTAs that have left; the last one zeroes all four for the next launch
 };
 
 struct StepKArgs {
@@ -460,7 +460,8 @@ struct Smem {
 // statistics, 4 + 3 w barrier passed; 13 / 14 vote partials / normalisers, 20 votes done;
 // 28 + l histogram level l built, 21 levels, 22 candidates, 23 flags; 10 last gather landed,
 // 9 last round list built, 11 attended, 24 partials written, 25 last barrier, 26 merged, 27
-// end. (The marks of waves past the first share slots 5..19 with the others.)
+// end. (The marks of waves past the first share slots 5..19 with the others; slots 17 and 18
+// also take the latest start and end over all CTAs.)
 #define TS_MARK(i)                                                     \
   do {                                                                 \
     if (c == 0 && tid == 0 && a.phase_ns) a.phase_ns[i] = globaltimer_ns(); \
@@ -671,7 +672,7 @@ __device__ __noinline__ bool cuda_scan_wave(const StepKArgs& a, Smem& sm, unsign
 
 
 template <typename KT, int D, int HKV, int G>
-__global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_kernel(const __grid_constant__ StepKArgs a) {
+__device__ __forceinline__ void step_body(const StepKArgs& a) {
   using S = StepShape<KT, D, HKV, G>;
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ Smem sm;
@@ -2488,6 +2489,27 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
   TS_MARK(27);
 }
 
+template <typename KT, int D, int HKV, int G>
+__global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_kernel(const __grid_constant__ StepKArgs a) {
+  // diagnosis: the latest CTA start (slot 17) and the latest CTA end (slot 18) of the launch
+  if (threadIdx.x == 0 && a.phase_ns) atomicMax(&a.phase_ns[17], globaltimer_ns());
+  step_body<KT, D, HKV, G>(a);
+  if (threadIdx.x == 0 && a.phase_ns) atomicMax(&a.phase_ns[18], globaltimer_ns());
+  // Every CTA leaves through here, whichever way the body ended; thread 0 is the only one that
+  // touches the barrier words, so once every CTA's thread 0 has counted itself out the last one
+  // zeroes them for the next launch (no memset between launches).
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&a.gsync->exits, 1u) + 1u == gridDim.x) {
+      a.gsync->count = 0u;
+      a.gsync->abort = 0u;
+      a.gsync->claim = 0u;
+      a.gsync->exits = 0u;
+      __threadfence();
+    }
+  }
+}
+
 // ------------------------------------------------------------------- launch
 
 // Tensor map of a bf16 K pool seen as [num_pages * 128 rows][d]: boxes of 64 elements x 128 rows
@@ -2664,7 +2686,6 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
     }
   }
   a.flag_cap = flag_cap;
-  if (cudaMemsetAsync(ctx->gsync, 0, sizeof(GridSync), s) != cudaSuccess) return TS_ERR_CUDA;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(ctx->step_grid);
   lc.blockDim = dim3(S::THREADS);
