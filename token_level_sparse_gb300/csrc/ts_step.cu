@@ -447,7 +447,9 @@ struct Smem {
   int wsum[33];
   int flag;
   float red_f[3][32];
-  int red_i[2][32];
+  int red_i[3][32];
+  int sel_a[kMaxB], sel_c[kMaxB], sel_lo[kMaxB];  // per segment: my selected tokens, those in [s_end, ls),
+                                                  // those below s_end (list in the scratch, ascending)
   int toks[kMaxRound];
   int tval[kMaxRound];
   int my_seg_of[kMaxB];    // segment of sequence b in this CTA, or -1
@@ -1033,6 +1035,9 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     if (c == 0 && tid == 0) set_error(a.status, TS_ERR_SHAPE);
     return;  // the same decision in every CTA, before any grid barrier
   }
+  // my scratch region holds my logits until the votes, then my selected tokens (ascending, the
+  // list of segment sg from row seg_t0[sg])
+  int* const sel_list = reinterpret_cast<int*>(a.spill + (size_t)c * sm.region);
   TS_MARK(7);
   // the tensor-core scan runs this launch: warps 8.. finish the set-up while the pages stream
   const bool tc_scan = S::TC && sm.use_tc && (a.phases & kPhScore) && sm.ptot > 0;
@@ -1950,7 +1955,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       #pragma unroll 4
       for (int j = tid; j < m_cand; j += blockDim.x) scand[j] = __ldcg(&a.cands[(size_t)b * kCandCap + j]);
       __syncthreads();
-      int n_sel_cand = 0, n_sel_all = 0;
+      int n_sel_cand = 0, n_sel_lo = 0, n_list = 0;
       #pragma unroll 1
       for (int base = 0; base < nt; base += blockDim.x) {
         const int i = base + tid;
@@ -2018,26 +2023,36 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           if (rank_me) f = selflag[t0l + i];
         }
         if (i < nt) selflag[t0l + i] = (uint8_t)f;
-        n_sel_all += f;
+        {
+          // my selected tokens in ascending order, from row t0l of my scratch region (its logits are
+          // spent): the attention takes its own tokens and the outputs their positions from here
+          int ftot;
+          const int fr = block_scan(f, sm.wsum, ftot);
+          if (f) sel_list[t0l + n_list + fr] = t;
+          n_list += ftot;
+        }
         n_sel_cand += f && t >= st.s_end && t < st.ls;
-        __syncthreads();
+        n_sel_lo += f && t < st.s_end;
       }
       n_sel_cand = warp_sum_i(n_sel_cand);
-      n_sel_all = warp_sum_i(n_sel_all);
+      n_sel_lo = warp_sum_i(n_sel_lo);
       if (lane == 0) {
         sm.red_i[0][warp] = n_sel_cand;
-        sm.red_i[1][warp] = n_sel_all;
+        sm.red_i[2][warp] = n_sel_lo;
       }
       __syncthreads();
       if (tid == 0) {
-        int tc = 0, ta = 0;
+        int tc = 0, tlo = 0;
         #pragma unroll 1
         for (int w = 0; w < S::NW; ++w) {
           tc += sm.red_i[0][w];
-          ta += sm.red_i[1][w];
+          tlo += sm.red_i[2][w];
         }
         a.cta_cnt[((size_t)b * nCTA + c) * 3 + 0] = tc;
-        a.cta_cnt[((size_t)b * nCTA + c) * 3 + 1] = ta;
+        a.cta_cnt[((size_t)b * nCTA + c) * 3 + 1] = n_list;
+        sm.sel_a[sg] = n_list;
+        sm.sel_c[sg] = tc;
+        sm.sel_lo[sg] = tlo;
       }
       __syncthreads();
     }
@@ -2098,7 +2113,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       const int nmid = ct_hi - ct_lo;
       const int sgi = sm.my_seg_of[b];
       const bool own = !given && !st.hit && sgi >= 0;
-      const int own_n = own ? sm.seg_ntok[sgi] : 0;
+      const int own_nc = own ? sm.sel_c[sgi] : 0;
+      const int* own_lst = own ? sel_list + sm.seg_t0[sgi] + sm.sel_lo[sgi] : nullptr;
       const int own_lp0 = own ? sm.seg_lp0[sgi] : 0, own_t0 = own ? sm.seg_t0[sgi] : 0;
       const int nfix_mine = c < nfix ? (nfix - c + nCTA - 1) / nCTA : 0;
       float qreg[S::GP][EPL];
@@ -2115,7 +2131,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
 #pragma unroll
       for (int k = 0; k < NG; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       int fdone = 0;     // fixed tokens of mine already taken
-      int opos = 0;      // next own token (segment-local) to examine
+      int opos = 0;      // next own token (position in my list)
       bool ok = true;
       // bulk copies of the K and V rows of every KV head of list entries [j0, j1)
       auto gather_rows = [&](int j0, int j1) {
@@ -2165,30 +2181,19 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           __syncthreads();
           gather_rows(0, nf);
         }
-        while (own && opos < own_n && cnt < around) {
-          // one chunk of blockDim own tokens; take as many selected ones as fit
-          const int i = opos + tid;
-          const int t = own_lp0 * S::P + i;
-          const bool take = i < own_n && selflag[own_t0 + i] && t >= st.s_end && t < st.ls;
-          int tot;
-          const int r = block_scan(take ? 1 : 0, sm.wsum, tot);
-          const int room = around - cnt;
-          if (take && r < room) {
-            const int lpg = (own_t0 + i) / S::P;   // my page of the token
+        if (own && opos < own_nc && cnt < around) {
+          // my selected tokens in [s_end, ls), in list order, as many as fit
+          const int take = min(around - cnt, own_nc - opos);
+          #pragma unroll 1
+          for (int r = tid; r < take; r += blockDim.x) {
+            const int t = own_lst[opos + r];
+            const int lpg = (own_t0 + (t - own_lp0 * S::P)) / S::P;   // my page of the token
             sm.toks[cnt + r] = t;
             sm.tval[cnt + r] = lpg < kMaxPagesCta ? sm.my_pages[lpg]
                                                   : a.page_table[(size_t)b * a.pt_stride + t / S::P];
           }
-          if (tot <= room) {
-            opos += blockDim.x;
-            cnt += tot;
-          } else {
-            // stop right after the room-th taken token of the chunk
-            if (take && r == room - 1) sm.flag = i + 1;
-            __syncthreads();
-            opos = sm.flag;
-            cnt = around;
-          }
+          opos += take;
+          cnt += take;
           __syncthreads();
         }
         TS_MARK(9);
@@ -2437,7 +2442,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         continue;
       }
       const int tot_c = sm.tot_c[b], tot_a = sm.tot_a[b];
-      int pre_c = sm.pre_c[b], pre_a = sm.pre_a[b];
+      const int pre_c = sm.pre_c[b], pre_a = sm.pre_a[b];
       const int total = st.s_end + tot_c + (st.n - st.ls);
       const bool fits = total <= a.idx_stride;
       const bool cfits = a.ct != nullptr && tot_a <= a.cap;
@@ -2468,21 +2473,16 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       }
       const int sgi = sm.my_seg_of[b];
       if (sgi < 0) continue;
-      const int tl0 = sm.seg_lp0[sgi] * S::P, nt = sm.seg_ntok[sgi], t0l = sm.seg_t0[sgi];
+      // my selected tokens from the ascending list: all of them into C_T, those in [s_end, ls)
+      // into the index list after the sinks
+      const int* lst = sel_list + sm.seg_t0[sgi];
+      const int na = sm.sel_a[sgi], nlo = sm.sel_lo[sgi], nc = sm.sel_c[sgi];
       int32_t* ctb = cfits ? a.ct + (size_t)b * a.cap : nullptr;
       #pragma unroll 1
-      for (int base = 0; base < nt; base += blockDim.x) {
-        const int i = base + tid;
-        const int t = tl0 + i;
-        const bool f = i < nt && selflag[t0l + i];
-        const bool fc = f && t >= st.s_end && t < st.ls;
-        int ta, tc;
-        const int ra = block_scan(f ? 1 : 0, sm.wsum, ta);
-        const int rc = block_scan(fc ? 1 : 0, sm.wsum, tc);
-        if (f && ctb) ctb[pre_a + ra] = t;
-        if (fc && fits) ib[st.s_end + pre_c + rc] = t;
-        pre_a += ta;
-        pre_c += tc;
+      for (int j = tid; j < na; j += blockDim.x) {
+        const int t = lst[j];
+        if (ctb) ctb[pre_a + j] = t;
+        if (fits && j >= nlo && j < nlo + nc) ib[st.s_end + pre_c + (j - nlo)] = t;
       }
     }
   }
