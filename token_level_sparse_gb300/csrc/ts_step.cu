@@ -50,6 +50,7 @@ constexpr int kMaxAttH = 64;       // query heads of the attention phase
 constexpr int kPreFix = 512;       // fixed attention tokens of a CTA resolved at set-up
 constexpr int kMaxPagesCta = 1024; // page ids of a CTA's range kept in shared memory
 constexpr int kScanClaim = 2;      // pages per claim of a shared tensor-core scan
+constexpr int kVoteBufs = 2;       // shared-memory buffers of logit chunks for the votes
 constexpr int kMaxSlots = 12;      // ring slots (runtime count per launch)
 constexpr int64_t kLogitL2Budget = 48ll << 20;  // default bytes of logits one scan wave keeps in L2
 // radix levels over the vote bits (votes are >= +0, bit 31 is always 0): bits 30..17, 16..6,
@@ -684,7 +685,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
   __shared__ __align__(8) uint64_t drainb;            // every MMA issued has completed
   __shared__ __align__(8) uint64_t abar;
   __shared__ __align__(8) uint64_t xbar;              // bulk copies of partials (vote, merge)
-  __shared__ __align__(8) uint64_t vbar[2];           // chunks of my logits for the votes
+  __shared__ __align__(8) uint64_t vbar[kVoteBufs];  // chunks of my logits for the votes
 
   const int nslot = a.nslot;
   unsigned char* ring = dsm;                                               // nslot x STAGE_BYTES of K
@@ -730,8 +731,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     mbar_init(&drainb, 1);
     mbar_init(&abar, 1);
     mbar_init(&xbar, 1);
-    mbar_init(&vbar[0], 1);
-    mbar_init(&vbar[1], 1);
+    for (int i = 0; i < kVoteBufs; ++i) mbar_init(&vbar[i], 1);
     mbar_fence_init();
     sm.timed_out = 0;
     sm.gepoch = 0u;
@@ -1170,7 +1170,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
   // ========================================================================= SCORE
   if ((a.phases & kPhScore) && sm.ptot > 0) {   // nothing to scan when every sequence hits
     // my logits [row = token of my range][HW] pass through shared memory past the vote scratch
-    // in chunks of whole rows by bulk copy, two buffers when the range does not fit at once
+    // in chunks of whole rows by bulk copy: at once when the range fits, else through
+    // kVoteBufs buffers with all but one in flight
     const size_t vsb = ((size_t)kMaxB * kMaxWaveHeads * 8 + (size_t)nCTA * H * 8 + S::NW * 32 * 8 + 15) &
                        ~(size_t)15;
     float* vbuf = reinterpret_cast<float*>(ring + vsb);
@@ -1178,16 +1179,17 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     uint32_t vph = 0u;                                             // phase bit of each chunk buffer
     auto chunk_rows = [&](int HW) -> int {
       const int fit = (int)(((size_t)(a.dyn_bytes - a.flag_cap) - vsb) / ((size_t)HW * 4));
-      return vrows <= fit ? vrows : max(16, (fit / 2) & ~15);
+      return vrows <= fit ? vrows : max(16, (fit / kVoteBufs) & ~15);
     };
     auto issue_chunk = [&](const float* eb, int k, int HW, int crow) {   // thread 0
       const uint32_t bytes = (uint32_t)min(crow, vrows - k * crow) * (uint32_t)HW * 4u;
       const unsigned char* src = reinterpret_cast<const unsigned char*>(eb + (size_t)k * crow * HW);
-      unsigned char* dst = reinterpret_cast<unsigned char*>(vbuf + (size_t)(k & 1) * crow * HW);
+      unsigned char* dst = reinterpret_cast<unsigned char*>(vbuf + (size_t)(k % kVoteBufs) * crow * HW);
       fence_proxy_async_global();
-      mbar_arrive_expect_tx(&vbar[k & 1], bytes);
+      mbar_arrive_expect_tx(&vbar[k % kVoteBufs], bytes);
       #pragma unroll 1
-      for (uint32_t o = 0; o < bytes; o += 32768u) bulk_g2s(dst + o, src + o, min(32768u, bytes - o), &vbar[k & 1]);
+      for (uint32_t o = 0; o < bytes; o += 32768u)
+        bulk_g2s(dst + o, src + o, min(32768u, bytes - o), &vbar[k % kVoteBufs]);
     };
     // each head's normaliser over the CTAs of the sequence, then the votes of my tokens for
     // heads [g0 G, g0 G + HW); eb holds my logits [row][HW], of which the first `pre` chunks
@@ -1246,7 +1248,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       const int crow = chunk_rows(HW), nch = (vrows + crow - 1) / crow;
       if (tid == 0)
         #pragma unroll 1
-        for (int k = pre; k < min(nch, 2); ++k) issue_chunk(eb, k, HW, crow);
+        for (int k = pre; k < min(nch, kVoteBufs); ++k) issue_chunk(eb, k, HW, crow);
       const int q4 = HW >> 2;
       int lpt = 1;                                  // lanes per row, one float4 (4 heads) each
       while (lpt < q4) lpt <<= 1;
@@ -1254,18 +1256,21 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       const int tpi = 32 / lpt, rl = lane / lpt, qd = lane % lpt;
       #pragma unroll 1
       for (int k = 0; k < nch; ++k) {
-        const bool landed = mbar_wait(&vbar[k & 1], (vph >> (k & 1)) & 1u);
-        vph ^= 1u << (k & 1);
+        const int kb = k % kVoteBufs;
+        const bool landed = mbar_wait(&vbar[kb], (vph >> kb) & 1u);
+        vph ^= 1u << kb;
         if (!__syncthreads_and(landed)) {
           if (tid == 0) {
             set_error(a.status, TS_ERR_TIMEOUT);
             atomicExch(&a.gsync->abort, 1u);
-            if (k + 1 < nch) mbar_wait(&vbar[(k + 1) & 1], (vph >> ((k + 1) & 1)) & 1u);   // in flight
+            #pragma unroll 1
+            for (int j = k + 1; j < min(nch, k + kVoteBufs); ++j)   // copies in flight land first
+              mbar_wait(&vbar[j % kVoteBufs], (vph >> (j % kVoteBufs)) & 1u);
           }
           return false;
         }
         const int r0 = k * crow, r1 = min(vrows, r0 + crow);
-        const float* cb = vbuf + (size_t)(k & 1) * crow * HW;   // row r at cb + (r - r0) HW
+        const float* cb = vbuf + (size_t)kb * crow * HW;   // row r at cb + (r - r0) HW
         #pragma unroll 1
         for (int sg = 0; sg < sm.nseg; ++sg) {
           const int b = sm.seg_b[sg], t0 = sm.seg_t0[sg];
@@ -1313,8 +1318,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
             }
           }
         }
-        __syncthreads();                            // buffer k & 1 is free again
-        if (tid == 0 && k + 2 < nch) issue_chunk(eb, k + 2, HW, crow);
+        __syncthreads();                            // buffer kb is free again
+        if (tid == 0 && k + kVoteBufs < nch) issue_chunk(eb, k + kVoteBufs, HW, crow);
       }
       __syncthreads();
       return true;
@@ -1645,8 +1650,9 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
 
   TS_MARK(20);
   // ======================================================================== SELECT
-  if (a.phases & kPhSelect) {
-    if (!(a.phases & kPhScore) && sm.ptot > 0) {
+  // (nothing to select when every sequence hits or is empty: no pages were partitioned)
+  if ((a.phases & kPhSelect) && sm.ptot > 0) {
+    if (!(a.phases & kPhScore)) {
       if (!grid_sync(a.gsync, a.status, &sm.gepoch)) return;   // the histograms are zero everywhere
     }
     // shared memory while selecting, one use after another: this CTA's histogram (counts,
@@ -1943,114 +1949,134 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     }
 
     TS_MARK(22);
-    // ---- the selection flag of each of my tokens, and the counts for output positions
+    // ---- the selection flag of each of my tokens (a byte), then my selected tokens as an ascending
+    // list and the counts for the output positions. Warp w takes a contiguous run of the
+    // segment's tokens, so per-warp counts give positions in token order without a block scan.
     #pragma unroll 1
     for (int sg = 0; sg < sm.nseg; ++sg) {
       const int b = sm.seg_b[sg];
       const SeqState& st = sm.seq[b];
       const int tl0 = sm.seg_lp0[sg] * S::P, t0l = sm.seg_t0[sg], nt = sm.seg_ntok[sg];
       const float* vb = a.vote + (size_t)b * a.vote_stride;
-      int tie_base = st.tie_mode ? sm.tie_base[sg] : 0;
+      uint8_t* fl = selflag + t0l;
+      const int per = ((nt + S::NW * 32 - 1) / (S::NW * 32)) * 32;   // tokens per warp, whole 32s
+      const int w0 = min(nt, warp * per), w1 = min(nt, w0 + per);
       const int m_cand = st.cand ? (int)min(__ldcg(&a.cand_n[b]), (unsigned)kCandCap) : 0;
       #pragma unroll 4
       for (int j = tid; j < m_cand; j += blockDim.x) scand[j] = __ldcg(&a.cands[(size_t)b * kCandCap + j]);
-      __syncthreads();
-      int n_sel_cand = 0, n_sel_lo = 0, n_list = 0;
+      // (1) classes: 0 out, 1 selected, 2 to be ranked against the gathered candidates, 3 an exact
+      // tie of the crossing value (eight loads in flight per lane)
+      int nties = 0;
       #pragma unroll 1
-      for (int base = 0; base < nt; base += blockDim.x) {
-        const int i = base + tid;
-        const int t = tl0 + i;
-        int f = 0;
-        bool tie = false, rank_me = false;
-        uint32_t key = 0;
-        if (i < nt && t >= st.lo && t < st.hi) {
-          key = __float_as_uint(__ldcg(vb + t));
-          if (st.all) {
-            f = 1;
-          } else if ((key & st.mask) > st.prefix) {
-            f = 1;
-          } else if ((key & st.mask) == st.prefix) {
-            if (st.cand) rank_me = true;
-            else if (st.tie_mode) tie = true;
-          }
-        }
-        if (st.tie_mode) {
-          int tie_tot;
-          const int tr = block_scan(tie ? 1 : 0, sm.wsum, tie_tot);
-          if (tie) f = (tie_base + tr) < st.ties;
-          tie_base += tie_tot;
-        }
-        // candidates: one warp ranks one candidate against the gathered list
-        if (st.cand) {
-          int nr;
-          const int rr = block_scan(rank_me ? 1 : 0, sm.wsum, nr);
-          #pragma unroll 1
-          for (int r0 = 0; r0 < nr; r0 += kMaxRound) {
-            const int nrr = min(kMaxRound, nr - r0);
-            const int rrr = rr - r0;
-            if (rank_me && rrr >= 0 && rrr < kMaxRound) {
-              sm.toks[rrr] = i;
-              sm.tval[rrr] = (int)key;
-            }
-            __syncthreads();
-            #pragma unroll 1
-            for (int q = warp; q < nrr; q += S::NW) {
-              const int ii = sm.toks[q];
-              const uint32_t kk = (uint32_t)sm.tval[q];
-              const unsigned long long me = ((unsigned long long)kk << 32) | (0xffffffffu - (uint32_t)(tl0 + ii));
-              unsigned above = 0;
-              unsigned long long cum = 0;
-              #pragma unroll 1
-              for (int j = lane; j < m_cand; j += 32) {
-                const unsigned long long y = scand[j];
-                if (y > me) {
-                  ++above;
-                  if (topp) cum += to_fx(__uint_as_float((uint32_t)(y >> 32)));
-                }
-              }
+      for (int i0 = w0; i0 < w1; i0 += 8 * 32) {
+        uint32_t key[8];
 #pragma unroll
-              for (int d = 16; d >= 1; d >>= 1) {
-                above += __shfl_xor_sync(kFull, above, d);
-                cum += __shfl_xor_sync(kFull, cum, d);
-              }
-              if (lane == 0) {
-                const int sel = topp ? (cum < st.mass_rem) : (above < (unsigned)st.k_rem);
-                selflag[t0l + ii] = (uint8_t)sel;
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * 32 + lane;
+          key[u] = i < w1 ? __float_as_uint(__ldcg(vb + tl0 + i)) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + u * 32 + lane, t = tl0 + i;
+          if (i >= w1) continue;
+          uint8_t cls = 0;
+          if (t >= st.lo && t < st.hi) {
+            const uint32_t km = key[u] & st.mask;
+            if (st.all || km > st.prefix) cls = 1;
+            else if (km == st.prefix) cls = st.cand ? 2 : (st.tie_mode ? 3 : 0);
+          }
+          fl[i] = cls;
+          nties += cls == 3;
+        }
+      }
+      __syncthreads();                                    // the candidates are in shared memory
+      // (2) exact ties, in token order: the first st.ties of them over the sequence are taken
+      if (st.tie_mode) {
+        nties = warp_sum_i(nties);
+        if (lane == 0) sm.red_i[0][warp] = nties;
+        __syncthreads();
+        int off = sm.tie_base[sg];
+        #pragma unroll 1
+        for (int w = 0; w < warp; ++w) off += sm.red_i[0][w];
+        #pragma unroll 1
+        for (int i0 = w0; i0 < w1; i0 += 32) {
+          const int i = i0 + lane;
+          const bool tie = i < w1 && fl[i] == 3;
+          const unsigned bal = __ballot_sync(kFull, tie);
+          if (tie) fl[i] = (off + __popc(bal & ((1u << lane) - 1u))) < st.ties ? 1 : 0;
+          off += __popc(bal);
+        }
+        __syncthreads();                                  // red_i is reused below
+      }
+      // (3) tokens of the crossing bin: the warp ranks each against the gathered list
+      if (st.cand) {
+        #pragma unroll 1
+        for (int i0 = w0; i0 < w1; i0 += 32) {
+          unsigned bal = __ballot_sync(kFull, i0 + lane < w1 && fl[i0 + lane] == 2);
+          while (bal) {
+            const int ii = i0 + __ffs(bal) - 1;
+            bal &= bal - 1u;
+            const uint32_t kk = __float_as_uint(__ldcg(vb + tl0 + ii));
+            const unsigned long long me = ((unsigned long long)kk << 32) | (0xffffffffu - (uint32_t)(tl0 + ii));
+            unsigned above = 0;
+            unsigned long long cum = 0;
+            #pragma unroll 1
+            for (int j = lane; j < m_cand; j += 32) {
+              const unsigned long long y = scand[j];
+              if (y > me) {
+                ++above;
+                if (topp) cum += to_fx(__uint_as_float((uint32_t)(y >> 32)));
               }
             }
-            __syncthreads();
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1) {
+              above += __shfl_xor_sync(kFull, above, d);
+              cum += __shfl_xor_sync(kFull, cum, d);
+            }
+            if (lane == 0) fl[ii] = (topp ? (cum < st.mass_rem) : (above < (unsigned)st.k_rem)) ? 1 : 0;
+            __syncwarp();
           }
-          if (rank_me) f = selflag[t0l + i];
         }
-        if (i < nt) selflag[t0l + i] = (uint8_t)f;
-        {
-          // my selected tokens in ascending order, from row t0l of my scratch region (its logits are
-          // spent): the attention takes its own tokens and the outputs their positions from here
-          int ftot;
-          const int fr = block_scan(f, sm.wsum, ftot);
-          if (f) sel_list[t0l + n_list + fr] = t;
-          n_list += ftot;
-        }
-        n_sel_cand += f && t >= st.s_end && t < st.ls;
-        n_sel_lo += f && t < st.s_end;
       }
-      n_sel_cand = warp_sum_i(n_sel_cand);
-      n_sel_lo = warp_sum_i(n_sel_lo);
+      // (4) counts per warp (all, in [s_end, ls), below s_end), then the list in token order; my
+      // scratch region's logits are spent, the list of this segment starts at its row t0l
+      int na = 0, nc = 0, nlo = 0;
+      #pragma unroll 1
+      for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane, t = tl0 + i;
+        const bool f = i < w1 && fl[i] == 1;
+        na += __popc(__ballot_sync(kFull, f));
+        nc += __popc(__ballot_sync(kFull, f && t >= st.s_end && t < st.ls));
+        nlo += __popc(__ballot_sync(kFull, f && t < st.s_end));
+      }
       if (lane == 0) {
-        sm.red_i[0][warp] = n_sel_cand;
-        sm.red_i[2][warp] = n_sel_lo;
+        sm.red_i[0][warp] = na;
+        sm.red_i[1][warp] = nc;
+        sm.red_i[2][warp] = nlo;
       }
       __syncthreads();
+      int off = 0;
+      #pragma unroll 1
+      for (int w = 0; w < warp; ++w) off += sm.red_i[0][w];
+      #pragma unroll 1
+      for (int i0 = w0; i0 < w1; i0 += 32) {
+        const int i = i0 + lane;
+        const bool f = i < w1 && fl[i] == 1;
+        const unsigned bal = __ballot_sync(kFull, f);
+        if (f) sel_list[t0l + off + __popc(bal & ((1u << lane) - 1u))] = tl0 + i;
+        off += __popc(bal);
+      }
       if (tid == 0) {
-        int tc = 0, tlo = 0;
+        int ta = 0, tc = 0, tlo = 0;
         #pragma unroll 1
         for (int w = 0; w < S::NW; ++w) {
-          tc += sm.red_i[0][w];
+          ta += sm.red_i[0][w];
+          tc += sm.red_i[1][w];
           tlo += sm.red_i[2][w];
         }
         a.cta_cnt[((size_t)b * nCTA + c) * 3 + 0] = tc;
-        a.cta_cnt[((size_t)b * nCTA + c) * 3 + 1] = n_list;
-        sm.sel_a[sg] = n_list;
+        a.cta_cnt[((size_t)b * nCTA + c) * 3 + 1] = ta;
+        sm.sel_a[sg] = ta;
         sm.sel_c[sg] = tc;
         sm.sel_lo[sg] = tlo;
       }
@@ -2573,7 +2599,7 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   if (nslot < S::MIN_SLOTS || dyn - flag_cap < lvl_bins(0) * 12 || dyn - flag_cap < kCandCap * 8 ||
       dyn - flag_cap < kMaxB * 128 * 12 ||
       dyn - flag_cap < kMaxB * kMaxWaveHeads * 8 + ctx->num_sms * ctx->cfg.n_q_heads * 8 + 2 * 16 * 32 * 4 + 16 +
-                           2 * 16 * kMaxWaveHeads * 4 ||   // vote scratch, then two chunks of 16 logit rows
+                           kVoteBufs * 16 * kMaxWaveHeads * 4 ||   // vote scratch, then the chunks of 16 logit rows
       dyn < ctx->num_sms * (D * 4 + 8 + 4) + 8 + 16 + S::THREADS * 16)   // the merge's rows, pairs, weights
     return TS_ERR_UNSUPPORTED;
   if (!ensure_smem<step_kernel<KT, D, HKV, G>>((size_t)dyn, ctx->device)) {
