@@ -1884,49 +1884,86 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     }
 
     TS_MARK(21);
-    // ---- gather the crossing-bin tokens (candidates); per-CTA exact-tie counts
+    // ---- (1) the class of each of my tokens, a byte in the flags: 0 out, 1 selected, 2 in the
+    // crossing bin (ranked below against every CTA's), 3 an exact tie of the crossing value. Warp
+    // w takes a contiguous run of the segment's tokens, so per-warp counts give positions in token
+    // order. Crossing-bin tokens are appended to the sequence's candidate list; exact ties are
+    // counted per CTA.
     int need_cand = 0, need_tie = 0;
     #pragma unroll 1
     for (int b = 0; b < B; ++b) {
       need_cand |= sm.seq[b].cand;
       need_tie |= sm.seq[b].tie_mode;
     }
+    auto warp_run = [&](int nt, int& w0, int& w1) {
+      const int per = ((nt + S::NW * 32 - 1) / (S::NW * 32)) * 32;   // tokens per warp, whole 32s
+      w0 = min(nt, warp * per);
+      w1 = min(nt, w0 + per);
+    };
     #pragma unroll 1
     for (int sg = 0; sg < sm.nseg; ++sg) {
       const int b = sm.seg_b[sg];
       const SeqState& st = sm.seq[b];
-      if (!st.cand && !st.tie_mode) continue;
-      const int tl0 = sm.seg_lp0[sg] * S::P;
-      const int lo = max(st.lo, tl0), hi = min(st.hi, tl0 + sm.seg_ntok[sg]);
+      const int tl0 = sm.seg_lp0[sg] * S::P, nt = sm.seg_ntok[sg];
       const float* vb = a.vote + (size_t)b * a.vote_stride;
-      int n_eq = 0;
+      uint8_t* fl = selflag + sm.seg_t0[sg];
+      int w0, w1;
+      warp_run(nt, w0, w1);
+      int nties = 0;
       #pragma unroll 1
-      for (int t0 = lo; t0 < hi; t0 += blockDim.x) {
-        const int t = t0 + tid;
-        bool is = false;
-        uint32_t key = 0;
-        if (t < hi) {
-          key = __float_as_uint(__ldcg(vb + t));
-          is = (key & st.mask) == st.prefix;
+      for (int i0 = w0; i0 < w1; i0 += 4 * 32) {   // four loads in flight per lane
+        uint32_t key[4];
+        uint8_t cls[4];
+        unsigned cm = 0;                              // bit u: token u of this lane is in the crossing bin
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * 32 + lane;
+          key[u] = i < w1 ? __float_as_uint(__ldcg(vb + tl0 + i)) : 0u;
         }
-        if (st.tie_mode) {
-          n_eq += is;
-          continue;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = i0 + u * 32 + lane, t = tl0 + i;
+          cls[u] = 0;
+          if (i < w1 && t >= st.lo && t < st.hi) {
+            const uint32_t km = key[u] & st.mask;
+            if (st.all || km > st.prefix) cls[u] = 1;
+            else if (km == st.prefix) cls[u] = st.cand ? 2 : (st.tie_mode ? 3 : 0);
+          }
+          if (i < w1) fl[i] = cls[u];
+          nties += cls[u] == 3;
+          cm |= (unsigned)(cls[u] == 2) << u;
         }
-        const unsigned bal = __ballot_sync(kFull, is);
-        unsigned base = 0;
-        if (lane == 0 && bal) base = atomicAdd(&a.cand_n[b], (unsigned)__popc(bal));
-        base = __shfl_sync(kFull, base, 0);
-        if (is) {
-          const unsigned pos = base + __popc(bal & ((1u << lane) - 1u));
-          if (pos < (unsigned)kCandCap)
-            a.cands[(size_t)b * kCandCap + pos] = ((unsigned long long)key << 32) | (0xffffffffu - (uint32_t)t);
+        if (__any_sync(kFull, cm != 0)) {
+          #pragma unroll 1
+          for (int u = 0; u < 4; ++u) {
+            const bool is = (cm >> u) & 1u;
+            const unsigned bal = __ballot_sync(kFull, is);
+            if (!bal) continue;
+            unsigned base = 0;
+            if (lane == 0) base = atomicAdd(&a.cand_n[b], (unsigned)__popc(bal));
+            base = __shfl_sync(kFull, base, 0);
+            const unsigned pos = base + __popc(bal & ((1u << lane) - 1u));
+            uint32_t kk = key[0];
+#pragma unroll
+            for (int v = 1; v < 4; ++v)
+              if (u == v) kk = key[v];
+            if (is && pos < (unsigned)kCandCap)
+              a.cands[(size_t)b * kCandCap + pos] =
+                  ((unsigned long long)kk << 32) | (0xffffffffu - (uint32_t)(tl0 + i0 + u * 32 + lane));
+          }
         }
       }
       if (st.tie_mode) {
-        int tot;
-        block_scan(n_eq, sm.wsum, tot);
-        if (tid == 0) a.cta_cnt[((size_t)b * nCTA + c) * 3 + 2] = tot;
+        nties = warp_sum_i(nties);
+        if (lane == 0) sm.red_i[0][warp] = nties;
+        __syncthreads();
+        if (tid == 0) {
+          int tot = 0;
+          #pragma unroll 1
+          for (int w = 0; w < S::NW; ++w) tot += sm.red_i[0][w];
+          a.cta_cnt[((size_t)b * nCTA + c) * 3 + 2] = tot;
+        }
+        __syncthreads();
       }
     }
     if (need_cand || need_tie) {
@@ -1949,9 +1986,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     }
 
     TS_MARK(22);
-    // ---- the selection flag of each of my tokens (a byte), then my selected tokens as an ascending
-    // list and the counts for the output positions. Warp w takes a contiguous run of the
-    // segment's tokens, so per-warp counts give positions in token order without a block scan.
+    // ---- (2) exact ties and crossing-bin tokens decided, then my selected tokens as an ascending
+    // list and the counts for the output positions
     #pragma unroll 1
     for (int sg = 0; sg < sm.nseg; ++sg) {
       const int b = sm.seg_b[sg];
@@ -1959,40 +1995,17 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       const int tl0 = sm.seg_lp0[sg] * S::P, t0l = sm.seg_t0[sg], nt = sm.seg_ntok[sg];
       const float* vb = a.vote + (size_t)b * a.vote_stride;
       uint8_t* fl = selflag + t0l;
-      const int per = ((nt + S::NW * 32 - 1) / (S::NW * 32)) * 32;   // tokens per warp, whole 32s
-      const int w0 = min(nt, warp * per), w1 = min(nt, w0 + per);
+      int w0, w1;
+      warp_run(nt, w0, w1);
       const int m_cand = st.cand ? (int)min(__ldcg(&a.cand_n[b]), (unsigned)kCandCap) : 0;
       #pragma unroll 4
       for (int j = tid; j < m_cand; j += blockDim.x) scand[j] = __ldcg(&a.cands[(size_t)b * kCandCap + j]);
-      // (1) classes: 0 out, 1 selected, 2 to be ranked against the gathered candidates, 3 an exact
-      // tie of the crossing value (eight loads in flight per lane)
-      int nties = 0;
-      #pragma unroll 1
-      for (int i0 = w0; i0 < w1; i0 += 8 * 32) {
-        uint32_t key[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = i0 + u * 32 + lane;
-          key[u] = i < w1 ? __float_as_uint(__ldcg(vb + tl0 + i)) : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = i0 + u * 32 + lane, t = tl0 + i;
-          if (i >= w1) continue;
-          uint8_t cls = 0;
-          if (t >= st.lo && t < st.hi) {
-            const uint32_t km = key[u] & st.mask;
-            if (st.all || km > st.prefix) cls = 1;
-            else if (km == st.prefix) cls = st.cand ? 2 : (st.tie_mode ? 3 : 0);
-          }
-          fl[i] = cls;
-          nties += cls == 3;
-        }
-      }
-      __syncthreads();                                    // the candidates are in shared memory
-      // (2) exact ties, in token order: the first st.ties of them over the sequence are taken
+      __syncthreads();
+      // exact ties in token order: the first st.ties of them over the sequence are taken
       if (st.tie_mode) {
-        nties = warp_sum_i(nties);
+        int nties = 0;
+        #pragma unroll 1
+        for (int i0 = w0; i0 < w1; i0 += 32) nties += __popc(__ballot_sync(kFull, i0 + lane < w1 && fl[i0 + lane] == 3));
         if (lane == 0) sm.red_i[0][warp] = nties;
         __syncthreads();
         int off = sm.tie_base[sg];
@@ -2008,7 +2021,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         }
         __syncthreads();                                  // red_i is reused below
       }
-      // (3) tokens of the crossing bin: the warp ranks each against the gathered list
+      // tokens of the crossing bin: the warp ranks each against the gathered list
       if (st.cand) {
         #pragma unroll 1
         for (int i0 = w0; i0 < w1; i0 += 32) {
@@ -2038,7 +2051,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           }
         }
       }
-      // (4) counts per warp (all, in [s_end, ls), below s_end), then the list in token order; my
+      // counts per warp (all, in [s_end, ls), below s_end), then the list in token order; my
       // scratch region's logits are spent, the list of this segment starts at its row t0l
       int na = 0, nc = 0, nlo = 0;
       #pragma unroll 1
