@@ -51,6 +51,8 @@ constexpr int kPreFix = 512;       // fixed attention tokens of a CTA resolved a
 constexpr int kMaxPagesCta = 1024; // page ids of a CTA's range kept in shared memory
 constexpr int kScanClaim = 2;      // pages per claim of a shared tensor-core scan
 constexpr int kVoteBufs = 2;       // shared-memory buffers of logit chunks for the votes
+constexpr int kMaxGrid = 256;      // CTAs of the persistent launch (one per SM)
+static_assert(2 * kMaxGrid + 1 <= kMaxPagesCta, "balanced-attention offsets share the page-id array");
 constexpr int kMaxSlots = 12;      // ring slots (runtime count per launch)
 constexpr int64_t kLogitL2Budget = 48ll << 20;  // default bytes of logits one scan wave keeps in L2
 // radix levels over the vote bits (votes are >= +0, bit 31 is always 0): bits 30..17, 16..6,
@@ -190,7 +192,7 @@ struct StepKArgs {
   unsigned long long* mass;    // [B][kHistPerSeq]
   unsigned* cand_n;            // [B]
   unsigned long long* cands;   // [B][kCandCap]  (key << 32 | ~index)
-  int* cta_cnt;                // [B][nCTA][3]  cand-range selected, all selected, ties
+  int* cta_cnt;                // [B][nCTA][4]  cand-range selected, all selected, ties, selected below s_end
   float* apart;                // [B][nCTA][H][D + 2]
   float* spill;                // per CTA: logits [tok][wave head]
   float2* wpart;               // per CTA: [segment][scan warp][head] (max, sum exp) of a wave
@@ -442,7 +444,13 @@ struct Smem {
   int tc_img_of[kMaxB];            // image of sequence b, or -1
   uint32_t tmem;                   // TMEM base address of the accumulators
   int acc_tl[2], acc_nv[2], acc_sg[2];  // per accumulator buffer: first token, valid rows, segment
-  int my_pages[kMaxPagesCta];  // physical page ids of my range (first kMaxPagesCta pages)
+  union {
+    int my_pages[kMaxPagesCta];  // physical page ids of my range (first kMaxPagesCta pages)
+    struct {                     // balanced attention (my_pages unused then): a sequence's per-CTA
+      int pref[kMaxGrid + 1];    // offsets in its concatenated lists, and each CTA's count below s_end
+      int nlo[kMaxGrid];
+    } bal;
+  };
   int timed_out;
   unsigned gepoch;                 // grid barriers passed (thread 0)
   int wsum[33];
@@ -1961,7 +1969,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           int tot = 0;
           #pragma unroll 1
           for (int w = 0; w < S::NW; ++w) tot += sm.red_i[0][w];
-          a.cta_cnt[((size_t)b * nCTA + c) * 3 + 2] = tot;
+          a.cta_cnt[((size_t)b * nCTA + c) * 4 + 2] = tot;
         }
         __syncthreads();
       }
@@ -1978,7 +1986,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         int s = 0;
         if (st.tie_mode)
           #pragma unroll 1
-          for (int cc = st.first_cta + lane; cc < c; cc += 32) s += __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 3 + 2]);
+          for (int cc = st.first_cta + lane; cc < c; cc += 32) s += __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 4 + 2]);
         s = warp_sum_i(s);
         if (lane == 0) sm.tie_base[sg] = s;
       }
@@ -2087,8 +2095,9 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           tc += sm.red_i[1][w];
           tlo += sm.red_i[2][w];
         }
-        a.cta_cnt[((size_t)b * nCTA + c) * 3 + 0] = tc;
-        a.cta_cnt[((size_t)b * nCTA + c) * 3 + 1] = ta;
+        a.cta_cnt[((size_t)b * nCTA + c) * 4 + 0] = tc;
+        a.cta_cnt[((size_t)b * nCTA + c) * 4 + 1] = ta;
+        a.cta_cnt[((size_t)b * nCTA + c) * 4 + 3] = tlo;
         sm.sel_a[sg] = ta;
         sm.sel_c[sg] = tc;
         sm.sel_lo[sg] = tlo;
@@ -2098,6 +2107,11 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
   }
 
   TS_MARK(23);
+  // With top-p the selected tokens can crowd into a few CTAs' ranges: after one more barrier
+  // every CTA takes an equal share of each sequence's selected tokens (the CTAs' lists in
+  // order, a fixed assignment) instead of its own
+  const bool bal = a.mode == TS_SELECT_TOPP && (a.phases & kPhSelect) && (a.phases & kPhAttend) && sm.ptot > 0;
+  if (bal && !grid_sync(a.gsync, a.status, &sm.gepoch)) return;
   // ======================================================================== ATTEND
   // My tokens per sequence: a round-robin share of the fixed ones (sinks and
   // window, the cached part of a hit, or the caller's index list) and my own
@@ -2151,9 +2165,31 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       }
       const int nmid = ct_hi - ct_lo;
       const int sgi = sm.my_seg_of[b];
-      const bool own = !given && !st.hit && sgi >= 0;
-      const int own_nc = own ? sm.sel_c[sgi] : 0;
-      const int* own_lst = own ? sel_list + sm.seg_t0[sgi] + sm.sel_lo[sgi] : nullptr;
+      const bool own = !given && !st.hit && (bal ? st.pg1 > st.pg0 : sgi >= 0);
+      int own_nc = own && !bal ? sm.sel_c[sgi] : 0, own_s0 = 0;
+      const int* own_lst = own && !bal ? sel_list + sm.seg_t0[sgi] + sm.sel_lo[sgi] : nullptr;
+      if (own && bal) {
+        // the sequence's CTAs' counts of selected tokens in [s_end, ls): prefix offsets, and my share
+        int tot = 0;
+        #pragma unroll 1
+        for (int c0 = 0; c0 < nCTA; c0 += blockDim.x) {
+          const int cc = c0 + tid;
+          const bool mine = cc >= st.first_cta && cc <= st.last_cta;
+          const int x = mine ? __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 4 + 0]) : 0;
+          const int xlo = mine ? __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 4 + 3]) : 0;
+          int t_;
+          const int r = block_scan(x, sm.wsum, t_);
+          if (cc < nCTA) {
+            sm.bal.pref[cc] = tot + r;
+            sm.bal.nlo[cc] = xlo;
+          }
+          tot += t_;
+        }
+        if (tid == 0) sm.bal.pref[nCTA] = tot;
+        own_s0 = (int)((int64_t)c * tot / nCTA);
+        own_nc = (int)((int64_t)(c + 1) * tot / nCTA) - own_s0;
+        __syncthreads();
+      }
       const int own_lp0 = own ? sm.seg_lp0[sgi] : 0, own_t0 = own ? sm.seg_t0[sgi] : 0;
       const int nfix_mine = c < nfix ? (nfix - c + nCTA - 1) / nCTA : 0;
       float qreg[S::GP][EPL];
@@ -2225,11 +2261,27 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           const int take = min(around - cnt, own_nc - opos);
           #pragma unroll 1
           for (int r = tid; r < take; r += blockDim.x) {
-            const int t = own_lst[opos + r];
-            const int lpg = (own_t0 + (t - own_lp0 * S::P)) / S::P;   // my page of the token
+            int t, page;
+            if (bal) {
+              // position p of the sequence's concatenated lists: the CTA cc whose offsets hold it
+              const int p = own_s0 + opos + r;
+              int lo = st.first_cta, hi = st.last_cta;
+              while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (sm.bal.pref[mid] <= p) lo = mid;
+                else hi = mid - 1;
+              }
+              const int* lst = reinterpret_cast<const int*>(a.spill + (size_t)lo * sm.region) +
+                               (max(st.pg0, lo * sm.ppc) - lo * sm.ppc) * S::P + sm.bal.nlo[lo];
+              t = __ldcg(lst + (p - sm.bal.pref[lo]));
+              page = a.page_table[(size_t)b * a.pt_stride + t / S::P];
+            } else {
+              t = own_lst[opos + r];
+              const int lpg = (own_t0 + (t - own_lp0 * S::P)) / S::P;   // my page of the token
+              page = lpg < kMaxPagesCta ? sm.my_pages[lpg] : a.page_table[(size_t)b * a.pt_stride + t / S::P];
+            }
             sm.toks[cnt + r] = t;
-            sm.tval[cnt + r] = lpg < kMaxPagesCta ? sm.my_pages[lpg]
-                                                  : a.page_table[(size_t)b * a.pt_stride + t / S::P];
+            sm.tval[cnt + r] = page;
           }
           opos += take;
           cnt += take;
@@ -2430,8 +2482,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       if (!st.hit)
         #pragma unroll 8
         for (int cc = st.first_cta + lane; cc <= st.last_cta; cc += 32) {
-          const int xc = __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 3 + 0]);
-          const int xa = __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 3 + 1]);
+          const int xc = __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 4 + 0]);
+          const int xa = __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 4 + 1]);
           if (cc < c) {
             pc += xc;
             pa += xa;
@@ -2629,6 +2681,7 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
     if (oe != cudaSuccess || per_sm < 1) return TS_ERR_COOP_UNAVAILABLE;
     ctx->step_grid = ctx->num_sms;
   }
+  if (ctx->step_grid > kMaxGrid) return TS_ERR_UNSUPPORTED;
   const ts_config& cfg = ctx->cfg;
   StepKArgs a{};
   a.phases = c.phases;
