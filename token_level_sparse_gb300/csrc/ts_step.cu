@@ -2307,7 +2307,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         }
         // ---- (1) scores: warp -> (its KV head, tokens wsl, wsl + NWG, ...); lane holds EPL dims,
         // the G dot products are reduced across the warp so that lane `which` ends with head `which`
-#pragma unroll 2
+#pragma unroll 4   // independent tokens: their loads and shuffle trees overlap
         for (int j = wsl; j < cnt; j += NWG) {
           float kf[EPL];
           load_elems<KT, EPL>(Ks + ((size_t)j * HKV + gw) * D + lane * EPL, kf);
@@ -2358,9 +2358,32 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           if (qd < NGRP) {
             const int h = qd / D4, d4 = qd % D4, g = h / G;
             const float corr = sm.att_c[h];
+            // four tokens per step into two accumulators: the loads of a step are in flight together
             float4 acc = make_float4(o[k].x * corr, o[k].y * corr, o[k].z * corr, o[k].w * corr);
+            float4 acc2 = make_float4(0.f, 0.f, 0.f, 0.f);
+            int t = 0;
             #pragma unroll 1
-            for (int t = 0; t < cnt; ++t) {
+            for (; t + 4 <= cnt; t += 4) {
+              float w[4], vf[4][4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                w[u] = Ps[h * ldp + t + u];
+                load_elems<KT, 4>(Vs + ((size_t)(t + u) * HKV + g) * D + d4 * 4, vf[u]);
+              }
+#pragma unroll
+              for (int u = 0; u < 4; u += 2) {
+                acc.x = fmaf(w[u], vf[u][0], acc.x);
+                acc.y = fmaf(w[u], vf[u][1], acc.y);
+                acc.z = fmaf(w[u], vf[u][2], acc.z);
+                acc.w = fmaf(w[u], vf[u][3], acc.w);
+                acc2.x = fmaf(w[u + 1], vf[u + 1][0], acc2.x);
+                acc2.y = fmaf(w[u + 1], vf[u + 1][1], acc2.y);
+                acc2.z = fmaf(w[u + 1], vf[u + 1][2], acc2.z);
+                acc2.w = fmaf(w[u + 1], vf[u + 1][3], acc2.w);
+              }
+            }
+            #pragma unroll 1
+            for (; t < cnt; ++t) {
               const float w = Ps[h * ldp + t];
               float vf[4];
               load_elems<KT, 4>(Vs + ((size_t)t * HKV + g) * D + d4 * 4, vf);
@@ -2369,7 +2392,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
               acc.z = fmaf(w, vf[2], acc.z);
               acc.w = fmaf(w, vf[3], acc.w);
             }
-            o[k] = acc;
+            o[k] = make_float4(acc.x + acc2.x, acc.y + acc2.y, acc.z + acc2.z, acc.w + acc2.w);
           }
         }
         __syncthreads();
