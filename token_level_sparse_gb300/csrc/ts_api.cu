@@ -132,8 +132,8 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   chk(alloc(&ctx->cands, B * 2048));
   chk(alloc(&ctx->cta_cnt, B * NS * 4));
   chk(alloc(&ctx->apart, B * NS * H * (D + 2) + 2 * B * H));   // (max, sum) rows padded to an even count
-  // per CTA: [sequence][scan warp][head] pairs (CUDA-core scan) or [2][128 rows][head] (tensor-core scan)
-  chk(alloc(&ctx->step_wpart, NS * std::max<size_t>(B * kMaxScanWarps, 2 * 128) * kMaxScanG * 2));
+  // per CTA: [sequence][scan warp][head] (max, sum exp) pairs of the CUDA-core scan
+  chk(alloc(&ctx->step_wpart, NS * B * kMaxScanWarps * kMaxScanG * 2));
   chk(alloc(&ctx->gsync, 4));
   if (e == cudaSuccess) chk(cudaMemset(ctx->gsync, 0, 4 * sizeof(unsigned)));   // then kept zero by each launch
   chk(alloc(&ctx->phase_ns, 32));

@@ -80,7 +80,7 @@ struct ts_ctx {
     alignas(64) unsigned char map[128];
   } kmaps[8];
   int kmap_next = 0;
-  float* step_wpart = nullptr;           // per SM: scan (max, sum exp) pairs, see the persistent kernel
+  float* step_wpart = nullptr;           // per SM: CUDA-core scan (max, sum exp) pairs, see the persistent kernel
   unsigned* gsync = nullptr;             // grid barrier state (4 words)
   unsigned long long* phase_ns = nullptr;  // [32] phase boundary times of the last step kernel
   bool use_step = true;                  // the persistent kernel is available

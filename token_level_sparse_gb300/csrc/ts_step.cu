@@ -214,10 +214,6 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   return v;
 }
 
-__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // All CTAs of the cooperative grid meet here. The arrival counter only grows
@@ -491,7 +487,7 @@ __device__ __noinline__ bool cuda_scan_wave(const StepKArgs& a, Smem& sm, unsign
   const int c = blockIdx.x, nCTA = gridDim.x;
   const int B = a.B, H = a.H;
   const int nslot = a.nslot;
-  const int hpw = sm.hpw, HW = hpw * G, nwaves = sm.nwaves;
+  const int hpw = sm.hpw, HW = hpw * G;
   const int pps = HKV / hpw;                       // pages per stage
   const int np = sm.p1 - sm.p0;
   const int nstages = (np + pps - 1) / pps;
@@ -695,8 +691,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
   __shared__ __align__(8) uint64_t xbar;              // bulk copies of partials (vote, merge)
   __shared__ __align__(8) uint64_t vbar[kVoteBufs];  // chunks of my logits for the votes
 
-  const int nslot = a.nslot;
-  unsigned char* ring = dsm;                                               // nslot x STAGE_BYTES of K
+  unsigned char* ring = dsm;                                               // a.nslot x STAGE_BYTES of K
   uint8_t* selflag = dsm + a.dyn_bytes - a.flag_cap;                       // selection flags of my tokens
   // tensor-core scan: 1024-aligned ring of pages, then the query-term images of two sequences
   unsigned char* tcr = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(dsm) + 1023) & ~(uintptr_t)1023);
@@ -1336,10 +1331,11 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     if constexpr (S::TC) {
       if (sm.use_tc) {
         scanned = true;
-        // ---- pages of my range through a ring of TMA tiles; one elected thread multiplies each
-        // page (128 rows = H_kv heads x 16 tokens) by the query terms of its sequence into a
-        // TMEM accumulator (two buffers); four warps read the accumulators out: logits to the
-        // scratch, running (max, sum exp) per row and head in registers
+        // ---- pages of my range (or claimed ones) through a ring of TMA tiles fed by warp 0; one
+        // elected thread of warp 1 multiplies each page (128 rows = H_kv heads x 16 tokens) by the
+        // query terms of its sequence into a TMEM accumulator (two buffers); warps 4..7 read the
+        // accumulators out: logits to the scratch, running (max, sum 2^x) per row and head in
+        // registers, reduced into the CTA's partials at the end; warps 8.. finish the set-up
         const int nsl = a.nslot_tc;
         float* eb = a.spill + (size_t)c * sm.region;             // [tok_stride][H]
         if (warp == 2) {
