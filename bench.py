@@ -265,8 +265,12 @@ class DecodeBench:
         self.params = T.params(mode=T.TS_SELECT_TOPP if topp else T.TS_SELECT_TOPK, k=sp.k, top_p=sp.top_p,
                                n_sink=sp.n_sink, n_local=sp.n_local, theta=theta)
         z = dict(device=device)
-        self.q_buf = [torch.zeros(B, H, d, **z) for _ in range(L)]
-        self.seq_buf = torch.zeros(B, dtype=torch.int32, **z)
+        # the step's queries (every layer) and lengths in one device block, so that the end-to-end
+        # loop moves them with one copy
+        nq = B * H * d
+        self.in_buf = torch.zeros(L * nq + B, dtype=torch.int32, **z)
+        self.q_buf = [self.in_buf[l * nq:(l + 1) * nq].view(torch.float32).view(B, H, d) for l in range(L)]
+        self.seq_buf = self.in_buf[L * nq:]
         self.seq_all = torch.stack([wl.seq_lens(t) for t in range(sp.steps)])
         self.idx = [torch.zeros(B, cap, dtype=torch.int32, **z) for _ in range(L)]
         self.count = [torch.zeros(B, dtype=torch.int32, **z) for _ in range(L)]
@@ -403,14 +407,18 @@ class DecodeBench:
 
     def e2e(self, steps):
         """The same decode steps through the public call with host buffers: every step
-        copies its query, lengths and the new token's K/V rows from pinned host memory,
-        runs ts_decode_step per layer, and reads the attention output back."""
+        copies its queries and lengths (one packed block) and the new token's K/V rows from
+        pinned host memory, runs ts_decode_step per layer, and reads the attention output back."""
         torch, T = self.torch, self.T
         wl, sp = self.wl, self.sp
         L, B = sp.layers, sp.batch
         P = sp.page_size
-        q_host = [[wl.q[t][l].cpu().pin_memory() for l in range(L)] for t in range(sp.steps)]
-        seq_host = self.seq_all.cpu().pin_memory()
+        # per step, the queries of every layer and the lengths packed as the device block is
+        in_host = []
+        for t in range(sp.steps):
+            blk = torch.cat([wl.q[t][l].reshape(-1).cpu().view(torch.int32) for l in range(L)] +
+                            [self.seq_all[t].cpu()])
+            in_host.append(blk.pin_memory())
         pt_host = wl.page_table.cpu()
         kv_host = []
         for t in range(sp.steps):
@@ -431,12 +439,8 @@ class DecodeBench:
             t = i % sp.steps
             if t == 0:
                 self.cache.reset()
-            h2d = 0
-            for l in range(L):
-                self.q_buf[l].copy_(q_host[t][l], non_blocking=True)
-                h2d += q_host[t][l].numel() * 4
-            self.seq_buf.copy_(seq_host[t], non_blocking=True)
-            h2d += B * 4
+            self.in_buf.copy_(in_host[t], non_blocking=True)
+            h2d = in_host[t].numel() * 4
             for (l, page, slot, kr, vr) in kv_host[t]:
                 wl.k_pool[l][page, :, slot, :].copy_(kr, non_blocking=True)
                 wl.v_pool[l][page, :, slot, :].copy_(vr, non_blocking=True)
