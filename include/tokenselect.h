@@ -178,7 +178,14 @@ ts_status ts_sparse_attend_noalloc(int n_q_heads, int n_kv_heads, int head_dim, 
  * cache check (when cache != NULL and theta <= 1), score and vote for the
  * sequences that miss, selection (and cache update), sparse attention.
  * hit uint8 [B] (may be NULL) receives the cache decisions. vote receives the
- * votes of the missing sequences (may be NULL: context scratch is used). */
+ * votes of the missing sequences (may be NULL: context scratch is used).
+ * Supported geometries run as one cooperative launch; repeated calls on the
+ * same inputs give bit-identical results. Environment switches read at each
+ * call (comparisons and tests): TOKENSELECT_MULTI_KERNEL=1 (read at ts_create)
+ * keeps the multi-kernel path; TOKENSELECT_NO_TC=1 scans on CUDA cores instead
+ * of tensor cores; TOKENSELECT_SCAN_CLAIM=1 lets the CTAs claim scan pages from
+ * a shared counter when at most two sequences are scanned (faster where SM
+ * bandwidth differs, but no longer bit-identical from run to run). */
 ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q,
                          const void* k_pool, const void* v_pool, const int32_t* page_table,
                          const int32_t* seq_lens, int B, const ts_select_params* params,
