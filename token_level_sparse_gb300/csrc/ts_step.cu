@@ -4,26 +4,32 @@
 //
 // The method is TokenSelect's (deep notes: Appendix Algorithm 1 and 2, "Head
 // soft vote", "Formalising selective sparse attention"; review: section 4.2).
-// The GB300 mapping:
-//  * one CTA per SM: one producer warp streams the KV pages of a contiguous
-//    range of the concatenated (missing) sequences into a shared-memory ring
-//    with 1-D bulk copies (TMA); up to 16 consumer warps hold the G queries of
-//    a KV head in registers and read every K element once;
-//  * each head's logits stay in shared memory as exp(l - m_cta); per-CTA
-//    (max, sum) partials cross CTAs through a grid barrier, after which every
-//    CTA forms its tokens' votes with one FMA per (token, head). When the
-//    logits of all heads do not fit, the heads are scanned in waves (one
-//    barrier per wave) and the votes accumulate in global memory;
-//  * selection: radix histograms of the vote bit pattern, aggregated in
-//    shared memory and added with integer atomics (order-free, hence
-//    deterministic); as soon as the crossing bin holds at most 2048 tokens
-//    they are gathered and each CTA ranks its own candidates exactly (ties
-//    go to the lower index; top-p mass in 2^-40 fixed point);
-//  * attention: every CTA attends its own selected tokens plus a round-robin
-//    share of the sinks, window and cached indices, gathering K/V rows by
-//    bulk copy; per-CTA (max, sum, o) partials are merged after one barrier.
+// The GB300 mapping, one CTA per SM and grid barriers between phases:
+//  * score: each CTA scans a contiguous range of the concatenated (missing)
+//    sequences' pages. Warp 0 feeds a ring of tiled TMA loads (one page of all
+//    KV heads = 128 rows); one thread of warp 1 issues tcgen05 MMAs of each
+//    page against the query heads (each fp32 query split into three bf16
+//    terms) into double-buffered TMEM accumulators; warps 4..7 read them out,
+//    write the logits (base-2 units) to scratch and keep per-row running
+//    (max, sum), reduced into per-CTA partials. Geometries without the tensor
+//    core scan use a CUDA-core scan (cuda_scan_wave) in waves of KV heads;
+//  * vote: after the barrier every CTA forms the per-head normalisers from the
+//    CTA partials and the votes of its own tokens from its logits, which come
+//    back into shared memory by bulk copy;
+//  * selection: radix histograms of the vote bit pattern, aggregated in shared
+//    memory and added with integer atomics (order-free, hence deterministic);
+//    once the crossing bin holds at most 2048 tokens they are gathered and
+//    ranked exactly (ties go to the lower index; top-p mass in 2^-40 fixed
+//    point). Each CTA then writes its selected tokens as an ascending list into
+//    its spent logit scratch;
+//  * attention: every CTA attends its own selected tokens (with top-p an equal
+//    share of every CTA's lists) plus a round-robin share of the sinks, window
+//    and cached indices, gathering K/V rows by bulk copy; per-CTA (max, sum, o)
+//    partials are merged after one more barrier, and the index lists and the
+//    Selection Cache entries are written from the per-CTA lists.
 // Grid barriers and mbarrier waits are bounded by %globaltimer; on time-out
-// the kernel records TS_ERR_TIMEOUT and returns.
+// the kernel records TS_ERR_TIMEOUT and returns. The last CTA to leave zeroes
+// the barrier words for the next launch.
 #include <algorithm>
 #include <cfloat>
 #include <cmath>
@@ -193,8 +199,8 @@ struct StepKArgs {
   unsigned* cand_n;            // [B]
   unsigned long long* cands;   // [B][kCandCap]  (key << 32 | ~index)
   int* cta_cnt;                // [B][nCTA][4]  cand-range selected, all selected, ties, selected below s_end
-  float* apart;                // [B][nCTA][H][D + 2]
-  float* spill;                // per CTA: logits [tok][wave head]
+  float* apart;                // o [B][H][parts][nCTA][D / parts], then (max, sum) [B][H][nCTA even]
+  float* spill;                // per CTA: logits [tok][wave head], later its selected tokens (ascending)
   float2* wpart;               // per CTA: [segment][scan warp][head] (max, sum exp) of a wave
   int64_t spill_floats;
   int64_t l2_budget;           // bytes of logits one scan wave may keep in L2
