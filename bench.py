@@ -9,7 +9,9 @@ geometry at N = 131072 (batch 1, 32 query / 8 KV heads, d 128, bf16 KV,
 k 2048 + 4 sinks + 512 local, theta 0.9, a 64-step AR(1) query trajectory);
 timed steps cycle through that trajectory with a fresh Selection Cache at the
 start of each pass. Inputs are synthetic and already resident in HBM; L2 is
-flushed (a 256 MB write) before every timed step, outside the step's events.
+flushed before every timed step, outside the step's events (a 256 MB write,
+then a 256 MB read so that no dirty line of the flush is left to be written
+back inside the step).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -82,7 +84,12 @@ PHASES = {0: "start", 1: "setup", 5: "lengths", 6: "cache-test", 7: "partition",
           3: "stats", 4: "scan-barrier", 13: "vote-partials", 14: "vote-norm", 20: "votes",
           28: "hist0", 29: "hist1", 30: "hist2", 21: "levels", 22: "candidates", 23: "flags",
           10: "gathered", 15: "att-scores", 16: "att-weights", 9: "rounds", 11: "attended", 24: "partials", 25: "last-barrier",
-          26: "merged", 27: "end", 17: "last-cta-start", 18: "last-cta-end"}
+          26: "merged", 27: "end", 17: "last-cta-start", 18: "last-cta-end",
+          32: "v-chunk", 33: "h0-start", 34: "h0-zeroed", 35: "h0-counted", 36: "h0-barrier",
+          37: "h1-start", 38: "h1-zeroed", 39: "h1-counted", 40: "h1-barrier", 41: "h2-start",
+          42: "h2-zeroed", 43: "h2-counted", 44: "h2-barrier", 45: "coarse", 46: "fine", 47: "classified",
+          48: "cand-barrier", 49: "cand-fetched", 50: "ranked", 51: "att-q", 52: "att-fixed", 53: "att-own",
+          54: "merge-fetched", 55: "counts"}
 
 
 def print_phases(b, step):
@@ -278,8 +285,17 @@ class DecodeBench:
         self.lse = [torch.zeros(B, H, **z) for _ in range(L)]
         self.hit = [torch.zeros(B, dtype=torch.uint8, **z) for _ in range(L)]
         self.flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, **z)
+        self.flush_r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, **z)
+        self.flush_sink = torch.zeros((), dtype=torch.float32, **z)
         self.graph = None
         self.pattern = {}      # trajectory step -> its hits and bytes, from run()
+
+    def flush_l2(self):
+        """Evicts L2 before a timed step: a write of a buffer larger than L2, then a read of
+        another one, so that the dirty lines of the write are written back here, outside the
+        step's events, and the step starts with an L2 of clean lines it does not use."""
+        self.flush.zero_()
+        self.torch.sum(self.flush_r, 0, out=self.flush_sink)
 
     def _launch(self, l, q=None, seq=None):
         T = self.T
@@ -336,7 +352,7 @@ class DecodeBench:
                 self.cache.reset()
             self._stage(t)
             if flush:
-                self.flush.zero_()
+                self.flush_l2()
             timed = i >= warmup
             if timed:
                 ev[i - warmup][0].record()
@@ -389,7 +405,7 @@ class DecodeBench:
             if t == 0:
                 self.cache.reset()
             if flush:
-                self.flush.zero_()
+                self.flush_l2()
             ev[i][0].record()
             self.graphs[t].replay()
             ev[i][1].record()
@@ -661,7 +677,7 @@ def main(argv=None):
     dev_s = max_over_ranks(s["ms_per_step"] * len(rec) / 1000.0, ws, dev)
     value = ws * len(rec) / dev_s
 
-    e2e = bench.e2e(min(args.steps, 4 * TRAJ))
+    e2e = bench.e2e(min(max(args.steps, 2 * TRAJ), 4 * TRAJ))
     e2e_v = max_over_ranks(1.0 / e2e["value"], ws, dev)
     e2e["value"] = ws / e2e_v
 
@@ -714,7 +730,7 @@ def main(argv=None):
         "config": {"workload": "llama3-8b-gqa-n128k: B1, H32/Hkv8, d128, bf16 KV in 16-token pages, "
                                "N0=131072 (+1 per step), k2048 + 4 sinks + 512 local, Selection Cache theta 0.9, "
                                "64-step AR(1) query trajectory cycled with a fresh cache each pass",
-                   "l2": "flushed before every timed step (256 MB write, outside the step events)",
+                   "l2": "flushed before every timed step (256 MB write, then 256 MB read: no dirty lines left; outside the step events)",
                    "launch": "one CUDA graph per step (cache check, score, vote, select, attend), steps "
                              "enqueued back to back; per-launch kernel times from a loop synchronised "
                              "after every step",

@@ -65,6 +65,16 @@ typedef enum {
 
 enum { TS_KV_F32 = 0, TS_KV_BF16 = 1 };
 enum { TS_SELECT_TOPK = 0, TS_SELECT_TOPP = 1 };
+/* Selection function whose per-token score the top-k ranks (TokenSelect deep
+ * notes, "Evolution of the selection function"; TokenSelect review, section
+ * 3.1 and the ablation of section 4.4 / table 4):
+ *  HEAD_SOFT_VOTE  v_i = sum_h softmax(scale q_h.K^T)_i  (the method);
+ *  LOGIT_SUM       s_i = sum_h scale q_h.k_{g(h),i}: plain TopK(Q.K^T) of the
+ *                  concatenated heads, dominated by high-norm heads (signed);
+ *  HEAD_HARD_VOTE  c_i = number of query heads whose own top-k over the
+ *                  candidates [s, N-w) (ties to the lower index) holds i.
+ * The two ablations serve top-k only and run on the multi-kernel path. */
+enum { TS_SCORE_HEAD_SOFT_VOTE = 0, TS_SCORE_LOGIT_SUM = 1, TS_SCORE_HEAD_HARD_VOTE = 2 };
 
 /* Shape of the model's attention and of the caller's pools, fixed per context. */
 typedef struct {
@@ -88,6 +98,7 @@ typedef struct {
   float top_p;            /* mass fraction for TOPP; >= 1 keeps every token     */
   float theta;            /* cache threshold; > 1 never hits                    */
   float softmax_scale;    /* alpha; 0 means 1/sqrt(d)                           */
+  int score_fn;           /* TS_SCORE_*; 0 (the head soft vote) by default      */
 } ts_select_params;
 
 /* Context: validates and records cfg, allocates the device scratch for
@@ -122,6 +133,18 @@ ts_status ts_score(ts_ctx* ctx, const float* q, const void* k_pool, const int32_
                    const int32_t* seq_lens, int B, const uint8_t* skip, float scale,
                    float* vote, int64_t vote_stride, void* stream);
 
+/* The per-token score of one selection function (params->score_fn, TS_SCORE_*)
+ * for the top-k of ts_select: HEAD_SOFT_VOTE computes exactly what ts_score
+ * does; LOGIT_SUM writes the signed sums of the per-head logits (rank them by
+ * passing the same params to ts_select); HEAD_HARD_VOTE runs one top-k per
+ * query head over the candidates [s, N-w) of params (k, n_sink, n_local; ties
+ * to the lower index) and writes the vote counts as floats (exact small
+ * integers, 0 outside the candidates). Every entry i < seq_lens[b] of a row
+ * that is not skipped is written; layout and scale as in ts_score. */
+ts_status ts_score_fn(ts_ctx* ctx, const ts_select_params* params, const float* q, const void* k_pool,
+                      const int32_t* page_table, const int32_t* seq_lens, int B, const uint8_t* skip,
+                      float* vote, int64_t vote_stride, void* stream);
+
 /* Selection (top-k or top-p) united with sinks and window, ascending.
  * For each b: if hit != NULL and hit[b] != 0, the index set is rebuilt from
  * the cache entry (cached part within [s, N-w), plus the current sinks and
@@ -130,7 +153,9 @@ ts_status ts_score(ts_ctx* ctx, const float* q, const void* k_pool, const int32_
  * the vote go to the lower index. idx int32 [B][idx_stride] receives the
  * count[b] indices; a count above idx_stride (or a selected part above the
  * cache capacity) records TS_ERR_CAPACITY and writes nothing past the end.
- * q may be NULL when cache is NULL. */
+ * q may be NULL when cache is NULL. With params->score_fn == LOGIT_SUM the
+ * scores are ranked as signed values; top-p needs the head soft vote (its
+ * mass is the vote's), else TS_ERR_INVALID_ARG. */
 ts_status ts_select(ts_ctx* ctx, ts_cache* cache, int layer, const float* q, const float* vote,
                     int64_t vote_stride, const int32_t* seq_lens, int B, const uint8_t* hit,
                     const ts_select_params* params, int32_t* idx, int64_t idx_stride,
@@ -154,10 +179,12 @@ ts_status ts_sparse_attend(ts_ctx* ctx, const float* q, const void* k_pool, cons
  * so cannot create a context (ts_create allocates its scratch).
  * Its scratch (split partials, merge counters, a fallback status slot) is one
  * fixed static device array of 4 MiB + 16 KiB in the library, held by every
- * GPU that loads the library until the process exits. Limits: B <= 48 and
- * B * H_kv * G * (d + 2) <= 2^20 floats (one split per (sequence, KV head)
- * at that size); beyond them the call returns TS_ERR_SCRATCH_LIMIT and
- * enqueues nothing. It calls no cudaMalloc/cudaFree. The first call on a
+ * GPU that loads the library until the process exits. Limits: B <= 48,
+ * n_kv_heads <= 64 (one merge counter per (sequence, KV head) in the head of
+ * the array) and B * H_kv * G * (d + 2) <= 2^20 floats (one split per
+ * (sequence, KV head) at that size); beyond them the call returns
+ * TS_ERR_SCRATCH_LIMIT and enqueues nothing. A NaN scale returns
+ * TS_ERR_INVALID_ARG, as in ts_sparse_attend. It calls no cudaMalloc/cudaFree. The first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) and the
  * SM count: make that first call before any stream capture on that device.
  * Every call clears the merge counters, then uses the shared array: calls
@@ -180,17 +207,59 @@ ts_status ts_sparse_attend_noalloc(int n_q_heads, int n_kv_heads, int head_dim, 
  * hit uint8 [B] (may be NULL) receives the cache decisions. vote receives the
  * votes of the missing sequences (may be NULL: context scratch is used).
  * Supported geometries run as one cooperative launch; repeated calls on the
- * same inputs give bit-identical results. Environment switches read at each
- * call (comparisons and tests): TOKENSELECT_MULTI_KERNEL=1 (read at ts_create)
- * keeps the multi-kernel path; TOKENSELECT_NO_TC=1 scans on CUDA cores instead
- * of tensor cores; TOKENSELECT_SCAN_CLAIM=1 lets the CTAs claim scan pages from
- * a shared counter when at most two sequences are scanned (faster where SM
- * bandwidth differs, but no longer bit-identical from run to run). */
+ * same inputs give bit-identical results. params->score_fn other than the
+ * head soft vote (the ablations) runs the multi-kernel path with that
+ * selection function (the vote buffer then holds its scores). Environment switches, read once by
+ * ts_create (comparisons and tests): TOKENSELECT_MULTI_KERNEL=1 keeps the
+ * multi-kernel path; TOKENSELECT_NO_TC=1 scans on CUDA cores instead of tensor
+ * cores; TOKENSELECT_SCAN_CLAIM=1 lets the CTAs claim scan pages from a shared
+ * counter when at most two sequences are scanned (faster where SM bandwidth
+ * differs, but no longer bit-identical from run to run);
+ * TOKENSELECT_L2_BUDGET_MB sets the logit bytes one CUDA-core scan wave may
+ * keep in L2; TS_DEBUG prints launch diagnostics. */
 ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q,
                          const void* k_pool, const void* v_pool, const int32_t* page_table,
                          const int32_t* seq_lens, int B, const ts_select_params* params,
                          float* vote, int64_t vote_stride, int32_t* idx, int64_t idx_stride,
                          int32_t* count, float* out, float* lse, uint8_t* hit, void* stream);
+
+/* Chunk-wise prefill selection (TokenSelect deep notes, "Optimising the
+ * selection frequency of the prefill stage"; review, section 3.2): the c
+ * queries of a prefill chunk, q fp32 [B][c][H][d] (16-byte aligned), are
+ * averaged into one query per sequence, (1/c) sum_i q[b][i]; that mean query
+ * is scored and selects once (head soft vote, top-k over [s, N-w) united
+ * with sinks and window, ties to the lower index; no Selection Cache in
+ * prefill), writing vote (or context scratch when NULL), idx [B][idx_stride]
+ * ascending and count [B] as ts_decode_step does. The chunk's own tokens must
+ * already be cached as the last c of seq_lens[b] tokens: query i attends to
+ * the selected tokens at positions <= seq_lens[b] - c + i (causal), giving
+ * out fp32 [B][c][H][d] and lse fp32 [B][c][H] (or NULL). The attention runs
+ * on the tensor cores for bf16 pools with d = 64 or 128 (else
+ * TS_ERR_UNSUPPORTED). params must be top-k with the head soft vote. */
+ts_status ts_prefill_chunk(ts_ctx* ctx, const float* q, int c, const void* k_pool, const void* v_pool,
+                           const int32_t* page_table, const int32_t* seq_lens, int B,
+                           const ts_select_params* params, float* vote, int64_t vote_stride,
+                           int32_t* idx, int64_t idx_stride, int32_t* count, float* out, float* lse,
+                           void* stream);
+
+/* Failure detection (no counterpart in the pages; the library's own safety
+ * net). Every wait of the persistent decode-step kernel - its grid barriers
+ * and its copy, tensor-core and accumulator waits - gives up after `ns`
+ * nanoseconds (default 1 s): the kernel then records TS_ERR_TIMEOUT, raises an
+ * abort word that the other CTAs see at their next barrier, waits (bounded)
+ * for its own copies in flight, frees its tensor memory and returns, so the
+ * context stays usable. The waits of the separate calls (ts_score,
+ * ts_sparse_attend) keep the 1 s bound. ns == 0 is TS_ERR_INVALID_ARG. */
+ts_status ts_set_wait_limit(ts_ctx* ctx, uint64_t ns);
+
+/* Fault injection for tests of the time-out path: the NEXT persistent
+ * decode-step launch of this context makes CTA `cta` leave at its grid
+ * barrier number `barrier` (0 = the first) without arriving, so that every
+ * other CTA's bounded wait runs out (TS_ERR_TIMEOUT through ts_get_status).
+ * Nothing faults, traps or hangs: the run-out is the ordinary bounded-wait
+ * path, and the launch after it starts from clean barrier words. The request
+ * is consumed by that one launch; a cta beyond the grid injects nothing. */
+ts_status ts_inject_barrier_skip(ts_ctx* ctx, int cta, int barrier);
 
 /* Synchronises `stream`, then reads and clears the device status word.
  * *device_status receives TS_OK or the first device error since the last read. */
@@ -231,9 +300,10 @@ ts_status ts_kernel_count(ts_ctx* ctx, int64_t* out);
  * 2+3w / 3+3w / 4+3w: wave w scanned / partials written / barrier passed,
  * 20: scoring done, 21: radix levels done, 22: candidates gathered,
  * 23: selection done, 24: attention done, 25: last barrier passed,
- * 26: outputs merged, 27: end; 0 where not reached). Synchronises `stream`,
- * copies 32 values to out32 (host) and clears them. */
-ts_status ts_debug_phase_ns(ts_ctx* ctx, uint64_t* out32, void* stream);
+ * 26: outputs merged, 27: end; 32..63 finer points inside the phases, see
+ * the kernel source; 0 where not reached). Synchronises `stream`, copies 64
+ * values to out64 (host) and clears them. */
+ts_status ts_debug_phase_ns(ts_ctx* ctx, uint64_t* out64, void* stream);
 
 /* Library version, e.g. 100 for 0.1.0. */
 int ts_version(void);

@@ -21,7 +21,7 @@ pages give it. Sources (page title, then section / equation):
 * [SeqO1]     SequenceO1 blog, section 3.2 (keep the tokens whose cumulative
   importance reaches a fraction p) - used for the top-p variant only.
 
-Readings where the pages are silent or garbled (each is listed in the design doc):
+Readings where the pages are silent or garbled:
 
 R1  The vote softmax uses the attention scale alpha = 1/sqrt(d) (the printed
     vote omits it; the attention equations carry it). alpha is a parameter.
@@ -42,6 +42,20 @@ R7  A hit reuses only the selected part C_T; sinks and window are rebuilt at
 R8  Ties in the vote go to the lower token index. Index sets are returned in
     ascending order.
 R9  The current token is the last cached position N-1, so the window holds it.
+R10 The plain TopK selection function TopK(Q . K_cache^T) scores token i by the
+    dot product of the concatenated multi-head query with the token's
+    concatenated keys, i.e. the sum over query heads of the (scaled) per-head
+    logits: the reading that makes it "dominated by the heads with the largest
+    logit norms", as the pages say it is.
+R12 Chunk-wise prefill selection: the cache already holds the chunk's c tokens
+    (length n, the chunk at positions n-c .. n-1); the c queries are averaged
+    into one query, which selects once (head soft vote, top-k over [s, n-w),
+    united with sinks and window, no Selection Cache in prefill); chunk query
+    i then attends causally to the selected tokens at positions <= n-c+i.
+R11 The head hard vote counts, per token, the query heads whose own TopK
+    (k tokens, over the same candidates [s, N-w) as R3, ties to the lower
+    index) contains it, then takes the TopK of the counts (ties to the lower
+    index).
 
 Parity pins for every function live in ``tests/test_oracle_pins.py``.
 """
@@ -57,7 +71,8 @@ __all__ = [
     "as_f64", "gather_rows", "head_logits", "soft_vote", "log_normalisers",
     "budget_segments", "select_topk", "select_topp", "refresh_hit",
     "sparse_attention", "dense_attention", "cosine", "CacheState",
-    "cache_decision", "decode_step", "default_scale",
+    "cache_decision", "decode_step", "default_scale", "logit_sum_scores",
+    "hard_vote_counts", "selection_scores", "SCORE_FNS", "prefill_chunk",
 ]
 
 
@@ -204,6 +219,53 @@ def refresh_hit(part: np.ndarray, n: int, n_sink: int, n_local: int) -> np.ndarr
     return _union_fixed(part, n, n_sink, n_local)
 
 
+# ------------------------------------------------ selection-function ablations
+
+def logit_sum_scores(logits: np.ndarray) -> np.ndarray:
+    """s_i = sum_h l[h, i]: the plain TopK selection function's score (reading R10).
+
+    TS-notes, "Evolution of the selection function": T_topk = TopK(Q . K_cache^T),
+    the dot product of the current query with the cached keys; over all heads
+    at once that is the concatenated query against the concatenated keys, the
+    sum of the per-head logits. TS-review section 3.1: dominated by high-norm
+    heads.
+    """
+    return np.asarray(logits, dtype=np.float64).sum(axis=0)
+
+
+def hard_vote_counts(logits: np.ndarray, n: int, k: int, n_sink: int, n_local: int) -> np.ndarray:
+    """c_i = sum_h [i in TopK_k(l[h, candidates])] (reading R11).
+
+    TS-notes, "Evolution of the selection function": T_head-vote =
+    TopK(sum_h I(i in TopK(Q^h . K_cache^h^T))), a 0/1 vote of every head's own
+    top-k. Each head's TopK runs over the candidates [s, N-w) with ties to the
+    lower index; tokens outside the candidates get no vote.
+    """
+    s_end, local_start = budget_segments(n, n_sink, n_local)
+    cand = np.arange(s_end, local_start)
+    counts = np.zeros(n)
+    for h in range(logits.shape[0]):
+        top = _order_desc(logits[h], cand)[:max(0, k)]
+        counts[top] += 1.0
+    return counts
+
+
+SCORE_FNS = ("soft_vote", "logit_sum", "hard_vote")
+
+
+def selection_scores(logits: np.ndarray, score_fn: str, n: int, k: int, n_sink: int, n_local: int):
+    """The per-token score whose TopK is the selection: head soft vote (the method's),
+    or one of the two selection functions it is compared with (TS-notes, "Evolution of
+    the selection function"; TS-review section 4.4, table 4)."""
+    if score_fn == "soft_vote":
+        return soft_vote(logits)
+    if score_fn == "logit_sum":
+        return logit_sum_scores(logits)
+    if score_fn == "hard_vote":
+        return hard_vote_counts(logits, n, k, n_sink, n_local)
+    raise ValueError(score_fn)
+
+
 # ---------------------------------------------------------------- attention
 
 def sparse_attention(q: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray,
@@ -282,15 +344,19 @@ def cache_decision(state: CacheState, q: np.ndarray, theta: float):
 def decode_step(state: CacheState, q: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray,
                 page_row: np.ndarray, n: int, *, mode: str = "topk", k: int = 2048,
                 n_sink: int = 4, n_local: int = 512, top_p: float = 0.9,
-                theta: float = 0.9, scale: Optional[float] = None) -> dict:
+                theta: float = 0.9, scale: Optional[float] = None,
+                score_fn: str = "soft_vote") -> dict:
     """One decode step of one (sequence, layer): cache check, score, select, attend.
 
     TS-notes, "TokenSelect overall flow" (paged dot product -> head soft vote
     -> paged attention over the selected tokens) wrapped in Algorithm 1. On a
     miss the cache takes the new selected part and the query; on a hit the
-    cached part is reused.
+    cached part is reused. score_fn selects the selection function: the head soft
+    vote (default) or one of the ablations (logit_sum, hard_vote; top-k only).
     """
     q = np.asarray(q, dtype=np.float64)
+    if score_fn != "soft_vote" and mode != "topk":
+        raise ValueError("the ablation selection functions are defined for top-k only")
     hit, c = cache_decision(state, q, theta)
     res = {"hit": hit, "cos": c}
     if hit:
@@ -298,7 +364,7 @@ def decode_step(state: CacheState, q: np.ndarray, k_pool: np.ndarray, v_pool: np
         idx = refresh_hit(part, n, n_sink, n_local)
     else:
         logits = head_logits(q, k_pool, page_row, n, scale)
-        vote = soft_vote(logits)
+        vote = selection_scores(logits, score_fn, n, k, n_sink, n_local)
         if mode == "topk":
             idx, part = select_topk(vote, n, k, n_sink, n_local)
         elif mode == "topp":
@@ -313,3 +379,34 @@ def decode_step(state: CacheState, q: np.ndarray, k_pool: np.ndarray, v_pool: np
     out, lse = sparse_attention(q, k_pool, v_pool, page_row, idx, scale)
     res.update(idx=idx, part=part, out=out, lse=lse)
     return res
+
+
+# ---------------------------------------------------- chunk-wise prefill (R12)
+
+def prefill_chunk(q_chunk: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray, page_row: np.ndarray,
+                  n: int, *, k: int = 2048, n_sink: int = 4, n_local: int = 512,
+                  scale: Optional[float] = None) -> dict:
+    """One chunk of c prefill queries: one selection from their mean, causal sparse attention.
+
+    TS-notes, "Optimising the selection frequency of the prefill stage": the c
+    queries of a chunk Q_C are averaged, (1/c) sum_i (Q_C)_i, and that mean
+    query goes through the selection function once; the chunk shares the
+    result. TS-review section 3.2 (closing paragraph): prefill uses no
+    Selection Cache. Reading R12 places the chunk at the end of the n cached
+    tokens and masks each query causally. Returns the index set (ascending),
+    out [c, H, d], lse [c, H] and the mean query's vote.
+    """
+    q_chunk = np.asarray(q_chunk, dtype=np.float64)
+    c = q_chunk.shape[0]
+    if not 1 <= c <= n:
+        raise ValueError("the chunk must hold 1..n queries")
+    q_mean = q_chunk.sum(axis=0) / c
+    vote = soft_vote(head_logits(q_mean, k_pool, page_row, n, scale))
+    idx, part = select_topk(vote, n, k, n_sink, n_local)
+    H, d = q_chunk.shape[1], q_chunk.shape[2]
+    out = np.zeros((c, H, d))
+    lse = np.full((c, H), -np.inf)
+    for i in range(c):
+        visible = idx[idx <= n - c + i]
+        out[i], lse[i] = sparse_attention(q_chunk[i], k_pool, v_pool, page_row, visible, scale)
+    return {"idx": idx, "part": part, "out": out, "lse": lse, "vote": vote, "q_mean": q_mean}

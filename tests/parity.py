@@ -19,6 +19,21 @@ Tolerances (written here, used by every parity test):
 * cache decisions: equal, except when |cos - theta| <= COS_BAND, where the
   GPU's decision is replayed in the oracle. The GPU forms the cosine from
   fp32 partial sums of 4096 products (relative error ~1e-7).
+* tie-band margin: the set comparison above only means something if the GPU
+  decides every token outside the band like the oracle. Each set check
+  measures NEAR_ERR, the largest |v_gpu - v| / tau over the tokens whose
+  oracle vote lies within NEAR_WIN of tau (the tokens a rounding error could
+  move across the cut), and MARGIN, the smallest |v - tau| / tau over the
+  tokens outside the band. Tokens outside the band but within
+  MARGIN_FACTOR * NEAR_ERR of tau are "at risk": for each of them the check
+  compares the GPU's own decision (its vote against its own threshold vote)
+  with the oracle's and fails on any difference, and the number of at-risk
+  tokens is reported, so a pass never rests on an unexamined token. fp32
+  resolution bounds NEAR_ERR from below: near-threshold tokens of these
+  workloads take most of their vote from high-scale heads where the logit is
+  about 50, and an fp32 logit of 50 is resolved to about 2e-6, so a few
+  times 1e-6 relative is the floor of any fp32 pipeline there, above the
+  1e-6 band.
 * votes: |v_gpu - v| <= VOTE_REL * v elementwise. Each vote is a sum over
   heads of exp(l - L) with l an fp32 dot product of up to 128 bf16*bf16
   products (exact) accumulated in fp32 (16-term chains, then a tree) and
@@ -42,6 +57,8 @@ ATTN_REL = 2e-3
 LSE_ABS = 1e-3
 COS_BAND = 1e-6
 VOTE_REL = 1e-4
+NEAR_WIN = 1e-4
+MARGIN_FACTOR = 2.0
 
 
 def tsl():
@@ -169,23 +186,61 @@ def threshold_topk(vote, n, k, n_sink, n_local):
     return vote[order[k - 1]]
 
 
-def check_topk_set(gpu_idx, ref_idx, vote, n, k, n_sink, n_local, where=""):
+def band_margin(vote, gpu_vote, tau, n, where="", gpu_set=None, ref_set=None, lo=0, hi=None):
+    """(near_err, margin, at_risk) around the threshold vote tau. Every token of the selection
+    domain [lo, hi) outside the tie band and within MARGIN_FACTOR * near_err of tau must be in
+    the GPU's set exactly when it is in the oracle's."""
+    if gpu_vote is None or tau is None or not tau > 0:
+        return None
+    hi = n if hi is None else hi
+    v = vote[:n]
+    gv = gpu_vote[:n].astype(np.float64)
+    rel = np.abs(v - tau) / tau
+    near = rel <= NEAR_WIN
+    if not near.any():
+        near = rel <= np.sort(rel)[min(63, n - 1)]
+    near_err = float(np.max(np.abs(gv[near] - v[near])) / tau)
+    out = rel > TIE_REL
+    margin = float(rel[out].min()) if out.any() else math.inf
+    risk = np.nonzero(out & (rel <= MARGIN_FACTOR * near_err))[0]
+    risk = risk[(risk >= lo) & (risk < hi)]
+    if risk.size and gpu_set is not None and ref_set is not None:
+        wrong = [int(i) for i in risk if (int(i) in gpu_set) != (int(i) in ref_set)]
+        assert not wrong, (f"{where}: at-risk tokens decided against the oracle: {wrong[:5]} "
+                           f"(rel {[float(rel[i]) for i in wrong[:5]]}, near error {near_err:.2e})")
+    return near_err, margin, int(risk.size)
+
+
+@dataclass
+class SetCheck:
+    swaps: int
+    near_err: float = 0.0
+    margin: float = math.inf
+    at_risk: int = 0
+
+
+def check_topk_set(gpu_idx, ref_idx, vote, n, k, n_sink, n_local, where="", gpu_vote=None):
     g, o = set(map(int, gpu_idx)), set(map(int, ref_idx))
     assert len(gpu_idx) == len(g), f"{where}: duplicate indices"
     assert np.all(np.diff(gpu_idx) > 0), f"{where}: not ascending"
     assert len(g) == len(o), f"{where}: count {len(g)} vs oracle {len(o)}"
-    diff = g ^ o
-    if not diff:
-        return 0
     tau = threshold_topk(vote, n, k, n_sink, n_local)
+    bm = None
+    if tau is not None:
+        s_end, ls = O.budget_segments(n, n_sink, n_local)
+        bm = band_margin(vote, gpu_vote, tau, n, where, g, o, s_end, ls)
+    diff = g ^ o
+    res = SetCheck(len(diff), *(bm if bm else ()))
+    if not diff:
+        return res
     assert tau is not None, f"{where}: sets differ although every candidate is taken"
     bad = [i for i in diff if abs(vote[i] - tau) > TIE_REL * tau]
     assert not bad, f"{where}: {len(bad)} tokens differ outside the tie band, e.g. {bad[:5]} " \
                     f"(rel {[abs(vote[i] - tau) / tau for i in bad[:5]]})"
-    return len(diff)
+    return res
 
 
-def check_topp_set(gpu_idx, vote, n, p, H, n_sink, n_local, where=""):
+def check_topp_set(gpu_idx, vote, n, p, H, n_sink, n_local, where="", gpu_vote=None):
     g = set(map(int, gpu_idx))
     assert len(gpu_idx) == len(g) and np.all(np.diff(gpu_idx) > 0), f"{where}: not a strictly ascending set"
     order = np.argsort(-vote[:n], kind="stable")
@@ -195,6 +250,7 @@ def check_topp_set(gpu_idx, vote, n, p, H, n_sink, n_local, where=""):
     fixed = set(range(s_end)) | set(range(ls, n))
     if p >= 1.0:
         cuts = [n]
+        m_o = n
     else:
         m_o = min(n, int(np.searchsorted(cum, target, side="left")) + 1)
         cuts = {m_o}
@@ -209,7 +265,9 @@ def check_topp_set(gpu_idx, vote, n, p, H, n_sink, n_local, where=""):
         tau = vote[order[m - 1]]
         bad = [i for i in diff if abs(vote[i] - tau) > TIE_REL * tau]
         if not bad and len(g) == len(exp):
-            return len(diff)
+            # the matching cut's threshold: at-risk tokens around it are decided as the oracle does
+            bm = band_margin(vote, gpu_vote, tau, n, where, g, exp, s_end, ls) if m < n else None
+            return SetCheck(len(diff), *(bm if bm else ()))
         last_err = f"cut {m}: {len(diff)} differ, {len(bad)} outside the band"
     raise AssertionError(f"{where}: top-p set matches no admissible cut ({last_err}); |gpu|={len(g)}")
 
@@ -236,6 +294,15 @@ class TrajectoryReport:
     replays: int = 0
     band_swaps: int = 0
     worst_vote_rel: float = 0.0
+    near_err: float = 0.0          # largest GPU vote error near a threshold (relative to it)
+    margin: float = math.inf       # closest out-of-band token to a threshold (relative)
+    at_risk: int = 0               # out-of-band tokens within 2 x near_err, each checked
+
+    def add(self, sc):
+        self.band_swaps += sc.swaps
+        self.near_err = max(self.near_err, sc.near_err)
+        self.margin = min(self.margin, sc.margin)
+        self.at_risk += sc.at_risk
 
 
 def run_trajectory(wl, steps, layers=(0,), theta=None, mode=None, top_p=None, check_votes=True,
@@ -277,12 +344,12 @@ def run_trajectory(wl, steps, layers=(0,), theta=None, mode=None, top_p=None, ch
                         assert not bad, f"{where}: hit set differs outside the band: {bad[:5]}"
                         rep.band_swaps += len(diff)
                     else:
-                        rep.band_swaps += check_topk_set(g["idx"][b], r["idx"], r["vote"], n, ora.k, ora.n_sink,
-                                                         ora.n_local, where)
+                        rep.add(check_topk_set(g["idx"][b], r["idx"], r["vote"], n, ora.k, ora.n_sink,
+                                               ora.n_local, where, gpu_vote=g["vote"][b]))
                 else:
                     if not r["hit"]:
-                        rep.band_swaps += check_topp_set(g["idx"][b], r["vote"], n, ora.top_p, H, ora.n_sink,
-                                                         ora.n_local, where)
+                        rep.add(check_topp_set(g["idx"][b], r["vote"], n, ora.top_p, H, ora.n_sink,
+                                               ora.n_local, where, gpu_vote=g["vote"][b]))
                     else:
                         gi, oi = set(map(int, g["idx"][b])), set(map(int, r["idx"]))
                         if gi != oi:

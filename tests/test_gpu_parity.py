@@ -2,8 +2,10 @@
 
 Small sizes check every output of every step (several score CTAs, ragged last
 pages, several selection chunks); the full sizes of the 128K, batched and
-top-p workloads run the same comparison on fewer steps, and the 1M-token layer
-on one step.
+top-p workloads run the same comparison on fewer steps (both cache settings,
+both top-p masses), and the 1M-token workload at its stated shape of 8 layers
+with the cache off and at theta 0.9. Multi-layer cases check that every layer
+keeps its own Selection Cache entry.
 """
 import pytest
 import torch
@@ -15,11 +17,12 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-def _run(sp, steps, **kw):
-    wl = W.generate(sp, DEV)
+def _run(sp, steps, wl=None, **kw):
+    wl = wl if wl is not None else W.generate(sp, DEV)
     rep = run_trajectory(wl, steps, **kw)
     print(f"{sp.name}: steps={rep.steps} hits={rep.hits} replays={rep.replays} "
-          f"band_swaps={rep.band_swaps} worst_vote_rel={rep.worst_vote_rel:.2e}")
+          f"band_swaps={rep.band_swaps} worst_vote_rel={rep.worst_vote_rel:.2e} "
+          f"near_tau_err={rep.near_err:.2e} margin={rep.margin:.2e} at_risk={rep.at_risk}")
     return rep
 
 
@@ -66,6 +69,20 @@ def test_llama_batched_many_short_sequences():
     # a CTA range meets three or more sequences: the CUDA-core scan takes over
     sp = W.spec(1, n0=(300, 17, 2000, 45, 999, 5), n0_range=None, batch=6, steps=2, k=128, n_local=32)
     _run(sp, 2, theta=2.0)
+
+
+@pytest.mark.parametrize("multi", [False, True])
+def test_llama_three_layers_with_cache(multi):
+    # every layer keeps its own Selection Cache entry (C_Q, C_T, counts): layers > 0 read and
+    # write at their own offsets, on the persistent kernel and on the multi-kernel path
+    sp = W.spec(1, n0=(6007,), layers=3, steps=4, k=384, n_local=96)
+    rep = _run(sp, 4, layers=(0, 1, 2), multi_kernel=multi)
+    assert rep.steps == 4 * 3      # (step, layer) pairs
+
+
+def test_qwen_batched_layers_with_cache():
+    sp = W.spec(2, n0=(1800, 3333, 950), n0_range=None, batch=3, layers=2, steps=3, k=200, n_local=40)
+    _run(sp, 3, layers=(0, 1))
 
 
 def test_tiny_fp32_separate_calls_all_miss():
@@ -120,17 +137,28 @@ def test_llama_128k_full():
     _run(sp, 6)
 
 
-def test_qwen_batched_full():
-    sp = W.spec(2, steps=2)
-    _run(sp, 2, theta=2.0)
+@pytest.mark.parametrize("theta", [2.0, 0.9])
+def test_qwen_batched_full(theta):
+    sp = W.spec(2, steps=3)
+    _run(sp, 3 if theta <= 1.0 else 2, theta=theta)
 
 
-def test_topp_256k_full():
-    sp = W.spec(4, steps=2)
+@pytest.mark.parametrize("p", [0.9, 0.99])
+def test_topp_256k_full(p):
+    sp = W.spec(4, steps=2, top_p=p)
     _run(sp, 2)
 
 
-def test_llama_1m_one_layer_full():
-    sp = W.spec(3, layers=1, steps=1)
-    _run(sp, 1, theta=2.0)
+def test_llama_1m_8layers_full():
+    # the 1M-token workload at its stated shape: 8 layers of 1M tokens (4 GB of K+V each), every
+    # layer with its own Selection Cache entry; two steps with the cache off, then two with
+    # theta 0.9 on the same inputs
+    sp = W.spec(3, steps=2)
+    wl = W.generate(sp, DEV)
+    layers = tuple(range(sp.layers))
+    r0 = _run(sp, 2, wl=wl, layers=layers, theta=2.0)
+    assert r0.steps == 2 * sp.layers and r0.hits == 0      # (step, layer) pairs
+    r1 = _run(sp, 2, wl=wl, layers=layers, theta=0.9)
+    assert r1.steps == 2 * sp.layers
+    del wl
     torch.cuda.empty_cache()

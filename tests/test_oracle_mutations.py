@@ -35,6 +35,15 @@ MUTATIONS = {
                         "return as_f64(pool[pages, g, (tokens // P) % P, :])"),
     "cosine normalisation": ("return float(a @ b) / (na * nb)", "return float(a @ b) / (na * na)"),
     "bf16 widening shift": ("<< np.uint32(16)", "<< np.uint32(15)"),
+    "hard vote over all tokens": ("top = _order_desc(logits[h], cand)[:max(0, k)]",
+                                  "top = _order_desc(logits[h], np.arange(n))[:max(0, k)]"),
+    "hard vote takes k + 1": ("top = _order_desc(logits[h], cand)[:max(0, k)]",
+                              "top = _order_desc(logits[h], cand)[:max(0, k + 1)]"),
+    "prefill mean drops a query": ("q_mean = q_chunk.sum(axis=0) / c", "q_mean = q_chunk[1:].sum(axis=0) / c"),
+    "prefill not causal": ("visible = idx[idx <= n - c + i]", "visible = idx"),
+    "prefill causal off by one": ("visible = idx[idx <= n - c + i]", "visible = idx[idx < n - c + i]"),
+    "logit sum as max": ("return np.asarray(logits, dtype=np.float64).sum(axis=0)",
+                         "return np.asarray(logits, dtype=np.float64).max(axis=0)"),
 }
 
 

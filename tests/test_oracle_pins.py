@@ -452,3 +452,185 @@ def test_equal_keys_tie_exactly_and_go_to_lower_index():
     assert len(set(v[tied].tolist())) == 1
     _, part = O.select_topk(v, n, 3, 0, 0)
     assert list(part) == tied[:3]
+
+
+# ------------------------------------------- selection-function ablations (R10, R11)
+
+def test_ablation_selectors_golden():
+    g = GOLD["ablation_selectors"]
+    lg = np.array(g["logits"], dtype=np.float64)
+    n, k, s, w = g["n"], g["k"], g["n_sink"], g["n_local"]
+    c = O.hard_vote_counts(lg, n, k, s, w)
+    assert c.tolist() == g["hard_vote_counts"]
+    idx, _ = O.select_topk(c, n, k, s, w)
+    assert idx.tolist() == g["hard_vote_idx"]
+    ls = O.logit_sum_scores(lg)
+    assert ls.tolist() == g["logit_sum"]
+    idx, _ = O.select_topk(ls, n, k, s, w)
+    assert idx.tolist() == g["logit_sum_idx"]
+
+
+def _brute_topk(scores, cand, k):
+    """The k-subset of cand with the largest score sum; ties -> lexicographically smallest."""
+    best, best_key = None, None
+    for sub in itertools.combinations(cand, min(k, len(cand))):
+        key = (sum(scores[i] for i in sub), tuple(-i for i in sub))
+        if best_key is None or key > best_key:
+            best, best_key = sub, key
+    return sorted(best)
+
+
+def test_hard_vote_brute_force_with_ties():
+    rng = np.random.default_rng(7)
+    for trial in range(40):
+        H, n, k = 3, 11, int(rng.integers(1, 5))
+        lg = rng.integers(0, 4, size=(H, n)).astype(np.float64)     # many ties
+        s, w = 1, 2
+        cand = list(range(s, n - w))
+        counts = np.zeros(n)
+        for h in range(H):
+            for i in _brute_topk(lg[h], cand, k):
+                counts[i] += 1
+        assert np.array_equal(O.hard_vote_counts(lg, n, k, s, w), counts)
+        _, part = O.select_topk(counts, n, k, s, w)
+        assert list(part) == _brute_topk(counts, cand, k)
+
+
+def test_logit_sum_is_the_concatenated_dot_product():
+    # GQA 4/2: the concatenated query against each token's keys, each KV head repeated for its
+    # G query heads, is one flat dot product per token
+    rng = np.random.default_rng(3)
+    H, Hkv, d, n = 4, 2, 8, 37
+    G = H // Hkv
+    q = rng.normal(size=(H, d))
+    pool = rng.normal(size=(3, Hkv, 16, d))
+    pt = np.array([2, 0, 1], dtype=np.int32)
+    lg = O.head_logits(q, pool, pt, n)
+    flat = np.empty(n)
+    for i in range(n):
+        rows = pool[pt[i // 16], :, i % 16, :]                  # [Hkv][d]
+        kcat = np.repeat(rows, G, axis=0).reshape(-1)            # [H*d]
+        flat[i] = np.dot(q.reshape(-1), kcat) / math.sqrt(d)
+    assert np.allclose(O.logit_sum_scores(lg), flat, rtol=1e-12, atol=1e-12)
+
+
+def test_single_head_all_selection_functions_agree():
+    rng = np.random.default_rng(5)
+    n, k, s, w = 300, 17, 4, 20
+    lg = rng.normal(size=(1, n)) * 3.0
+    sets = [tuple(O.select_topk(O.selection_scores(lg, f, n, k, s, w), n, k, s, w)[0]) for f in O.SCORE_FNS]
+    assert sets[0] == sets[1] == sets[2]
+
+
+def test_logit_sum_is_dominated_by_the_high_norm_head_and_soft_vote_is_not():
+    # the pages' reason for the head soft vote: one head with logits a thousand times larger
+    # decides the plain TopK alone, while the soft vote weighs every head's softmax equally
+    rng = np.random.default_rng(9)
+    H, n, k, s, w = 4, 400, 10, 0, 0
+    lg = rng.normal(size=(H, n))
+    lg[2] *= 1000.0
+    part_sum = O.select_topk(O.logit_sum_scores(lg), n, k, s, w)[1]
+    part_h2 = O.select_topk(lg[2], n, k, s, w)[1]
+    assert list(part_sum) == list(part_h2)
+    part_soft = O.select_topk(O.soft_vote(lg), n, k, s, w)[1]
+    assert set(part_soft) != set(part_h2)
+
+
+def test_identical_heads_hard_vote_is_the_single_head_topk():
+    rng = np.random.default_rng(11)
+    n, k, s, w = 200, 12, 4, 16
+    row = rng.normal(size=n)
+    lg = np.stack([row] * 5)
+    c = O.hard_vote_counts(lg, n, k, s, w)
+    assert set(np.unique(c)) <= {0.0, 5.0}
+    assert list(O.select_topk(c, n, k, s, w)[1]) == list(O.select_topk(row, n, k, s, w)[1])
+
+
+def test_decode_step_with_ablation_scores():
+    wl = W.generate(W.spec(0, steps=1), "cpu")
+    kp, vp, pt = W.host_copy(wl.k_pool[0]), W.host_copy(wl.v_pool[0]), W.host_copy(wl.page_table)
+    q = W.host_copy(wl.q[0][0])[0]
+    n = wl.n0[0]
+    lg = O.head_logits(q, kp, pt[0], n)
+    for f in O.SCORE_FNS:
+        r = O.decode_step(O.CacheState(), q, kp, vp, pt[0], n, k=64, n_sink=4, n_local=16, theta=2.0, score_fn=f)
+        exp, _ = O.select_topk(O.selection_scores(lg, f, n, 64, 4, 16), n, 64, 4, 16)
+        assert np.array_equal(r["idx"], exp)
+    with pytest.raises(ValueError):
+        O.decode_step(O.CacheState(), q, kp, vp, pt[0], n, mode="topp", score_fn="hard_vote")
+
+
+# ------------------------------------------------------- chunk-wise prefill (R12)
+
+def _tiny_pools(rng, Hkv=2, d=8, pages=5):
+    kp = rng.normal(size=(pages, Hkv, 16, d))
+    vp = rng.normal(size=(pages, Hkv, 16, d))
+    pt = rng.permutation(pages).astype(np.int32)
+    return kp, vp, pt
+
+
+def test_prefill_chunk_of_one_is_a_decode_step():
+    rng = np.random.default_rng(21)
+    kp, vp, pt = _tiny_pools(rng)
+    n, H = 70, 4
+    q = rng.normal(size=(1, H, 8))
+    r = O.prefill_chunk(q, kp, vp, pt, n, k=9, n_sink=2, n_local=6)
+    d = O.decode_step(O.CacheState(), q[0], kp, vp, pt, n, k=9, n_sink=2, n_local=6, theta=2.0)
+    assert np.array_equal(r["idx"], d["idx"])
+    assert np.allclose(r["out"][0], d["out"], rtol=1e-12, atol=1e-12)
+    assert np.allclose(r["lse"][0], d["lse"], rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_dense_closed_form_is_causal_sdpa():
+    # k + s + w >= n: every token is selected, so each chunk query sees exactly the tokens up to
+    # its own position: the causal attention of the last c positions over the whole cache
+    rng = np.random.default_rng(22)
+    kp, vp, pt = _tiny_pools(rng)
+    n, c, H, Hkv, d = 53, 7, 4, 2, 8
+    G = H // Hkv
+    q = rng.normal(size=(c, H, d))
+    r = O.prefill_chunk(q, kp, vp, pt, n, k=200, n_sink=2, n_local=6)
+    assert np.array_equal(r["idx"], np.arange(n))
+    K = np.stack([kp[pt[i // 16], :, i % 16, :] for i in range(n)], axis=1)     # [Hkv][n][d]
+    V = np.stack([vp[pt[i // 16], :, i % 16, :] for i in range(n)], axis=1)
+    Kq = torch.tensor(np.repeat(K, G, axis=0))                                  # [H][n][d]
+    Vq = torch.tensor(np.repeat(V, G, axis=0))
+    Q = torch.tensor(q.transpose(1, 0, 2))                                      # [H][c][d]
+    pos = torch.arange(n - c, n).view(c, 1)
+    mask = torch.arange(n).view(1, n) <= pos                                    # [c][n]
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, Kq, Vq, attn_mask=mask).numpy()
+    assert np.allclose(r["out"], ref.transpose(1, 0, 2), rtol=1e-10, atol=1e-10)
+
+
+def test_prefill_selection_ignores_the_order_of_the_chunk():
+    rng = np.random.default_rng(23)
+    kp, vp, pt = _tiny_pools(rng)
+    n, c = 64, 6
+    q = rng.normal(size=(c, 4, 8))
+    a = O.prefill_chunk(q, kp, vp, pt, n, k=7, n_sink=2, n_local=5)
+    b = O.prefill_chunk(q[::-1].copy(), kp, vp, pt, n, k=7, n_sink=2, n_local=5)
+    assert np.array_equal(a["idx"], b["idx"])
+    assert np.allclose(a["q_mean"], q.mean(axis=0), rtol=1e-14, atol=1e-14)
+
+
+def test_prefill_selection_brute_force_on_the_mean_query():
+    rng = np.random.default_rng(24)
+    kp, vp, pt = _tiny_pools(rng, pages=1)
+    n, c, k, s, w = 14, 3, 4, 1, 2
+    q = rng.normal(size=(c, 4, 8))
+    r = O.prefill_chunk(q, kp, vp, pt, n, k=k, n_sink=s, n_local=w)
+    # the soft vote of the mean query, from scores computed without the oracle's helpers
+    qm = q.mean(axis=0)
+    alpha = 1 / math.sqrt(8)
+    v = np.zeros(n)
+    for h in range(4):
+        sc = np.array([alpha * float(qm[h] @ kp[pt[0], h // 2, i]) for i in range(n)])
+        e = np.exp(sc - sc.max())
+        v += e / e.sum()
+    best = _brute_topk(v, list(range(s, n - w)), k)
+    assert list(r["part"]) == best
+    # query i of the chunk sees no token after its own position
+    for i in range(c):
+        vis = r["idx"][r["idx"] <= n - c + i]
+        o, _ = O.sparse_attention(q[i], kp, vp, pt, vis)
+        assert np.allclose(r["out"][i], o, rtol=1e-13, atol=1e-13)

@@ -18,14 +18,18 @@ from ctypes import POINTER, c_char_p, c_double, c_float, c_int, c_int64, c_void_
 __all__ = [
     "TokenSelectError", "Config", "SelectParams", "library", "library_path",
     "TS_KV_F32", "TS_KV_BF16", "TS_SELECT_TOPK", "TS_SELECT_TOPP", "STATUS",
+    "TS_SCORE_HEAD_SOFT_VOTE", "TS_SCORE_LOGIT_SUM", "TS_SCORE_HEAD_HARD_VOTE", "ts_score_fn",
+    "ts_prefill_chunk",
     "ts_create", "ts_destroy", "ts_cache_create", "ts_cache_destroy", "ts_cache_reset",
     "ts_cache_check", "ts_score", "ts_select", "ts_sparse_attend", "ts_decode_step",
     "ts_get_status", "ts_status_str", "ts_version", "ts_profile_enable", "ts_profile_read",
-    "ts_kernel_count", "ts_debug_phase_ns", "ts_sparse_attend_noalloc", "Context", "Cache", "Profile", "PROF_FAMILIES",
+    "ts_kernel_count", "ts_debug_phase_ns", "ts_sparse_attend_noalloc", "ts_set_wait_limit",
+    "ts_inject_barrier_skip", "Context", "Cache", "Profile", "PROF_FAMILIES",
 ]
 
 TS_KV_F32, TS_KV_BF16 = 0, 1
 TS_SELECT_TOPK, TS_SELECT_TOPP = 0, 1
+TS_SCORE_HEAD_SOFT_VOTE, TS_SCORE_LOGIT_SUM, TS_SCORE_HEAD_HARD_VOTE = 0, 1, 2
 STATUS = {
     0: "TS_OK", 1: "TS_ERR_INVALID_ARG", 2: "TS_ERR_SHAPE", 3: "TS_ERR_UNSUPPORTED",
     4: "TS_ERR_CUDA", 5: "TS_ERR_PAGE_OOB", 6: "TS_ERR_CAPACITY", 7: "TS_ERR_TIMEOUT",
@@ -57,7 +61,7 @@ PROF_FAMILIES = ("check", "score", "vote", "select", "attend", "step")
 
 class SelectParams(ctypes.Structure):
     _fields_ = [("mode", c_int), ("k", c_int), ("n_sink", c_int), ("n_local", c_int),
-                ("top_p", c_float), ("theta", c_float), ("softmax_scale", c_float)]
+                ("top_p", c_float), ("theta", c_float), ("softmax_scale", c_float), ("score_fn", c_int)]
 
 
 _lib = None
@@ -73,6 +77,8 @@ _SIGS = {
                                c_void_p, c_void_p]),
     "ts_score": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p,
                          c_float, c_void_p, c_int64, c_void_p]),
+    "ts_score_fn": (c_int, [c_void_p, POINTER(SelectParams), c_void_p, c_void_p, c_void_p, c_void_p, c_int,
+                            c_void_p, c_void_p, c_int64, c_void_p]),
     "ts_select": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int64, c_void_p, c_int,
                           c_void_p, POINTER(SelectParams), c_void_p, c_int64, c_void_p, c_void_p]),
     "ts_sparse_attend": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -81,6 +87,11 @@ _SIGS = {
                                c_void_p, c_int, POINTER(SelectParams), c_void_p, c_int64, c_void_p,
                                c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "ts_get_status": (c_int, [c_void_p, POINTER(c_int), c_void_p]),
+    "ts_prefill_chunk": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
+                                 POINTER(SelectParams), c_void_p, c_int64, c_void_p, c_int64, c_void_p, c_void_p,
+                                 c_void_p, c_void_p]),
+    "ts_set_wait_limit": (c_int, [c_void_p, ctypes.c_uint64]),
+    "ts_inject_barrier_skip": (c_int, [c_void_p, c_int, c_int]),
     "ts_profile_enable": (c_int, [c_void_p, c_int]),
     "ts_profile_read": (c_int, [c_void_p, c_void_p, c_int]),
     "ts_kernel_count": (c_int, [c_void_p, POINTER(c_int64)]),
@@ -130,10 +141,11 @@ def _s(stream):
     return stream.cuda_stream
 
 
-def _params(mode=TS_SELECT_TOPK, k=2048, n_sink=4, n_local=512, top_p=0.9, theta=0.9, softmax_scale=0.0):
+def _params(mode=TS_SELECT_TOPK, k=2048, n_sink=4, n_local=512, top_p=0.9, theta=0.9, softmax_scale=0.0,
+            score_fn=TS_SCORE_HEAD_SOFT_VOTE):
     if isinstance(mode, SelectParams):
         return mode
-    return SelectParams(mode, k, n_sink, n_local, top_p, theta, softmax_scale)
+    return SelectParams(mode, k, n_sink, n_local, top_p, theta, softmax_scale, score_fn)
 
 
 # ---------------------------------------------------------------- raw calls
@@ -180,6 +192,11 @@ def ts_score(ctx, q, k_pool, page_table, seq_lens, B, skip, scale, vote, vote_st
                               _p(vote), vote_stride, _s(stream)), "ts_score")
 
 
+def ts_score_fn(ctx, params, q, k_pool, page_table, seq_lens, B, skip, vote, vote_stride, stream=None) -> None:
+    _check(library().ts_score_fn(ctx, ctypes.byref(params), _p(q), _p(k_pool), _p(page_table), _p(seq_lens), B,
+                                 _p(skip), _p(vote), vote_stride, _s(stream)), "ts_score_fn")
+
+
 def ts_select(ctx, cache, layer, q, vote, vote_stride, seq_lens, B, hit, params, idx, idx_stride, count,
               stream=None) -> None:
     _check(library().ts_select(ctx, cache, layer, _p(q), _p(vote), vote_stride, _p(seq_lens), B, _p(hit),
@@ -217,6 +234,21 @@ def ts_get_status(ctx, stream=None) -> int:
     return v.value
 
 
+def ts_prefill_chunk(ctx, q, c, k_pool, v_pool, page_table, seq_lens, B, params, vote, vote_stride, idx,
+                     idx_stride, count, out, lse=None, stream=None) -> None:
+    _check(library().ts_prefill_chunk(ctx, _p(q), c, _p(k_pool), _p(v_pool), _p(page_table), _p(seq_lens), B,
+                                      ctypes.byref(params), _p(vote), vote_stride, _p(idx), idx_stride, _p(count),
+                                      _p(out), _p(lse), _s(stream)), "ts_prefill_chunk")
+
+
+def ts_set_wait_limit(ctx, ns: int) -> None:
+    _check(library().ts_set_wait_limit(ctx, int(ns)), "ts_set_wait_limit")
+
+
+def ts_inject_barrier_skip(ctx, cta: int, barrier: int) -> None:
+    _check(library().ts_inject_barrier_skip(ctx, cta, barrier), "ts_inject_barrier_skip")
+
+
 def ts_profile_enable(ctx, on: bool) -> None:
     _check(library().ts_profile_enable(ctx, 1 if on else 0), "ts_profile_enable")
 
@@ -230,7 +262,7 @@ def ts_profile_read(ctx, keep: bool = False) -> dict:
 
 def ts_debug_phase_ns(ctx, stream=None) -> list:
     """Phase-boundary times (ns) of CTA 0 in the last persistent step kernel."""
-    buf = (ctypes.c_uint64 * 32)()
+    buf = (ctypes.c_uint64 * 64)()
     _check(library().ts_debug_phase_ns(ctx, buf, _s(stream)), "ts_debug_phase_ns")
     return list(buf)
 
@@ -271,6 +303,10 @@ class Context:
         ts_score(self.handle, q, k_pool, page_table, seq_lens, q.shape[0], skip, scale, vote,
                  vote.stride(0), stream)
 
+    def score_fn(self, params, q, k_pool, page_table, seq_lens, vote, skip=None, stream=None):
+        ts_score_fn(self.handle, params, q, k_pool, page_table, seq_lens, q.shape[0], skip, vote, vote.stride(0),
+                    stream)
+
     def select(self, vote, seq_lens, params, idx, count, cache=None, layer=0, q=None, hit=None, stream=None):
         ts_select(self.handle, cache.handle if cache else None, layer, q, vote, vote.stride(0), seq_lens,
                   seq_lens.shape[0], hit, params, idx, idx.stride(0), count, stream)
@@ -284,6 +320,12 @@ class Context:
         ts_decode_step(self.handle, cache.handle if cache else None, layer, q, k_pool, v_pool, page_table,
                        seq_lens, q.shape[0], params, vote, vote.stride(0) if vote is not None else 0, idx,
                        idx.stride(0), count, out, lse, hit, stream)
+
+    def prefill_chunk(self, q, k_pool, v_pool, page_table, seq_lens, params, idx, count, out, lse=None, vote=None,
+                      stream=None):
+        """q [B][c][H][d]: one selection from the chunk's mean query, causal attention of every query."""
+        ts_prefill_chunk(self.handle, q, q.shape[1], k_pool, v_pool, page_table, seq_lens, q.shape[0], params,
+                         vote, vote.stride(0) if vote is not None else 0, idx, idx.stride(0), count, out, lse, stream)
 
     def status(self, stream=None) -> int:
         return ts_get_status(self.handle, stream)

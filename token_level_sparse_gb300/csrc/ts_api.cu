@@ -37,6 +37,7 @@ void free_ctx_buffers(ts_ctx* c) {
   cudaFree(c->attn_part);
   cudaFree(c->vote);
   cudaFree(c->hit);
+  cudaFree(c->qmean);
   cudaFree(c->step_partials);
   cudaFree(c->step_hist);
   cudaFree(c->step_mass);
@@ -59,6 +60,11 @@ bool valid_params(const ts_select_params* p) {
   if (p->k < 0 || p->n_sink < 0 || p->n_local < 0) return false;
   if (p->mode == TS_SELECT_TOPP && !(p->top_p > 0.f)) return false;
   if (std::isnan(p->theta) || std::isnan(p->softmax_scale)) return false;
+  if (p->score_fn != TS_SCORE_HEAD_SOFT_VOTE && p->score_fn != TS_SCORE_LOGIT_SUM &&
+      p->score_fn != TS_SCORE_HEAD_HARD_VOTE)
+    return false;
+  // the ablation selection functions are ranked by top-k only (top-p's mass is the soft vote's)
+  if (p->score_fn != TS_SCORE_HEAD_SOFT_VOTE && p->mode != TS_SELECT_TOPK) return false;
   return true;
 }
 
@@ -102,8 +108,16 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   ts_ctx* ctx = new (std::nothrow) ts_ctx();
   if (!ctx) return TS_ERR_CUDA;
   ctx->cfg = c;
+  // environment switches, read here once (never per call):
   // TOKENSELECT_MULTI_KERNEL=1 keeps ts_decode_step on the multi-kernel path (tests, comparisons)
   if (const char* env = std::getenv("TOKENSELECT_MULTI_KERNEL")) ctx->use_step = !(env[0] == '1');
+  ctx->debug = std::getenv("TS_DEBUG") != nullptr;
+  if (const char* env = std::getenv("TOKENSELECT_NO_TC")) ctx->no_tc = env[0] == '1';
+  if (const char* env = std::getenv("TOKENSELECT_SCAN_CLAIM")) ctx->scan_claim = env[0] == '1';
+  if (const char* env = std::getenv("TOKENSELECT_L2_BUDGET_MB")) {
+    const long mb = std::strtol(env, nullptr, 10);
+    if (mb > 0) ctx->l2_budget = (int64_t)mb << 20;
+  }
   if (cudaGetDevice(&ctx->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess) {
     delete ctx;
@@ -136,7 +150,7 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   chk(alloc(&ctx->step_wpart, NS * B * kMaxScanWarps * kMaxScanG * 2));
   chk(alloc(&ctx->gsync, 4));
   if (e == cudaSuccess) chk(cudaMemset(ctx->gsync, 0, 4 * sizeof(unsigned)));   // then kept zero by each launch
-  chk(alloc(&ctx->phase_ns, 32));
+  chk(alloc(&ctx->phase_ns, 64));
   chk(alloc(&ctx->partials, B * ctx->score_max_chunks * H));
   chk(alloc(&ctx->stats, B * H));
   chk(alloc(&ctx->counters, B * kCounterSlots));
@@ -147,12 +161,13 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   chk(alloc(&ctx->attn_part, B * HKV * kAttnMaxSplits * G * (D + 2)));
   chk(alloc(&ctx->vote, B * T));
   chk(alloc(&ctx->hit, B));
+  chk(alloc(&ctx->qmean, B * H * D));
   if (e == cudaSuccess) chk(cudaMemset(ctx->status, 0, sizeof(int)));
   if (e == cudaSuccess) chk(cudaMemset(ctx->counters, 0, B * kCounterSlots * sizeof(unsigned)));
   if (e == cudaSuccess) chk(cudaMemset(ctx->hist, 0, B * 2048 * sizeof(unsigned)));
   if (e == cudaSuccess) chk(cudaMemset(ctx->mass_hist, 0, B * 2048 * sizeof(unsigned long long)));
   if (e == cudaSuccess) chk(cudaMemset(ctx->hit, 0, B));
-  if (e == cudaSuccess) chk(cudaMemset(ctx->phase_ns, 0, 32 * sizeof(unsigned long long)));
+  if (e == cudaSuccess) chk(cudaMemset(ctx->phase_ns, 0, 64 * sizeof(unsigned long long)));
   if (e == cudaSuccess) chk(cudaDeviceSynchronize());
   if (e != cudaSuccess) {
     free_ctx_buffers(ctx);
@@ -235,6 +250,22 @@ ts_status ts_score(ts_ctx* ctx, const float* q, const void* k_pool, const int32_
   return launch_score(ctx, c, as_stream(stream));
 }
 
+ts_status ts_score_fn(ts_ctx* ctx, const ts_select_params* params, const float* q, const void* k_pool,
+                      const int32_t* page_table, const int32_t* seq_lens, int B, const uint8_t* skip,
+                      float* vote, int64_t vote_stride, void* stream) {
+  if (!ctx || !q || !k_pool || !page_table || !seq_lens || !vote || !valid_params(params))
+    return TS_ERR_INVALID_ARG;
+  if (B < 1 || B > ctx->cfg.max_batch || vote_stride < ctx->max_tokens) return TS_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(k_pool) % 16 != 0) return TS_ERR_INVALID_ARG;
+  ScoreCall c{q, k_pool, page_table, seq_lens, skip, B, resolve_scale(ctx, params->softmax_scale), vote,
+              vote_stride};
+  c.fn = params->score_fn;
+  c.k = params->k;
+  c.n_sink = params->n_sink;
+  c.n_local = params->n_local;
+  return launch_score(ctx, c, as_stream(stream));
+}
+
 ts_status ts_select(ts_ctx* ctx, ts_cache* cache, int layer, const float* q, const float* vote,
                     int64_t vote_stride, const int32_t* seq_lens, int B, const uint8_t* hit,
                     const ts_select_params* params, int32_t* idx, int64_t idx_stride, int32_t* count,
@@ -284,7 +315,7 @@ ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q
   const bool use_cache = cache != nullptr && params->theta <= 1.f;
   uint8_t* hbuf = hit ? hit : ctx->hit;
   ts_status st = TS_OK;
-  if (ctx->use_step && step_supported(ctx->cfg) && B <= 64) {
+  if (ctx->use_step && step_supported(ctx->cfg) && B <= 64 && params->score_fn == TS_SCORE_HEAD_SOFT_VOTE) {
     // one persistent cooperative kernel for the whole step
     if (!use_cache && hit && cudaMemsetAsync(hit, 0, B, s) != cudaSuccess) return TS_ERR_CUDA;
     StepCall sc{};
@@ -310,7 +341,7 @@ ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q
     sc.out = out;
     sc.lse = lse;
     st = launch_step(ctx, sc, s);
-    if (std::getenv("TS_DEBUG")) std::fprintf(stderr, "ts decode step: persistent kernel -> %s\n", ts_status_str(st));
+    if (ctx->debug) std::fprintf(stderr, "ts decode step: persistent kernel -> %s\n", ts_status_str(st));
     if (st != TS_ERR_COOP_UNAVAILABLE) return st;
     ctx->use_step = false;  // the multi-kernel path below from now on
   }
@@ -322,6 +353,10 @@ ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q
   }
   const uint8_t* skip = use_cache ? hbuf : nullptr;
   ScoreCall sc{q, k_pool, page_table, seq_lens, skip, B, scale, vote, vote_stride};
+  sc.fn = params->score_fn;
+  sc.k = params->k;
+  sc.n_sink = params->n_sink;
+  sc.n_local = params->n_local;
   st = launch_score(ctx, sc, s);
   if (st != TS_OK) return st;
   SelectCall sel{cache, layer, q, vote, vote_stride, seq_lens, B, skip, *params, idx, idx_stride, count};
@@ -331,12 +366,70 @@ ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q
   return launch_attend(ctx, ac, s);
 }
 
-ts_status ts_debug_phase_ns(ts_ctx* ctx, uint64_t* out32, void* stream) {
-  if (!ctx || !out32) return TS_ERR_INVALID_ARG;
+ts_status ts_prefill_chunk(ts_ctx* ctx, const float* q, int c, const void* k_pool, const void* v_pool,
+                           const int32_t* page_table, const int32_t* seq_lens, int B, const ts_select_params* params,
+                           float* vote, int64_t vote_stride, int32_t* idx, int64_t idx_stride, int32_t* count,
+                           float* out, float* lse, void* stream) {
+  if (!ctx || !q || !k_pool || !v_pool || !page_table || !seq_lens || !idx || !count || !out ||
+      !valid_params(params))
+    return TS_ERR_INVALID_ARG;
+  if (params->mode != TS_SELECT_TOPK || params->score_fn != TS_SCORE_HEAD_SOFT_VOTE) return TS_ERR_INVALID_ARG;
+  if (c < 1 || B < 1 || B > ctx->cfg.max_batch || idx_stride < 1) return TS_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(k_pool) % 16 != 0 || reinterpret_cast<uintptr_t>(v_pool) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(q) % 16 != 0)
+    return TS_ERR_INVALID_ARG;
+  if (!chunk_attend_supported(ctx->cfg)) return TS_ERR_UNSUPPORTED;
+  if (!vote) {
+    vote = ctx->vote;
+    vote_stride = ctx->max_tokens;
+  }
+  if (vote_stride < ctx->max_tokens) return TS_ERR_SHAPE;
+  cudaStream_t s = as_stream(stream);
+  const float scale = resolve_scale(ctx, params->softmax_scale);
+  // (1) the mean query of every chunk
+  ts_status st = launch_chunk_mean(ctx, q, c, B, ctx->qmean, s);
+  if (st != TS_OK) return st;
+  // (2) one selection from it: score, vote and top-k (the persistent kernel without its attention)
+  st = TS_ERR_COOP_UNAVAILABLE;
+  if (ctx->use_step && step_supported(ctx->cfg) && B <= 64) {
+    StepCall sc{};
+    sc.phases = kPhaseScore | kPhaseSelect;
+    sc.B = B;
+    sc.q = ctx->qmean;
+    sc.k_pool = k_pool;
+    sc.v_pool = v_pool;
+    sc.page_table = page_table;
+    sc.seq_lens = seq_lens;
+    sc.scale = scale;
+    sc.theta = 2.f;
+    sc.params = *params;
+    sc.vote = vote;
+    sc.vote_stride = vote_stride;
+    sc.idx = idx;
+    sc.idx_stride = idx_stride;
+    sc.count = count;
+    st = launch_step(ctx, sc, s);
+    if (st != TS_OK && st != TS_ERR_COOP_UNAVAILABLE) return st;
+  }
+  if (st != TS_OK) {
+    ScoreCall scc{ctx->qmean, k_pool, page_table, seq_lens, nullptr, B, scale, vote, vote_stride};
+    st = launch_score(ctx, scc, s);
+    if (st != TS_OK) return st;
+    SelectCall sel{nullptr, 0, ctx->qmean, vote, vote_stride, seq_lens, B, nullptr, *params, idx, idx_stride, count};
+    st = launch_select(ctx, sel, s);
+    if (st != TS_OK) return st;
+  }
+  // (3) the chunk's queries attend causally to the shared selection, on the tensor cores
+  ChunkAttendCall ac{q, c, k_pool, v_pool, page_table, seq_lens, idx, idx_stride, count, B, scale, out, lse};
+  return launch_chunk_attend(ctx, ac, s);
+}
+
+ts_status ts_debug_phase_ns(ts_ctx* ctx, uint64_t* out64, void* stream) {
+  if (!ctx || !out64) return TS_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return TS_ERR_CUDA;
-  if (cudaMemcpy(out32, ctx->phase_ns, 32 * sizeof(uint64_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpy(out64, ctx->phase_ns, 64 * sizeof(uint64_t), cudaMemcpyDeviceToHost) != cudaSuccess)
     return TS_ERR_CUDA;
-  return cudaMemset(ctx->phase_ns, 0, 32 * sizeof(uint64_t)) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
+  return cudaMemset(ctx->phase_ns, 0, 64 * sizeof(uint64_t)) == cudaSuccess ? TS_OK : TS_ERR_CUDA;
 }
 
 ts_status ts_kernel_count(ts_ctx* ctx, int64_t* out) {
@@ -369,6 +462,19 @@ ts_status ts_profile_read(ts_ctx* ctx, ts_profile* out, int keep) {
     out->launches[b.family] += 1;
   }
   if (!keep) ctx->prof_used = 0;
+  return TS_OK;
+}
+
+ts_status ts_set_wait_limit(ts_ctx* ctx, uint64_t ns) {
+  if (!ctx || ns == 0) return TS_ERR_INVALID_ARG;
+  ctx->wait_ns = ns;
+  return TS_OK;
+}
+
+ts_status ts_inject_barrier_skip(ts_ctx* ctx, int cta, int barrier) {
+  if (!ctx || cta < 0 || barrier < 0) return TS_ERR_INVALID_ARG;
+  ctx->inject_skip_cta = cta;
+  ctx->inject_skip_barrier = barrier;
   return TS_OK;
 }
 

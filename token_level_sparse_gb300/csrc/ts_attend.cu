@@ -297,6 +297,7 @@ ts_status launch_attend(ts_ctx* ctx, const AttendCall& a, cudaStream_t s) {
 // counters (kCounterSlots per sequence) and a fallback status slot,
 // [16 KiB, end) split partials.
 
+#include <cmath>
 #include <mutex>
 
 namespace ts {
@@ -372,6 +373,7 @@ extern "C" ts_status ts_sparse_attend_noalloc(int n_q_heads, int n_kv_heads, int
       max_pages_per_seq < 1 || idx_stride < 1 || B < 1)
     return TS_ERR_INVALID_ARG;
   if (kv_dtype != TS_KV_F32 && kv_dtype != TS_KV_BF16) return TS_ERR_INVALID_ARG;
+  if (std::isnan(scale)) return TS_ERR_INVALID_ARG;   // the same argument check as ts_sparse_attend
   if (reinterpret_cast<uintptr_t>(k_pool) % 16 != 0 || reinterpret_cast<uintptr_t>(v_pool) % 16 != 0)
     return TS_ERR_INVALID_ARG;
   if (B > kNoAllocMaxBatch || n_kv_heads > kCounterSlots - 2) return TS_ERR_SCRATCH_LIMIT;

@@ -15,7 +15,8 @@
 namespace ts {
 
 constexpr unsigned kFull = 0xffffffffu;
-// Upper bound on any single wait inside a kernel (nanoseconds).
+// Default upper bound on any single wait inside a kernel (nanoseconds); the persistent
+// decode-step kernel takes its bound from the context (ts_set_wait_limit).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
 __device__ __forceinline__ void set_error(int* status, int code) {
@@ -71,12 +72,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete; false after the limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Waits for the phase with the given parity to complete; false once limit_ns have passed.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
   return true;
 }
@@ -89,6 +90,23 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
           smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
+}
+
+// 16 bytes global -> shared without passing through registers (cp.async, cached in L2
+// only). For gathers of many short rows: every thread keeps several in flight, where one
+// bulk copy per row would queue the rows one after another in the copy engine. Completed by
+// cp_async_commit + cp_async_wait_all (an ordinary memory access, like a load).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Order-preserving unsigned key of a float (both signs): larger values give larger keys;
+// -0 and +0 map to the key of +0, so they tie as the values do.
+__device__ __forceinline__ uint32_t ordered_key(float v) {
+  const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
+  return u ^ ((u >> 31) ? 0xffffffffu : 0x80000000u);
 }
 
 // An L2 policy that evicts first: for data streamed once (the K scan) so it does

@@ -2,6 +2,7 @@
 // kernel file exports to the C ABI layer.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -63,6 +64,7 @@ struct ts_ctx {
   float* attn_part = nullptr;            // [max_batch][H_kv][attn_splits][G*(D+2)]
   float* vote = nullptr;                 // [max_batch][max_tokens] (decode step)
   uint8_t* hit = nullptr;                // [max_batch] (decode step)
+  float* qmean = nullptr;                // [max_batch][H][d] mean query of a prefill chunk
   int64_t kernels = 0;           // kernel launches issued
   // persistent decode-step kernel
   int step_grid = 0;                     // CTAs of the cooperative launch (0: not yet sized)
@@ -82,8 +84,16 @@ struct ts_ctx {
   int kmap_next = 0;
   float* step_wpart = nullptr;           // per SM: CUDA-core scan (max, sum exp) pairs, see the persistent kernel
   unsigned* gsync = nullptr;             // grid barrier state (4 words)
-  unsigned long long* phase_ns = nullptr;  // [32] phase boundary times of the last step kernel
+  unsigned long long* phase_ns = nullptr;  // [64] phase boundary times of the last step kernel
   bool use_step = true;                  // the persistent kernel is available
+  // settings read once at ts_create (environment) or set through the C ABI
+  bool debug = false;                    // TS_DEBUG: launch diagnostics on stderr
+  bool no_tc = false;                    // TOKENSELECT_NO_TC=1: CUDA-core scan only
+  bool scan_claim = false;               // TOKENSELECT_SCAN_CLAIM=1: scan pages claimed from a counter
+  int64_t l2_budget = 0;                 // TOKENSELECT_L2_BUDGET_MB: logits one scan wave keeps in L2 (0: default)
+  uint64_t wait_ns = 1000000000ull;      // bound on every wait of the persistent kernel (ts_set_wait_limit)
+  int inject_skip_cta = -1;              // ts_inject_barrier_skip: one launch, CTA leaves at a barrier
+  int inject_skip_barrier = -1;
   // kernel timing
   bool prof_on = false;
   int prof_used = 0;
@@ -118,6 +128,8 @@ struct ScoreCall {
   float scale;
   float* vote;
   int64_t vote_stride;
+  int fn = TS_SCORE_HEAD_SOFT_VOTE;   // selection function (TS_SCORE_*)
+  int k = 0, n_sink = 0, n_local = 0; // the hard vote's per-head top-k
 };
 
 struct SelectCall {
@@ -174,6 +186,22 @@ struct StepCall {
 };
 constexpr int kPhaseCheck = 1, kPhaseScore = 2, kPhaseSelect = 4, kPhaseAttend = 8;
 
+struct ChunkAttendCall {   // causal attention of a prefill chunk's c queries over one index set
+  const float* q;          // [B][c][H][d]
+  int c;
+  const void* k_pool;
+  const void* v_pool;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const int32_t* idx;
+  int64_t idx_stride;
+  const int32_t* count;
+  int B;
+  float scale;
+  float* out;              // [B][c][H][d]
+  float* lse;              // [B][c][H] or null
+};
+
 // Head geometries with a compiled kernel: (kv type flag, element type, d, H_kv, G).
 #define TS_STEP_GEOMETRIES(X)             \
   X(TS_KV_F32, float, 64, 4, 1)           \
@@ -191,6 +219,9 @@ bool score_supported(const ts_config& c);
 ts_status launch_score(ts_ctx* ctx, const ScoreCall& a, cudaStream_t s);
 ts_status launch_select(ts_ctx* ctx, const SelectCall& a, cudaStream_t s);
 ts_status launch_attend(ts_ctx* ctx, const AttendCall& a, cudaStream_t s);
+bool chunk_attend_supported(const ts_config& c);
+ts_status launch_chunk_mean(ts_ctx* ctx, const float* q, int c, int B, float* qm, cudaStream_t s);
+ts_status launch_chunk_attend(ts_ctx* ctx, const ChunkAttendCall& c, cudaStream_t s);
 ts_status launch_cache_check(ts_ctx* ctx, ts_cache* cache, int layer, const float* q, int B,
                              float theta, uint8_t* hit, float* cos_out, cudaStream_t s);
 ts_status launch_cache_reset(ts_cache* cache, cudaStream_t s);
@@ -200,14 +231,16 @@ inline ts_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TS_OK : 
 // Raises one kernel's dynamic shared-memory limit once per device (so no
 // attribute call happens inside a stream capture after the first launch on
 // that device). Templated on the kernel itself: one flag set per kernel.
+// The flag word is atomic: callers on several host threads may race here (the attribute
+// call itself is idempotent).
 template <auto Kernel>
 inline bool ensure_smem(size_t bytes, int device) {
-  static unsigned long long done = 0ull;  // one bit per device
+  static std::atomic<unsigned long long> done{0ull};  // one bit per device
   const unsigned long long bit = 1ull << (device & 63);
-  if (done & bit) return true;
+  if (done.load(std::memory_order_acquire) & bit) return true;
   if (cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) != cudaSuccess)
     return false;
-  done |= bit;
+  done.fetch_or(bit, std::memory_order_acq_rel);
   return true;
 }
 

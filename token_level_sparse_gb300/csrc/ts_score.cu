@@ -252,6 +252,7 @@ struct VoteKArgs {
   const float2* stats;
   float* vote;
   int64_t vote_stride;
+  int fn;              // TS_SCORE_*: soft vote, logit sum, or zeros for the hard vote's counts
 };
 
 constexpr int kVoteThreads = 256;
@@ -279,8 +280,117 @@ __global__ void __launch_bounds__(kVoteThreads) score_vote_kernel(VoteKArgs a) {
     const int t = t0 + i * kVoteThreads + threadIdx.x;
     if (t >= n) break;
     KahanF acc;
-    for (int h = 0; h < a.H; ++h) acc.add(expf(lb[(size_t)h * a.max_tokens + t] - sM[h]) * sIZ[h]);
+    if (a.fn == TS_SCORE_HEAD_SOFT_VOTE) {
+      for (int h = 0; h < a.H; ++h) acc.add(expf(lb[(size_t)h * a.max_tokens + t] - sM[h]) * sIZ[h]);
+    } else if (a.fn == TS_SCORE_LOGIT_SUM) {
+      // plain TopK(Q.K^T) over the concatenated heads: the sum of the per-head logits
+      for (int h = 0; h < a.H; ++h) acc.add(lb[(size_t)h * a.max_tokens + t]);
+    }   // the hard vote's counts start from zero and are added by hard_vote_kernel
     a.vote[(size_t)b * a.vote_stride + t] = acc.s - acc.c;
+  }
+}
+
+struct HardVoteKArgs {
+  const int32_t* seq_lens;
+  const uint8_t* skip;
+  int H;
+  const float* logits;
+  int max_tokens;
+  int k, n_sink, n_local;
+  float* vote;
+  int64_t vote_stride;
+};
+
+constexpr int kHardThreads = 1024;
+
+// Head hard vote (TokenSelect deep notes, "Evolution of the selection function":
+// TopK(sum_h I(i in TopK(Q^h K^h^T)))): CTA (h, b) finds query head h's own top-k over
+// the candidates [s_end, ls) of sequence b and adds one vote to each of its tokens.
+// The k-th logit is found by a radix select over the order-preserving 32-bit keys,
+// 8 bits per pass from the top (shared-memory histograms); tokens above it are taken,
+// and tokens equal to it in index order until k are taken. Votes are added as 1.0f:
+// sums of small integers are exact in fp32, so the order of the adds does not matter.
+__global__ void __launch_bounds__(kHardThreads) hard_vote_kernel(HardVoteKArgs a) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  if (a.skip && a.skip[b]) return;
+  const int n = a.seq_lens[b];
+  if (n < 0 || n > a.max_tokens) return;
+  int s_end, ls;
+  budget_segments(n, a.n_sink, a.n_local, s_end, ls);
+  const int lo = s_end, hi = ls, len = hi - lo;
+  if (a.k <= 0 || len <= 0) return;
+  float* vb = a.vote + (size_t)b * a.vote_stride;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (len <= a.k) {
+    for (int i = lo + tid; i < hi; i += blockDim.x) atomicAdd(&vb[i], 1.f);
+    return;
+  }
+  const float* row = a.logits + ((size_t)b * a.H + h) * a.max_tokens;
+  __shared__ unsigned hist[256];
+  __shared__ unsigned s_prefix, s_krem;
+  __shared__ int wcnt[32];
+  uint32_t prefix = 0u, mask = 0u;
+  unsigned krem = (unsigned)a.k;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0u;
+    __syncthreads();
+    for (int i = lo + tid; i < hi; i += blockDim.x) {
+      const uint32_t key = ordered_key(row[i]);
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // bins from the top: lane L sums bins 255 - 8L .. 248 - 8L, then a prefix over lanes
+      unsigned c = 0;
+      for (int j = 0; j < 8; ++j) c += hist[255 - 8 * lane - j];
+      unsigned inc = c;
+      for (int d = 1; d < 32; d <<= 1) {
+        const unsigned o = __shfl_up_sync(kFull, inc, d);
+        if (lane >= d) inc += o;
+      }
+      const unsigned ballot = __ballot_sync(kFull, inc - c < krem && inc >= krem);
+      const int L = __ffs(ballot) - 1;   // the domain holds more than k tokens: some lane crosses
+      if (ballot == 0u && lane == 0) {   // (unreachable) keep the state well defined
+        s_prefix = prefix;
+        s_krem = krem;
+      }
+      if (lane == L) {
+        unsigned before = inc - c;
+        for (int j = 0; j < 8; ++j) {
+          const int bin = 255 - 8 * L - j;
+          if (before + hist[bin] >= krem) {
+            s_prefix = prefix | ((uint32_t)bin << shift);
+            s_krem = krem - before;
+            break;
+          }
+          before += hist[bin];
+        }
+      }
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    krem = s_krem;
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+  // prefix is the k-th key; krem tokens equal to it are taken, lowest index first
+  unsigned taken = 0;
+  for (int base = lo; base < hi; base += blockDim.x) {
+    const int i = base + tid;
+    const uint32_t key = i < hi ? ordered_key(row[i]) : 0u;
+    const bool gt = i < hi && key > prefix, eq = i < hi && key == prefix;
+    const unsigned bal = __ballot_sync(kFull, eq);
+    if (lane == 0) wcnt[warp] = __popc(bal);
+    __syncthreads();
+    unsigned before = taken;
+    for (int w = 0; w < warp; ++w) before += wcnt[w];
+    unsigned tot = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += wcnt[w];
+    const unsigned rank = before + __popc(bal & ((1u << lane) - 1u));
+    if (gt || (eq && rank < krem)) atomicAdd(&vb[i], 1.f);
+    taken += tot;
+    __syncthreads();
   }
 }
 
@@ -314,10 +424,16 @@ ts_status run_score(ts_ctx* ctx, const ScoreCall& c, cudaStream_t s) {
     kern<<<dim3(ctx->score_max_chunks, c.B), S::THREADS, smem, s>>>(a);
   }
   ctx->kernels += 2;
-  VoteKArgs v{c.seq_lens, c.skip, H, ctx->logits, ctx->max_tokens, ctx->stats, c.vote, c.vote_stride};
+  VoteKArgs v{c.seq_lens, c.skip, H, ctx->logits, ctx->max_tokens, ctx->stats, c.vote, c.vote_stride, c.fn};
   {
     ProfScope ps(ctx, TS_PROF_VOTE, s);
     score_vote_kernel<<<dim3((ctx->max_tokens + kVoteTile - 1) / kVoteTile, c.B), kVoteThreads, 0, s>>>(v);
+    if (c.fn == TS_SCORE_HEAD_HARD_VOTE) {
+      HardVoteKArgs hv{c.seq_lens, c.skip, H, ctx->logits, ctx->max_tokens, c.k, c.n_sink, c.n_local,
+                       c.vote, c.vote_stride};
+      hard_vote_kernel<<<dim3(H, c.B), kHardThreads, 0, s>>>(hv);
+      ctx->kernels += 1;
+    }
   }
   return cuda_status(cudaGetLastError());
 }

@@ -49,7 +49,14 @@ struct SelKArgs {
   const float* q;
   int HD;
   int* status;
+  int signed_keys;     // scores of either sign (the logit-sum selection function): ordered keys
 };
+
+// The radix key of a score: its bit pattern for non-negative votes (the order of the values),
+// the order-preserving key of either sign otherwise.
+__device__ __forceinline__ uint32_t sel_key(float v, int signed_keys) {
+  return signed_keys ? ordered_key(v) : __float_as_uint(v);
+}
 
 // Length of sequence b, or -1 (recorded as an error) when out of range.
 __device__ __forceinline__ int seq_len(const SelKArgs& a, int b) {
@@ -157,7 +164,7 @@ __global__ void __launch_bounds__(kSelThreads) sel_pass_kernel(SelKArgs a, int p
   const int c0 = lo + blockIdx.x * kSelChunk, c1 = min(hi, c0 + kSelChunk);
   for (int t = c0 + tid; t < c1; t += kSelThreads) {
     const float v = vb[t];
-    const uint32_t key = __float_as_uint(v);
+    const uint32_t key = sel_key(v, a.signed_keys);
     if ((key & st.mask) == st.prefix) {
       const int bin = (key >> shift) & (nbins - 1);
       atomicAdd(&sh[bin], 1u);
@@ -266,7 +273,7 @@ __global__ void __launch_bounds__(kSelThreads) sel_count_kernel(SelKArgs a) {
   int gt_all = 0, eq_all = 0, gt_cand = 0, eq_cand = 0, eq_pre = 0;
   const float* vb = a.vote + (size_t)b * a.vote_stride;
   for (int t = c0 + threadIdx.x; t < c1; t += kSelThreads) {
-    const uint32_t key = __float_as_uint(vb[t]);
+    const uint32_t key = sel_key(vb[t], a.signed_keys);
     const bool gt = st.all || key > st.prefix;
     const bool eq = !st.all && key == st.prefix;
     const bool cand = t >= s_end && t < ls;
@@ -390,7 +397,7 @@ __global__ void __launch_bounds__(kSelThreads) sel_write_kernel(SelKArgs a) {
 #pragma unroll
   for (int i = 0; i < kSelPerThread; ++i) {
     const int t = t0 + i;
-    keys[i] = t < c1 ? __float_as_uint(vb[t]) : 0u;
+    keys[i] = t < c1 ? sel_key(vb[t], a.signed_keys) : 0u;
     n_eq += (t < c1 && !st.all && keys[i] == st.prefix);
   }
   int dummy;
@@ -500,6 +507,7 @@ ts_status launch_select(ts_ctx* ctx, const SelectCall& c, cudaStream_t s) {
   a.HD = cfg.n_q_heads * cfg.head_dim;
   a.q = c.q;
   a.status = ctx->status;
+  a.signed_keys = c.params.score_fn == TS_SCORE_LOGIT_SUM ? 1 : 0;
   if (c.cache) {
     const size_t mb = (size_t)cfg.max_batch;
     a.cq = c.cache->cq + (size_t)c.layer * mb * a.HD;

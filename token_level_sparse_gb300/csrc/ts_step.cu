@@ -171,6 +171,7 @@ struct StepKArgs {
   const int32_t* seq_lens;
   float scale;
   float scale_l2;              // scale x log2(e): the scan keeps its logits in base-2 units (exp2)
+  float scale_l2_lo;           // scale x log2(e) - scale_l2 (the constant to about 2^-48 relative)
   float theta;
   const uint8_t* hit_in;
   uint8_t* hit_out;
@@ -206,6 +207,8 @@ struct StepKArgs {
   int64_t l2_budget;           // bytes of logits one scan wave may keep in L2
   GridSync* gsync;
   int* status;
+  uint64_t wait_ns;            // bound on every wait of the launch
+  int skip_cta, skip_barrier;  // injected fault: CTA skip_cta leaves at its barrier skip_barrier (-1: none)
   unsigned long long* phase_ns;  // CTA 0's %globaltimer at phase boundaries (debug)
   int dyn_bytes;               // dynamic shared memory of the launch
   int nslot;                   // ring slots of STAGE_BYTES each
@@ -226,33 +229,41 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 // (zeroed before each launch): barrier e of the launch is passed once it
 // reaches (e + 1) x grid size, so the last CTA to arrive releases the others
 // with its own increment. *epoch (shared memory, thread 0 only) counts this
-// CTA's barriers. False after a time-out or an abort raised by another CTA;
-// the caller then returns.
-__device__ __noinline__ bool grid_sync(GridSync* gs, int* status, unsigned* epoch) {
+// CTA's barriers. Every wait is bounded by limit_ns. False after a time-out or
+// an abort raised by another CTA; the caller then returns. A host-injected
+// fault (skip_cta, skip_barrier >= 0, one launch only) makes CTA skip_cta leave
+// at its barrier skip_barrier without arriving, so that the others' bounded
+// wait runs out: the time-out path can be tested without hanging anything.
+__device__ __noinline__ bool grid_sync(GridSync* gs, int* status, unsigned* epoch, uint64_t limit_ns,
+                                       int skip_cta, int skip_barrier) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
     const unsigned target = (*epoch + 1u) * gridDim.x;
-    *epoch += 1u;
-    fence_acq_rel_gpu();                      // the CTA's writes (ordered by the CTA barrier) first
-    if (atomicAdd(&gs->count, 1u) + 1u < target) {
-      const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire(&gs->count) < target) {
-        if (ld_acquire(&gs->abort)) {
-          ok = 0;
-          break;
+    if ((int)blockIdx.x == skip_cta && (int)*epoch == skip_barrier) {
+      ok = 0;
+    } else {
+      *epoch += 1u;
+      fence_acq_rel_gpu();                      // the CTA's writes (ordered by the CTA barrier) first
+      if (atomicAdd(&gs->count, 1u) + 1u < target) {
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire(&gs->count) < target) {
+          if (ld_acquire(&gs->abort)) {
+            ok = 0;
+            break;
+          }
+          if (globaltimer_ns() - t0 > limit_ns) {
+            set_error(status, TS_ERR_TIMEOUT);
+            atomicExch(&gs->abort, 1u);
+            ok = 0;
+            break;
+          }
+          __nanosleep(32);
         }
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          set_error(status, TS_ERR_TIMEOUT);
-          atomicExch(&gs->abort, 1u);
-          ok = 0;
-          break;
-        }
-        __nanosleep(32);
       }
+      fence_acq_rel_gpu();                      // then everything the others wrote before arriving
     }
-    fence_acq_rel_gpu();                      // then everything the others wrote before arriving
     s_ok = ok;
   }
   __syncthreads();
@@ -468,13 +479,17 @@ struct Smem {
 
 // --------------------------------------------------------------- the kernel
 
-// CTA 0 records the time it reaches phase boundary i (0..31), for diagnosis: 0 start, 5 lengths
+// CTA 0 records the time it reaches phase boundary i (0..63), for diagnosis: 0 start, 5 lengths
 // read, 6 cache test, 7 partition, 1 set-up done; scan wave w: 2 + 3 w scanned, 3 + 3 w
 // statistics, 4 + 3 w barrier passed; 13 / 14 vote partials / normalisers, 20 votes done;
 // 28 + l histogram level l built, 21 levels, 22 candidates, 23 flags; 10 last gather landed,
 // 9 last round list built, 11 attended, 24 partials written, 25 last barrier, 26 merged, 27
-// end. (The marks of waves past the first share slots 5..19 with the others; slots 17 and 18
-// also take the latest start and end over all CTAs.)
+// end. Finer points: 32 vote chunk landed; 33 + 4 l / 34 + 4 l / 35 + 4 l / 36 + 4 l level l
+// histogram started / zeroed / counted (added: 28 + l) / barrier passed; 45 / 46 coarse / fine bins
+// fetched; 47 classified, 48 candidate barrier passed, 49 candidates fetched, 50 ranked; 51
+// attention queries loaded, 52 fixed rows requested, 53 own rows requested; 54 first merge
+// item fetched, 55 counts read. (The marks of waves past the first share slots 5..19 with the
+// others; slots 17 and 18 also take the latest start and end over all CTAs.)
 #define TS_MARK(i)                                                     \
   do {                                                                 \
     if (c == 0 && tid == 0 && a.phase_ns) a.phase_ns[i] = globaltimer_ns(); \
@@ -569,7 +584,7 @@ __device__ __noinline__ bool cuda_scan_wave(const StepKArgs& a, Smem& sm, unsign
     for (int si = 0; si < nstages; ++si) {
       const int u = stage_seq + si;
       const int s = u % nslot;
-      if (!mbar_wait(&full[s], (u / nslot) & 1)) {
+      if (!mbar_wait(&full[s], (u / nslot) & 1, a.wait_ns)) {
         set_error(a.status, TS_ERR_TIMEOUT);
         sm.timed_out = 1;
         break;
@@ -625,7 +640,7 @@ __device__ __noinline__ bool cuda_scan_wave(const StepKArgs& a, Smem& sm, unsign
         for (int jj = 0; jj < S::GP; ++jj) v[jj] = acc0[jj] + acc1[jj];
         int which;
         const float dot = transpose_reduce<S::GP, S::LPR>(v, lane, which);
-        const float x = slot < nv ? dot * a.scale_l2 : -INFINITY;
+        const float x = slot < nv ? fmaf(dot, a.scale_l2, dot * a.scale_l2_lo) : -INFINITY;
         if (writer && which < G) eb[(size_t)(tl + slot) * HW + gi * G + which] = x;
         // running max and compensated sum of exp over the rows of this step (lanes of equal `which`)
         float mi = x;
@@ -660,7 +675,7 @@ __device__ __noinline__ bool cuda_scan_wave(const StepKArgs& a, Smem& sm, unsign
     if (tid == 0) {
       // copies issued but never consumed land before the CTA leaves
       for (int ss = 0; ss < nslot; ++ss)
-        if (sm.slot_last[ss] >= 0) mbar_wait(&full[ss], (sm.slot_last[ss] / nslot) & 1);
+        if (sm.slot_last[ss] >= 0) mbar_wait(&full[ss], (sm.slot_last[ss] / nslot) & 1, a.wait_ns);
       atomicExch(&a.gsync->abort, 1u);   // the others leave at their next barrier
     }
     return false;
@@ -693,7 +708,6 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
   __shared__ __align__(8) uint64_t empty[kMaxSlots];  // tensor-core scan: ring slot read by its MMAs
   __shared__ __align__(8) uint64_t accf[2], acce[2];   // accumulator buffer written / read out
   __shared__ __align__(8) uint64_t drainb;            // every MMA issued has completed
-  __shared__ __align__(8) uint64_t abar;
   __shared__ __align__(8) uint64_t xbar;              // bulk copies of partials (vote, merge)
   __shared__ __align__(8) uint64_t vbar[kVoteBufs];  // chunks of my logits for the votes
 
@@ -716,7 +730,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       bulk_g2s(d0, s0, n0, &xbar);
       if (n1) bulk_g2s(d1, s1, n1, &xbar);
     }
-    const bool landed = mbar_wait(&xbar, xph);
+    const bool landed = mbar_wait(&xbar, xph, a.wait_ns);
     xph ^= 1u;
     const bool ok = __syncthreads_and(landed) != 0;
     if (!ok && tid == 0) set_error(a.status, TS_ERR_TIMEOUT);
@@ -738,7 +752,6 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       mbar_init(&acce[i], 128);   // every epilogue thread
     }
     mbar_init(&drainb, 1);
-    mbar_init(&abar, 1);
     mbar_init(&xbar, 1);
     for (int i = 0; i < kVoteBufs; ++i) mbar_init(&vbar[i], 1);
     mbar_fence_init();
@@ -826,7 +839,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           }
         }
       }
-      const bool landed = mbar_wait(&xbar, xph);
+      const bool landed = mbar_wait(&xbar, xph, a.wait_ns);
       xph ^= 1u;
       if (!__syncthreads_and(landed)) {
         if (tid == 0) {
@@ -1266,15 +1279,16 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       #pragma unroll 1
       for (int k = 0; k < nch; ++k) {
         const int kb = k % kVoteBufs;
-        const bool landed = mbar_wait(&vbar[kb], (vph >> kb) & 1u);
+        const bool landed = mbar_wait(&vbar[kb], (vph >> kb) & 1u, a.wait_ns);
         vph ^= 1u << kb;
+        TS_MARK(32);
         if (!__syncthreads_and(landed)) {
           if (tid == 0) {
             set_error(a.status, TS_ERR_TIMEOUT);
             atomicExch(&a.gsync->abort, 1u);
             #pragma unroll 1
             for (int j = k + 1; j < min(nch, k + kVoteBufs); ++j)   // copies in flight land first
-              mbar_wait(&vbar[j % kVoteBufs], (vph >> (j % kVoteBufs)) & 1u);
+              mbar_wait(&vbar[j % kVoteBufs], (vph >> (j % kVoteBufs)) & 1u, a.wait_ns);
           }
           return false;
         }
@@ -1359,7 +1373,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
             // page gp (of sequence b, physical page) into the next ring slot; false after a time-out
             auto put = [&](int gp, int b, int page) -> bool {
               const int s = u % nsl;
-              if (u >= nsl && !mbar_wait(&empty[s], ((u / nsl) - 1) & 1)) return false;
+              if (u >= nsl && !mbar_wait(&empty[s], ((u / nsl) - 1) & 1, a.wait_ns)) return false;
               const int lp = gp - sm.seq[b].pg0;
               const bool valid = page >= 0 && (int64_t)page < a.num_pages;
               sm.stage_tok[s][0] = gp * S::P;
@@ -1452,7 +1466,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
             }
             if (ok) {                                            // end of the stream: a slot with no page
               const int s = u % nsl;
-              if (u >= nsl && !mbar_wait(&empty[s], ((u / nsl) - 1) & 1)) {
+              if (u >= nsl && !mbar_wait(&empty[s], ((u / nsl) - 1) & 1, a.wait_ns)) {
                 ok = false;
               } else {
                 sm.stage_nv[s][0] = -1;
@@ -1472,7 +1486,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
             #pragma unroll 1
             for (int u = 0;; ++u) {
               const int s = u % nsl, buf = u & 1;
-              if (!mbar_wait(&full[s], (u / nsl) & 1) || (u >= 2 && !mbar_wait(&acce[buf], ((u >> 1) - 1) & 1))) {
+              if (!mbar_wait(&full[s], (u / nsl) & 1, a.wait_ns) || (u >= 2 && !mbar_wait(&acce[buf], ((u >> 1) - 1) & 1, a.wait_ns))) {
                 set_error(a.status, TS_ERR_TIMEOUT);
                 sm.timed_out = 1;
                 break;
@@ -1542,7 +1556,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           #pragma unroll 1
           for (int u = 0;; ++u) {
             const int buf = u & 1;
-            if (!__all_sync(kFull, mbar_wait(&accf[buf], (u >> 1) & 1))) {
+            if (!__all_sync(kFull, mbar_wait(&accf[buf], (u >> 1) & 1, a.wait_ns))) {
               if (lane == 0) {
                 set_error(a.status, TS_ERR_TIMEOUT);
                 sm.timed_out = 1;
@@ -1575,7 +1589,9 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
               const float hi = odd ? r[3 * G + 3 * j] : r[3 * j];
               const float mid = odd ? r[3 * G + 3 * j + 1] : r[3 * j + 1];
               const float lo = odd ? r[3 * G + 3 * j + 2] : r[3 * j + 2];
-              x[j] = t < nv ? ((lo + mid) + hi) * a.scale_l2 : -INFINITY;
+              // one rounding of the scaled dot product, with the scale constant in two parts
+              const float acc = (lo + mid) + hi;
+              x[j] = t < nv ? fmaf(acc, a.scale_l2, acc * a.scale_l2_lo) : -INFINITY;
             }
             float* dst = a.spill + (size_t)(tl + t) * H + g * G;
             if constexpr (G == 4) {
@@ -1603,7 +1619,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         }
         tc_fence_before();
         __syncthreads();
-        if (tid == 32 && !mbar_wait(&drainb, 0)) {               // every MMA issued has completed
+        if (tid == 32 && !mbar_wait(&drainb, 0, a.wait_ns)) {               // every MMA issued has completed
           set_error(a.status, TS_ERR_TIMEOUT);
           sm.timed_out = 1;
         }
@@ -1612,7 +1628,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           // copies issued but never consumed land before the CTA leaves
           #pragma unroll 1
           for (int ss = 0; ss < nsl; ++ss)
-            if (sm.slot_last[ss] >= 0) mbar_wait(&full[ss], (sm.slot_last[ss] / nsl) & 1);
+            if (sm.slot_last[ss] >= 0) mbar_wait(&full[ss], (sm.slot_last[ss] / nsl) & 1, a.wait_ns);
         }
         __syncthreads();
         if (warp == 2) {
@@ -1633,8 +1649,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           if (tid == 0) issue_chunk(eb, 0, H, chunk_rows(H));
         }
         TS_MARK(3);
-        if (!grid_sync(a.gsync, a.status, &sm.gepoch)) {
-          if (tid == 0 && pre) mbar_wait(&vbar[0], 0u);         // lands before the CTA leaves
+        if (!grid_sync(a.gsync, a.status, &sm.gepoch, a.wait_ns, a.skip_cta, a.skip_barrier)) {
+          if (tid == 0 && pre) mbar_wait(&vbar[0], 0u, a.wait_ns);         // lands before the CTA leaves
           return;
         }
         TS_MARK(4);
@@ -1651,7 +1667,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         if (!cuda_scan_wave<KT, D, HKV, G>(a, sm, ring, full, wv, stage_seq)) return;
         fence_proxy_async_global();
         TS_MARK(3 + 3 * min(wv, 5));
-        if (!grid_sync(a.gsync, a.status, &sm.gepoch)) return;
+        if (!grid_sync(a.gsync, a.status, &sm.gepoch, a.wait_ns, a.skip_cta, a.skip_barrier)) return;
         TS_MARK(4 + 3 * min(wv, 5));
         if (!vote_pass(eb, g0, HW, wv, 0)) return;
       }
@@ -1663,7 +1679,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
   // (nothing to select when every sequence hits or is empty: no pages were partitioned)
   if ((a.phases & kPhSelect) && sm.ptot > 0) {
     if (!(a.phases & kPhScore)) {
-      if (!grid_sync(a.gsync, a.status, &sm.gepoch)) return;   // the histograms are zero everywhere
+      if (!grid_sync(a.gsync, a.status, &sm.gepoch, a.wait_ns, a.skip_cta, a.skip_barrier)) return;   // the histograms are zero everywhere
     }
     // shared memory while selecting, one use after another: this CTA's histogram (counts,
     // then masses at a fixed offset); after the barrier, the global histograms of a batch of
@@ -1693,6 +1709,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         const int b = sm.seg_b[sg];
         const SeqState& st = sm.seq[b];
         if (st.done) continue;
+        TS_MARK(33 + 4 * level);
         #pragma unroll 1
         for (int i = tid; i < nbins / 4; i += blockDim.x) {
           reinterpret_cast<uint4*>(sh)[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -1702,6 +1719,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           }
         }
         __syncthreads();
+        TS_MARK(34 + 4 * level);
         const int tl0 = sm.seg_lp0[sg] * S::P;
         const int lo = max(st.lo, tl0), hi = min(st.hi, tl0 + sm.seg_ntok[sg]);
         const float* vb = a.vote + (size_t)b * a.vote_stride;
@@ -1718,6 +1736,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           if (topp && in) atomicAdd(&smh[bin], to_fx(v));
         }
         __syncthreads();
+        TS_MARK(35 + 4 * level);
         #pragma unroll 1
         for (int i4 = tid; i4 < nbins / 4; i4 += blockDim.x) {
           const uint4 cv = reinterpret_cast<const uint4*>(sh)[i4];
@@ -1755,7 +1774,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       }
       fence_proxy_async_global();   // the histograms are read back by bulk copy
       TS_MARK(28 + level);
-      if (!grid_sync(a.gsync, a.status, &sm.gepoch)) return;
+      if (!grid_sync(a.gsync, a.status, &sm.gepoch, a.wait_ns, a.skip_cta, a.skip_barrier)) return;
+      TS_MARK(36 + 4 * level);
       // every CTA finds the crossing bin of every unresolved sequence from shared copies of
       // the global histograms (bulk copies); level 0 in two steps: its 128 coarse bins, then
       // the 128 fine bins of the crossing coarse bin
@@ -1799,7 +1819,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
             if (topp) bulk_g2s(dm + b * 128, a.mass + (size_t)b * kHistPerSeq + off(b), 1024u, &xbar);
           }
         }
-        const bool landed = mbar_wait(&xbar, xph);
+        const bool landed = mbar_wait(&xbar, xph, a.wait_ns);
         xph ^= 1u;
         if (__syncthreads_and(landed)) return true;
         if (tid == 0) {
@@ -1812,6 +1832,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         unsigned* cc_ = reinterpret_cast<unsigned*>(bat);                                   // [B][128]
         unsigned long long* cm_ = reinterpret_cast<unsigned long long*>(bat + (size_t)B * 512);
         if (!fetch128(cc_, cm_, [](int) { return kCoarseOff; })) return;
+        TS_MARK(45);
         #pragma unroll 1
         for (int b = warp; b < B; b += S::NW) {
           SeqState& st = sm.seq[b];
@@ -1831,6 +1852,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         }
         __syncthreads();
         if (!fetch128(cc_, cm_, [&](int b) { return sm.x_bin[b] * 128; })) return;
+        TS_MARK(46);
         #pragma unroll 1
         for (int b = warp; b < B; b += S::NW) {
           SeqState& st = sm.seq[b];
@@ -1863,7 +1885,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
             }
           }
           {
-            const bool landed = mbar_wait(&xbar, xph);
+            const bool landed = mbar_wait(&xbar, xph, a.wait_ns);
             xph ^= 1u;
             if (!__syncthreads_and(landed)) {
               if (tid == 0) {
@@ -1976,9 +1998,11 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         __syncthreads();
       }
     }
+    TS_MARK(47);
     if (need_cand || need_tie) {
-      if (!grid_sync(a.gsync, a.status, &sm.gepoch)) return;
+      if (!grid_sync(a.gsync, a.status, &sm.gepoch, a.wait_ns, a.skip_cta, a.skip_barrier)) return;
     }
+    TS_MARK(48);
     if (need_tie) {
       // exact ties before mine, per segment, one warp each
       #pragma unroll 1
@@ -2011,6 +2035,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       #pragma unroll 4
       for (int j = tid; j < m_cand; j += blockDim.x) scand[j] = __ldcg(&a.cands[(size_t)b * kCandCap + j]);
       __syncthreads();
+      TS_MARK(49);
       // exact ties in token order: the first st.ties of them over the sequence are taken
       if (st.tie_mode) {
         int nties = 0;
@@ -2061,6 +2086,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           }
         }
       }
+      TS_MARK(50);
       // counts per warp (all, in [s_end, ls), below s_end), then the list in token order; my
       // scratch region's logits are spent, the list of this segment starts at its row t0l
       int na = 0, nc = 0, nlo = 0;
@@ -2113,7 +2139,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
   // every CTA takes an equal share of each sequence's selected tokens (the CTAs' lists in
   // order, a fixed assignment) instead of its own
   const bool bal = a.mode == TS_SELECT_TOPP && (a.phases & kPhSelect) && (a.phases & kPhAttend) && sm.ptot > 0;
-  if (bal && !grid_sync(a.gsync, a.status, &sm.gepoch)) return;
+  if (bal && !grid_sync(a.gsync, a.status, &sm.gepoch, a.wait_ns, a.skip_cta, a.skip_barrier)) return;
   // ======================================================================== ATTEND
   // My tokens per sequence: a round-robin share of the fixed ones (sinks and
   // window, the cached part of a hit, or the caller's index list) and my own
@@ -2147,7 +2173,6 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     // scores: warp -> one KV head (NW is a multiple of H_kv), its G queries in registers
     constexpr int NWG = S::NW / HKV;
     const int gw = warp % HKV, wsl = warp / HKV;
-    uint32_t aphase = 0;
     #pragma unroll 1
     for (int b = 0; b < B; ++b) {
       const SeqState& st = sm.seq[b];
@@ -2204,28 +2229,33 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         sm.att_m[tid] = -INFINITY;
         sm.att_l[tid] = 0.f;
       }
+      TS_MARK(51);
       float4 o[NG];
 #pragma unroll
       for (int k = 0; k < NG; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       int fdone = 0;     // fixed tokens of mine already taken
       int opos = 0;      // next own token (position in my list)
-      bool ok = true;
-      // bulk copies of the K and V rows of every KV head of list entries [j0, j1)
+      // the K and V rows of every KV head of list entries [j0, j1), 16 bytes per thread and copy
+      // (all of them in flight at once), as one commit group
       auto gather_rows = [&](int j0, int j1) {
-        #pragma unroll 1
-        for (int i = tid; i < 2 * (j1 - j0) * HKV; i += blockDim.x) {
-          const int ti = j0 + i / (2 * HKV), rem = i % (2 * HKV), g = rem >> 1, isv = rem & 1;
+        constexpr int CPR = S::ROW_BYTES / 16;         // 16-byte chunks of a row
+        static_assert(S::ROW_BYTES % 16 == 0, "rows of whole 16-byte chunks");
+        #pragma unroll 2
+        for (int i = tid; i < 2 * (j1 - j0) * HKV * CPR; i += blockDim.x) {
+          const int rr = i / CPR, ch = i % CPR;
+          const int ti = j0 + rr / (2 * HKV), rem = rr % (2 * HKV), g = rem >> 1, isv = rem & 1;
           const int t = sm.toks[ti];
           const int page = sm.tval[ti];
           size_t off = 0;
           if (page >= 0 && (int64_t)page < a.num_pages) {
             off = (((size_t)page * HKV + g) * S::P + (t % S::P)) * S::ROW_BYTES;
-          } else if (rem == 0) {
+          } else if (rem == 0 && ch == 0) {
             set_error(a.status, TS_ERR_PAGE_OOB);
           }
-          bulk_g2s((isv ? Vs : Ks) + ((size_t)ti * HKV + g) * D, (isv ? a.v_pool : a.k_pool) + off,
-                   S::ROW_BYTES, &abar);
+          cp_async16(reinterpret_cast<unsigned char*>((isv ? Vs : Ks) + ((size_t)ti * HKV + g) * D) + ch * 16,
+                     (isv ? a.v_pool : a.k_pool) + off + ch * 16);
         }
+        cp_async_commit();
       };
       __syncthreads();
       while (true) {
@@ -2254,10 +2284,10 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         cnt = nf;
         // the fixed tokens' rows start moving now; the own selected ones are listed meanwhile
         if (nf > 0) {
-          if (tid == 0) mbar_expect_tx(&abar, (uint32_t)(nf * S::TOKEN_BYTES));
           __syncthreads();
           gather_rows(0, nf);
         }
+        TS_MARK(52);
         if (own && opos < own_nc && cnt < around) {
           // my selected tokens in [s_end, ls), in list order, as many as fit
           const int take = min(around - cnt, own_nc - opos);
@@ -2291,22 +2321,13 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         }
         TS_MARK(9);
         if (cnt == 0) break;                          // uniform: same counters in every thread
-        // ---- the own tokens' rows; the phase completes with this arrive and every row
-        if (tid == 0) mbar_arrive_expect_tx(&abar, (uint32_t)((cnt - nf) * S::TOKEN_BYTES));
+        // ---- the own tokens' rows, then every row of the round has landed
         __syncthreads();
         gather_rows(nf, cnt);
-        const bool landed = mbar_wait(&abar, aphase);
-        aphase ^= 1u;
-        ok = __syncthreads_and(landed) != 0;
+        TS_MARK(53);
+        cp_async_wait_all();
+        __syncthreads();
         TS_MARK(10);
-        if (!ok) {
-          if (tid == 0) {
-            set_error(a.status, TS_ERR_TIMEOUT);
-            mbar_wait(&abar, aphase ^ 1u);   // copies still in flight land before the CTA leaves
-          }
-          __syncthreads();
-          break;
-        }
         // ---- (1) scores: warp -> (its KV head, tokens wsl, wsl + NWG, ...); lane holds EPL dims,
         // the G dot products are reduced across the warp so that lane `which` ends with head `which`
 #pragma unroll 4   // independent tokens: their loads and shuffle trees overlap
@@ -2399,10 +2420,6 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         }
         __syncthreads();
       }
-      if (!ok) {
-        if (tid == 0) atomicExch(&a.gsync->abort, 1u);   // the others leave the last barrier
-        return;
-      }
       TS_MARK(11);
       // ---- this CTA's partial of every query head (read back by bulk copy after the barrier)
 #pragma unroll
@@ -2422,7 +2439,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
   TS_MARK(24);
   // ============================================== outputs, after one more barrier
   if (!(a.phases & (kPhSelect | kPhAttend))) return;
-  if (!grid_sync(a.gsync, a.status, &sm.gepoch)) return;
+  if (!grid_sync(a.gsync, a.status, &sm.gepoch, a.wait_ns, a.skip_cta, a.skip_barrier)) return;
   TS_MARK(25);
   if (a.phases & kPhAttend) {
     // merge the CTA partials of one (sequence, query head, column part) per CTA pass: the item's
@@ -2444,6 +2461,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         if (tid == 0) atomicExch(&a.gsync->abort, 1u);
         return;
       }
+      TS_MARK(54);
       float M = -INFINITY;
       #pragma unroll 1
       for (int cc = lane; cc < nCTA; cc += 32) M = fmaxf(M, pml[cc].x);
@@ -2528,6 +2546,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       }
     }
     __syncthreads();
+    TS_MARK(55);
     // ascending index lists and Selection Cache entries
     #pragma unroll 1
     for (int b = 0; b < B; ++b) {
@@ -2673,7 +2692,7 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
         cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, ctx->device) != cudaSuccess)
       return TS_ERR_CUDA;
     smem_avail = min(min(optin, per_sm - reserved), kSmemLimit);
-    if (std::getenv("TS_DEBUG"))
+    if (ctx->debug)
       std::fprintf(stderr, "ts step: smem optin %d, per SM %d, reserved/block %d\n", optin, per_sm, reserved);
     // the whole unified L1/shared array as shared memory for this kernel
     if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
@@ -2693,10 +2712,10 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
       dyn < ctx->num_sms * (D * 4 + 8 + 4) + 8 + 16 + S::THREADS * 16)   // the merge's rows, pairs, weights
     return TS_ERR_UNSUPPORTED;
   if (!ensure_smem<step_kernel<KT, D, HKV, G>>((size_t)dyn, ctx->device)) {
-    if (std::getenv("TS_DEBUG")) std::fprintf(stderr, "ts step: smem attribute %d B refused\n", dyn);
+    if (ctx->debug) std::fprintf(stderr, "ts step: smem attribute %d B refused\n", dyn);
     return TS_ERR_CUDA;
   }
-  const bool debug = std::getenv("TS_DEBUG") != nullptr;
+  const bool debug = ctx->debug;
   if (ctx->step_grid <= 0) {
     int per_sm = 0;
     const cudaError_t oe = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, S::THREADS, (size_t)dyn);
@@ -2721,7 +2740,11 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   a.page_table = c.page_table;
   a.seq_lens = c.seq_lens;
   a.scale = c.scale;
-  a.scale_l2 = (float)((double)c.scale * 1.4426950408889634);
+  {
+    const double sl2 = (double)c.scale * 1.4426950408889634;
+    a.scale_l2 = (float)sl2;
+    a.scale_l2_lo = (float)(sl2 - (double)a.scale_l2);
+  }
   a.theta = c.theta;
   a.hit_in = c.hit_in;
   a.hit_out = c.hit_out;
@@ -2758,13 +2781,13 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   a.spill = ctx->logits;
   a.spill_floats = ctx->logits_floats;
   a.wpart = reinterpret_cast<float2*>(ctx->step_wpart);
-  a.l2_budget = kLogitL2Budget;
-  if (const char* env = std::getenv("TOKENSELECT_L2_BUDGET_MB")) {
-    const long mb = std::strtol(env, nullptr, 10);
-    if (mb > 0) a.l2_budget = (int64_t)mb << 20;
-  }
+  a.l2_budget = ctx->l2_budget > 0 ? ctx->l2_budget : kLogitL2Budget;
   a.gsync = reinterpret_cast<GridSync*>(ctx->gsync);
   a.status = ctx->status;
+  a.wait_ns = ctx->wait_ns;
+  a.skip_cta = ctx->inject_skip_cta;       // an injected fault applies to this launch only
+  a.skip_barrier = ctx->inject_skip_barrier;
+  ctx->inject_skip_cta = ctx->inject_skip_barrier = -1;
   a.phase_ns = ctx->phase_ns;
   a.dyn_bytes = dyn;
   a.nslot = nslot;
@@ -2774,9 +2797,7 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   if constexpr (S::TC) {
     // tensor-core scan: 1024-aligned ring of page tiles plus two query-term images
     const int nslot_tc = std::min(kMaxSlots, (dyn - flag_cap - 1024 - 2 * S::TC_BIMG) / S::TC_TILE);
-    const char* no_tc_env = std::getenv("TOKENSELECT_NO_TC");   // =1: CUDA-core scan (comparisons, tests)
-    const bool no_tc = no_tc_env && no_tc_env[0] == '1';
-    if (!no_tc && nslot_tc >= 2 && (c.phases & kPhScore) && c.k_pool && (reinterpret_cast<uintptr_t>(c.q) & 15) == 0) {
+    if (!ctx->no_tc && nslot_tc >= 2 && (c.phases & kPhScore) && c.k_pool && (reinterpret_cast<uintptr_t>(c.q) & 15) == 0) {
       auto& cache = ctx->kmaps;   // a few recent pools (one per layer in a decode loop)
       int hitc = -1;
       for (int i = 0; i < (int)(sizeof(cache) / sizeof(cache[0])); ++i)
@@ -2794,11 +2815,11 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
         std::memcpy(&a.tmap_k, cache[hitc].map, sizeof(CUtensorMap));
         a.tc = 1;
         a.nslot_tc = nslot_tc;
-        // =1: CTAs claim pages of one or two scanned sequences from a shared counter instead of
-        // each scanning its own range. Faster where bandwidth differs between SMs, but which
-        // CTA sums which pages then varies, so repeated runs may differ in the last bits.
-        const char* cl_env = std::getenv("TOKENSELECT_SCAN_CLAIM");
-        a.scan_dyn = cl_env && cl_env[0] == '1';
+        // CTAs may claim pages of one or two scanned sequences from a shared counter instead of
+        // each scanning its own range (TOKENSELECT_SCAN_CLAIM=1 at context creation). Faster where
+        // bandwidth differs between SMs, but which CTA sums which pages then varies, so repeated
+        // runs may differ in the last bits.
+        a.scan_dyn = ctx->scan_claim ? 1 : 0;
       }
     }
   }
