@@ -313,23 +313,26 @@ __global__ void __launch_bounds__(kCaThreads, 1) chunk_attend_kernel(const __gri
     }
   }
 
-  // ---- outputs: my row's half of the output columns, and the row's lse
-  if (ok && rg < rows) {
-    const int qi = rg / a.G, head = g * a.G + rg % a.G;
+  // ---- outputs: my row's half of the output columns, and the row's lse. The TMEM loads are
+  // warp-collective (.sync.aligned): every lane of the warp issues them whatever its row, and
+  // only the stores depend on the row being real
+  if (ok) {
+    const bool valid = rg < rows;
+    const int qi = valid ? rg / a.G : 0, head = valid ? g * a.G + rg % a.G : 0;
     float* dst = a.out + (((size_t)b * a.c + qi) * a.H + head) * D + chalf * (D / 2);
-    if (ntiles > 0 && l > 0.f) {
 #pragma unroll
-      for (int i = 0; i < D / 16; ++i) {
-        float o8[8];
+    for (int i = 0; i < D / 16; ++i) {
+      float o8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (ntiles > 0) {                                      // uniform over the CTA
         tmem_ld_x8(tO + lane_off + chalf * (D / 2) + 8 * i, o8);
         tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 8; ++e) dst[8 * i + e] = o8[e];
       }
-    } else {
-      for (int e = 0; e < D / 2; ++e) dst[e] = 0.f;
+      if (valid) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dst[8 * i + e] = l > 0.f ? o8[e] : 0.f;
+      }
     }
-    if (a.lse && chalf == 0) a.lse[((size_t)b * a.c + qi) * a.H + head] = l > 0.f ? m + logf(l) : -INFINITY;
+    if (valid && a.lse && chalf == 0) a.lse[((size_t)b * a.c + qi) * a.H + head] = l > 0.f ? m + logf(l) : -INFINITY;
   }
   if (!ok && tid == 0) mbar_wait(&mbar, phase, a.wait_ns);   // a late commit lands before TMEM is freed
   tc_fence_before();
