@@ -58,7 +58,8 @@ def parse_args(argv=None):
 
 # workload index, theta for the profiling cases
 CASES = {"n128k": (1, 0.9), "n128k-miss": (1, 2.0), "n1m-miss": (3, 2.0), "n1m-1layer-miss": ("3x1", 2.0),
-         "qwen-b8-miss": (2, 2.0), "topp-b4": (4, 0.9)}
+         "n256k-1layer-miss": ("3x1@256k", 2.0), "qwen-b8-miss": (2, 2.0), "topp-b4": (4, 0.9),
+         "prefill-n128k-c512": ("prefill", None)}
 
 
 def case_main(args):
@@ -67,7 +68,30 @@ def case_main(args):
 
     import workloads as W
     cfg, theta = CASES[args.case]
-    sp = W.spec(3, layers=1) if cfg == "3x1" else W.spec(cfg)
+    if cfg == "prefill":
+        # the 128K workload's 512-query prefill chunk, --steps calls of ts_prefill_chunk
+        import token_level_sparse_gb300 as T
+        sp = W.spec(1, steps=512)
+        wl = W.generate(sp, "cuda:0")
+        ctx = T.Context(sp.n_q_heads, sp.n_kv_heads, sp.head_dim, T.TS_KV_BF16, 1, wl.page_table.shape[1],
+                        wl.num_pages)
+        q = torch.stack([wl.q[i][0] for i in range(512)], dim=1).contiguous()
+        idx = torch.zeros(1, sp.k + sp.n_sink + sp.n_local, dtype=torch.int32, device="cuda:0")
+        cnt = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+        out = torch.zeros(1, 512, sp.n_q_heads, sp.head_dim, device="cuda:0")
+        prm = T.params(k=sp.k, n_sink=sp.n_sink, n_local=sp.n_local, theta=2.0)
+        for _ in range(args.steps):
+            ctx.prefill_chunk(q, wl.k_pool[0], wl.v_pool[0], wl.page_table, wl.seq_lens(0), prm, idx, cnt, out)
+        torch.cuda.synchronize()
+        assert ctx.status() == 0
+        print(f"case {args.case}: {args.steps} chunks")
+        return
+    if cfg == "3x1":
+        sp = W.spec(3, layers=1)
+    elif cfg == "3x1@256k":
+        sp = W.spec(3, layers=1, n0=(262144,))
+    else:
+        sp = W.spec(cfg)
     b = DecodeBench(sp, "cuda:0", theta=theta)
     if args.phases:
         for i in range(args.steps):
@@ -628,6 +652,189 @@ def reference_main(args):
                       "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
 
 
+def _event_ms(fn, iters, warmup):
+    """Mean device time (ms) of fn() over iters calls after warmup calls, CUDA events on the
+    current stream, synchronised on both sides."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def prefill_extra(dev, peaks, c=512):
+    """ts_prefill_chunk on the 128K workload with a chunk of c queries: the whole call (mean query,
+    persistent score + selection, tensor-core causal chunk attention) and the chunk attention's
+    own launch, against the dense bf16 tensor peak. Useful FLOPs count 2 x 2 x d per visible
+    (query, head, token): the scores and the weighted values, nothing for the extra query terms,
+    the second pass or the weight terms."""
+    import torch
+    import token_level_sparse_gb300 as T
+    import workloads as W
+    sp = W.spec(1, steps=c)
+    wl = W.generate(sp, dev)
+    B, H, d = 1, sp.n_q_heads, sp.head_dim
+    ctx = T.Context(H, sp.n_kv_heads, d, T.TS_KV_BF16, B, wl.page_table.shape[1], wl.num_pages)
+    q = torch.stack([wl.q[i][0] for i in range(c)], dim=1).contiguous()
+    idx = torch.zeros(B, sp.k + sp.n_sink + sp.n_local, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(B, dtype=torch.int32, device=dev)
+    out = torch.zeros(B, c, H, d, device=dev)
+    lse = torch.zeros(B, c, H, device=dev)
+    prm = T.params(k=sp.k, n_sink=sp.n_sink, n_local=sp.n_local, theta=2.0)
+    seq = wl.seq_lens(0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
+
+    def call():
+        flush.zero_()
+        ctx.prefill_chunk(q, wl.k_pool[0], wl.v_pool[0], wl.page_table, seq, prm, idx, cnt, out, lse)
+
+    call()
+    torch.cuda.synchronize()
+    ids = idx[0, :int(cnt[0])].cpu()
+    n = wl.n0[0]
+    vis = sum(int((ids <= n - c + i).sum()) for i in range(c))
+    flops = 4.0 * vis * H * d
+    ms_flush = _event_ms(lambda: flush.zero_(), 10, 3)
+    ms = _event_ms(call, 10, 3) - ms_flush
+    T.ts_profile_enable(ctx.handle, True)
+    T.ts_profile_read(ctx.handle)
+    for _ in range(10):
+        call()
+    torch.cuda.synchronize()
+    prof = T.ts_profile_read(ctx.handle)
+    att_ms, att_n = prof["attend"]
+    step_ms, step_n = prof["step"]
+    peak = peaks.get("bf16_tflops", 1925.7) if peaks else 1900.0
+    att_tf = flops / (att_ms / att_n * 1e-3) / 1e12 if att_n else None
+    st = T.ts_get_status(ctx.handle)
+    ctx.close()
+    return {"value": 1000.0 / ms, "unit": "chunks/s", "ms_per_chunk": ms, "chunk": c, "selected": int(cnt[0]),
+            "useful_gflop": flops / 1e9, "attend_us": 1000.0 * att_ms / max(1, att_n),
+            "select_us": 1000.0 * step_ms / max(1, step_n),
+            "roofline": {"bound": "tensor", "achieved": att_tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": att_tf / peak if att_tf else None,
+                         "kernel": "chunk_attend_kernel (tcgen05, causal, two passes)",
+                         "peak_source": "measured bf16_tflops (burst)" if peaks else "fallback"},
+            "status": st, "l2": "flushed before every call (256 MB write, outside the attend events)"}
+
+
+def ablation_extra(dev, fn_name):
+    """Decode steps of the 128K trajectory with an ablation selection function (multi-kernel path,
+    no cache: every step scores and selects)."""
+    import torch
+    import token_level_sparse_gb300 as T
+    import workloads as W
+    sp = W.spec(1, steps=8)
+    wl = W.generate(sp, dev)
+    ctx = T.Context(sp.n_q_heads, sp.n_kv_heads, sp.head_dim, T.TS_KV_BF16, 1, wl.page_table.shape[1], wl.num_pages)
+    fn = {"logit_sum": T.TS_SCORE_LOGIT_SUM, "hard_vote": T.TS_SCORE_HEAD_HARD_VOTE}[fn_name]
+    prm = T.params(k=sp.k, n_sink=sp.n_sink, n_local=sp.n_local, theta=2.0, score_fn=fn)
+    idx = torch.zeros(1, sp.k + sp.n_sink + sp.n_local, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.zeros(1, sp.n_q_heads, sp.head_dim, device=dev)
+    vote = torch.zeros(1, ctx.max_tokens, device=dev)
+    seq = wl.seq_lens(0)
+    q = wl.q[0][0]
+    ms = _event_ms(lambda: ctx.decode_step(q, wl.k_pool[0], wl.v_pool[0], wl.page_table, seq, prm, idx, cnt, out,
+                                           vote=vote), 10, 3)
+    st = T.ts_get_status(ctx.handle)
+    ctx.close()
+    return {"value": 1000.0 / ms, "unit": UNIT, "ms_per_step": ms, "status": st,
+            "l2": "not flushed: inputs larger than L2 (268 MB of K per step)"}
+
+
+OVERLAP_RHOS = (0.5, 0.7, 0.8, 0.85, 0.9, 0.925, 0.95, 0.975, 0.99, 0.999)
+
+
+def overlap_pairs(wl, rhos, draws, dev, seed=7):
+    """(rho, cosine, q1, q2) pairs: q2 = rho q1 + sqrt(1 - rho^2) eps with eps ~ N(0, 1) per element
+    (the workload's AR(1) step), rounded to bf16 values like the workload's queries."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    q1 = wl.q[0][0]
+    out = []
+    for rho in rhos:
+        for _ in range(draws):
+            eps = torch.randn(q1.shape, generator=g, device=dev)
+            q2 = (rho * q1 + math.sqrt(1.0 - rho * rho) * eps).to(torch.bfloat16).to(torch.float32).contiguous()
+            c = float(torch.nn.functional.cosine_similarity(q1.reshape(1, -1), q2.reshape(1, -1)))
+            out.append((rho, c, q1, q2))
+    return out
+
+
+def selected_part(T, ctx, wl, sp, q, idx, cnt, prm):
+    """The top-k part (without sinks and window) of one fresh selection through ts_decode_step."""
+    import torch
+    out = torch.zeros(1, sp.n_q_heads, sp.head_dim, device=q.device)
+    ctx.decode_step(q, wl.k_pool[0], wl.v_pool[0], wl.page_table, wl.seq_lens(0), prm, idx, cnt, out)
+    ids = idx[0, :int(cnt[0])].cpu().numpy()
+    n = wl.n0[0]
+    s_end, ls = min(sp.n_sink, n), max(min(sp.n_sink, n), n - sp.n_local)
+    return ids[(ids >= s_end) & (ids < ls)]
+
+
+def overlap_extra(dev, draws=4):
+    """Selection overlap against query cosine on the 128K workload (the TokenSelect review's
+    figure 3(b), on synthetic keys): for queries at a range of cosines to a base query, the
+    fraction of the base query's top-k part that the other query selects too."""
+    import numpy as np
+    import torch
+    import token_level_sparse_gb300 as T
+    import workloads as W
+    sp = W.spec(1, steps=1)
+    wl = W.generate(sp, dev)
+    ctx = T.Context(sp.n_q_heads, sp.n_kv_heads, sp.head_dim, T.TS_KV_BF16, 1, wl.page_table.shape[1], wl.num_pages)
+    prm = T.params(k=sp.k, n_sink=sp.n_sink, n_local=sp.n_local, theta=2.0)
+    idx = torch.zeros(1, sp.k + sp.n_sink + sp.n_local, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+    base = selected_part(T, ctx, wl, sp, wl.q[0][0], idx, cnt, prm)
+    curve = {}
+    for rho, c, _, q2 in overlap_pairs(wl, OVERLAP_RHOS, draws, dev):
+        part = selected_part(T, ctx, wl, sp, q2, idx, cnt, prm)
+        ov = float(np.intersect1d(base, part).size) / max(1, base.size)
+        curve.setdefault(rho, []).append((c, ov))
+    st = T.ts_get_status(ctx.handle)
+    ctx.close()
+    return {"k": sp.k, "draws_per_point": draws, "status": st,
+            "points": [{"rho": r, "cosine": float(np.mean([c for c, _ in v])),
+                        "overlap": float(np.mean([o for _, o in v]))} for r, v in sorted(curve.items())]}
+
+
+def recall_extra(dev, budget=2048):
+    """Recall@budget of the best tokens by vote when the same budget is spent on blocks of
+    1..128 tokens (the TokenSelect review's figure 2(b), on the 128K workload's needles)."""
+    import numpy as np
+    import torch
+    import token_level_sparse_gb300 as T
+    import workloads as W
+    sp = W.spec(1, steps=1)
+    wl = W.generate(sp, dev)
+    ctx = T.Context(sp.n_q_heads, sp.n_kv_heads, sp.head_dim, T.TS_KV_BF16, 1, wl.page_table.shape[1], wl.num_pages)
+    n = wl.n0[0]
+    seq = wl.seq_lens(0)
+    vote = torch.zeros(1, ctx.max_tokens, device=dev)
+    ctx.score(wl.q[0][0], wl.k_pool[0], wl.page_table, seq, vote)
+    idx = torch.zeros(1, budget + 128, dtype=torch.int32, device=dev)
+    cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+    v = vote.cpu().numpy()[0, :n].astype(np.float64)
+    top = set(np.argsort(-v, kind="stable")[:budget].tolist())
+    pts = []
+    for block in (1, 2, 4, 8, 16, 32, 64, 128):
+        ctx.select_blocks(vote, seq, block, budget, idx, cnt)
+        sel = idx[0, :int(cnt[0])].cpu().numpy()
+        pts.append({"block": block, "recall": len(top.intersection(sel.tolist())) / budget})
+    st = T.ts_get_status(ctx.handle)
+    ctx.close()
+    return {"budget": budget, "points": pts, "status": st}
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.cpu_baseline_only:
@@ -699,6 +906,24 @@ def main(argv=None):
             extras[name]["top_p"] = sp4.top_p
             extras[name]["l2"] = "not flushed: inputs larger than L2 (2.15 GB of K per step on a miss)"
             del b4
+            torch.cuda.empty_cache()
+        sp2 = W.spec(2)
+        for name, theta in (("qwen_b8_theta0.9", sp2.theta), ("qwen_b8_miss_only", 2.0)):
+            b2 = DecodeBench(sp2, dev, theta=theta, seed_offset=rank)
+            s2 = timed(b2, sp2.steps, 3, peak_gbs, flush=False)
+            extras[name] = {k: s2[k] for k in ("value", "ms_per_step", "hit_rate", "step_gbs", "score_gbs",
+                                              "miss_step_gbs", "score_us_per_launch") if k in s2}
+            if peak_gbs and "score_gbs" in s2:
+                extras[name]["score_frac_of_peak"] = s2["score_gbs"] / peak_gbs
+            extras[name]["l2"] = "not flushed: inputs larger than L2 (about 1 GB of K per step on a miss)"
+            del b2
+            torch.cuda.empty_cache()
+        extras["prefill_n128k_c512"] = prefill_extra(dev, peaks)
+        extras["selection_overlap_vs_cosine_n128k"] = overlap_extra(dev)
+        extras["recall_vs_block_size_n128k"] = recall_extra(dev)
+        torch.cuda.empty_cache()
+        for fn_name in ("logit_sum", "hard_vote"):
+            extras[f"ablation_{fn_name}_n128k"] = ablation_extra(dev, fn_name)
             torch.cuda.empty_cache()
         sp3 = W.spec(3)
         for name, theta in (("n1m_theta0.9", sp3.theta), ("n1m_miss_only", 2.0)):

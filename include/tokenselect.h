@@ -223,6 +223,19 @@ ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q
                          float* vote, int64_t vote_stride, int32_t* idx, int64_t idx_stride,
                          int32_t* count, float* out, float* lse, uint8_t* hit, void* stream);
 
+/* Block-level selection, the granularity the method argues against
+ * (TokenSelect review, figure 2(b): InfLLM-style methods keep or drop whole
+ * blocks; granularity 1 is token-level selection). From the votes of each
+ * sequence (non-negative, e.g. from ts_score): blocks of `block` consecutive
+ * tokens (the last one ragged) are scored by their largest vote, the
+ * budget / block best blocks are taken (ties to the lower block) and every
+ * token of them is written to idx [B][idx_stride] ascending, count [B]; a
+ * list longer than idx_stride records TS_ERR_CAPACITY. No sinks, window or
+ * cache: it serves the recall comparison of the two granularities. */
+ts_status ts_select_blocks(ts_ctx* ctx, const float* vote, int64_t vote_stride, const int32_t* seq_lens, int B,
+                           int block, int budget, int32_t* idx, int64_t idx_stride, int32_t* count,
+                           void* stream);
+
 /* Chunk-wise prefill selection (TokenSelect deep notes, "Optimising the
  * selection frequency of the prefill stage"; review, section 3.2): the c
  * queries of a prefill chunk, q fp32 [B][c][H][d] (16-byte aligned), are

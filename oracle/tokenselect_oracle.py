@@ -52,6 +52,21 @@ R12 Chunk-wise prefill selection: the cache already holds the chunk's c tokens
     into one query, which selects once (head soft vote, top-k over [s, n-w),
     united with sinks and window, no Selection Cache in prefill); chunk query
     i then attends causally to the selected tokens at positions <= n-c+i.
+R13 Lemma 1 (TS-notes, Appendix C): for one query head and dot-product top-k,
+    writing q2/|q2| = (q1/|q1|) cos t + p sin t with p a unit vector orthogonal
+    to q1, every score of q2 is |q2| (cos t . s1_i + sin t . p.k_i) with
+    s1_i = (q1/|q1|).k_i and |p.k_i| <= R = max_i |k_i|. The top-k cannot
+    change while cos t . D > 2 R sin t, D the gap between the k-th and the
+    (k+1)-th s1: the sufficient threshold is eps = 2R / sqrt(D^2 + 4R^2)
+    (the constant the pages' proof arrives at is not legible; this is the
+    plainest one the decomposition gives).
+R14 Block-level selection (the contrast of TS-review figure 2(b), InfLLM-style):
+    the n tokens form blocks of `block` consecutive tokens (the last one
+    ragged); a block's score is the largest vote of its tokens (a block is
+    taken as soon as one of its tokens matters, as the review describes);
+    the budget // block best blocks are taken (ties to the lower block) and
+    every token of them is selected. Recall@m of a selection is the share of
+    the m best tokens by vote (ties to the lower index) that it holds.
 R11 The head hard vote counts, per token, the query heads whose own TopK
     (k tokens, over the same candidates [s, N-w) as R3, ties to the lower
     index) contains it, then takes the TopK of the counts (ties to the lower
@@ -72,7 +87,8 @@ __all__ = [
     "budget_segments", "select_topk", "select_topp", "refresh_hit",
     "sparse_attention", "dense_attention", "cosine", "CacheState",
     "cache_decision", "decode_step", "default_scale", "logit_sum_scores",
-    "hard_vote_counts", "selection_scores", "SCORE_FNS", "prefill_chunk",
+    "hard_vote_counts", "selection_scores", "SCORE_FNS", "prefill_chunk", "lemma1_epsilon",
+    "selection_overlap", "select_blocks", "recall_at",
 ]
 
 
@@ -410,3 +426,56 @@ def prefill_chunk(q_chunk: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray, p
         visible = idx[idx <= n - c + i]
         out[i], lse[i] = sparse_attention(q_chunk[i], k_pool, v_pool, page_row, visible, scale)
     return {"idx": idx, "part": part, "out": out, "lse": lse, "vote": vote, "q_mean": q_mean}
+
+
+# ---------------------------------------- Selection Cache rationale (R13, figure 3(b))
+
+def lemma1_epsilon(q1: np.ndarray, keys: np.ndarray, k: int) -> float:
+    """Sufficient cosine above which TopK_k(q . K^T) equals TopK_k(q1 . K^T) (reading R13).
+
+    TS-notes, "Selection Cache" (the lemma: consecutive queries with cosine above
+    a threshold select the same top-k keys) and Appendix C (the proof by the
+    orthogonal decomposition q2 = q1 cos t + p sin t). keys [n, d], 0 < k < n.
+    Returns eps = 2R / sqrt(D^2 + 4R^2); 1.0 when the k-th and (k+1)-th scores tie.
+    """
+    keys = np.asarray(keys, dtype=np.float64)
+    q1 = np.asarray(q1, dtype=np.float64)
+    s1 = keys @ (q1 / math.sqrt(float(q1 @ q1)))
+    srt = np.sort(s1)[::-1]
+    gap = float(srt[k - 1] - srt[k])
+    R = float(np.sqrt((keys * keys).sum(axis=1)).max())
+    if gap <= 0.0:
+        return 1.0
+    return 2.0 * R / math.sqrt(gap * gap + 4.0 * R * R)
+
+
+def selection_overlap(a: np.ndarray, b: np.ndarray) -> float:
+    """|A n B| / |A|: the overlap rate of two selections (TS-review, figure 3(b))."""
+    a = np.asarray(a)
+    if a.size == 0:
+        return 1.0
+    return float(np.intersect1d(a, np.asarray(b)).size) / float(a.size)
+
+
+# ------------------------------------------- block-level selection contrast (R14)
+
+def select_blocks(vote: np.ndarray, n: int, budget: int, block: int) -> np.ndarray:
+    """Tokens of the budget // block best blocks of `block` tokens by their largest vote (R14).
+
+    TS-review, figure 2(b) and observation 1 (block-level methods such as InfLLM
+    take whole blocks; selection granularity 1 is token-level selection).
+    Returns the selected token indices, ascending.
+    """
+    vote = np.asarray(vote, dtype=np.float64)[:n]
+    nb = -(-n // block)
+    scores = np.array([vote[j * block:min(n, (j + 1) * block)].max() for j in range(nb)])
+    take = min(nb, max(0, budget // block))
+    blocks = np.argsort(-scores, kind="stable")[:take]
+    toks = [np.arange(j * block, min(n, (j + 1) * block)) for j in sorted(blocks.tolist())]
+    return np.concatenate(toks).astype(np.int64) if toks else np.zeros(0, dtype=np.int64)
+
+
+def recall_at(selected: np.ndarray, vote: np.ndarray, n: int, m: int) -> float:
+    """|selected n TopM(vote)| / m, ties to the lower index (R14; TS-review figure 2(b))."""
+    top = _order_desc(np.asarray(vote, dtype=np.float64), np.arange(n))[:m]
+    return float(np.intersect1d(top, np.asarray(selected)).size) / float(m)

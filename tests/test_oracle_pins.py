@@ -634,3 +634,85 @@ def test_prefill_selection_brute_force_on_the_mean_query():
         vis = r["idx"][r["idx"] <= n - c + i]
         o, _ = O.sparse_attention(q[i], kp, vp, pt, vis)
         assert np.allclose(r["out"][i], o, rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------- Lemma 1 (R13)
+
+def _topk_set(scores, k):
+    return set(np.argsort(-scores, kind="stable")[:k].tolist())
+
+
+def test_lemma1_threshold_is_sufficient():
+    # queries built at a cosine just above eps in random orthogonal directions never change the
+    # dot-product top-k
+    rng = np.random.default_rng(31)
+    for trial in range(30):
+        n, d, k = 200, 16, 10
+        K = rng.normal(size=(n, d))
+        q1 = rng.normal(size=d)
+        eps = O.lemma1_epsilon(q1, K, k)
+        base = _topk_set(K @ q1, k)
+        u = q1 / np.linalg.norm(q1)
+        for _ in range(20):
+            p = rng.normal(size=d)
+            p -= (p @ u) * u
+            p /= np.linalg.norm(p)
+            c = eps + (1.0 - eps) * rng.uniform(1e-3, 1.0)
+            q2 = (u * c + p * math.sqrt(1.0 - c * c)) * rng.uniform(0.5, 2.0)
+            assert O.cosine(q1, q2) > eps
+            assert _topk_set(K @ q2, k) == base
+
+
+def test_lemma1_bound_is_met_by_an_adversarial_direction():
+    # moving q1 towards the direction that favours the (k+1)-th key over the k-th swaps them once
+    # cot t < (difference of their orthogonal components) / gap: the lemma's bound lies at or above
+    # that critical cosine, and below it the selection does change
+    rng = np.random.default_rng(32)
+    n, d, k = 60, 8, 5
+    K = rng.normal(size=(n, d))
+    q1 = rng.normal(size=d)
+    u = q1 / np.linalg.norm(q1)
+    order = np.argsort(-(K @ u), kind="stable")
+    i, j = order[k - 1], order[k]
+    diff = K[j] - K[i]
+    perp = diff - (diff @ u) * u
+    p = perp / np.linalg.norm(perp)
+    gap = float((K[i] - K[j]) @ u)
+    t_crit = math.atan2(gap, float(np.linalg.norm(perp)))      # cot t = |perp| / gap
+    eps = O.lemma1_epsilon(q1, K, k)
+    assert eps >= math.cos(t_crit) - 1e-12
+    t = t_crit * 1.05
+    q2 = u * math.cos(t) + p * math.sin(t)
+    assert _topk_set(K @ q2, k) != _topk_set(K @ u, k)
+
+
+def test_selection_overlap_definition():
+    assert O.selection_overlap(np.array([1, 2, 3, 4]), np.array([3, 4, 5])) == 0.5
+    assert O.selection_overlap(np.array([7]), np.array([7])) == 1.0
+
+
+# ----------------------------------------------- block-level selection contrast (R14)
+
+def test_select_blocks_hand_case():
+    v = np.array([0.1, 0.9, 0.2, 0.2, 0.5, 0.0, 0.3, 0.3, 0.3, 0.1])
+    # blocks of 3: [0.1 0.9 0.2] [0.2 0.5 0.0] [0.3 0.3 0.3] [0.1] -> maxima 0.9, 0.5, 0.3, 0.1
+    assert O.select_blocks(v, 10, 6, 3).tolist() == [0, 1, 2, 3, 4, 5]
+    assert O.select_blocks(v, 10, 5, 3).tolist() == [0, 1, 2]          # 5 // 3 = one block
+    assert O.select_blocks(v, 10, 12, 3).tolist() == list(range(10))   # the ragged last block too
+    # token granularity: the budget best tokens, ties to the lower index
+    assert O.select_blocks(v, 10, 3, 1).tolist() == [1, 4, 6]
+    assert O.recall_at(np.array([1, 4, 6]), v, 10, 3) == 1.0
+    assert O.recall_at(np.array([0, 1, 2]), v, 10, 3) == pytest.approx(1 / 3)
+
+
+def test_block_granularity_one_is_token_topk_and_recall_falls_with_block_size():
+    # the review's figure 2(b) on scattered needles: token-level selection recalls every one of
+    # the best m tokens, 128-token blocks recall far fewer within the same budget
+    rng = np.random.default_rng(41)
+    n, m = 1 << 14, 256
+    v = rng.exponential(size=n) * 1e-3
+    v[rng.choice(n, m, replace=False)] += 1.0                         # isolated important tokens
+    assert O.recall_at(O.select_blocks(v, n, m, 1), v, n, m) == 1.0
+    rec = [O.recall_at(O.select_blocks(v, n, m, b), v, n, m) for b in (1, 4, 16, 64, 128)]
+    assert all(rec[i] >= rec[i + 1] for i in range(len(rec) - 1))
+    assert rec[-1] < 0.1

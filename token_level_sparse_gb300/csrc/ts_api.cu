@@ -38,6 +38,8 @@ void free_ctx_buffers(ts_ctx* c) {
   cudaFree(c->vote);
   cudaFree(c->hit);
   cudaFree(c->qmean);
+  cudaFree(c->blk_len);
+  cudaFree(c->blk_idx);
   cudaFree(c->step_partials);
   cudaFree(c->step_hist);
   cudaFree(c->step_mass);
@@ -139,7 +141,7 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   ctx->logits_floats = (int64_t)(B * H * T + H * NS * 2 * kPage);
   chk(alloc(&ctx->status, 1));
   chk(alloc(&ctx->logits, (size_t)ctx->logits_floats));
-  chk(alloc(&ctx->step_partials, B * NS * H));
+  chk(alloc(&ctx->step_partials, B * NS * 2 * H));   // two partial rows per CTA where a tile holds two pages
   chk(alloc(&ctx->step_hist, B * kStepHistPerSeq));
   chk(alloc(&ctx->step_mass, B * kStepHistPerSeq));
   chk(alloc(&ctx->cand_n, B));
@@ -162,6 +164,8 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   chk(alloc(&ctx->vote, B * T));
   chk(alloc(&ctx->hit, B));
   chk(alloc(&ctx->qmean, B * H * D));
+  chk(alloc(&ctx->blk_len, B));
+  chk(alloc(&ctx->blk_idx, B * T + B));
   if (e == cudaSuccess) chk(cudaMemset(ctx->status, 0, sizeof(int)));
   if (e == cudaSuccess) chk(cudaMemset(ctx->counters, 0, B * kCounterSlots * sizeof(unsigned)));
   if (e == cudaSuccess) chk(cudaMemset(ctx->hist, 0, B * 2048 * sizeof(unsigned)));
@@ -422,6 +426,15 @@ ts_status ts_prefill_chunk(ts_ctx* ctx, const float* q, int c, const void* k_poo
   // (3) the chunk's queries attend causally to the shared selection, on the tensor cores
   ChunkAttendCall ac{q, c, k_pool, v_pool, page_table, seq_lens, idx, idx_stride, count, B, scale, out, lse};
   return launch_chunk_attend(ctx, ac, s);
+}
+
+ts_status ts_select_blocks(ts_ctx* ctx, const float* vote, int64_t vote_stride, const int32_t* seq_lens, int B,
+                           int block, int budget, int32_t* idx, int64_t idx_stride, int32_t* count, void* stream) {
+  if (!ctx || !vote || !seq_lens || !idx || !count) return TS_ERR_INVALID_ARG;
+  if (block < 1 || budget < 0) return TS_ERR_INVALID_ARG;
+  if (B < 1 || B > ctx->cfg.max_batch || vote_stride < ctx->max_tokens || idx_stride < 1) return TS_ERR_SHAPE;
+  return launch_select_blocks(ctx, vote, vote_stride, seq_lens, B, block, budget, idx, idx_stride, count,
+                              as_stream(stream));
 }
 
 ts_status ts_debug_phase_ns(ts_ctx* ctx, uint64_t* out64, void* stream) {

@@ -65,11 +65,13 @@ struct ts_ctx {
   float* vote = nullptr;                 // [max_batch][max_tokens] (decode step)
   uint8_t* hit = nullptr;                // [max_batch] (decode step)
   float* qmean = nullptr;                // [max_batch][H][d] mean query of a prefill chunk
+  int32_t* blk_len = nullptr;            // [max_batch] block counts (block-level selection)
+  int32_t* blk_idx = nullptr;            // [max_batch][max_tokens] selected blocks, then [max_batch] counts
   int64_t kernels = 0;           // kernel launches issued
   // persistent decode-step kernel
   int step_grid = 0;                     // CTAs of the cooperative launch (0: not yet sized)
   int64_t logits_floats = 0;             // size of `logits` (also the step kernel's spill area)
-  float2* step_partials = nullptr;       // [max_batch][num_sms][H]
+  float2* step_partials = nullptr;       // [max_batch][num_sms][tile pages (1 or 2)][H]
   unsigned* step_hist = nullptr;         // [3][max_batch][2048]
   unsigned long long* step_mass = nullptr;  // [3][max_batch][2048]
   unsigned* cand_n = nullptr;            // [max_batch]
@@ -220,6 +222,9 @@ ts_status launch_score(ts_ctx* ctx, const ScoreCall& a, cudaStream_t s);
 ts_status launch_select(ts_ctx* ctx, const SelectCall& a, cudaStream_t s);
 ts_status launch_attend(ts_ctx* ctx, const AttendCall& a, cudaStream_t s);
 bool chunk_attend_supported(const ts_config& c);
+ts_status launch_select_blocks(ts_ctx* ctx, const float* vote, int64_t vote_stride, const int32_t* seq_lens, int B,
+                               int block, int budget, int32_t* idx, int64_t idx_stride, int32_t* count,
+                               cudaStream_t s);
 ts_status launch_chunk_mean(ts_ctx* ctx, const float* q, int c, int B, float* qm, cudaStream_t s);
 ts_status launch_chunk_attend(ts_ctx* ctx, const ChunkAttendCall& c, cudaStream_t s);
 ts_status launch_cache_check(ts_ctx* ctx, ts_cache* cache, int layer, const float* q, int B,

@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kCaThreads, 1) chunk_attend_kernel(const __gri
   unsigned char* sK = sQ + 3 * S::QT;       // K tile, then P term 0 of the same tile
   unsigned char* sV = sK + S::KP;           // V^T tile
   unsigned char* sP1 = sV + S::VT;          // P term 1
-  __shared__ int s_tok[kCaTok], s_page[kCaTok];
+  __shared__ int s_tok[2][kCaTok], s_page[2][kCaTok];   // token lists of two key tiles
   __shared__ float s_m[2][kCaRows], s_l[2][kCaRows];
   __shared__ uint32_t s_tmem;
   __shared__ __align__(8) uint64_t mbar;
@@ -107,8 +107,10 @@ __global__ void __launch_bounds__(kCaThreads, 1) chunk_attend_kernel(const __gri
   const int cnt = max(0, min(a.count[b], (int)a.idx_stride));
   const int ntiles = (cnt + kCaTok - 1) / kCaTok;
 
-  // ---- the query rows of this tile as three bf16 terms, K-major and swizzled
+  // ---- the query rows of this tile as three bf16 terms, K-major and swizzled; when every query
+  // element is a bf16 value (its mid and lo terms are zero) only the first term is multiplied
   constexpr int CPR = D / 8;                            // 8-element chunks of a query row
+  int extra = 0;
   for (int i = tid; i < 3 * kCaRows * CPR; i += kCaThreads) {
     const int term = i / (kCaRows * CPR), rem = i % (kCaRows * CPR), r = rem / CPR, ch = rem % CPR;
     const int rg = r0 + r;
@@ -125,8 +127,10 @@ __global__ void __launch_bounds__(kCaThreads, 1) chunk_attend_kernel(const __gri
     for (int e = 0; e < 4; ++e)
       w[e] = (uint32_t)__bfloat16_as_ushort(bf16_split_term(e8[2 * e], term)) |
              ((uint32_t)__bfloat16_as_ushort(bf16_split_term(e8[2 * e + 1], term)) << 16);
+    if (term > 0) extra |= (w[0] | w[1] | w[2] | w[3]) & 0x7fff7fffu;   // a non-zero mid or lo term
     *reinterpret_cast<uint4*>(sQ + term * S::QT + opnd_offset(r, ch * 8, kCaRows)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
+  const int nterms = __syncthreads_or(extra) ? 3 : 1;
   fence_proxy_async();
   if (warp == 0) {
     tmem_alloc(&s_tmem, 256);                           // S: columns 0..127, O: 128..255
@@ -162,154 +166,191 @@ __global__ void __launch_bounds__(kCaThreads, 1) chunk_attend_kernel(const __gri
     return true;
   };
 
-  for (int pass = 0; pass < 2 && ok; ++pass) {
-    for (int kt = 0; kt < ntiles && ok; ++kt) {
-      // ---- the tile's tokens and pages
-      if (tid < kCaTok) {
-        const int j = kt * kCaTok + tid;
-        int t = -1, page = -1;
-        if (j < cnt) {
-          t = a.idx[(size_t)b * a.idx_stride + j];
-          if (t >= 0 && t < a.max_tokens) page = a.page_table[(size_t)b * a.pt_stride + t / kPage];
-          if (page < 0 || (int64_t)page >= a.num_pages) {
-            set_error(a.status, TS_ERR_PAGE_OOB);
-            page = -1;
-          }
-        }
-        s_tok[tid] = page >= 0 ? t : -1;
-        s_page[tid] = page;
-      }
-      __syncthreads();
-      // ---- K rows by cp.async into the swizzled tile (missing tokens read row 0: masked below)
-      for (int i = tid; i < kCaTok * CPR; i += kCaThreads) {
-        const int r = i / CPR, ch = i % CPR, page = s_page[r];
-        const size_t off = page >= 0 ? (((size_t)page * a.HKV + g) * kPage + s_tok[r] % kPage) * S::ROW_BYTES : 0;
-        cp_async16(sK + opnd_offset(r, ch * 8, kCaTok), a.k_pool + off + ch * 16);
-      }
-      cp_async_commit();
-      if (pass == 1) {
-        // V rows transposed into V^T [d][token] (K-major over the tokens): lane = token, so the
-        // 2-byte stores of a warp fill consecutive columns of one row
-        for (int i = tid; i < kCaTok * CPR; i += kCaThreads) {
-          const int r = i % kCaTok, ch = i / kCaTok, page = s_page[r];
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (page >= 0)
-            v = *reinterpret_cast<const uint4*>(a.v_pool + (((size_t)page * a.HKV + g) * kPage + s_tok[r] % kPage) *
-                                                               S::ROW_BYTES + ch * 16);
-          const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            *reinterpret_cast<uint16_t*>(sV + opnd_offset(ch * 8 + e, r, D)) =
-                (uint16_t)((w4[e >> 1] >> (16 * (e & 1))) & 0xffffu);
+  // the tokens and pages of key tile kt into list buffer lb (threads below 128)
+  auto list_tile = [&](int kt, int lb) {
+    if (tid < kCaTok) {
+      const int j = kt * kCaTok + tid;
+      int t = -1, page = -1;
+      if (j < cnt) {
+        t = a.idx[(size_t)b * a.idx_stride + j];
+        if (t >= 0 && t < a.max_tokens) page = a.page_table[(size_t)b * a.pt_stride + t / kPage];
+        if (page < 0 || (int64_t)page >= a.num_pages) {
+          set_error(a.status, TS_ERR_PAGE_OOB);
+          page = -1;
         }
       }
-      cp_async_wait_all();
-      fence_proxy_async();
-      tc_fence_before();
-      __syncthreads();
-      // ---- S = Q K^T: three query terms into one accumulator
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t q0 = smem_addr(sQ), k0 = smem_addr(sK);
-#pragma unroll 1
-        for (int term = 0; term < 3; ++term)
-#pragma unroll
-          for (int h = 0; h < S::HALVES; ++h)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_bf16(tS, sdesc_sw128(q0 + term * S::QT + h * (kCaRows * 128) + ks * 32),
-                        sdesc_sw128(k0 + h * (kCaTok * 128) + ks * 32), idesc, (term | h | ks) != 0);
-        umma_commit(&mbar);
-      }
-      if (!wait_mma()) {
-        ok = false;
-        break;
-      }
-      // ---- my 64 score columns, masked (causal, missing tokens) and scaled
-      float x[64];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        tmem_ld_x8(tS + lane_off + chalf * 64 + 8 * i, *reinterpret_cast<float(*)[8]>(x + 8 * i));
-      tmem_wait_ld();
-#pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const int t = s_tok[chalf * 64 + j];
-        x[j] = (t >= 0 && t <= qpos) ? x[j] * a.scale : -INFINITY;
-      }
-      if (pass == 0) {
-        // running max and sum of exponentials of my row over my columns
-        float tm = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) tm = fmaxf(tm, x[j]);
-        if (tm > -INFINITY) {
-          const float mn = fmaxf(m, tm);
-          float s = 0.f;
-#pragma unroll
-          for (int j = 0; j < 64; ++j) s += x[j] > -INFINITY ? expf(x[j] - mn) : 0.f;
-          l = (m > -INFINITY ? l * expf(m - mn) : 0.f) + s;
-          m = mn;
-        }
-        tc_fence_before();
-        __syncthreads();                        // every score read before the next tile's MMAs
-      } else {
-        // normalised weights as two bf16 terms: P0 into the spent K tile, P1 into its own
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          uint32_t w0[4], w1[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float p2[2];
-#pragma unroll
-            for (int z = 0; z < 2; ++z) {
-              const float xx = x[8 * u + 2 * e + z];
-              p2[z] = (xx > -INFINITY && l > 0.f) ? expf(xx - m) * inv : 0.f;
-            }
-            const __nv_bfloat16 h0 = __float2bfloat16_rn(p2[0]), h1 = __float2bfloat16_rn(p2[1]);
-            const __nv_bfloat16 l0 = __float2bfloat16_rn(p2[0] - __bfloat162float(h0));
-            const __nv_bfloat16 l1 = __float2bfloat16_rn(p2[1] - __bfloat162float(h1));
-            w0[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-            w1[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
-          }
-          const uint32_t off = opnd_offset(row, chalf * 64 + 8 * u, kCaRows);
-          *reinterpret_cast<uint4*>(sK + off) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-          *reinterpret_cast<uint4*>(sP1 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        // ---- O += P V^T: two weight terms
-        if (tid == 0) {
-          tc_fence_after();
-          const uint32_t v0 = smem_addr(sV);
-#pragma unroll 1
-          for (int term = 0; term < 2; ++term) {
-            const uint32_t p0 = smem_addr(term == 0 ? sK : sP1);
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int ks = 0; ks < 4; ++ks)
-                umma_bf16(tO, sdesc_sw128(p0 + h * (kCaRows * 128) + ks * 32),
-                          sdesc_sw128(v0 + h * (D * 128) + ks * 32), idesc_o, (kt | term | h | ks) != 0);
-          }
-          umma_commit(&mbar);
-        }
-        if (!wait_mma()) {
-          ok = false;
-          break;
-        }
-      }
+      s_tok[lb][tid] = page >= 0 ? t : -1;
+      s_page[lb][tid] = page;
     }
-    if (pass == 0 && ok) {
-      // the row's max and sum over both column halves
-      s_m[chalf][row] = m;
-      s_l[chalf][row] = l;
+  };
+  // the K rows of list lb into the swizzled tile at dst by cp.async, one commit group (missing
+  // tokens read row 0 of the pool: masked when the scores are read)
+  auto gather_k = [&](int lb, unsigned char* dst) {
+    for (int i = tid; i < kCaTok * CPR; i += kCaThreads) {
+      const int r = i / CPR, ch = i % CPR, page = s_page[lb][r];
+      const size_t off = page >= 0 ? (((size_t)page * a.HKV + g) * kPage + s_tok[lb][r] % kPage) * S::ROW_BYTES : 0;
+      cp_async16(dst + opnd_offset(r, ch * 8, kCaTok), a.k_pool + off + ch * 16);
+    }
+    cp_async_commit();
+  };
+  // S = Q K^T of the K tile at kbuf: the query terms into one accumulator
+  auto issue_scores = [&](const unsigned char* kbuf) {
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t q0 = smem_addr(sQ), k0 = smem_addr(kbuf);
+#pragma unroll 1
+      for (int term = 0; term < nterms; ++term)
+#pragma unroll
+        for (int h = 0; h < S::HALVES; ++h)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tS, sdesc_sw128(q0 + term * S::QT + h * (kCaRows * 128) + ks * 32),
+                      sdesc_sw128(k0 + h * (kCaTok * 128) + ks * 32), idesc, (term | h | ks) != 0);
+      umma_commit(&mbar);
+    }
+  };
+  // my 64 score columns, masked (causal, missing tokens) and scaled
+  float x[64];
+  auto read_scores = [&](int lb) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      tmem_ld_x8(tS + lane_off + chalf * 64 + 8 * i, *reinterpret_cast<float(*)[8]>(x + 8 * i));
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 64; ++j) {
+      const int t = s_tok[lb][chalf * 64 + j];
+      x[j] = (t >= 0 && t <= qpos) ? x[j] * a.scale : -INFINITY;
+    }
+  };
+
+  // ---- pass 1: every row's max and sum of exponentials. K tiles alternate between the K
+  // buffer and the (not yet needed) V buffer, so the next tile's rows land during this one's scores
+  if (ntiles > 0) {
+    list_tile(0, 0);
+    __syncthreads();
+    gather_k(0, sK);
+  }
+  for (int kt = 0; kt < ntiles; ++kt) {
+    const int lb = kt & 1;
+    unsigned char* kb = lb ? sV : sK;
+    if (kt + 1 < ntiles) {
+      list_tile(kt + 1, lb ^ 1);
       __syncthreads();
-      const float m0 = s_m[0][row], m1 = s_m[1][row], M = fmaxf(m0, m1);
-      l = M > -INFINITY ? (m0 > -INFINITY ? s_l[0][row] * expf(m0 - M) : 0.f) +
-                              (m1 > -INFINITY ? s_l[1][row] * expf(m1 - M) : 0.f)
-                        : 0.f;
-      m = M;
+      gather_k(lb ^ 1, lb ? sK : sV);
+      cp_async_wait_but_one();
+    } else {
+      cp_async_wait_all();
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    issue_scores(kb);
+    if (!wait_mma()) {
+      ok = false;
+      break;
+    }
+    read_scores(lb);
+    float tm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 64; ++j) tm = fmaxf(tm, x[j]);
+    if (tm > -INFINITY) {
+      const float mn = fmaxf(m, tm);
+      float sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) sum += x[j] > -INFINITY ? expf(x[j] - mn) : 0.f;
+      l = (m > -INFINITY ? l * expf(m - mn) : 0.f) + sum;
+      m = mn;
+    }
+    tc_fence_before();
+    __syncthreads();                            // scores read and list buffer free before they are reused
+  }
+  cp_async_wait_all();                          // nothing left in flight (a time-out leaves the loop early)
+  if (ok) {
+    // the row's max and sum over both column halves
+    s_m[chalf][row] = m;
+    s_l[chalf][row] = l;
+    __syncthreads();
+    const float m0 = s_m[0][row], m1 = s_m[1][row], M = fmaxf(m0, m1);
+    l = M > -INFINITY ? (m0 > -INFINITY ? s_l[0][row] * expf(m0 - M) : 0.f) +
+                            (m1 > -INFINITY ? s_l[1][row] * expf(m1 - M) : 0.f)
+                      : 0.f;
+    m = M;
+  }
+
+  // ---- pass 2: the scores again, normalised weights P, O += P V^T
+  for (int kt = 0; kt < ntiles && ok; ++kt) {
+    list_tile(kt, 0);
+    __syncthreads();
+    gather_k(0, sK);
+    // V rows transposed into V^T [d][token] (K-major over the tokens): lane = token, so the
+    // 2-byte stores of a warp fill consecutive columns of one row
+    for (int i = tid; i < kCaTok * CPR; i += kCaThreads) {
+      const int r = i % kCaTok, ch = i / kCaTok, page = s_page[0][r];
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (page >= 0)
+        v = *reinterpret_cast<const uint4*>(a.v_pool + (((size_t)page * a.HKV + g) * kPage + s_tok[0][r] % kPage) *
+                                                           S::ROW_BYTES + ch * 16);
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        *reinterpret_cast<uint16_t*>(sV + opnd_offset(ch * 8 + e, r, D)) =
+            (uint16_t)((w4[e >> 1] >> (16 * (e & 1))) & 0xffffu);
+    }
+    cp_async_wait_all();
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    issue_scores(sK);
+    if (!wait_mma()) {
+      ok = false;
+      break;
+    }
+    read_scores(0);
+    // normalised weights as two bf16 terms: P0 into the spent K tile, P1 into its own
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      uint32_t w0[4], w1[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float p2[2];
+#pragma unroll
+        for (int z = 0; z < 2; ++z) {
+          const float xx = x[8 * u + 2 * e + z];
+          p2[z] = (xx > -INFINITY && l > 0.f) ? expf(xx - m) * inv : 0.f;
+        }
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(p2[0]), h1 = __float2bfloat16_rn(p2[1]);
+        const __nv_bfloat16 l0 = __float2bfloat16_rn(p2[0] - __bfloat162float(h0));
+        const __nv_bfloat16 l1 = __float2bfloat16_rn(p2[1] - __bfloat162float(h1));
+        w0[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        w1[e] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+      }
+      const uint32_t off = opnd_offset(row, chalf * 64 + 8 * u, kCaRows);
+      *reinterpret_cast<uint4*>(sK + off) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+      *reinterpret_cast<uint4*>(sP1 + off) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    // ---- O += P V^T: two weight terms
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t v0 = smem_addr(sV);
+#pragma unroll 1
+      for (int term = 0; term < 2; ++term) {
+        const uint32_t p0 = smem_addr(term == 0 ? sK : sP1);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tO, sdesc_sw128(p0 + h * (kCaRows * 128) + ks * 32),
+                      sdesc_sw128(v0 + h * (D * 128) + ks * 32), idesc_o, (kt | term | h | ks) != 0);
+      }
+      umma_commit(&mbar);
+    }
+    if (!wait_mma()) {
+      ok = false;
+      break;
     }
   }
 

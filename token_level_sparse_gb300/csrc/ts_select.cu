@@ -12,6 +12,8 @@
 // For top-p the histogram also carries the vote mass in 2^-40 fixed point,
 // so the mass sums are exact integers too. Equal votes at the threshold are
 // taken in index order by a final count + write pass.
+#include <algorithm>
+
 #include "ts_common.cuh"
 
 namespace ts {
@@ -534,6 +536,108 @@ ts_status launch_select(ts_ctx* ctx, const SelectCall& c, cudaStream_t s) {
   }
   sel_count_kernel<<<grid, kSelThreads, 0, s>>>(a);
   sel_write_kernel<<<grid, kSelThreads, 0, s>>>(a);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace ts
+
+// ------------------------------------------------ block-level selection contrast
+//
+// The selection granularity the method argues against (TokenSelect review,
+// figure 2(b), observation 1: block-level methods such as InfLLM keep or drop
+// whole blocks of consecutive tokens): blocks of `block` tokens are scored by
+// their largest vote, the budget / block best blocks are taken (ties to the
+// lower block) by the same radix top-k, and every token of them is selected.
+
+namespace ts {
+namespace {
+
+// bscore[b][j] = max of the votes of block j of sequence b; nblk[b] = its block count
+__global__ void block_max_kernel(const float* vote, int64_t vote_stride, const int32_t* seq_lens, int max_tokens,
+                                 int block, float* bscore, int64_t bs_stride, int32_t* nblk, int* status) {
+  const int b = blockIdx.y;
+  int n = seq_lens[b];
+  if (n < 0 || n > max_tokens) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_error(status, TS_ERR_SEQ_LEN);
+    n = 0;
+  }
+  const int nb = (n + block - 1) / block;
+  if (blockIdx.x == 0 && threadIdx.x == 0) nblk[b] = nb;
+  const float* vb = vote + (size_t)b * vote_stride;
+  for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < nb; j += gridDim.x * blockDim.x) {
+    float m = 0.f;                       // votes are >= 0
+    const int t1 = min(n, (j + 1) * block);
+    for (int t = j * block; t < t1; ++t) m = fmaxf(m, vb[t]);
+    bscore[(size_t)b * bs_stride + j] = m;
+  }
+}
+
+// the tokens of the selected blocks (ascending block indices) as an ascending token list
+__global__ void block_expand_kernel(const int32_t* bidx, int64_t bidx_stride, const int32_t* bcount,
+                                    const int32_t* seq_lens, int max_tokens, int block, int32_t* idx,
+                                    int64_t idx_stride, int32_t* count, int* status) {
+  const int b = blockIdx.x;
+  int n = seq_lens[b];
+  if (n < 0 || n > max_tokens) n = 0;
+  const int nsel = max(0, bcount[b]);
+  const int32_t* bl = bidx + (size_t)b * bidx_stride;
+  int total = 0;
+  if (nsel > 0) {
+    const int last = bl[nsel - 1];
+    total = (nsel - 1) * block + (min(n, (last + 1) * block) - last * block);
+  }
+  if (total > idx_stride) {
+    if (threadIdx.x == 0) {
+      set_error(status, TS_ERR_CAPACITY);
+      count[b] = 0;
+    }
+    return;
+  }
+  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    const int j = i / block;                     // only the last selected block can be ragged
+    idx[(size_t)b * idx_stride + i] = bl[j] * block + (i % block);
+  }
+  if (threadIdx.x == 0) count[b] = total;
+}
+
+}  // namespace
+
+ts_status launch_select_blocks(ts_ctx* ctx, const float* vote, int64_t vote_stride, const int32_t* seq_lens, int B,
+                               int block, int budget, int32_t* idx, int64_t idx_stride, int32_t* count,
+                               cudaStream_t s) {
+  const int mt = ctx->max_tokens;
+  // block scores in the logit scratch, block counts and the selected blocks in the selection scratch
+  float* bscore = ctx->logits;
+  int32_t* nblk = ctx->blk_len;
+  int32_t* bidx = ctx->blk_idx;
+  ctx->kernels += 2;
+  block_max_kernel<<<dim3(std::min(1024, (mt / block + 255) / 256 + 1), B), 256, 0, s>>>(
+      vote, vote_stride, seq_lens, mt, block, bscore, mt, nblk, ctx->status);
+  if (cudaGetLastError() != cudaSuccess) return TS_ERR_CUDA;
+  SelectCall sel{};
+  sel.cache = nullptr;
+  sel.layer = 0;
+  sel.q = nullptr;
+  sel.vote = bscore;
+  sel.vote_stride = mt;
+  sel.seq_lens = nblk;
+  sel.B = B;
+  sel.hit = nullptr;
+  sel.params.mode = TS_SELECT_TOPK;
+  sel.params.k = budget / block;
+  sel.params.n_sink = 0;
+  sel.params.n_local = 0;
+  sel.params.top_p = 1.f;
+  sel.params.theta = 2.f;
+  sel.params.softmax_scale = 0.f;
+  sel.params.score_fn = TS_SCORE_HEAD_SOFT_VOTE;
+  sel.idx = bidx;
+  sel.idx_stride = mt;
+  sel.count = bidx + (size_t)ctx->cfg.max_batch * mt;   // counts after the lists
+  ts_status st = launch_select(ctx, sel, s);
+  if (st != TS_OK) return st;
+  block_expand_kernel<<<B, 256, 0, s>>>(bidx, mt, sel.count, seq_lens, mt, block, idx, idx_stride, count,
+                                        ctx->status);
   return cuda_status(cudaGetLastError());
 }
 

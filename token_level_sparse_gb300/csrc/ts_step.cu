@@ -60,6 +60,8 @@ constexpr int kVoteBufs = 2;       // shared-memory buffers of logit chunks for 
 constexpr int kMaxGrid = 256;      // CTAs of the persistent launch (one per SM)
 static_assert(2 * kMaxGrid + 1 <= kMaxPagesCta, "balanced-attention offsets share the page-id array");
 constexpr int kMaxSlots = 12;      // ring slots (runtime count per launch)
+constexpr int kNoPage = -2147483647 - 1;  // a tile's second page is absent (not an invalid page id)
+constexpr int kAbsentRows = -2;           // valid-row count of an absent page of a tile: nothing is stored
 constexpr int64_t kLogitL2Budget = 48ll << 20;  // default bytes of logits one scan wave keeps in L2
 // radix levels over the vote bits (votes are >= +0, bit 31 is always 0): bits 30..17, 16..6,
 // 5..0. The first level is fine enough that its crossing bin usually holds few enough tokens
@@ -135,15 +137,22 @@ struct StepShape {
   static_assert((HKV * G) % 2 == 0, "rows of H (max, sum) pairs are whole 16-byte blocks");
   // tensor-core scan (bf16 pages of 128 rows = H_kv x 16 tokens): one M = 128 tcgen05.mma
   // tile per page against all query heads, each split into three bf16 terms
-  static constexpr bool TC = std::is_same<KT, __nv_bfloat16>::value && HKV * P == 128 && (D == 128 || D == 64) &&
-                             3 * HKV * G <= 256 && G <= 8;
+  // a page of every KV head is HKV x 16 rows: 128 rows fill one M = 128 tile, 64 rows (4 KV heads)
+  // take two pages of the same sequence per tile
+  static constexpr int TC_ROWS = HKV * P;
+  static constexpr int TC_PAGES = TC_ROWS == 64 ? 2 : 1;
+  static constexpr bool TC = std::is_same<KT, __nv_bfloat16>::value && (TC_ROWS == 128 || TC_ROWS == 64) &&
+                             (D == 128 || D == 64) && 3 * HKV * G <= 256 && G <= 8;
   static constexpr int TC_N = (3 * HKV * G + 15) / 16 * 16;           // B rows (q terms), multiple of 16
   static constexpr int TC_HALVES = D / 64;                             // 128-byte swizzle rows per K row
-  static constexpr int TC_TILE = 128 * D * 2;                          // one page of K
+  static constexpr int TC_TILE = 128 * D * 2;                          // one M = 128 tile of K (1 or 2 pages)
+  static constexpr int TC_PAGE_BYTES = TC_ROWS * D * 2;                // one page of K
+  static constexpr int PV = TC_PAGES;                                  // partial rows per CTA (one per tile half)
+  static_assert(TC_PAGE_BYTES * TC_PAGES <= TC_TILE, "the pages of a tile fit its slot");
   static constexpr int TC_BIMG = TC_N * D * 2;                         // one sequence's query terms
   static constexpr int TC_COLS = TC_N <= 32 ? 32 : (TC_N <= 64 ? 64 : (TC_N <= 128 ? 128 : 256));
   static constexpr int TC_NLD = (6 * G + 7) / 8;                       // 8-column loads per epilogue warp
-  static_assert(!TC || (2 * TC_COLS <= 512 && 6 * G * 3 + 8 * TC_NLD <= TC_COLS && NW >= 8 && TC_HALVES >= 1 &&
+  static_assert(!TC || (2 * TC_COLS <= 512 && 6 * G * (HKV / 2 - 1) + 8 * TC_NLD <= TC_COLS && NW >= 8 && TC_HALVES >= 1 &&
                         TC_BIMG % 1024 == 0 && TC_TILE % 1024 == 0), "tensor-core scan");
   static_assert(G <= kMaxG, "heads per KV head");
   static_assert(NCW <= kMaxScanWarps && NCW % HKV == 0, "scan warps split evenly over the KV heads");
@@ -157,7 +166,7 @@ struct GridSync {
 };
 
 struct StepKArgs {
-  CUtensorMap tmap_k;          // K pool as [num_pages * H_kv * 16][d] bf16, box 64 x 128, 128-byte swizzle
+  CUtensorMap tmap_k;          // K pool as [num_pages * H_kv * 16][d] bf16, box 64 x (H_kv * 16), 128-byte swizzle
   int tc;                      // the tensor-core scan may run (map encoded, geometry supported)
   int nslot_tc;                // its ring slots
   int scan_dyn;                // it may share pages out by claims when at most two sequences scan
@@ -456,7 +465,8 @@ struct Smem {
   int tc_nimg, tc_seq[2];          // query images of the scan and the sequence of each
   int tc_img_of[kMaxB];            // image of sequence b, or -1
   uint32_t tmem;                   // TMEM base address of the accumulators
-  int acc_tl[2], acc_nv[2], acc_sg[2];  // per accumulator buffer: first token, valid rows, segment
+  int acc_tl[2][2], acc_nv[2][2], acc_sg[2];  // per accumulator buffer: first token and valid rows of each
+                                              // page of the tile, segment
   union {
     int my_pages[kMaxPagesCta];  // physical page ids of my range (first kMaxPagesCta pages)
     struct {                     // balanced attention (my_pages unused then): a sequence's per-CTA
@@ -692,7 +702,11 @@ __device__ __noinline__ bool cuda_scan_wave(const StepKArgs& a, Smem& sm, unsign
       if (lane < wph) mz = wp[((size_t)sg * S::NCW + gi * wph + lane) * G + w];
       const float m = warp_max(mz.x);
       const float z = warp_sum_comp((m > -INFINITY && mz.y > 0.f) ? mz.y * exp2f(mz.x - m) : 0.f);
-      if (lane == 0) a.partials[((size_t)sm.seg_b[sg] * nCTA + c) * H + g0 * G + hl] = make_float2(m, z);
+      if (lane == 0) {
+        float2* pr = a.partials + (((size_t)sm.seg_b[sg] * nCTA + c) * S::PV) * H + g0 * G + hl;
+        pr[0] = make_float2(m, z);
+        if (S::PV == 2) pr[H] = make_float2(-INFINITY, 0.f);
+      }
     }
   }
   return true;
@@ -1111,7 +1125,10 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     }
   };
   if (c == 0 && tid < B && (a.phases & kPhCheck) && a.hit_out) a.hit_out[tid] = (uint8_t)sm.seq[tid].hit;
-  if (!tc_scan) late_setup(tid, (int)blockDim.x);
+  // (with 16 warps the tensor-core scan leaves warps 8.. free to do it while the pages stream; a
+  // block of 8 warps has none, so it is done here first)
+  const bool late_in_scan = tc_scan && S::NW > 8;
+  if (!late_in_scan) late_setup(tid, (int)blockDim.x);
   if constexpr (S::TC) {
     if (sm.use_tc) {
       // B operand of each of my (at most two) sequences: row n = 3 h + term holds that term of
@@ -1194,7 +1211,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     // my logits [row = token of my range][HW] pass through shared memory past the vote scratch
     // in chunks of whole rows by bulk copy: at once when the range fits, else through
     // kVoteBufs buffers with all but one in flight
-    const size_t vsb = ((size_t)kMaxB * kMaxWaveHeads * 8 + (size_t)nCTA * H * 8 + S::NW * 32 * 8 + 15) &
+    const size_t vsb = ((size_t)kMaxB * kMaxWaveHeads * 8 + (size_t)nCTA * S::PV * H * 8 + S::NW * 32 * 8 + 15) &
                        ~(size_t)15;
     float* vbuf = reinterpret_cast<float*>(ring + vsb);
     const int vrows = (sm.p1 - sm.p0) * S::P;
@@ -1224,17 +1241,18 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         const SeqState& st = sm.seq[sm.seg_b[sg]];
         // a shared scan leaves partials of every sequence in every CTA
         const int fc = sm.scan_dyn ? 0 : st.first_cta, ncta = sm.scan_dyn ? nCTA : st.last_cta - st.first_cta + 1;
-        float* rmx = reinterpret_cast<float*>(pcs + (size_t)ncta * H);   // [NW][32] per-slice maxima
+        const int nrow = ncta * S::PV;                                    // partial rows: PV per CTA
+        float* rmx = reinterpret_cast<float*>(pcs + (size_t)nrow * H);   // [NW][32] per-slice maxima
         float* rz = rmx + S::NW * 32;                                    // [NW][32] per-slice sums
-        if (!bulk_fetch(pcs, a.partials + ((size_t)sm.seg_b[sg] * nCTA + fc) * H,
-                        (uint32_t)(ncta * H * sizeof(float2)), nullptr, nullptr, 0u)) {
+        if (!bulk_fetch(pcs, a.partials + ((size_t)sm.seg_b[sg] * nCTA + fc) * S::PV * H,
+                        (uint32_t)(nrow * H * sizeof(float2)), nullptr, nullptr, 0u)) {
           if (tid == 0) atomicExch(&a.gsync->abort, 1u);
           return false;
         }
         TS_MARK(13);
         // lane = head of the wave, warp = a slice of the CTAs: conflict-free rows of H pairs
-        const int per = (ncta + S::NW - 1) / S::NW;
-        const int c0 = min(ncta, warp * per), c1 = min(ncta, c0 + per);
+        const int per = (nrow + S::NW - 1) / S::NW;
+        const int c0 = min(nrow, warp * per), c1 = min(nrow, c0 + per);
         const bool lh = lane < HW;
         float m = -INFINITY;
         if (lh)
@@ -1370,24 +1388,36 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           if (lane == 0) {                                       // producer
             const uint64_t pol = l2_evict_first_policy();
             int u = 0;                                           // ring uses so far
-            // page gp (of sequence b, physical page) into the next ring slot; false after a time-out
-            auto put = [&](int gp, int b, int page) -> bool {
+            // pages gp (and gp + 1 when a tile takes two: page2 != kNoPage) of sequence b, physical
+            // ids page / page2, into the next ring slot, page i at row i * TC_ROWS of the tile;
+            // false after a time-out
+            auto put = [&](int gp, int b, int page, int page2) -> bool {
               const int s = u % nsl;
               if (u >= nsl && !mbar_wait(&empty[s], ((u / nsl) - 1) & 1, a.wait_ns)) return false;
-              const int lp = gp - sm.seq[b].pg0;
-              const bool valid = page >= 0 && (int64_t)page < a.num_pages;
-              sm.stage_tok[s][0] = gp * S::P;
-              sm.stage_b[s][0] = b;
-              sm.stage_nv[s][0] = valid ? min(S::P, sm.seq[b].n - lp * S::P) : 0;
+              uint32_t bytes = 0;
+              bool valid[S::TC_PAGES];
+#pragma unroll
+              for (int pi = 0; pi < S::TC_PAGES; ++pi) {
+                const int pg = pi == 0 ? page : page2, lp = gp + pi - sm.seq[b].pg0;
+                const bool present = pi == 0 || page2 != kNoPage;
+                valid[pi] = present && pg >= 0 && (int64_t)pg < a.num_pages;
+                if (present && !valid[pi]) set_error(a.status, TS_ERR_PAGE_OOB);
+                sm.stage_tok[s][pi] = (gp + pi) * S::P;
+                sm.stage_b[s][pi] = b;
+                sm.stage_nv[s][pi] = !present ? kAbsentRows : (valid[pi] ? min(S::P, sm.seq[b].n - lp * S::P) : 0);
+                bytes += valid[pi] ? (uint32_t)S::TC_PAGE_BYTES : 0u;
+              }
               sm.slot_last[s] = u;
-              if (valid) {
-                mbar_arrive_expect_tx(&full[s], (uint32_t)S::TC_TILE);
-      #pragma unroll
-                for (int h = 0; h < S::TC_HALVES; ++h)
-                  tma_load_2d(tcr + (size_t)s * S::TC_TILE + h * (S::TC_TILE / S::TC_HALVES), &a.tmap_k, h * 64,
-                              page * 128, &full[s], pol);
+              if (bytes) {
+                mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+                for (int pi = 0; pi < S::TC_PAGES; ++pi)
+                  if (valid[pi])
+#pragma unroll
+                    for (int h = 0; h < S::TC_HALVES; ++h)
+                      tma_load_2d(tcr + (size_t)s * S::TC_TILE + h * (S::TC_TILE / S::TC_HALVES) + pi * (S::TC_ROWS * 128),
+                                  &a.tmap_k, h * 64, (pi == 0 ? page : page2) * S::TC_ROWS, &full[s], pol);
               } else {
-                set_error(a.status, TS_ERR_PAGE_OOB);
                 mbar_arrive(&full[s]);
               }
               ++u;
@@ -1424,8 +1454,29 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
 #pragma unroll
                   for (int k = 1; k < kScanClaim; ++k)
                     if (j == k) pj = pid[k];
-                  if (ok && cur + j < sm.ptot) ok = put(cur + j, cur + j >= split ? b1 : b0, pj);
+                  if (ok && cur + j < sm.ptot) ok = put(cur + j, cur + j >= split ? b1 : b0, pj, kNoPage);
                 }
+              }
+            } else if constexpr (S::TC_PAGES == 2) {
+              // my range in tiles of two pages of the same sequence (one where a sequence ends); the
+              // next tile's page ids load while the current one is put
+              int sg = 0;
+              auto ids = [&](int g0, int& b, int& i0, int& i1) {
+                while (sg + 1 < sm.nseg && g0 >= sm.seg_pend[sg]) ++sg;
+                b = sm.seg_b[sg];
+                i0 = a.page_table[(size_t)b * a.pt_stride + (g0 - sm.seq[b].pg0)];
+                i1 = (g0 + 1 < sm.p1 && g0 + 1 < sm.seg_pend[sg])
+                         ? a.page_table[(size_t)b * a.pt_stride + (g0 + 1 - sm.seq[b].pg0)]
+                         : kNoPage;
+              };
+              int gp = sm.p0, nb = 0, n0 = 0, n1 = kNoPage;
+              if (gp < sm.p1) ids(gp, nb, n0, n1);
+              #pragma unroll 1
+              while (ok && gp < sm.p1) {
+                const int cg = gp, cb = nb, c0 = n0, c1 = n1;
+                gp += c1 != kNoPage ? 2 : 1;
+                if (gp < sm.p1) ids(gp, nb, n0, n1);
+                ok = put(cg, cb, c0, c1);
               }
             } else {
               // my range, eight pages at a time; the next eight page ids load while the ring takes
@@ -1460,7 +1511,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
                       pj = pid[k];
                       bj = pb[k];
                     }
-                  if (ok && gp0 + j < sm.p1) ok = put(gp0 + j, bj, pj);
+                  if (ok && gp0 + j < sm.p1) ok = put(gp0 + j, bj, pj, kNoPage);
                 }
               }
             }
@@ -1493,16 +1544,19 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
               }
               tc_fence_after();
               const int nv = sm.stage_nv[s][0];
-              sm.acc_nv[buf] = nv;
+              const int nv2 = S::TC_PAGES == 2 ? sm.stage_nv[s][1] : 0;
+              sm.acc_nv[buf][0] = nv;
+              sm.acc_nv[buf][1] = nv2;
               if (nv < 0) {                // end of the stream, forwarded to the epilogue
                 umma_commit(&accf[buf]);
                 mbar_arrive(&accf[buf]);
                 break;
               }
               const int sgi = sm.tc_img_of[sm.stage_b[s][0]];
-              sm.acc_tl[buf] = sm.stage_tok[s][0];
+              sm.acc_tl[buf][0] = sm.stage_tok[s][0];
+              sm.acc_tl[buf][1] = sm.stage_tok[s][1];
               sm.acc_sg[buf] = sgi;
-              if (nv > 0) {
+              if (nv > 0 || nv2 > 0) {
                 const uint32_t a0 = smem_addr(tcr + (size_t)s * S::TC_TILE);
                 const uint32_t b0 = smem_addr(tcb + (size_t)sgi * S::TC_BIMG);
 #pragma unroll
@@ -1518,21 +1572,26 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
             }
             umma_commit(&drainb);
           }
-        } else if (warp >= 4 && warp < 8) {                      // epilogue: thread = row (head g, slot t)
-          const int q4 = warp & 3, row = q4 * 32 + lane, g = row >> 4, t = row & 15;
+        } else if (warp >= 4 && warp < 8) {                      // epilogue: thread = row (page, head g, slot t)
+          const int q4 = warp & 3, row = q4 * 32 + lane;
+          const int half = S::TC_PAGES == 2 ? (q4 >> 1) : 0;    // the page of the tile
+          const int prow = row - half * S::TC_ROWS, g = prow >> 4, t = prow & 15;
           const bool odd = (g & 1) != 0;                         // second KV head of the warp's columns
-          const uint32_t tq = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(6 * G * q4);
+          const int cb = q4 % (HKV / 2);                         // the warp's pair of KV heads
+          const uint32_t tq = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(6 * G * cb);
           float run_m[G];
           KahanF run_z[G];
           int cur = -1;
           // the partials of (image, head): the 16 rows of KV head g are 16 lanes of this warp; images
           // this CTA never meets stay (-inf, 0)
-          float2* pt = a.partials + (size_t)c * H + g * G;        // + sequence * nCTA * H + j
+          // (each tile half has its own partial row: the vote pass merges the PV rows of every CTA)
+          float2* pt = a.partials + ((size_t)c * S::PV + half) * H + g * G;   // + sequence * nCTA * PV * H + j
           if (t == 0)
             #pragma unroll 1
             for (int im = 0; im < sm.tc_nimg; ++im)
 #pragma unroll
-              for (int j = 0; j < G; ++j) pt[(size_t)sm.tc_seq[im] * nCTA * H + j] = make_float2(-INFINITY, 0.f);
+              for (int j = 0; j < G; ++j)
+                pt[(size_t)sm.tc_seq[im] * nCTA * S::PV * H + j] = make_float2(-INFINITY, 0.f);
           auto flush = [&]() {                                   // whole warp (cur is uniform)
             if (cur < 0) return;
 #pragma unroll
@@ -1550,7 +1609,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
                 z = sum;
                 zl = (zl + ol) + err;
               }
-              if (t == 0) pt[(size_t)sm.tc_seq[cur] * nCTA * H + j] = make_float2(m, z + zl);
+              if (t == 0) pt[(size_t)sm.tc_seq[cur] * nCTA * S::PV * H + j] = make_float2(m, z + zl);
             }
           };
           #pragma unroll 1
@@ -1564,9 +1623,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
               break;
             }
             tc_fence_after();
-            const int nv = sm.acc_nv[buf];
-            if (nv < 0) break;
-            const int tl = sm.acc_tl[buf], sgi = sm.acc_sg[buf];
+            if (sm.acc_nv[buf][0] < 0) break;
+            const int tl = sm.acc_tl[buf][half], sgi = sm.acc_sg[buf], nvh = sm.acc_nv[buf][half];
             float r[8 * S::TC_NLD];
 #pragma unroll
             for (int i = 0; i < S::TC_NLD; ++i)
@@ -1591,14 +1649,17 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
               const float lo = odd ? r[3 * G + 3 * j + 2] : r[3 * j + 2];
               // one rounding of the scaled dot product, with the scale constant in two parts
               const float acc = (lo + mid) + hi;
-              x[j] = t < nv ? fmaf(acc, a.scale_l2, acc * a.scale_l2_lo) : -INFINITY;
+              x[j] = t < nvh ? fmaf(acc, a.scale_l2, acc * a.scale_l2_lo) : -INFINITY;
             }
+            // (the rows of an absent second page belong to no token of this tile: nothing to store)
             float* dst = a.spill + (size_t)(tl + t) * H + g * G;
-            if constexpr (G == 4) {
-              *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
-            } else {
+            if (nvh != kAbsentRows) {
+              if constexpr (G == 4) {
+                *reinterpret_cast<float4*>(dst) = make_float4(x[0], x[1], x[2], x[3]);
+              } else {
 #pragma unroll
-              for (int j = 0; j < G; ++j) dst[j] = x[j];
+                for (int j = 0; j < G; ++j) dst[j] = x[j];
+              }
             }
 #pragma unroll
             for (int j = 0; j < G; ++j) {
@@ -2647,10 +2708,10 @@ __global__ void __launch_bounds__(StepShape<KT, D, HKV, G>::THREADS, 1) step_ker
 
 // ------------------------------------------------------------------- launch
 
-// Tensor map of a bf16 K pool seen as [num_pages * 128 rows][d]: boxes of 64 elements x 128 rows
-// (one page), 128-byte swizzle. The encoder comes from the driver through the runtime, so the
+// Tensor map of a bf16 K pool seen as [num_pages * rows][d], rows = H_kv x 16 (one page of every
+// KV head): boxes of 64 elements x `rows` rows (one page), 128-byte swizzle. The encoder comes from the driver through the runtime, so the
 // library needs no link against the driver library. False when it cannot be encoded.
-bool encode_kmap(CUtensorMap* map, const void* k_pool, int64_t num_pages, int d) {
+bool encode_kmap(CUtensorMap* map, const void* k_pool, int64_t num_pages, int d, int rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static bool looked = false;
   if (!looked) {
@@ -2663,11 +2724,11 @@ bool encode_kmap(CUtensorMap* map, const void* k_pool, int64_t num_pages, int d)
       encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   if (!encode || (reinterpret_cast<uintptr_t>(k_pool) & 15) != 0 || num_pages <= 0 ||
-      num_pages * 128 > (int64_t)0x7fffffff)
+      num_pages * rows > (int64_t)0x7fffffff)
     return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)num_pages * 128};
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)num_pages * rows};
   const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, (cuuint32_t)rows};
   const cuuint32_t estr[2] = {1, 1};
   return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(k_pool), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -2707,7 +2768,7 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   // per-warp reductions; the merge one (sequence, head)'s CTA rows)
   if (nslot < S::MIN_SLOTS || dyn - flag_cap < lvl_bins(0) * 12 || dyn - flag_cap < kCandCap * 8 ||
       dyn - flag_cap < kMaxB * 128 * 12 ||
-      dyn - flag_cap < kMaxB * kMaxWaveHeads * 8 + ctx->num_sms * ctx->cfg.n_q_heads * 8 + 2 * 16 * 32 * 4 + 16 +
+      dyn - flag_cap < kMaxB * kMaxWaveHeads * 8 + ctx->num_sms * S::PV * ctx->cfg.n_q_heads * 8 + 2 * 16 * 32 * 4 + 16 +
                            kVoteBufs * 16 * kMaxWaveHeads * 4 ||   // vote scratch, then the chunks of 16 logit rows
       dyn < ctx->num_sms * (D * 4 + 8 + 4) + 8 + 16 + S::THREADS * 16)   // the merge's rows, pairs, weights
     return TS_ERR_UNSUPPORTED;
@@ -2806,7 +2867,7 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
         hitc = ctx->kmap_next;
         ctx->kmap_next = (ctx->kmap_next + 1) % (int)(sizeof(cache) / sizeof(cache[0]));
         cache[hitc].pool = nullptr;
-        if (encode_kmap(reinterpret_cast<CUtensorMap*>(cache[hitc].map), c.k_pool, cfg.num_pages, D)) {
+        if (encode_kmap(reinterpret_cast<CUtensorMap*>(cache[hitc].map), c.k_pool, cfg.num_pages, D, S::TC_ROWS)) {
           cache[hitc].pool = c.k_pool;
           cache[hitc].num_pages = cfg.num_pages;
         }
@@ -2819,7 +2880,7 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
         // each scanning its own range (TOKENSELECT_SCAN_CLAIM=1 at context creation). Faster where
         // bandwidth differs between SMs, but which CTA sums which pages then varies, so repeated
         // runs may differ in the last bits.
-        a.scan_dyn = ctx->scan_claim ? 1 : 0;
+        a.scan_dyn = (ctx->scan_claim && S::TC_PAGES == 1) ? 1 : 0;   // tiles of one page only
       }
     }
   }
