@@ -434,6 +434,7 @@ struct SeqState {        // per sequence, identical in every CTA
   unsigned long long mass_rem;
   int ties;                        // ties to take in tie mode
   int first_cta, last_cta;         // CTAs whose page range covers the sequence
+  int fx_base, fx_stride;          // CTAs fx_base .. + fx_stride - 1 share its fixed attention tokens
   int pg0, pg1;                    // its pages in the concatenated scan space
 };
 
@@ -775,7 +776,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
 
   // ------------------------------------------------ setup: lengths, cache test, partition
   // one round of independent loads per sequence: length, cache entry state
-  const bool have_cache = a.ct != nullptr && a.filled != nullptr;
+  // (a cache entry matters only when a hit is possible: a cache test, or hits given by the caller)
+  const bool have_cache = a.ct != nullptr && a.filled != nullptr && ((a.phases & kPhCheck) || a.hit_in != nullptr);
   #pragma unroll 1
   for (int b = tid; b < B; b += blockDim.x) {
     int n = a.seq_lens[b];
@@ -1053,15 +1055,31 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     sm.spill_ok = (int64_t)nCTA * sm.region <= a.spill_floats && sm.tok_stride <= a.flag_cap &&
                   hpw * G <= kMaxWaveHeads;
     sm.flag = 0;
-    // attention: how many fixed tokens (round-robin share) of every sequence are mine
+    // attention: how many fixed tokens of every sequence are mine. A scanned sequence's fixed
+    // tokens go round-robin over the CTAs that hold its pages (they attend its selected tokens
+    // anyway), so a CTA attends only the sequences of its own range; hits, and top-p (whose
+    // selected tokens are shared out over every CTA), use every CTA
+    // (a batch of top-k sequences instead gives every sequence its own group of CTAs, which
+    // shares out its fixed and selected tokens evenly: attend_grouped below)
+    const bool sel_att = (a.phases & kPhSelect) && (a.phases & kPhAttend);
+    const bool bal_mode = a.mode == TS_SELECT_TOPP && sel_att;
+    const bool grp_mode = a.mode == TS_SELECT_TOPK && sel_att && B > 1 && ptot > 0;
     int tot = 0;
     #pragma unroll 1
     for (int b = 0; b < B; ++b) {
-      const SeqState& st = sm.seq[b];
+      SeqState& st = sm.seq[b];
       int nfix = st.s_end + (st.n - st.ls);
       if (st.hit && a.ct) nfix += sm.ct_hi[b] - sm.ct_lo[b];
+      const bool ranged = !bal_mode && st.pg1 > st.pg0;
+      st.fx_base = ranged ? st.first_cta : 0;
+      st.fx_stride = ranged ? st.last_cta - st.first_cta + 1 : nCTA;
+      if (grp_mode) {
+        st.fx_base = (int)((int64_t)b * nCTA / B);
+        st.fx_stride = (int)((int64_t)(b + 1) * nCTA / B) - st.fx_base;
+      }
+      const int rel = c - st.fx_base;
       sm.pf_off[b] = tot;
-      tot += c < nfix ? (nfix - c + nCTA - 1) / nCTA : 0;
+      tot += (rel >= 0 && rel < st.fx_stride && rel < nfix) ? (nfix - rel + st.fx_stride - 1) / st.fx_stride : 0;
     }
     sm.pf_off[B] = tot;
     sm.pf_ok = (a.phases & kPhAttend) && (a.phases & kPhSelect) && tot <= kPreFix;
@@ -1096,7 +1114,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         int b = 0;
         while (b + 1 < B && sm.pf_off[b + 1] <= i) ++b;
         const SeqState& st = sm.seq[b];
-        const int f = c + (i - sm.pf_off[b]) * nCTA;
+        const int f = (c - st.fx_base) + (i - sm.pf_off[b]) * st.fx_stride;
         const int nmid = (st.hit && a.ct) ? sm.ct_hi[b] - sm.ct_lo[b] : 0;
         int t;
         if (f < st.s_end) {
@@ -2200,7 +2218,14 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
   // every CTA takes an equal share of each sequence's selected tokens (the CTAs' lists in
   // order, a fixed assignment) instead of its own
   const bool bal = a.mode == TS_SELECT_TOPP && (a.phases & kPhSelect) && (a.phases & kPhAttend) && sm.ptot > 0;
-  if (bal && !grid_sync(a.gsync, a.status, &sm.gepoch, a.wait_ns, a.skip_cta, a.skip_barrier)) return;
+  // A batch of top-k sequences: sequence b's fixed and selected tokens are shared out evenly over
+  // its group of CTAs [fx_base, fx_base + fx_stride), so that short sequences (few CTAs hold their
+  // pages) do not load a few CTAs with every one of their tokens
+  const bool attend_grouped = a.mode == TS_SELECT_TOPK && (a.phases & kPhSelect) && (a.phases & kPhAttend) &&
+                              B > 1 && sm.ptot > 0;
+  if ((bal || attend_grouped) && !grid_sync(a.gsync, a.status, &sm.gepoch, a.wait_ns, a.skip_cta, a.skip_barrier))
+    return;
+  const bool shared_lists = bal || attend_grouped;   // selected tokens read from every CTA's list
   // ======================================================================== ATTEND
   // My tokens per sequence: a round-robin share of the fixed ones (sinks and
   // window, the cached part of a hit, or the caller's index list) and my own
@@ -2253,10 +2278,12 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       }
       const int nmid = ct_hi - ct_lo;
       const int sgi = sm.my_seg_of[b];
-      const bool own = !given && !st.hit && (bal ? st.pg1 > st.pg0 : sgi >= 0);
-      int own_nc = own && !bal ? sm.sel_c[sgi] : 0, own_s0 = 0;
-      const int* own_lst = own && !bal ? sel_list + sm.seg_t0[sgi] + sm.sel_lo[sgi] : nullptr;
-      if (own && bal) {
+      const bool in_group = c >= st.fx_base && c < st.fx_base + st.fx_stride;
+      const bool own = !given && !st.hit &&
+                       (bal ? st.pg1 > st.pg0 : (attend_grouped ? (st.pg1 > st.pg0 && in_group) : sgi >= 0));
+      int own_nc = own && !shared_lists ? sm.sel_c[sgi] : 0, own_s0 = 0;
+      const int* own_lst = own && !shared_lists ? sel_list + sm.seg_t0[sgi] + sm.sel_lo[sgi] : nullptr;
+      if (own && shared_lists) {
         // the sequence's CTAs' counts of selected tokens in [s_end, ls): prefix offsets, and my share
         int tot = 0;
         #pragma unroll 1
@@ -2274,12 +2301,24 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           tot += t_;
         }
         if (tid == 0) sm.bal.pref[nCTA] = tot;
-        own_s0 = (int)((int64_t)c * tot / nCTA);
-        own_nc = (int)((int64_t)(c + 1) * tot / nCTA) - own_s0;
+        // my equal share: of every CTA (top-p), or of the sequence's group
+        const int sh0 = bal ? 0 : st.fx_base, shn = bal ? nCTA : st.fx_stride;
+        own_s0 = (int)((int64_t)(c - sh0) * tot / shn);
+        own_nc = (int)((int64_t)(c - sh0 + 1) * tot / shn) - own_s0;
         __syncthreads();
       }
       const int own_lp0 = own ? sm.seg_lp0[sgi] : 0, own_t0 = own ? sm.seg_t0[sgi] : 0;
-      const int nfix_mine = c < nfix ? (nfix - c + nCTA - 1) / nCTA : 0;
+      const int fstride = given ? nCTA : st.fx_stride;
+      const int fbase = given ? 0 : st.fx_base;
+      const int nfix_mine = (c - fbase >= 0 && c - fbase < fstride && c - fbase < nfix)
+                                ? (nfix - (c - fbase) + fstride - 1) / fstride
+                                : 0;
+      if (!own && nfix_mine == 0) {
+        // nothing of this sequence here: an empty partial (the merge gives it weight 0)
+        if (tid < HQ) aml[((size_t)b * H + tid) * nCTAp + c] = make_float2(-INFINITY, 0.f);
+        fence_proxy_async_global();
+        continue;
+      }
       float qreg[S::GP][EPL];
 #pragma unroll
       for (int h = 0; h < S::GP; ++h)
@@ -2331,7 +2370,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
             t = sm.pf_t[sm.pf_off[b] + fdone + i];
             page = sm.pf_p[sm.pf_off[b] + fdone + i];
           } else {
-            const int f = c + (fdone + i) * nCTA;
+            const int f = (c - fbase) + (fdone + i) * fstride;
             if (given) t = gib[f];
             else if (f < st.s_end) t = f;
             else if (f < st.s_end + nmid) t = __ldcg(ctb + ct_lo + (f - st.s_end));
@@ -2355,7 +2394,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           #pragma unroll 1
           for (int r = tid; r < take; r += blockDim.x) {
             int t, page;
-            if (bal) {
+            if (shared_lists) {
               // position p of the sequence's concatenated lists: the CTA cc whose offsets hold it
               const int p = own_s0 + opos + r;
               int lo = st.first_cta, hi = st.last_cta;
