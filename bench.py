@@ -446,55 +446,72 @@ class DecodeBench:
         return rec
 
     def e2e(self, steps):
-        """The same decode steps through the public call with host buffers: every step
-        copies its queries and lengths (one packed block) and the new token's K/V rows from
-        pinned host memory, runs ts_decode_step per layer, and reads the attention output back."""
+        """The same decode steps through the public calls with host buffers: every step copies one
+        packed pinned block (the queries of every layer, the lengths, and the new token's K/V rows
+        of every layer and sequence) to the device, appends the K/V rows to the paged pools
+        (ts_append_kv), runs ts_decode_step per layer, and reads every layer's attention output
+        back in one copy."""
         torch, T = self.torch, self.T
         wl, sp = self.wl, self.sp
-        L, B = sp.layers, sp.batch
+        L, B, H, Hkv, d = sp.layers, sp.batch, sp.n_q_heads, sp.n_kv_heads, sp.head_dim
         P = sp.page_size
-        # per step, the queries of every layer and the lengths packed as the device block is
-        in_host = []
-        for t in range(sp.steps):
-            blk = torch.cat([wl.q[t][l].reshape(-1).cpu().view(torch.int32) for l in range(L)] +
-                            [self.seq_all[t].cpu()])
-            in_host.append(blk.pin_memory())
+        kvb = 2 if sp.kv_dtype == "bf16" else 4
+        nq, nkv = L * B * H * d * 4, L * B * Hkv * d * kvb
+
+        def up16(x):
+            return (x + 15) // 16 * 16
+        o_seq = nq
+        o_k = up16(o_seq + B * 4)
+        o_v = up16(o_k + nkv)
+        size = up16(o_v + nkv)
+        dev = wl.page_table.device
+        blk_dev = torch.zeros(size, dtype=torch.uint8, device=dev)
+        q_dev = blk_dev[:nq].view(torch.float32).view(L, B, H, d)
+        seq_dev = blk_dev[o_seq:o_seq + B * 4].view(torch.int32)
+        kdt = torch.bfloat16 if kvb == 2 else torch.float32
+        k_dev = blk_dev[o_k:o_k + nkv].view(kdt).view(L, B, Hkv, d)
+        v_dev = blk_dev[o_v:o_v + nkv].view(kdt).view(L, B, Hkv, d)
         pt_host = wl.page_table.cpu()
-        kv_host = []
+        blocks = []
         for t in range(sp.steps):
-            per = []
+            h = torch.zeros(size, dtype=torch.uint8)
+            h[:nq] = torch.stack([wl.q[t][l].cpu() for l in range(L)]).reshape(-1).view(torch.uint8)
+            h[o_seq:o_seq + B * 4] = self.seq_all[t].cpu().view(torch.uint8)
+            ks, vs = [], []
             for l in range(L):
                 for b in range(B):
-                    pos = wl.n0[b] + t - 1
+                    pos = wl.n0[b] + t - 1           # the current token: the last cached position
                     page, slot = int(pt_host[b, pos // P]), pos % P
-                    per.append((l, page, slot, wl.k_pool[l][page, :, slot, :].cpu().pin_memory(),
-                                wl.v_pool[l][page, :, slot, :].cpu().pin_memory()))
-            kv_host.append(per)
-        out_host = [torch.empty(B, sp.n_q_heads, sp.head_dim).pin_memory() for _ in range(L)]
+                    ks.append(wl.k_pool[l][page, :, slot, :].cpu())
+                    vs.append(wl.v_pool[l][page, :, slot, :].cpu())
+            h[o_k:o_k + nkv] = torch.stack(ks).reshape(-1).view(torch.uint8)
+            h[o_v:o_v + nkv] = torch.stack(vs).reshape(-1).view(torch.uint8)
+            blocks.append(h.pin_memory())
+        out_dev = torch.zeros(L, B, H, d, device=dev)
+        out_host = torch.empty(L, B, H, d).pin_memory()
+        ctxh, cacheh = self.ctx.handle, self.cache.handle
         self.cache.reset()
         torch.cuda.synchronize()
-        h2d = d2h = 0
         t0 = time.perf_counter()
         for i in range(steps):
             t = i % sp.steps
             if t == 0:
                 self.cache.reset()
-            self.in_buf.copy_(in_host[t], non_blocking=True)
-            h2d = in_host[t].numel() * 4
-            for (l, page, slot, kr, vr) in kv_host[t]:
-                wl.k_pool[l][page, :, slot, :].copy_(kr, non_blocking=True)
-                wl.v_pool[l][page, :, slot, :].copy_(vr, non_blocking=True)
-                h2d += kr.numel() * kr.element_size() * 2
+            blk_dev.copy_(blocks[t], non_blocking=True)
             for l in range(L):
-                self._launch(l)
-            d2h = 0
-            for l in range(L):
-                out_host[l].copy_(self.out[l], non_blocking=True)
-                d2h += out_host[l].numel() * 4
+                T.ts_append_kv(ctxh, k_dev[l], v_dev[l], wl.page_table, seq_dev, B, wl.k_pool[l], wl.v_pool[l])
+                T.ts_decode_step(ctxh, cacheh, l, q_dev[l], wl.k_pool[l], wl.v_pool[l], wl.page_table, seq_dev, B,
+                                 self.params, None, 0, self.idx[l], self.idx[l].stride(0), self.count[l],
+                                 out_dev[l], self.lse[l], self.hit[l])
+            out_host.copy_(out_dev, non_blocking=True)
             torch.cuda.synchronize()
         wall = time.perf_counter() - t0
-        return dict(value=steps / wall, unit=UNIT, h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
-                    steps=steps, note="ts_decode_step per layer, host buffers pinned, no graph")
+        st = T.ts_get_status(ctxh)
+        if st != 0:
+            raise RuntimeError(f"device status {T.STATUS.get(st, st)}")
+        return dict(value=steps / wall, unit=UNIT, h2d_bytes_per_step=size, d2h_bytes_per_step=out_host.numel() * 4,
+                    steps=steps, note="per step: one packed pinned H2D copy (queries, lengths, new K/V rows), "
+                                      "ts_append_kv and ts_decode_step per layer, one D2H copy of the outputs; no graph")
 
 
 def summarise(bench, rec, peak_gbs):

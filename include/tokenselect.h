@@ -223,6 +223,16 @@ ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q
                          float* vote, int64_t vote_stride, int32_t* idx, int64_t idx_stride,
                          int32_t* count, float* out, float* lse, uint8_t* hit, void* stream);
 
+/* Appends the current token's K and V rows to the paged pools before a
+ * decode step (the harness step of reading R9: the current token is the last
+ * cached position). For each b, k_new / v_new [B][H_kv][d] (device, kv_dtype
+ * elements, 16-byte aligned) are written to pool[page][g][slot] of position
+ * seq_lens[b] - 1, page = page_table[b][(seq_lens[b] - 1) / page_size]. A
+ * length outside [1, max tokens] records TS_ERR_SEQ_LEN, a page outside the
+ * pool TS_ERR_PAGE_OOB (nothing is written for that sequence). */
+ts_status ts_append_kv(ts_ctx* ctx, const void* k_new, const void* v_new, const int32_t* page_table,
+                       const int32_t* seq_lens, int B, void* k_pool, void* v_pool, void* stream);
+
 /* Block-level selection, the granularity the method argues against
  * (TokenSelect review, figure 2(b): InfLLM-style methods keep or drop whole
  * blocks; granularity 1 is token-level selection). From the votes of each

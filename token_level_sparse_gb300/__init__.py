@@ -19,7 +19,7 @@ __all__ = [
     "TokenSelectError", "Config", "SelectParams", "library", "library_path",
     "TS_KV_F32", "TS_KV_BF16", "TS_SELECT_TOPK", "TS_SELECT_TOPP", "STATUS",
     "TS_SCORE_HEAD_SOFT_VOTE", "TS_SCORE_LOGIT_SUM", "TS_SCORE_HEAD_HARD_VOTE", "ts_score_fn",
-    "ts_prefill_chunk", "ts_select_blocks",
+    "ts_prefill_chunk", "ts_select_blocks", "ts_append_kv",
     "ts_create", "ts_destroy", "ts_cache_create", "ts_cache_destroy", "ts_cache_reset",
     "ts_cache_check", "ts_score", "ts_select", "ts_sparse_attend", "ts_decode_step",
     "ts_get_status", "ts_status_str", "ts_version", "ts_profile_enable", "ts_profile_read",
@@ -87,6 +87,7 @@ _SIGS = {
                                c_void_p, c_int, POINTER(SelectParams), c_void_p, c_int64, c_void_p,
                                c_int64, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     "ts_get_status": (c_int, [c_void_p, POINTER(c_int), c_void_p]),
+    "ts_append_kv": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p]),
     "ts_select_blocks": (c_int, [c_void_p, c_void_p, c_int64, c_void_p, c_int, c_int, c_int, c_void_p, c_int64,
                                  c_void_p, c_void_p]),
     "ts_prefill_chunk": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
@@ -248,6 +249,11 @@ def ts_select_blocks(ctx, vote, vote_stride, seq_lens, B, block, budget, idx, id
                                       idx_stride, _p(count), _s(stream)), "ts_select_blocks")
 
 
+def ts_append_kv(ctx, k_new, v_new, page_table, seq_lens, B, k_pool, v_pool, stream=None) -> None:
+    _check(library().ts_append_kv(ctx, _p(k_new), _p(v_new), _p(page_table), _p(seq_lens), B, _p(k_pool),
+                                  _p(v_pool), _s(stream)), "ts_append_kv")
+
+
 def ts_set_wait_limit(ctx, ns: int) -> None:
     _check(library().ts_set_wait_limit(ctx, int(ns)), "ts_set_wait_limit")
 
@@ -333,6 +339,10 @@ class Context:
         """q [B][c][H][d]: one selection from the chunk's mean query, causal attention of every query."""
         ts_prefill_chunk(self.handle, q, q.shape[1], k_pool, v_pool, page_table, seq_lens, q.shape[0], params,
                          vote, vote.stride(0) if vote is not None else 0, idx, idx.stride(0), count, out, lse, stream)
+
+    def append_kv(self, k_new, v_new, page_table, seq_lens, k_pool, v_pool, stream=None):
+        """k_new / v_new [B][H_kv][d]: the current token's rows into position seq_lens[b] - 1."""
+        ts_append_kv(self.handle, k_new, v_new, page_table, seq_lens, seq_lens.shape[0], k_pool, v_pool, stream)
 
     def select_blocks(self, vote, seq_lens, block, budget, idx, count, stream=None):
         ts_select_blocks(self.handle, vote, vote.stride(0), seq_lens, seq_lens.shape[0], block, budget, idx,

@@ -428,6 +428,15 @@ ts_status ts_prefill_chunk(ts_ctx* ctx, const float* q, int c, const void* k_poo
   return launch_chunk_attend(ctx, ac, s);
 }
 
+ts_status ts_append_kv(ts_ctx* ctx, const void* k_new, const void* v_new, const int32_t* page_table,
+                       const int32_t* seq_lens, int B, void* k_pool, void* v_pool, void* stream) {
+  if (!ctx || !k_new || !v_new || !page_table || !seq_lens || !k_pool || !v_pool) return TS_ERR_INVALID_ARG;
+  if (B < 1 || B > ctx->cfg.max_batch) return TS_ERR_SHAPE;
+  for (const void* p : {k_new, v_new, static_cast<const void*>(k_pool), static_cast<const void*>(v_pool)})
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0) return TS_ERR_INVALID_ARG;
+  return launch_append_kv(ctx, k_new, v_new, page_table, seq_lens, B, k_pool, v_pool, as_stream(stream));
+}
+
 ts_status ts_select_blocks(ts_ctx* ctx, const float* vote, int64_t vote_stride, const int32_t* seq_lens, int B,
                            int block, int budget, int32_t* idx, int64_t idx_stride, int32_t* count, void* stream) {
   if (!ctx || !vote || !seq_lens || !idx || !count) return TS_ERR_INVALID_ARG;

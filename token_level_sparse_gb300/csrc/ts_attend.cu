@@ -297,6 +297,52 @@ ts_status launch_attend(ts_ctx* ctx, const AttendCall& a, cudaStream_t s) {
 // counters (kCounterSlots per sequence) and a fallback status slot,
 // [16 KiB, end) split partials.
 
+namespace ts {
+namespace {
+
+// The new token of each sequence (its last cached position, seq_lens[b] - 1) into the paged
+// pools: rows k_new / v_new [B][H_kv][d] (element bytes es) to pool[page][g][slot][:], one
+// 16-byte chunk per thread.
+__global__ void append_kv_kernel(const unsigned char* k_new, const unsigned char* v_new, const int32_t* page_table,
+                                 int pt_stride, const int32_t* seq_lens, int max_tokens, int64_t num_pages, int HKV,
+                                 int row_bytes, unsigned char* k_pool, unsigned char* v_pool, int* status) {
+  const int b = blockIdx.x;
+  const int n = seq_lens[b];
+  if (n < 1 || n > max_tokens) {
+    if (threadIdx.x == 0) set_error(status, TS_ERR_SEQ_LEN);
+    return;
+  }
+  const int t = n - 1;
+  const int page = page_table[(size_t)b * pt_stride + t / kPage];
+  if (page < 0 || (int64_t)page >= num_pages) {
+    if (threadIdx.x == 0) set_error(status, TS_ERR_PAGE_OOB);
+    return;
+  }
+  const int cpr = row_bytes / 16;
+  for (int i = threadIdx.x; i < 2 * HKV * cpr; i += blockDim.x) {
+    const int isv = i / (HKV * cpr), rem = i % (HKV * cpr), g = rem / cpr, ch = rem % cpr;
+    const unsigned char* src = (isv ? v_new : k_new) + ((size_t)b * HKV + g) * row_bytes + ch * 16;
+    unsigned char* dst = (isv ? v_pool : k_pool) + (((size_t)page * HKV + g) * kPage + t % kPage) * row_bytes + ch * 16;
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+  }
+}
+
+}  // namespace
+
+ts_status launch_append_kv(ts_ctx* ctx, const void* k_new, const void* v_new, const int32_t* page_table,
+                           const int32_t* seq_lens, int B, void* k_pool, void* v_pool, cudaStream_t s) {
+  const ts_config& c = ctx->cfg;
+  const int row_bytes = c.head_dim * (c.kv_dtype == TS_KV_BF16 ? 2 : 4);
+  ctx->kernels += 1;
+  append_kv_kernel<<<B, 128, 0, s>>>(static_cast<const unsigned char*>(k_new), static_cast<const unsigned char*>(v_new),
+                                     page_table, c.max_pages_per_seq, seq_lens, ctx->max_tokens, c.num_pages,
+                                     c.n_kv_heads, row_bytes, static_cast<unsigned char*>(k_pool),
+                                     static_cast<unsigned char*>(v_pool), ctx->status);
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace ts
+
 #include <cmath>
 #include <mutex>
 

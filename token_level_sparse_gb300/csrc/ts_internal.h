@@ -222,6 +222,8 @@ ts_status launch_score(ts_ctx* ctx, const ScoreCall& a, cudaStream_t s);
 ts_status launch_select(ts_ctx* ctx, const SelectCall& a, cudaStream_t s);
 ts_status launch_attend(ts_ctx* ctx, const AttendCall& a, cudaStream_t s);
 bool chunk_attend_supported(const ts_config& c);
+ts_status launch_append_kv(ts_ctx* ctx, const void* k_new, const void* v_new, const int32_t* page_table,
+                           const int32_t* seq_lens, int B, void* k_pool, void* v_pool, cudaStream_t s);
 ts_status launch_select_blocks(ts_ctx* ctx, const float* vote, int64_t vote_stride, const int32_t* seq_lens, int B,
                                int block, int budget, int32_t* idx, int64_t idx_stride, int32_t* count,
                                cudaStream_t s);
