@@ -254,16 +254,18 @@ def step_source_sha256() -> str:
     return h.hexdigest()
 
 
-def step_traffic():
-    """Per-launch DRAM bytes of the persistent step kernel at 128K (miss step) from the
-    committed ncu summary, or None when absent or taken on another kernel revision."""
+def step_traffic(tag="n128k"):
+    """Per-launch DRAM bytes of the persistent step kernel on a miss step (tag n128k: the 128K
+    workload; n1m: one 1M-token layer) from the committed ncu summaries, or None when absent or
+    taken on another kernel revision."""
     sha = step_source_sha256()
     prof = os.path.join(ROOT, "profiles")
     if not os.path.isdir(prof):
         return None
     for fn in sorted(os.listdir(prof)):
         if fn.endswith(".md"):
-            m = re.search(r"step_traffic_bytes_per_launch_n128k:\s*([0-9.e+]+)\s+step_source_sha256:\s*([0-9a-f]{64})",
+            m = re.search(r"step_traffic_bytes_per_launch_" + tag +
+                          r":\s*([0-9.e+]+)\s+step_source_sha256:\s*([0-9a-f]{64})",
                           open(os.path.join(prof, fn)).read())
             if m and m.group(2) == sha:
                 return float(m.group(1))
@@ -983,7 +985,7 @@ def main(argv=None):
         # the same kernel on the 1M-token, 8-layer workload's miss steps (per-launch bytes / time)
         "roofline_n1m": ({"bound": "hbm", "achieved": extras["n1m_miss_only"]["score_gbs"], "peak": peak_gbs,
                           "unit": "GB/s", "frac": extras["n1m_miss_only"]["score_gbs"] / peak_gbs,
-                          "traffic": None, "kernel": kname,
+                          "traffic": step_traffic("n1m"), "kernel": kname,
                           "us_per_launch": extras["n1m_miss_only"].get("score_us_per_launch")}
                          if "score_gbs" in extras.get("n1m_miss_only", {}) else None),
         "gpu_launches": bench.kernels_per_step * len(rec), "kernels_per_step": bench.kernels_per_step,
