@@ -59,6 +59,7 @@ def parse_args(argv=None):
 # workload index, theta for the profiling cases
 CASES = {"n128k": (1, 0.9), "n128k-miss": (1, 2.0), "n1m-miss": (3, 2.0), "n1m-1layer-miss": ("3x1", 2.0),
          "n256k-1layer-miss": ("3x1@256k", 2.0), "qwen-b8-miss": (2, 2.0), "topp-b4": (4, 0.9),
+         "topp-b4-miss": (4, 2.0),
          "prefill-n128k-c512": ("prefill", None)}
 
 

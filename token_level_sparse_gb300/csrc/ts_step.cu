@@ -54,6 +54,7 @@ constexpr int kMaxWaveHeads = 32;  // query heads of one scan wave
 constexpr int kMaxG = kMaxScanG;   // query heads per KV head
 constexpr int kMaxAttH = 64;       // query heads of the attention phase
 constexpr int kPreFix = 512;       // fixed attention tokens of a CTA resolved at set-up
+constexpr int kOwnBatch = 1024;    // attention: selected tokens (and pages) looked up from other CTAs' lists at once
 constexpr int kMaxPagesCta = 1024; // page ids of a CTA's range kept in shared memory
 constexpr int kScanClaim = 2;      // pages per claim of a shared tensor-core scan
 constexpr int kVoteBufs = 2;       // shared-memory buffers of logit chunks for the votes
@@ -1808,11 +1809,24 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           const uint32_t key = __float_as_uint(v);
           const bool in = (key & st.mask) == st.prefix;
           const int bin = in ? (int)((key >> shift) & (nbins - 1)) : -1;
-          // lanes with the same bin add once (the votes of a sequence crowd into few bins)
-          const unsigned peers = __match_any_sync(__activemask(), bin);
+          // lanes with the same bin add once (the votes of a sequence crowd into few bins): the
+          // count by the group's size, the top-p mass by the leader's sum of the group's masses
+          // (staged in the selection-flag area, not yet in use)
+          const unsigned am = __activemask();
+          const unsigned peers = __match_any_sync(am, bin);
           const int leader = __ffs(peers) - 1;
           if (in && lane == leader) atomicAdd(&sh[bin], (unsigned)__popc(peers));
-          if (topp && in) atomicAdd(&smh[bin], to_fx(v));
+          if (topp) {
+            unsigned long long* ms = reinterpret_cast<unsigned long long*>(selflag) + warp * 32;
+            ms[lane] = in ? to_fx(v) : 0ull;
+            __syncwarp(am);
+            if (in && lane == leader) {
+              unsigned long long sum = 0ull;
+              for (unsigned pm = peers; pm; pm &= pm - 1u) sum += ms[__ffs(pm) - 1];
+              atomicAdd(&smh[bin], sum);
+            }
+            __syncwarp(am);
+          }
         }
         __syncthreads();
         TS_MARK(35 + 4 * level);
@@ -2250,7 +2264,10 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     constexpr int NG = (NGRP + S::THREADS - 1) / S::THREADS;
     static_assert(HQ <= kMaxAttH && D % 32 == 0, "attention layout");
     const bool given = !(a.phases & kPhSelect);
-    const int stage_bytes = a.dyn_bytes - a.flag_cap;
+    // the staging area ends with the batch of looked-up selected tokens and their pages
+    const int stage_bytes = a.dyn_bytes - a.flag_cap - 2 * kOwnBatch * (int)sizeof(int);
+    int* const ob_t = reinterpret_cast<int*>(dsm + stage_bytes);
+    int* const ob_p = ob_t + kOwnBatch;
     const int around = min(kMaxRound, (stage_bytes - HQ * 4) / (S::TOKEN_BYTES + HQ * 4));
     KT* Ks = reinterpret_cast<KT*>(dsm);
     KT* Vs = Ks + (size_t)around * HKV * D;
@@ -2335,6 +2352,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       for (int k = 0; k < NG; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       int fdone = 0;     // fixed tokens of mine already taken
       int opos = 0;      // next own token (position in my list)
+      int ob0 = 0, ob_end = 0;   // my share's positions [ob0, ob_end) looked up in ob_t / ob_p
       // the K and V rows of every KV head of list entries [j0, j1), 16 bytes per thread and copy
       // (all of them in flight at once), as one commit group
       auto gather_rows = [&](int j0, int j1) {
@@ -2391,12 +2409,14 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         if (own && opos < own_nc && cnt < around) {
           // my selected tokens in [s_end, ls), in list order, as many as fit
           const int take = min(around - cnt, own_nc - opos);
-          #pragma unroll 1
-          for (int r = tid; r < take; r += blockDim.x) {
-            int t, page;
-            if (shared_lists) {
-              // position p of the sequence's concatenated lists: the CTA cc whose offsets hold it
-              const int p = own_s0 + opos + r;
+          if (shared_lists && opos + take > ob_end) {
+            // the next batch of my share: every entry looked up at once (position in the sequence's
+            // concatenated lists -> the CTA whose list holds it -> the token -> its page)
+            ob0 = opos;
+            ob_end = min(own_nc, opos + kOwnBatch);
+            #pragma unroll 1
+            for (int r = tid; r < ob_end - ob0; r += blockDim.x) {
+              const int p = own_s0 + ob0 + r;
               int lo = st.first_cta, hi = st.last_cta;
               while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
@@ -2405,8 +2425,18 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
               }
               const int* lst = reinterpret_cast<const int*>(a.spill + (size_t)lo * sm.region) +
                                (max(st.pg0, lo * sm.ppc) - lo * sm.ppc) * S::P + sm.bal.nlo[lo];
-              t = __ldcg(lst + (p - sm.bal.pref[lo]));
-              page = a.page_table[(size_t)b * a.pt_stride + t / S::P];
+              const int t = __ldcg(lst + (p - sm.bal.pref[lo]));
+              ob_t[r] = t;
+              ob_p[r] = a.page_table[(size_t)b * a.pt_stride + t / S::P];
+            }
+            __syncthreads();
+          }
+          #pragma unroll 1
+          for (int r = tid; r < take; r += blockDim.x) {
+            int t, page;
+            if (shared_lists) {
+              t = ob_t[opos - ob0 + r];
+              page = ob_p[opos - ob0 + r];
             } else {
               t = own_lst[opos + r];
               const int lpg = (own_t0 + (t - own_lp0 * S::P)) / S::P;   // my page of the token
