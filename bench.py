@@ -769,6 +769,45 @@ def ablation_extra(dev, fn_name):
             "l2": "not flushed: inputs larger than L2 (268 MB of K per step)"}
 
 
+def page1_extra(dev):
+    """Miss steps of the 128K trajectory on a token-granular pool (one token per page), which
+    runs the separate kernels, beside the same separate kernels on 16-token pages."""
+    import os
+    import torch
+    import token_level_sparse_gb300 as T
+    import workloads as W
+    res = {}
+    for P in (1, 16):
+        sp = W.spec(1, steps=4, page_size=P)
+        wl = W.generate(sp, dev)
+        prev = os.environ.get("TOKENSELECT_MULTI_KERNEL")
+        os.environ["TOKENSELECT_MULTI_KERNEL"] = "1"
+        try:
+            ctx = T.Context(sp.n_q_heads, sp.n_kv_heads, sp.head_dim, T.TS_KV_BF16, 1, wl.page_table.shape[1],
+                            wl.num_pages, page_size=P)
+        finally:
+            if prev is None:
+                del os.environ["TOKENSELECT_MULTI_KERNEL"]
+            else:
+                os.environ["TOKENSELECT_MULTI_KERNEL"] = prev
+        prm = T.params(k=sp.k, n_sink=sp.n_sink, n_local=sp.n_local, theta=2.0)
+        idx = torch.zeros(1, sp.k + sp.n_sink + sp.n_local, dtype=torch.int32, device=dev)
+        cnt = torch.zeros(1, dtype=torch.int32, device=dev)
+        out = torch.zeros(1, sp.n_q_heads, sp.head_dim, device=dev)
+        seq = wl.seq_lens(0)
+        q = wl.q[0][0]
+        ms = _event_ms(lambda: ctx.decode_step(q, wl.k_pool[0], wl.v_pool[0], wl.page_table, seq, prm, idx, cnt,
+                                               out), 10, 3)
+        res[f"page_size_{P}"] = {"value": 1000.0 / ms, "unit": UNIT, "ms_per_step": ms,
+                                 "status": T.ts_get_status(ctx.handle)}
+        ctx.close()
+        del wl
+        torch.cuda.empty_cache()
+    res["path"] = "separate kernels (cache check, score, vote, select, attend), every step a miss"
+    res["l2"] = "not flushed: inputs larger than L2 (268 MB of K per step)"
+    return res
+
+
 OVERLAP_RHOS = (0.5, 0.7, 0.8, 0.85, 0.9, 0.925, 0.95, 0.975, 0.99, 0.999)
 
 
@@ -941,6 +980,7 @@ def main(argv=None):
         extras["prefill_n128k_c512"] = prefill_extra(dev, peaks)
         extras["selection_overlap_vs_cosine_n128k"] = overlap_extra(dev)
         extras["recall_vs_block_size_n128k"] = recall_extra(dev)
+        extras["token_granular_pool_n128k"] = page1_extra(dev)
         torch.cuda.empty_cache()
         for fn_name in ("logit_sum", "hard_vote"):
             extras[f"ablation_{fn_name}_n128k"] = ablation_extra(dev, fn_name)

@@ -81,7 +81,8 @@ typedef struct {
   int n_q_heads;          /* H                                                  */
   int n_kv_heads;         /* H_kv, divides H                                    */
   int head_dim;           /* d (64 or 128)                                      */
-  int page_size;          /* P tokens per page (16)                             */
+  int page_size;          /* P tokens per page: 16, or 1 for a token-granular   */
+                          /* pool (one token per page; separate kernels only)   */
   int kv_dtype;           /* TS_KV_F32 or TS_KV_BF16                            */
   int max_batch;          /* largest B of any call                              */
   int max_pages_per_seq;  /* page-table row stride; max tokens = this * P       */
@@ -209,7 +210,8 @@ ts_status ts_sparse_attend_noalloc(int n_q_heads, int n_kv_heads, int head_dim, 
  * Supported geometries run as one cooperative launch; repeated calls on the
  * same inputs give bit-identical results. params->score_fn other than the
  * head soft vote (the ablations) runs the multi-kernel path with that
- * selection function (the vote buffer then holds its scores). Environment switches, read once by
+ * selection function (the vote buffer then holds its scores); so does a
+ * context with one-token pages. Environment switches, read once by
  * ts_create (comparisons and tests): TOKENSELECT_MULTI_KERNEL=1 keeps the
  * multi-kernel path; TOKENSELECT_NO_TC=1 scans on CUDA cores instead of tensor
  * cores; TOKENSELECT_SCAN_CLAIM=1 lets the CTAs claim scan pages from a shared

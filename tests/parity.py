@@ -96,7 +96,7 @@ class GpuRunner:
         os.environ["TOKENSELECT_MULTI_KERNEL"] = "1" if multi_kernel else "0"
         try:
             self.ctx = T.Context(sp.n_q_heads, sp.n_kv_heads, sp.head_dim, kv_flag(T, sp), B,
-                                 wl.page_table.shape[1], wl.num_pages)
+                                 wl.page_table.shape[1], wl.num_pages, page_size=sp.page_size)
         finally:
             if prev is None:
                 del os.environ["TOKENSELECT_MULTI_KERNEL"]

@@ -9,13 +9,16 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
+@pytest.mark.parametrize("page_size", [16, 1])
 @pytest.mark.parametrize("cfg", [0, 2])
-def test_append_writes_the_last_position_and_nothing_else(cfg):
+def test_append_writes_the_last_position_and_nothing_else(cfg, page_size):
     T = tsl()
-    sp = W.spec(cfg, steps=2) if cfg == 0 else W.spec(2, n0=(1000, 37, 4096), n0_range=None, batch=3, steps=2)
+    sp = (W.spec(cfg, steps=2, page_size=page_size) if cfg == 0 else
+          W.spec(2, n0=(1000, 37, 4096), n0_range=None, batch=3, steps=2, page_size=page_size))
     wl = W.generate(sp, DEV)
     B, Hkv, d = sp.batch, sp.n_kv_heads, sp.head_dim
-    ctx = T.Context(sp.n_q_heads, Hkv, d, kv_flag(T, sp), B, wl.page_table.shape[1], wl.num_pages)
+    ctx = T.Context(sp.n_q_heads, Hkv, d, kv_flag(T, sp), B, wl.page_table.shape[1], wl.num_pages,
+                    page_size=sp.page_size)
     dt = wl.k_pool[0].dtype
     g = torch.Generator(device=DEV)
     g.manual_seed(5)
@@ -28,7 +31,7 @@ def test_append_writes_the_last_position_and_nothing_else(cfg):
     ek, ev = wl.k_pool[0].clone(), wl.v_pool[0].clone()
     for b in range(B):
         pos = int(seq[b]) - 1
-        page, slot = int(wl.page_table[b, pos // 16]), pos % 16
+        page, slot = int(wl.page_table[b, pos // page_size]), pos % page_size
         ek[page, :, slot, :] = k_new[b]
         ev[page, :, slot, :] = v_new[b]
     assert torch.equal(kp, ek) and torch.equal(vp, ev)

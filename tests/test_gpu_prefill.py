@@ -27,7 +27,8 @@ def _run(sp, c, check_every=1):
     T = tsl()
     wl = W.generate(sp, DEV)
     B, H, d = sp.batch, sp.n_q_heads, sp.head_dim
-    ctx = T.Context(H, sp.n_kv_heads, d, kv_flag(T, sp), B, wl.page_table.shape[1], wl.num_pages)
+    ctx = T.Context(H, sp.n_kv_heads, d, kv_flag(T, sp), B, wl.page_table.shape[1], wl.num_pages,
+                    page_size=sp.page_size)
     q = torch.stack([wl.q[i][0] for i in range(c)], dim=1).contiguous()          # [B][c][H][d]
     cap = sp.k + sp.n_sink + sp.n_local
     idx = torch.full((B, cap), -1, dtype=torch.int32, device=DEV)
@@ -120,3 +121,9 @@ def test_prefill_rejects_what_it_does_not_serve():
         ctx.prefill_chunk(q, wl.k_pool[0], wl.v_pool[0], wl.page_table, wl.seq_lens(0), T.params(k=64), idx, cnt, out)
     assert e.value.status == T.STATUS_CODE["TS_ERR_UNSUPPORTED"]
     ctx.close()
+
+
+def test_prefill_page1_pool():
+    # one token per page: the chunk's selection on the separate kernels, attention rows by token
+    sp = W.spec(1, n0=(5003,), steps=40, k=512, n_local=128, page_size=1)
+    _run(sp, 40)

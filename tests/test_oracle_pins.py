@@ -153,6 +153,30 @@ def test_page_permutation_invariance():
     assert np.array_equal(a1[0], a2[0]) and np.array_equal(a1[1], a2[1])
 
 
+def test_one_token_pages_hold_the_same_sequence():
+    # token granularity (page size 1, TokenSelect review, section 3.4): token i sits in page
+    # page_row[i], slot 0. The same logical cache in 16-token pages and in one-token pages gives
+    # the same rows, votes, selection and attention.
+    q, kp, vp, pt = _random_case(5, n=70)
+    n = 70
+    perm = np.random.default_rng(6).permutation(n + 9)[:n]          # one page per token
+    kp1 = np.zeros((n + 9, kp.shape[1], 1, kp.shape[3]))
+    vp1 = np.zeros_like(kp1)
+    for i in range(n):
+        kp1[perm[i], :, 0] = kp[pt[i // 16], :, i % 16]
+        vp1[perm[i], :, 0] = vp[pt[i // 16], :, i % 16]
+    pt1 = perm.astype(np.int32)
+    for g in range(kp.shape[1]):
+        assert np.array_equal(O.gather_rows(kp1, pt1, np.arange(n), g), O.gather_rows(kp, pt, np.arange(n), g))
+    v16 = O.soft_vote(O.head_logits(q, kp, pt, n))
+    v1 = O.soft_vote(O.head_logits(q, kp1, pt1, n))
+    assert np.array_equal(v16, v1)
+    idx = O.select_topk(v1, n, 8, 2, 5)[0]
+    a16 = O.sparse_attention(q, kp, vp, pt, idx)
+    a1 = O.sparse_attention(q, kp1, vp1, pt1, idx)
+    assert np.array_equal(a16[0], a1[0]) and np.array_equal(a16[1], a1[1])
+
+
 # ------------------------------------------------------------ invariants
 
 def test_vote_sums_to_H_and_is_positive():

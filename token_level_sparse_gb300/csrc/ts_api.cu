@@ -102,9 +102,9 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   if (c.n_q_heads < 1 || c.n_kv_heads < 1 || c.n_q_heads % c.n_kv_heads != 0) return TS_ERR_INVALID_ARG;
   if (c.max_batch < 1 || c.max_pages_per_seq < 1 || c.num_pages < 1 || c.head_dim < 1) return TS_ERR_INVALID_ARG;
   if (c.kv_dtype != TS_KV_F32 && c.kv_dtype != TS_KV_BF16) return TS_ERR_INVALID_ARG;
-  if (c.page_size != kPage) return TS_ERR_UNSUPPORTED;
+  if (c.page_size != kPage && c.page_size != 1) return TS_ERR_UNSUPPORTED;
   if (c.n_kv_heads > kCounterSlots - 2 || c.n_q_heads > 256) return TS_ERR_UNSUPPORTED;
-  if ((int64_t)c.max_pages_per_seq * kPage > (int64_t)1 << 30) return TS_ERR_SHAPE;
+  if ((int64_t)c.max_pages_per_seq * c.page_size > (int64_t)1 << 30) return TS_ERR_SHAPE;
   if (!score_supported(c)) return TS_ERR_UNSUPPORTED;
 
   ts_ctx* ctx = new (std::nothrow) ts_ctx();
@@ -113,6 +113,10 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   // environment switches, read here once (never per call):
   // TOKENSELECT_MULTI_KERNEL=1 keeps ts_decode_step on the multi-kernel path (tests, comparisons)
   if (const char* env = std::getenv("TOKENSELECT_MULTI_KERNEL")) ctx->use_step = !(env[0] == '1');
+  // the persistent kernel's TMA page tiles are 16 tokens: a token-granular pool (one token per
+  // page) takes the multi-kernel path
+  if (c.page_size != kPage) ctx->use_step = false;
+  ctx->page_shift = c.page_size == kPage ? 4 : 0;
   ctx->debug = std::getenv("TS_DEBUG") != nullptr;
   if (const char* env = std::getenv("TOKENSELECT_NO_TC")) ctx->no_tc = env[0] == '1';
   if (const char* env = std::getenv("TOKENSELECT_SCAN_CLAIM")) ctx->scan_claim = env[0] == '1';
@@ -126,8 +130,8 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
     return TS_ERR_CUDA;
   }
   const size_t B = c.max_batch, H = c.n_q_heads, HKV = c.n_kv_heads, G = H / HKV, D = c.head_dim;
-  ctx->max_tokens = c.max_pages_per_seq * kPage;
-  ctx->score_max_chunks = (c.max_pages_per_seq + kScorePagesPerCta - 1) / kScorePagesPerCta;
+  ctx->max_tokens = c.max_pages_per_seq * c.page_size;
+  ctx->score_max_chunks = (ctx->max_tokens + kScorePagesPerCta * kPage - 1) / (kScorePagesPerCta * kPage);
   ctx->sel_max_chunks = (ctx->max_tokens + kSelChunk - 1) / kSelChunk;
   ctx->attn_splits = kAttnMaxSplits;
   const size_t T = ctx->max_tokens;

@@ -48,6 +48,7 @@ struct AttKArgs {
   const unsigned char* v_pool;
   const int32_t* page_table;
   int pt_stride;
+  int page_shift;  // log2 of the page size: 4 (16 tokens) or 0 (one token per page)
   int64_t num_pages;
   int max_tokens;
   const int32_t* idx;
@@ -116,9 +117,10 @@ __global__ void __launch_bounds__(AttShape<KT, D, G>::THREADS) attend_kernel(Att
       const int j = i >> 1;
       const int t = ib[s0 + j];
       int page = -1;
-      if (t >= 0 && t < a.max_tokens) page = pt[t / kPage];
+      if (t >= 0 && t < a.max_tokens) page = pt[t >> a.page_shift];
       const bool valid = page >= 0 && (int64_t)page < a.num_pages;
-      const size_t off = valid ? (((size_t)page * a.HKV + g) * kPage + (t % kPage)) * S::ROW_BYTES : 0;
+      const int slot = t & ((1 << a.page_shift) - 1);
+      const size_t off = valid ? ((((size_t)page * a.HKV + g) << a.page_shift) + slot) * S::ROW_BYTES : 0;
       if (i & 1) {
         bulk_g2s(Vs + (size_t)j * D, a.v_pool + off, S::ROW_BYTES, &bar);
       } else {
@@ -245,6 +247,7 @@ ts_status run_attend(ts_ctx* ctx, const AttendCall& c, cudaStream_t s) {
   a.v_pool = static_cast<const unsigned char*>(c.v_pool);
   a.page_table = c.page_table;
   a.pt_stride = cfg.max_pages_per_seq;
+  a.page_shift = ctx->page_shift;
   a.num_pages = cfg.num_pages;
   a.max_tokens = ctx->max_tokens;
   a.idx = c.idx;
@@ -304,7 +307,8 @@ namespace {
 // pools: rows k_new / v_new [B][H_kv][d] (element bytes es) to pool[page][g][slot][:], one
 // 16-byte chunk per thread.
 __global__ void append_kv_kernel(const unsigned char* k_new, const unsigned char* v_new, const int32_t* page_table,
-                                 int pt_stride, const int32_t* seq_lens, int max_tokens, int64_t num_pages, int HKV,
+                                 int pt_stride, int page_shift, const int32_t* seq_lens, int max_tokens,
+                                 int64_t num_pages, int HKV,
                                  int row_bytes, unsigned char* k_pool, unsigned char* v_pool, int* status) {
   const int b = blockIdx.x;
   const int n = seq_lens[b];
@@ -313,7 +317,7 @@ __global__ void append_kv_kernel(const unsigned char* k_new, const unsigned char
     return;
   }
   const int t = n - 1;
-  const int page = page_table[(size_t)b * pt_stride + t / kPage];
+  const int page = page_table[(size_t)b * pt_stride + (t >> page_shift)];
   if (page < 0 || (int64_t)page >= num_pages) {
     if (threadIdx.x == 0) set_error(status, TS_ERR_PAGE_OOB);
     return;
@@ -322,7 +326,8 @@ __global__ void append_kv_kernel(const unsigned char* k_new, const unsigned char
   for (int i = threadIdx.x; i < 2 * HKV * cpr; i += blockDim.x) {
     const int isv = i / (HKV * cpr), rem = i % (HKV * cpr), g = rem / cpr, ch = rem % cpr;
     const unsigned char* src = (isv ? v_new : k_new) + ((size_t)b * HKV + g) * row_bytes + ch * 16;
-    unsigned char* dst = (isv ? v_pool : k_pool) + (((size_t)page * HKV + g) * kPage + t % kPage) * row_bytes + ch * 16;
+    unsigned char* dst = (isv ? v_pool : k_pool) +
+                         ((((size_t)page * HKV + g) << page_shift) + (t & ((1 << page_shift) - 1))) * row_bytes + ch * 16;
     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
   }
 }
@@ -335,7 +340,8 @@ ts_status launch_append_kv(ts_ctx* ctx, const void* k_new, const void* v_new, co
   const int row_bytes = c.head_dim * (c.kv_dtype == TS_KV_BF16 ? 2 : 4);
   ctx->kernels += 1;
   append_kv_kernel<<<B, 128, 0, s>>>(static_cast<const unsigned char*>(k_new), static_cast<const unsigned char*>(v_new),
-                                     page_table, c.max_pages_per_seq, seq_lens, ctx->max_tokens, c.num_pages,
+                                     page_table, c.max_pages_per_seq, ctx->page_shift, seq_lens, ctx->max_tokens,
+                                     c.num_pages,
                                      c.n_kv_heads, row_bytes, static_cast<unsigned char*>(k_pool),
                                      static_cast<unsigned char*>(v_pool), ctx->status);
   return cuda_status(cudaGetLastError());
@@ -435,6 +441,7 @@ extern "C" ts_status ts_sparse_attend_noalloc(int n_q_heads, int n_kv_heads, int
   a.v_pool = static_cast<const unsigned char*>(v_pool);
   a.page_table = page_table;
   a.pt_stride = max_pages_per_seq;
+  a.page_shift = 4;
   a.num_pages = num_pages;
   a.max_tokens = max_pages_per_seq * kPage;
   a.idx = idx;

@@ -88,6 +88,7 @@ struct ts_ctx {
   unsigned* gsync = nullptr;             // grid barrier state (4 words)
   unsigned long long* phase_ns = nullptr;  // [64] phase boundary times of the last step kernel
   bool use_step = true;                  // the persistent kernel is available
+  int page_shift = 4;                    // log2 of the page size (16 tokens, or 1)
   // settings read once at ts_create (environment) or set through the C ABI
   bool debug = false;                    // TS_DEBUG: launch diagnostics on stderr
   bool no_tc = false;                    // TOKENSELECT_NO_TC=1: CUDA-core scan only

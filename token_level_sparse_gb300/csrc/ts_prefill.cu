@@ -46,11 +46,12 @@ __global__ void chunk_mean_kernel(const float* q, int c, int HD, int B, float* q
 struct CaArgs {
   const float* q;              // [B][c][H][D] chunk queries
   int c, H, HKV, G;
-  const unsigned char* k_pool; // [num_pages][H_kv][16][D] bf16
+  const unsigned char* k_pool; // [num_pages][H_kv][page size][D] bf16
   const unsigned char* v_pool;
   int64_t num_pages;
   const int32_t* page_table;
   int pt_stride;
+  int page_shift;              // log2 of the page size: 4 (16 tokens) or 0 (one token per page)
   const int32_t* seq_lens;
   int max_tokens;
   const int32_t* idx;          // [B][idx_stride] ascending
@@ -166,6 +167,10 @@ __global__ void __launch_bounds__(kCaThreads, 1) chunk_attend_kernel(const __gri
     return true;
   };
 
+  // row of (page, KV head g, token t) in the pool [page][H_kv][page size][D]
+  auto pool_row = [&](int page, int g, int t) -> size_t {
+    return (((size_t)page * a.HKV + g) << a.page_shift) + (t & ((1 << a.page_shift) - 1));
+  };
   // the tokens and pages of key tile kt into list buffer lb (threads below 128)
   auto list_tile = [&](int kt, int lb) {
     if (tid < kCaTok) {
@@ -173,7 +178,7 @@ __global__ void __launch_bounds__(kCaThreads, 1) chunk_attend_kernel(const __gri
       int t = -1, page = -1;
       if (j < cnt) {
         t = a.idx[(size_t)b * a.idx_stride + j];
-        if (t >= 0 && t < a.max_tokens) page = a.page_table[(size_t)b * a.pt_stride + t / kPage];
+        if (t >= 0 && t < a.max_tokens) page = a.page_table[(size_t)b * a.pt_stride + (t >> a.page_shift)];
         if (page < 0 || (int64_t)page >= a.num_pages) {
           set_error(a.status, TS_ERR_PAGE_OOB);
           page = -1;
@@ -188,7 +193,7 @@ __global__ void __launch_bounds__(kCaThreads, 1) chunk_attend_kernel(const __gri
   auto gather_k = [&](int lb, unsigned char* dst) {
     for (int i = tid; i < kCaTok * CPR; i += kCaThreads) {
       const int r = i / CPR, ch = i % CPR, page = s_page[lb][r];
-      const size_t off = page >= 0 ? (((size_t)page * a.HKV + g) * kPage + s_tok[lb][r] % kPage) * S::ROW_BYTES : 0;
+      const size_t off = page >= 0 ? pool_row(page, g, s_tok[lb][r]) * S::ROW_BYTES : 0;
       cp_async16(dst + opnd_offset(r, ch * 8, kCaTok), a.k_pool + off + ch * 16);
     }
     cp_async_commit();
@@ -288,8 +293,7 @@ __global__ void __launch_bounds__(kCaThreads, 1) chunk_attend_kernel(const __gri
       const int r = i % kCaTok, ch = i / kCaTok, page = s_page[0][r];
       uint4 v = make_uint4(0u, 0u, 0u, 0u);
       if (page >= 0)
-        v = *reinterpret_cast<const uint4*>(a.v_pool + (((size_t)page * a.HKV + g) * kPage + s_tok[0][r] % kPage) *
-                                                           S::ROW_BYTES + ch * 16);
+        v = *reinterpret_cast<const uint4*>(a.v_pool + pool_row(page, g, s_tok[0][r]) * S::ROW_BYTES + ch * 16);
       const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int e = 0; e < 8; ++e)
@@ -421,6 +425,7 @@ ts_status launch_chunk_attend(ts_ctx* ctx, const ChunkAttendCall& c, cudaStream_
   a.num_pages = cfg.num_pages;
   a.page_table = c.page_table;
   a.pt_stride = cfg.max_pages_per_seq;
+  a.page_shift = ctx->page_shift;
   a.seq_lens = c.seq_lens;
   a.max_tokens = ctx->max_tokens;
   a.idx = c.idx;

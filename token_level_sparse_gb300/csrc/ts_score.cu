@@ -29,7 +29,7 @@ constexpr int cclamp(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi 
 
 template <typename KT, int D, int HKV, int G>
 struct ScoreShape {
-  static constexpr int P = kPage;
+  static constexpr int P = kPage;                      // tokens per stage: one 16-token page, or 16 one-token pages
   static constexpr int EPC = KV<KT>::kPerChunk;        // elements per 16-byte chunk
   static constexpr int GP = cpow2(G);                   // heads padded to a power of two
   static constexpr int CPL = (GP * 2 * EPC <= 64) ? 2 : 1;  // chunks per lane (q registers <= 64)
@@ -42,7 +42,7 @@ struct ScoreShape {
   static constexpr int ITERS = ROWS / RPW;
   static constexpr int PPC = kScorePagesPerCta;
   static constexpr int TOK = PPC * P;                   // tokens per CTA
-  static constexpr int STAGE_BYTES = HKV * P * D * (int)sizeof(KT);  // one page, all KV heads
+  static constexpr int STAGE_BYTES = HKV * P * D * (int)sizeof(KT);  // 16 tokens, all KV heads
   static constexpr int NST = cclamp(131072 / STAGE_BYTES, 2, 8);
   static constexpr int THREADS = (NCW + 1) * 32;
   static_assert(D % DPL == 0 && 32 % LPR == 0, "row split");
@@ -72,6 +72,7 @@ struct ScoreKArgs {
   float2* stats;
   unsigned* counters;
   int* status;
+  int page_size;               // 16, or 1 for a token-granular pool
 };
 
 template <typename KT, int D, int HKV, int G>
@@ -114,35 +115,61 @@ __global__ void __launch_bounds__(ScoreShape<KT, D, HKV, G>::THREADS, 1)
   __syncthreads();
 
   if (warp == S::NCW) {
-    // ---------------- producer: one lane streams the CTA's pages through the ring
-    if (lane == 0) {
-      const int32_t* pt = a.page_table + (size_t)b * a.pt_stride + page0;
-      const unsigned char* pool = static_cast<const unsigned char*>(a.k_pool);
-      int issued = 0;
-      for (int p = 0; p < np; ++p) {
-        const int s = p % S::NST;
-        if (p >= S::NST && !mbar_wait(&empty[s], ((p / S::NST) - 1) & 1)) {
-          set_error(a.status, TS_ERR_TIMEOUT);
-          break;
-        }
-        const int page = pt[p];
-        const bool ok = page >= 0 && (int64_t)page < a.num_pages;
-        s_valid[s] = ok;
-        if (ok) {
-          mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
-          bulk_g2s(stages + (size_t)s * S::STAGE_BYTES, pool + (size_t)page * S::STAGE_BYTES,
-                   S::STAGE_BYTES, &full[s]);
-        } else {
-          set_error(a.status, TS_ERR_PAGE_OOB);
-          mbar_arrive(&full[s]);
-        }
-        ++issued;
+    // ---------------- producer: the warp streams the CTA's stages through the ring (lane 0
+    // waits and arms the barrier; with one-token pages each lane fetches one token)
+    const unsigned char* pool = static_cast<const unsigned char*>(a.k_pool);
+    constexpr uint32_t kRow = D * (uint32_t)sizeof(KT);
+    int issued = 0;
+    for (int p = 0; p < np; ++p) {
+      const int s = p % S::NST;
+      int free_ok = 1;
+      if (lane == 0 && p >= S::NST) free_ok = mbar_wait(&empty[s], ((p / S::NST) - 1) & 1);
+      if (!__shfl_sync(kFull, free_ok, 0)) {
+        if (lane == 0) set_error(a.status, TS_ERR_TIMEOUT);
+        break;
       }
-      // No copy may still be landing in shared memory when the CTA exits.
+      unsigned char* dst = stages + (size_t)s * S::STAGE_BYTES;
+      if (a.page_size == S::P) {
+        // one page: every KV head's 16 rows, contiguous in the pool and in the stage
+        if (lane == 0) {
+          const int page = a.page_table[(size_t)b * a.pt_stride + page0 + p];
+          const bool ok = page >= 0 && (int64_t)page < a.num_pages;
+          s_valid[s] = ok;
+          if (ok) {
+            mbar_arrive_expect_tx(&full[s], S::STAGE_BYTES);
+            bulk_g2s(dst, pool + (size_t)page * S::STAGE_BYTES, S::STAGE_BYTES, &full[s]);
+          } else {
+            set_error(a.status, TS_ERR_PAGE_OOB);
+            mbar_arrive(&full[s]);
+          }
+        }
+      } else {
+        // token-granular pool (one token per page): the stage's 16 tokens come from their own
+        // pages, token r's rows [H_kv][d] (contiguous in its page) to token-major rows (r, g)
+        // of the stage; tokens past the sequence are not copied (their logits are masked)
+        const int t0 = tok0 + p * S::P;
+        const int nr = min(S::P, n - t0);
+        int page = -1;
+        if (lane < nr) page = a.page_table[(size_t)b * a.pt_stride + t0 + lane];
+        const bool ok = page >= 0 && (int64_t)page < a.num_pages;
+        const unsigned good = __ballot_sync(kFull, lane < nr && ok);
+        if (lane == 0) {
+          const bool all = __popc(good) == nr;
+          s_valid[s] = all;
+          if (!all) set_error(a.status, TS_ERR_PAGE_OOB);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)__popc(good) * HKV * kRow);
+        }
+        __syncwarp();
+        if (lane < nr && ok)
+          bulk_g2s(dst + (size_t)lane * HKV * kRow, pool + (size_t)page * HKV * kRow, HKV * kRow, &full[s]);
+      }
+      ++issued;
+    }
+    // No copy may still be landing in shared memory when the CTA exits.
+    if (lane == 0)
       for (int p = max(0, issued - S::NST); p < issued; ++p) {
         if (!mbar_wait(&full[p % S::NST], (p / S::NST) & 1)) set_error(a.status, TS_ERR_TIMEOUT);
       }
-    }
   } else {
     // ---------------- consumers: warp -> (KV head g, rows of each page)
     const int g = warp / S::WPH;
@@ -159,6 +186,7 @@ __global__ void __launch_bounds__(ScoreShape<KT, D, HKV, G>::THREADS, 1)
           qr[j][c * S::EPC + e] = (j < G) ? qh[(lin + c * S::LPR) * S::EPC + e] : 0.f;
     }
     const bool writer = (lin & (S::LPR / S::GP - 1)) == 0;
+    const bool token_major = a.page_size != S::P;   // one-token pages: stage rows (token, g)
     for (int p = 0; p < np; ++p) {
       const int s = p % S::NST;
       if (!mbar_wait(&full[s], (p / S::NST) & 1)) {
@@ -170,7 +198,7 @@ __global__ void __launch_bounds__(ScoreShape<KT, D, HKV, G>::THREADS, 1)
 #pragma unroll
       for (int it = 0; it < S::ITERS; ++it) {
         const int row = row0 + it * S::RPW + lrow;
-        const KT* rp = st + ((size_t)g * S::P + row) * D;
+        const KT* rp = st + (token_major ? (size_t)row * HKV + g : (size_t)g * S::P + row) * D;
         float acc0[S::GP], acc1[S::GP];
 #pragma unroll
         for (int j = 0; j < S::GP; ++j) acc0[j] = acc1[j] = 0.f;
@@ -419,6 +447,7 @@ ts_status run_score(ts_ctx* ctx, const ScoreCall& c, cudaStream_t s) {
   a.stats = ctx->stats;
   a.counters = ctx->counters;
   a.status = ctx->status;
+  a.page_size = ctx->cfg.page_size;
   {
     ProfScope ps(ctx, TS_PROF_SCORE, s);
     kern<<<dim3(ctx->score_max_chunks, c.B), S::THREADS, smem, s>>>(a);
