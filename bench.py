@@ -59,7 +59,7 @@ def parse_args(argv=None):
 # workload index, theta for the profiling cases
 CASES = {"n128k": (1, 0.9), "n128k-miss": (1, 2.0), "n1m-miss": (3, 2.0), "n1m-1layer-miss": ("3x1", 2.0),
          "n256k-1layer-miss": ("3x1@256k", 2.0), "qwen-b8-miss": (2, 2.0), "topp-b4": (4, 0.9),
-         "topp-b4-miss": (4, 2.0),
+         "topp-b4-miss": (4, 2.0), "topp-b4-64k-miss": ("4@64k", 2.0),
          "prefill-n128k-c512": ("prefill", None)}
 
 
@@ -91,6 +91,8 @@ def case_main(args):
         sp = W.spec(3, layers=1)
     elif cfg == "3x1@256k":
         sp = W.spec(3, layers=1, n0=(262144,))
+    elif cfg == "4@64k":
+        sp = W.spec(4, n0=(65536,) * 4)
     else:
         sp = W.spec(cfg)
     b = DecodeBench(sp, "cuda:0", theta=theta)

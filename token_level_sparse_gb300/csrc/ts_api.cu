@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <new>
 
 #include "ts_internal.h"
@@ -40,6 +41,7 @@ void free_ctx_buffers(ts_ctx* c) {
   cudaFree(c->qmean);
   cudaFree(c->blk_len);
   cudaFree(c->blk_idx);
+  cudaFree(c->sel_rows);
   cudaFree(c->step_partials);
   cudaFree(c->step_hist);
   cudaFree(c->step_mass);
@@ -120,6 +122,12 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   ctx->debug = std::getenv("TS_DEBUG") != nullptr;
   if (const char* env = std::getenv("TOKENSELECT_NO_TC")) ctx->no_tc = env[0] == '1';
   if (const char* env = std::getenv("TOKENSELECT_SCAN_CLAIM")) ctx->scan_claim = env[0] == '1';
+  // TOKENSELECT_TOPP_ATTEND=gather / range: the persistent kernel's top-p attention always shares
+  // the selected tokens out over the CTAs, or always attends each CTA's own range (when it may)
+  if (const char* env = std::getenv("TOKENSELECT_TOPP_ATTEND")) {
+    if (std::strcmp(env, "gather") == 0) ctx->range_attend = 0;
+    if (std::strcmp(env, "range") == 0) ctx->range_attend = 2;
+  }
   if (const char* env = std::getenv("TOKENSELECT_L2_BUDGET_MB")) {
     const long mb = std::strtol(env, nullptr, 10);
     if (mb > 0) ctx->l2_budget = (int64_t)mb << 20;
@@ -170,6 +178,7 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   chk(alloc(&ctx->qmean, B * H * D));
   chk(alloc(&ctx->blk_len, B));
   chk(alloc(&ctx->blk_idx, B * T + B));
+  chk(alloc(&ctx->sel_rows, NS * kStepFlagCap));
   if (e == cudaSuccess) chk(cudaMemset(ctx->status, 0, sizeof(int)));
   if (e == cudaSuccess) chk(cudaMemset(ctx->counters, 0, B * kCounterSlots * sizeof(unsigned)));
   if (e == cudaSuccess) chk(cudaMemset(ctx->hist, 0, B * 2048 * sizeof(unsigned)));

@@ -10,6 +10,7 @@
 
 namespace ts {
 
+constexpr int kStepFlagCap = 8192;   // persistent kernel: most tokens of one CTA's page range
 constexpr int kPage = 16;            // tokens per page (the only page size compiled)
 constexpr int kScorePagesPerCta = 16;  // pages of one sequence per score CTA
 constexpr int kSelThreads = 512;     // select kernels: threads per CTA
@@ -67,6 +68,7 @@ struct ts_ctx {
   float* qmean = nullptr;                // [max_batch][H][d] mean query of a prefill chunk
   int32_t* blk_len = nullptr;            // [max_batch] block counts (block-level selection)
   int32_t* blk_idx = nullptr;            // [max_batch][max_tokens] selected blocks, then [max_batch] counts
+  int32_t* sel_rows = nullptr;           // persistent kernel: per CTA, its selected tokens [kStepFlagCap]
   int64_t kernels = 0;           // kernel launches issued
   // persistent decode-step kernel
   int step_grid = 0;                     // CTAs of the cooperative launch (0: not yet sized)
@@ -89,6 +91,7 @@ struct ts_ctx {
   unsigned long long* phase_ns = nullptr;  // [64] phase boundary times of the last step kernel
   bool use_step = true;                  // the persistent kernel is available
   int page_shift = 4;                    // log2 of the page size (16 tokens, or 1)
+  int range_attend = 1;                  // top-p attention over each CTA's range: 0 never, 1 when dense, 2 always
   // settings read once at ts_create (environment) or set through the C ABI
   bool debug = false;                    // TS_DEBUG: launch diagnostics on stderr
   bool no_tc = false;                    // TOKENSELECT_NO_TC=1: CUDA-core scan only

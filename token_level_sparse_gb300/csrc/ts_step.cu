@@ -55,6 +55,8 @@ constexpr int kMaxG = kMaxScanG;   // query heads per KV head
 constexpr int kMaxAttH = 64;       // query heads of the attention phase
 constexpr int kPreFix = 512;       // fixed attention tokens of a CTA resolved at set-up
 constexpr int kOwnBatch = 1024;    // attention: selected tokens (and pages) looked up from other CTAs' lists at once
+constexpr int kRangeSlots = 4;     // range attention: ring slots of one V page and its logit rows
+constexpr float kRescaleGap = 8.f; // range attention: a logit this far (base 2) above the running max rescales
 constexpr int kMaxPagesCta = 1024; // page ids of a CTA's range kept in shared memory
 constexpr int kScanClaim = 2;      // pages per claim of a shared tensor-core scan
 constexpr int kVoteBufs = 2;       // shared-memory buffers of logit chunks for the votes
@@ -211,7 +213,7 @@ struct StepKArgs {
   unsigned long long* cands;   // [B][kCandCap]  (key << 32 | ~index)
   int* cta_cnt;                // [B][nCTA][4]  cand-range selected, all selected, ties, selected below s_end
   float* apart;                // o [B][H][parts][nCTA][D / parts], then (max, sum) [B][H][nCTA even]
-  float* spill;                // per CTA: logits [tok][wave head], later its selected tokens (ascending)
+  float* spill;                // per CTA: logits [tok][wave head]
   float2* wpart;               // per CTA: [segment][scan warp][head] (max, sum exp) of a wave
   int64_t spill_floats;
   int64_t l2_budget;           // bytes of logits one scan wave may keep in L2
@@ -222,7 +224,9 @@ struct StepKArgs {
   unsigned long long* phase_ns;  // CTA 0's %globaltimer at phase boundaries (debug)
   int dyn_bytes;               // dynamic shared memory of the launch
   int nslot;                   // ring slots of STAGE_BYTES each
-  int flag_cap;                // bytes reserved at the tail for selection flags
+  int flag_cap;                // bytes reserved at the tail for selection flags (one per token)
+  int* sel_rows;               // per CTA [flag_cap]: its selected tokens, ascending per segment
+  int range_attend;            // top-p attention over each CTA's own range: 0 never, 1 when dense, 2 always
 };
 
 // -------------------------------------------------------------- grid barrier
@@ -474,6 +478,7 @@ struct Smem {
     struct {                     // balanced attention (my_pages unused then): a sequence's per-CTA
       int pref[kMaxGrid + 1];    // offsets in its concatenated lists, and each CTA's count below s_end
       int nlo[kMaxGrid];
+      int range_b[kMaxB];        // sequence b attended over each CTA's own range (range_attend)
     } bal;
   };
   int timed_out;
@@ -714,6 +719,240 @@ __device__ __noinline__ bool cuda_scan_wave(const StepKArgs& a, Smem& sm, unsign
   return true;
 }
 
+
+// Range attention, for dense selections (top-p keeping a large share of a sequence): I attend the
+// tokens of my own scanned range of sequence b that are selected, sinks or in the window. Their
+// logits are the scan's (base 2, still in my scratch region), so K is not read again; each page
+// with an attended token brings its V rows of every KV head and its 16 logit rows into a ring by
+// bulk copy. Weights are 2^(l - m) against a running max m per head, which moves only when a logit
+// passes it by more than kRescaleGap (then sums and outputs are rescaled once). A thread owns (KV
+// head, 8 columns) for the G query heads of that KV head over a share of each page's tokens, in
+// packed fp32 pairs. The
+// CTA's partial (o, max in natural units, sum) goes where the gathered attention puts it. False
+// after a time-out (recorded, the abort word raised, the copies in flight waited for).
+template <typename KT, int D, int HKV, int G>
+__device__ __noinline__ bool range_attend(const StepKArgs& a, Smem& sm, unsigned char* stage, int stage_bytes,
+                                          const uint8_t* selflag, int b, int sgi, float* ao, float2* aml,
+                                          int nCTAp, int dq) {
+  using S = StepShape<KT, D, HKV, G>;
+  constexpr int HQ = HKV * G, D4 = D / 4, D8 = D / 8, PVT = HKV * D8, NSPL = S::THREADS / PVT;
+  constexpr int EPC = KV<KT>::kPerChunk;             // elements of a 16-byte chunk of V
+  constexpr int VPAGE = S::STAGE_BYTES;              // one V page of every KV head, [g][16][D]
+  constexpr int LROWS = S::P * HQ * 4;               // its 16 logit rows [16][H]
+  constexpr int SLOT = VPAGE + 2 * LROWS;            // then the weights [16][H]
+  static_assert(S::THREADS % PVT == 0 && S::P * HQ <= S::THREADS && SLOT % 16 == 0 && D % 8 == 0 && 8 % EPC == 0,
+                "range attention layout");
+  constexpr float kLn2 = 0.693147180559945309f;
+  const int tid = threadIdx.x, c = blockIdx.x, nCTA = gridDim.x;
+  const SeqState& st = sm.seq[b];
+  const int t0l = sm.seg_t0[sgi], lp0 = sm.seg_lp0[sgi], ntok = sm.seg_ntok[sgi];
+  const int npg = (ntok + S::P - 1) / S::P;
+  const uint8_t* fl = selflag + t0l;                                   // my flags of the segment
+  const float* eb = a.spill + (size_t)c * sm.region + (size_t)t0l * HQ;  // its logit rows
+  const int nslot =
+      min(kRangeSlots, (stage_bytes - kRangeSlots * 8 - (2 * (a.flag_cap / S::P) + kRangeSlots) * 4) / SLOT);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage + (size_t)nslot * SLOT);
+  int* plist = reinterpret_cast<int*>(bars + kRangeSlots);            // my pages with an attended token
+  int* ppage = plist + a.flag_cap / S::P;                              // and their page ids
+  int* pv_ok = ppage + a.flag_cap / S::P;                              // per slot: its V page is valid
+  auto attended = [&](int i) -> bool {                                 // token lp0 * 16 + i of the sequence
+    const int t = lp0 * S::P + i;
+    return i < ntok && (t < st.s_end || t >= st.ls || fl[i] == 1);
+  };
+
+  // ---- the pages of my segment with at least one attended token, ascending
+  int nlist = 0;
+  #pragma unroll 1
+  for (int j0 = 0; j0 < npg; j0 += S::THREADS) {
+    const int j = j0 + tid;
+    int any = 0;
+    if (j < npg)
+      #pragma unroll 1
+      for (int r = 0; r < S::P && !any; ++r) any = attended(j * S::P + r);
+    int tot;
+    const int pos = block_scan(any, sm.wsum, tot);
+    if (any) {
+      plist[nlist + pos] = j;
+      ppage[nlist + pos] = a.page_table[(size_t)b * a.pt_stride + lp0 + j];
+    }
+    nlist += tot;
+  }
+  if (nlist == 0) {
+    if (tid < HQ) aml[((size_t)b * HQ + tid) * nCTAp + c] = make_float2(-INFINITY, 0.f);
+    fence_proxy_async_global();
+    __syncthreads();
+    return true;
+  }
+  if (tid == 0) {
+    #pragma unroll 1
+    for (int s = 0; s < nslot; ++s) mbar_init(&bars[s], 1);
+    mbar_fence_init();
+  }
+  if (tid < HQ) sm.att_m[tid] = -INFINITY;
+  __syncthreads();
+  // page k of the list into slot k % nslot (thread 0)
+  auto issue = [&](int k) {
+    const int s = k % nslot, j = plist[k], page = ppage[k];
+    const bool ok = page >= 0 && (int64_t)page < a.num_pages;
+    pv_ok[s] = ok;
+    unsigned char* dst = stage + (size_t)s * SLOT;
+    mbar_arrive_expect_tx(&bars[s], (ok ? VPAGE : 0) + LROWS);
+    if (ok) bulk_g2s(dst, a.v_pool + (size_t)page * VPAGE, VPAGE, &bars[s]);
+    else set_error(a.status, TS_ERR_PAGE_OOB);
+    bulk_g2s(dst + VPAGE, eb + (size_t)j * S::P * HQ, LROWS, &bars[s]);
+  };
+  if (tid == 0) {
+    fence_proxy_async_global();
+    #pragma unroll 1
+    for (int k = 0; k < min(nslot, nlist); ++k) issue(k);
+  }
+  // weights: thread (row r, head h); outputs: thread (split sp, KV head g, columns 8 d8 .. 8 d8 + 7)
+  const bool wt = tid < S::P * HQ;
+  const int wr = tid / HQ, wh = tid % HQ;
+  const int sp = tid / PVT, gd = tid % PVT, g = gd / D8, d8 = gd % D8;
+  KahanF lsum;
+  uint64_t acc[G][4];   // head jj, columns (8 d8 + 2 e, 8 d8 + 2 e + 1)
+#pragma unroll
+  for (int jj = 0; jj < G; ++jj) acc[jj][0] = acc[jj][1] = acc[jj][2] = acc[jj][3] = 0ull;   // (+0, +0)
+  #pragma unroll 1
+  for (int k = 0; k < nlist; ++k) {
+    const int s = k % nslot, j = plist[k];
+    const bool landed = mbar_wait(&bars[s], (k / nslot) & 1, a.wait_ns);
+    unsigned char* slot = stage + (size_t)s * SLOT;
+    const KT* Vp = reinterpret_cast<const KT*>(slot);
+    const float* Lp = reinterpret_cast<const float*>(slot + VPAGE);
+    float* Wp = reinterpret_cast<float*>(slot + VPAGE + LROWS);
+    float xl = -INFINITY;
+    bool att = false;
+    if (wt && landed) {
+      att = attended(j * S::P + wr) && pv_ok[s];
+      if (att) xl = Lp[wr * HQ + wh];
+    }
+    const bool need = att && xl - sm.att_m[wh] > kRescaleGap;   // (a max of -inf always rescales)
+    if (__syncthreads_or(!landed || need)) {
+      if (__syncthreads_or(!landed)) {
+        if (tid == 0) {
+          set_error(a.status, TS_ERR_TIMEOUT);
+          atomicExch(&a.gsync->abort, 1u);
+          const int issued = min(nlist, k == 0 ? nslot : k - 1 + nslot);
+          #pragma unroll 1
+          for (int kk = k; kk < issued; ++kk)                    // copies in flight land first
+            mbar_wait(&bars[kk % nslot], (kk / nslot) & 1, a.wait_ns);
+        }
+        return false;
+      }
+      // a new running max for the heads that passed it: the page's max, then the corrections
+      if (wt) Wp[tid] = xl;
+      __syncthreads();
+      if (tid < HQ) {
+        float pm = -INFINITY;
+        #pragma unroll 1
+        for (int r = 0; r < S::P; ++r) pm = fmaxf(pm, Wp[r * HQ + tid]);
+        const float m0 = sm.att_m[tid];
+        const float mn = fmaxf(m0, pm);
+        sm.att_c[tid] = m0 == -INFINITY ? 0.f : exp2f(m0 - mn);
+        sm.att_m[tid] = mn;
+      }
+      __syncthreads();
+      if (wt) {
+        lsum.s *= sm.att_c[wh];
+        lsum.c *= sm.att_c[wh];
+      }
+#pragma unroll
+      for (int jj = 0; jj < G; ++jj) {
+        const float f = sm.att_c[g * G + jj];
+        const uint64_t ff = pack_f2(f, f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[jj][e] = fma_f2(acc[jj][e], ff, 0ull);
+      }
+    }
+    // the slot of page k - 1 is free (every thread has passed its outputs): refill it
+    if (tid == 0 && k >= 1 && k - 1 + nslot < nlist) issue(k - 1 + nslot);
+    if (wt) {
+      const float w = att ? exp2f(xl - sm.att_m[wh]) : 0.f;
+      Wp[tid] = w;
+      lsum.add(w);
+    }
+    __syncthreads();
+    #pragma unroll 2
+    for (int r = sp; r < S::P; r += NSPL) {
+      float v[8];
+#pragma unroll
+      for (int ch = 0; ch < 8 / EPC; ++ch)
+        KV<KT>::unpack(lds128(Vp + ((size_t)g * S::P + r) * D + d8 * 8 + ch * EPC), v + ch * EPC);
+      uint64_t vp[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) vp[e] = pack_f2(v[2 * e], v[2 * e + 1]);
+      float wv[G];
+      if constexpr (G % 4 == 0) {                       // 16-byte aligned: rows of H floats, G | H
+#pragma unroll
+        for (int jj = 0; jj < G; jj += 4) {
+          const float4 w4 = *reinterpret_cast<const float4*>(Wp + r * HQ + g * G + jj);
+          wv[jj] = w4.x;
+          wv[jj + 1] = w4.y;
+          wv[jj + 2] = w4.z;
+          wv[jj + 3] = w4.w;
+        }
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < G; ++jj) wv[jj] = Wp[r * HQ + g * G + jj];
+      }
+#pragma unroll
+      for (int jj = 0; jj < G; ++jj) {
+        const uint64_t wb = pack_f2(wv[jj], wv[jj]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[jj][e] = fma_f2(vp[e], wb, acc[jj][e]);
+      }
+    }
+  }
+  // ---- every copy has landed and been read: the splits' outputs and the rows' sums, reduced in a
+  // fixed order into the CTA's partial
+  __syncthreads();
+  if (tid == 0)
+    #pragma unroll 1
+    for (int s = 0; s < nslot; ++s) mbar_inval(&bars[s]);
+  float* red = reinterpret_cast<float*>(stage);                  // [HQ][D]: the splits added in order
+  float* lred = red + (size_t)HQ * D;                            // [16][HQ]
+  if (wt) lred[tid] = lsum.s - lsum.c;
+  #pragma unroll 1
+  for (int x = 0; x < NSPL; ++x) {
+    if (sp == x)
+#pragma unroll
+      for (int jj = 0; jj < G; ++jj) {
+        float4* dst = reinterpret_cast<float4*>(red + (size_t)(g * G + jj) * D + d8 * 8);
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) unpack_f2(acc[jj][e], o[2 * e], o[2 * e + 1]);
+        float4 p0 = make_float4(o[0], o[1], o[2], o[3]), p1 = make_float4(o[4], o[5], o[6], o[7]);
+        if (x > 0) {
+          const float4 q0 = dst[0], q1 = dst[1];
+          p0 = make_float4(q0.x + p0.x, q0.y + p0.y, q0.z + p0.z, q0.w + p0.w);
+          p1 = make_float4(q1.x + p1.x, q1.y + p1.y, q1.z + p1.z, q1.w + p1.w);
+        }
+        dst[0] = p0;
+        dst[1] = p1;
+      }
+    __syncthreads();
+  }
+  const int Dq = D / dq;
+  #pragma unroll 1
+  for (int it = tid; it < HQ * D4; it += S::THREADS) {
+    const int h = it / D4, e4 = it % D4, qq = e4 / (Dq / 4);
+    reinterpret_cast<float4*>(ao + ((((size_t)b * HQ + h) * dq + qq) * nCTA + c) * Dq)[e4 % (Dq / 4)] =
+        reinterpret_cast<const float4*>(red + (size_t)h * D)[e4];
+  }
+  if (tid < HQ) {
+    KahanF z;
+    #pragma unroll 1
+    for (int r = 0; r < S::P; ++r) z.add(lred[r * HQ + tid]);
+    const float m2 = sm.att_m[tid], l = z.s - z.c;
+    aml[((size_t)b * HQ + tid) * nCTAp + c] =
+        (m2 > -INFINITY && l > 0.f) ? make_float2(m2 * kLn2, l) : make_float2(-INFINITY, 0.f);
+  }
+  fence_proxy_async_global();
+  __syncthreads();
+  return true;
+}
 
 template <typename KT, int D, int HKV, int G>
 __device__ __forceinline__ void step_body(const StepKArgs& a) {
@@ -1090,9 +1329,9 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     if (c == 0 && tid == 0) set_error(a.status, TS_ERR_SHAPE);
     return;  // the same decision in every CTA, before any grid barrier
   }
-  // my scratch region holds my logits until the votes, then my selected tokens (ascending, the
-  // list of segment sg from row seg_t0[sg])
-  int* const sel_list = reinterpret_cast<int*>(a.spill + (size_t)c * sm.region);
+  // my selected tokens, ascending: the list of segment sg from row seg_t0[sg] (my logits stay in
+  // my scratch region for the attention)
+  int* const sel_list = a.sel_rows + (size_t)c * a.flag_cap;
   TS_MARK(7);
   // the tensor-core scan runs this launch: warps 8.. finish the set-up while the pages stream
   const bool tc_scan = S::TC && sm.use_tc && (a.phases & kPhScore) && sm.ptot > 0;
@@ -2180,8 +2419,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         }
       }
       TS_MARK(50);
-      // counts per warp (all, in [s_end, ls), below s_end), then the list in token order; my
-      // scratch region's logits are spent, the list of this segment starts at its row t0l
+      // counts per warp (all, in [s_end, ls), below s_end), then the list in token order, the list
+      // of this segment from its row t0l
       int na = 0, nc = 0, nlo = 0;
       #pragma unroll 1
       for (int i0 = w0; i0 < w1; i0 += 32) {
@@ -2276,9 +2515,67 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     // scores: warp -> one KV head (NW is a multiple of H_kv), its G queries in registers
     constexpr int NWG = S::NW / HKV;
     const int gw = warp % HKV, wsl = warp / HKV;
+    constexpr bool kRangeGeom = D % 8 == 0 && S::THREADS % (HKV * (D / 8)) == 0 && S::P * HQ <= S::THREADS;
+    if (bal) {
+      // top-p sequences that take the range attention: every CTA attends the attended tokens of
+      // its own scanned range, when the selection is dense enough that streaming each range's
+      // pages beats sharing the tokens out (pages of the busiest range against the even share
+      // of tokens, in the ratio of their measured costs); the same decision in every CTA, from
+      // the per-CTA counts published before the barrier
+      constexpr int RSLOT = S::STAGE_BYTES + 2 * S::P * HQ * 4;
+      const int rslots =
+          min(kRangeSlots, (stage_bytes - kRangeSlots * 8 - (2 * (a.flag_cap / S::P) + kRangeSlots) * 4) / RSLOT);
+      const bool range_ok = kRangeGeom && bal && a.range_attend > 0 && sm.hpw == HKV && !sm.scan_dyn &&
+                            rslots >= 2 &&
+                            HQ * D * 4 + S::P * HQ * 4 <= rslots * RSLOT;
+      #pragma unroll 1
+      for (int b = 0; b < B; ++b) {
+        const SeqState& st = sm.seq[b];
+        int take = 0;
+        if (range_ok && !st.hit && st.pg1 > st.pg0) {
+          const int nfix = st.s_end + (st.n - st.ls);
+          int umax = 0, tot = 0;
+          #pragma unroll 1
+          for (int cc = st.first_cta + tid; cc <= st.last_cta; cc += blockDim.x) {
+            const int pages = min(st.pg1, (cc + 1) * sm.ppc) - max(st.pg0, cc * sm.ppc);
+            umax = max(umax, min(pages, __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 4 + 1]) + nfix));
+            tot += __ldcg(&a.cta_cnt[((size_t)b * nCTA + cc) * 4 + 0]);
+          }
+          umax = __reduce_max_sync(kFull, umax);
+          tot = __reduce_add_sync(kFull, tot);
+          if (lane == 0) {
+            sm.red_i[0][warp] = umax;
+            sm.red_i[1][warp] = tot;
+          }
+          __syncthreads();
+          if (tid == 0) {
+            #pragma unroll 1
+            for (int w = 1; w < S::NW; ++w) {
+              umax = max(umax, sm.red_i[0][w]);
+              tot += sm.red_i[1][w];
+            }
+            take = a.range_attend == 2 || (int64_t)umax * 4 * nCTA <= (int64_t)(tot + nfix) * 3;
+          }
+          __syncthreads();
+        }
+        if (tid == 0) sm.bal.range_b[b] = take;
+      }
+      __syncthreads();
+    }
     #pragma unroll 1
     for (int b = 0; b < B; ++b) {
       const SeqState& st = sm.seq[b];
+      if (bal && sm.bal.range_b[b]) {
+        const int sgr = sm.my_seg_of[b];
+        if (sgr >= 0) {
+          if constexpr (kRangeGeom)
+            if (!range_attend<KT, D, HKV, G>(a, sm, dsm, stage_bytes, selflag, b, sgr, ao, aml, nCTAp, dq)) return;
+        } else {
+          if (tid < HQ) aml[((size_t)b * H + tid) * nCTAp + c] = make_float2(-INFINITY, 0.f);
+          fence_proxy_async_global();
+        }
+        continue;
+      }
       const int32_t* gib = a.idx + (size_t)b * a.idx_stride;
       const int32_t* ctb = nullptr;
       int nfix, ct_lo = 0, ct_hi = 0;
@@ -2423,7 +2720,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
                 if (sm.bal.pref[mid] <= p) lo = mid;
                 else hi = mid - 1;
               }
-              const int* lst = reinterpret_cast<const int*>(a.spill + (size_t)lo * sm.region) +
+              const int* lst = a.sel_rows + (size_t)lo * a.flag_cap +
                                (max(st.pg0, lo * sm.ppc) - lo * sm.ppc) * S::P + sm.bal.nlo[lo];
               const int t = __ldcg(lst + (p - sm.bal.pref[lo]));
               ob_t[r] = t;
@@ -2829,7 +3126,7 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
       return TS_ERR_CUDA;
   }
   const int dyn = (smem_avail - static_bytes - 1024) / 128 * 128;
-  const int flag_cap = 8192;   // one byte per token of a CTA's range
+  const int flag_cap = kStepFlagCap;   // one byte per token of a CTA's range
   // ring slots of one stage of K each; the selection scratch and one
   // sequence's global histograms (with masses) alias the same space later
   const int nslot = std::min(kMaxSlots, (dyn - flag_cap) / S::STAGE_BYTES);
@@ -2954,6 +3251,8 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
     }
   }
   a.flag_cap = flag_cap;
+  a.sel_rows = ctx->sel_rows;
+  a.range_attend = ctx->range_attend;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(ctx->step_grid);
   lc.blockDim = dim3(S::THREADS);
