@@ -218,7 +218,11 @@ ts_status ts_sparse_attend_noalloc(int n_q_heads, int n_kv_heads, int head_dim, 
  * counter when at most two sequences are scanned (faster where SM bandwidth
  * differs, but no longer bit-identical from run to run);
  * TOKENSELECT_L2_BUDGET_MB sets the logit bytes one CUDA-core scan wave may
- * keep in L2; TS_DEBUG prints launch diagnostics. */
+ * keep in L2; TOKENSELECT_TOPP_ATTEND=gather / range / range_tc fixes the top-p
+ * attention (selected tokens shared out over the CTAs; each CTA's own scanned
+ * range from the scan's logits, P.V on CUDA cores or on the tensor cores),
+ * otherwise chosen per sequence by how dense the selection is; TS_DEBUG prints
+ * launch diagnostics. */
 ts_status ts_decode_step(ts_ctx* ctx, ts_cache* cache, int layer, const float* q,
                          const void* k_pool, const void* v_pool, const int32_t* page_table,
                          const int32_t* seq_lens, int B, const ts_select_params* params,

@@ -2,9 +2,11 @@
 
 Top-p can keep most of a sequence (SeqO1, section 3.2: the cumulative-importance rule adapts the
 budget to how flat the votes are). The persistent kernel then attends each CTA's own scanned
-range from the scan's logits, streaming whole V pages (`range`). Sparse selections keep the
-gathered attention, where the selected tokens are shared out evenly over all CTAs (`gather`).
-TOKENSELECT_TOPP_ATTEND, read when the context is created, forces one path for these tests.
+range from the scan's logits, streaming whole V pages (`range`, P.V on CUDA cores), or with P.V
+on the tensor cores for bf16 pools with d = 128 (`range_tc`, on request).
+Sparse selections keep the gathered attention, where the selected tokens are shared out evenly
+over all CTAs (`gather`). TOKENSELECT_TOPP_ATTEND, read when the context is created, forces one
+path for these tests.
 Checks:
 - trajectories against the oracle on each path (votes, index sets in the tie band, outputs
   within 2e-3 per row, lse within 1e-3);
@@ -24,24 +26,30 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
+def _set_path(monkeypatch, path):
+    if path == "auto":
+        monkeypatch.delenv("TOKENSELECT_TOPP_ATTEND", raising=False)
+    else:
+        monkeypatch.setenv("TOKENSELECT_TOPP_ATTEND", path)
+
+
 def _report(name, rep):
     print(f"{name}: steps={rep.steps} hits={rep.hits} band_swaps={rep.band_swaps} "
           f"worst_vote_rel={rep.worst_vote_rel:.2e} at_risk={rep.at_risk}")
 
 
-@pytest.mark.parametrize("path", ["range", "gather", "auto"])
+@pytest.mark.parametrize("path", ["range", "range_tc", "gather", "auto"])
 def test_topp_paths_against_the_oracle(path, monkeypatch):
-    if path != "auto":
-        monkeypatch.setenv("TOKENSELECT_TOPP_ATTEND", path)
+    _set_path(monkeypatch, path)
     for p in (0.9, 0.99):
         sp = W.spec(4, n0=(6000, 6000, 7000, 9000), steps=3, top_p=p)
         rep = run_trajectory(W.generate(sp, DEV), 3)
         _report(f"{path} p={p}", rep)
 
 
-@pytest.mark.parametrize("path", ["range", "gather"])
+@pytest.mark.parametrize("path", ["range", "range_tc", "gather"])
 def test_topp_every_token_on_both_paths(path, monkeypatch):
-    monkeypatch.setenv("TOKENSELECT_TOPP_ATTEND", path)
+    _set_path(monkeypatch, path)
     sp = W.spec(4, n0=(300, 4000, 17, 2500), steps=1, top_p=1.0, needles="lnN2")
     rep = run_trajectory(W.generate(sp, DEV), 1, theta=2.0)
     _report(path, rep)
@@ -51,24 +59,26 @@ def test_topp_paths_agree(monkeypatch):
     sp = W.spec(4, n0=(20000, 5000, 33000, 12000), steps=4, top_p=0.9)
     wl = W.generate(sp, DEV)
     res = {}
-    for path in ("gather", "range"):
-        monkeypatch.setenv("TOKENSELECT_TOPP_ATTEND", path)
+    for path in ("gather", "range", "range_tc"):
+        _set_path(monkeypatch, path)
         r = GpuRunner(wl, theta=2.0)
         res[path] = [r.step(t) for t in range(4)]
         r.ctx.close()
-    for t in range(4):
-        a, b = res["gather"][t], res["range"][t]
-        for i in range(sp.batch):
-            assert np.array_equal(a["idx"][i], b["idx"][i]), f"step {t} seq {i}: index sets differ"
-            check_attention(b["out"][i], b["lse"][i], a["out"][i], a["lse"][i], f"step {t} seq {i}")
+    for other in ("range", "range_tc"):
+        for t in range(4):
+            a, b = res["gather"][t], res[other][t]
+            for i in range(sp.batch):
+                where = f"{other} step {t} seq {i}"
+                assert np.array_equal(a["idx"][i], b["idx"][i]), f"{where}: index sets differ"
+                check_attention(b["out"][i], b["lse"][i], a["out"][i], a["lse"][i], where)
 
 
-@pytest.mark.parametrize("path", ["range", "gather"])
+@pytest.mark.parametrize("path", ["range", "range_tc", "gather"])
 def test_topp_growing_keys_rescale(path, monkeypatch):
     # key norms cycle 0.05, 1, 3, 6 over every four pages: within each CTA's range the logits'
     # max jumps by more than the rescale gap several times, so the range attention moves its
     # running max (and rescales its sums and outputs) on many pages
-    monkeypatch.setenv("TOKENSELECT_TOPP_ATTEND", path)
+    _set_path(monkeypatch, path)
     sp = W.spec(4, n0=(9000, 3000), batch=2, steps=2, top_p=0.95, needles="lnN2", key_scale="unit")
     wl = W.generate(sp, DEV)
     cyc = torch.tensor([0.05, 1.0, 3.0, 6.0], device=DEV)
@@ -82,9 +92,9 @@ def test_topp_growing_keys_rescale(path, monkeypatch):
     _report(path, rep)
 
 
-@pytest.mark.parametrize("path", ["range", "gather"])
+@pytest.mark.parametrize("path", ["range", "range_tc", "gather"])
 def test_topp_qwen_geometry(path, monkeypatch):
-    monkeypatch.setenv("TOKENSELECT_TOPP_ATTEND", path)
+    _set_path(monkeypatch, path)
     sp = W.spec(2, n0=(7000, 3100, 12000), n0_range=None, batch=3, steps=3, mode="topp", top_p=0.9,
                 needles="topp_mix")
     rep = run_trajectory(W.generate(sp, DEV), 3)
@@ -93,7 +103,7 @@ def test_topp_qwen_geometry(path, monkeypatch):
 
 @pytest.mark.parametrize("path", ["range", "gather"])
 def test_topp_fp32_small_heads(path, monkeypatch):
-    monkeypatch.setenv("TOKENSELECT_TOPP_ATTEND", path)
+    _set_path(monkeypatch, path)
     sp = W.spec(0, steps=4, mode="topp", top_p=0.9, n0=(1024,))
     rep = run_trajectory(W.generate(sp, DEV), 4)
     _report(path, rep)

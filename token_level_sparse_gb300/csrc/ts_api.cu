@@ -122,11 +122,16 @@ ts_status ts_create(ts_ctx** out, const ts_config* cfg) {
   ctx->debug = std::getenv("TS_DEBUG") != nullptr;
   if (const char* env = std::getenv("TOKENSELECT_NO_TC")) ctx->no_tc = env[0] == '1';
   if (const char* env = std::getenv("TOKENSELECT_SCAN_CLAIM")) ctx->scan_claim = env[0] == '1';
-  // TOKENSELECT_TOPP_ATTEND=gather / range: the persistent kernel's top-p attention always shares
-  // the selected tokens out over the CTAs, or always attends each CTA's own range (when it may)
+  // TOKENSELECT_TOPP_ATTEND=gather / range / range_tc: the persistent kernel's top-p attention
+  // always shares the selected tokens out over the CTAs, or always attends each CTA's own range
+  // (when it may), with P.V on CUDA cores or on the tensor cores (bf16, d = 128)
   if (const char* env = std::getenv("TOKENSELECT_TOPP_ATTEND")) {
     if (std::strcmp(env, "gather") == 0) ctx->range_attend = 0;
     if (std::strcmp(env, "range") == 0) ctx->range_attend = 2;
+    if (std::strcmp(env, "range_tc") == 0) {
+      ctx->range_attend = 2;
+      ctx->range_tc = true;
+    }
   }
   if (const char* env = std::getenv("TOKENSELECT_L2_BUDGET_MB")) {
     const long mb = std::strtol(env, nullptr, 10);

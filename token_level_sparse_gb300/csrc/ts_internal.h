@@ -80,11 +80,11 @@ struct ts_ctx {
   unsigned long long* cands = nullptr;   // [max_batch][2048]
   int* cta_cnt = nullptr;                // [max_batch][num_sms][3]
   float* apart = nullptr;                // attention partials: o [B][H][parts][num_sms][d / parts], (max, sum) [B][H][even]
-  struct KMap {                          // encoded TMA tensor maps of recent K pools
+  struct KMap {                          // encoded TMA tensor maps of recent K and V pools
     const void* pool = nullptr;
     int64_t num_pages = 0;
     alignas(64) unsigned char map[128];
-  } kmaps[8];
+  } kmaps[16];
   int kmap_next = 0;
   float* step_wpart = nullptr;           // per SM: CUDA-core scan (max, sum exp) pairs, see the persistent kernel
   unsigned* gsync = nullptr;             // grid barrier state (4 words)
@@ -92,6 +92,7 @@ struct ts_ctx {
   bool use_step = true;                  // the persistent kernel is available
   int page_shift = 4;                    // log2 of the page size (16 tokens, or 1)
   int range_attend = 1;                  // top-p attention over each CTA's range: 0 never, 1 when dense, 2 always
+  bool range_tc = false;                 // ... with P.V on the tensor cores (measured slower: opt-in)
   // settings read once at ts_create (environment) or set through the C ABI
   bool debug = false;                    // TS_DEBUG: launch diagnostics on stderr
   bool no_tc = false;                    // TOKENSELECT_NO_TC=1: CUDA-core scan only

@@ -56,7 +56,9 @@ constexpr int kMaxAttH = 64;       // query heads of the attention phase
 constexpr int kPreFix = 512;       // fixed attention tokens of a CTA resolved at set-up
 constexpr int kOwnBatch = 1024;    // attention: selected tokens (and pages) looked up from other CTAs' lists at once
 constexpr int kRangeSlots = 4;     // range attention: ring slots of one V page and its logit rows
+constexpr int kRangeSlotsTC = 6;   // the same on the tensor cores (a slot is free only once its MMAs are)
 constexpr float kRescaleGap = 8.f; // range attention: a logit this far (base 2) above the running max rescales
+constexpr int kStageMin = 160 * 1024;  // attention staging bytes every launch has (checked at launch)
 constexpr int kMaxPagesCta = 1024; // page ids of a CTA's range kept in shared memory
 constexpr int kScanClaim = 2;      // pages per claim of a shared tensor-core scan
 constexpr int kVoteBufs = 2;       // shared-memory buffers of logit chunks for the votes
@@ -170,6 +172,7 @@ struct GridSync {
 
 struct StepKArgs {
   CUtensorMap tmap_k;          // K pool as [num_pages * H_kv * 16][d] bf16, box 64 x (H_kv * 16), 128-byte swizzle
+  CUtensorMap tmap_v;          // V pool, the same view (the tensor-core range attention)
   int tc;                      // the tensor-core scan may run (map encoded, geometry supported)
   int nslot_tc;                // its ring slots
   int scan_dyn;                // it may share pages out by claims when at most two sequences scan
@@ -227,6 +230,7 @@ struct StepKArgs {
   int flag_cap;                // bytes reserved at the tail for selection flags (one per token)
   int* sel_rows;               // per CTA [flag_cap]: its selected tokens, ascending per segment
   int range_attend;            // top-p attention over each CTA's own range: 0 never, 1 when dense, 2 always
+  int tcv;                     // tmap_v is encoded: the range attention may run on the tensor cores
 };
 
 // -------------------------------------------------------------- grid barrier
@@ -874,8 +878,11 @@ __device__ __noinline__ bool range_attend(const StepKArgs& a, Smem& sm, unsigned
       lsum.add(w);
     }
     __syncthreads();
+    // only the page's rows of the sequence (past its end a row may hold anything, and a zero weight
+    // times a NaN is a NaN), none of a page outside the pool
+    const int nvr = pv_ok[s] ? min(S::P, ntok - j * S::P) : 0;
     #pragma unroll 2
-    for (int r = sp; r < S::P; r += NSPL) {
+    for (int r = sp; r < nvr; r += NSPL) {
       float v[8];
 #pragma unroll
       for (int ch = 0; ch < 8 / EPC; ++ch)
@@ -933,6 +940,308 @@ __device__ __noinline__ bool range_attend(const StepKArgs& a, Smem& sm, unsigned
         dst[1] = p1;
       }
     __syncthreads();
+  }
+  const int Dq = D / dq;
+  #pragma unroll 1
+  for (int it = tid; it < HQ * D4; it += S::THREADS) {
+    const int h = it / D4, e4 = it % D4, qq = e4 / (Dq / 4);
+    reinterpret_cast<float4*>(ao + ((((size_t)b * HQ + h) * dq + qq) * nCTA + c) * Dq)[e4 % (Dq / 4)] =
+        reinterpret_cast<const float4*>(red + (size_t)h * D)[e4];
+  }
+  if (tid < HQ) {
+    KahanF z;
+    #pragma unroll 1
+    for (int r = 0; r < S::P; ++r) z.add(lred[r * HQ + tid]);
+    const float m2 = sm.att_m[tid], l = z.s - z.c;
+    aml[((size_t)b * HQ + tid) * nCTAp + c] =
+        (m2 > -INFINITY && l > 0.f) ? make_float2(m2 * kLn2, l) : make_float2(-INFINITY, 0.f);
+  }
+  fence_proxy_async_global();
+  __syncthreads();
+  return true;
+}
+
+// Ring slots of the tensor-core range attention that fit `stage_bytes` of shared memory (its
+// base aligned up to 1024 bytes at most 1023 bytes on), or 0 when fewer than two fit.
+template <int D, int HKV, int G>
+__host__ __device__ constexpr int range_tc_slots(int stage_bytes, int flag_cap) {
+  constexpr int VPAGE = HKV * kPage * D * 2, LROWS = kPage * HKV * G * 4, BBUF = HKV * 16 * 32;
+  const int fixed = 1023 + 2 * BBUF + (kRangeSlotsTC + 2) * 8 + (2 * (flag_cap / kPage) + kRangeSlotsTC) * 4;
+  const int n = (stage_bytes - fixed) / (VPAGE + LROWS);
+  return n < 2 ? 0 : (n > kRangeSlotsTC ? kRangeSlotsTC : n);
+}
+
+// Range attention on the tensor cores (bf16 pools, d = 128): range_attend with O^T = V^T W per page
+// and KV head on tcgen05. The V page arrives by tiled TMA in the scan's 128-byte-swizzled layout
+// (rows (KV head g, token), 64 columns per half); read MN-major it is A, with M the 128 columns of
+// d and K the page's 16 tokens. B holds the KV head's weights as two bf16 terms per query head,
+// hi in row j and lo in row G + j, so that every product is exact in fp32: 16 rows of 16 tokens,
+// K-major without swizzle (core matrices of 8 rows x 8 tokens; the second 8 tokens 128 bytes on,
+// the second 8 rows 256 bytes on). The accumulator of KV head g is TMEM columns [16 g, 16 g + 16)
+// over lanes d; query head g G + j is the sum of its two columns. A move of the running max
+// rescales the accumulators in TMEM once the MMAs issued so far have completed. False after a
+// time-out (recorded, the abort word raised, the copies and MMAs in flight waited for, TMEM freed).
+template <typename KT, int D, int HKV, int G>
+__device__ __noinline__ bool range_attend_tc(const StepKArgs& a, Smem& sm, unsigned char* stage_raw, int stage_bytes,
+                                             const uint8_t* selflag, int b, int sgi, float* ao, float2* aml,
+                                             int nCTAp, int dq) {
+  using S = StepShape<KT, D, HKV, G>;
+  constexpr int HQ = HKV * G, D4 = D / 4;
+  constexpr int ROWS = HKV * S::P;                 // rows (g, token) of a V page
+  constexpr int VHALF = ROWS * 128;                // its 64-column half
+  constexpr int VPAGE = 2 * VHALF;
+  constexpr int LROWS = S::P * HQ * 4;             // the page's logit rows [16][H]
+  constexpr int BTILE = 16 * 32;                   // one KV head's weight rows (16 tokens each)
+  constexpr int BBUF = HKV * BTILE;
+  constexpr int NCOL = HKV * 16;
+  constexpr int TCOLS = NCOL <= 32 ? 32 : (NCOL <= 64 ? 64 : (NCOL <= 128 ? 128 : 256));
+  static_assert(D == 128 && 2 * G <= 16 && S::P * HQ <= S::THREADS && S::NW >= 4 && NCOL <= 256,
+                "tensor-core range attention");
+  constexpr float kLn2 = 0.693147180559945309f;
+  constexpr uint32_t idesc = idesc_bf16_f32_amn(128, 16);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, c = blockIdx.x, nCTA = gridDim.x;
+  const SeqState& st = sm.seq[b];
+  const int t0l = sm.seg_t0[sgi], lp0 = sm.seg_lp0[sgi], ntok = sm.seg_ntok[sgi];
+  const int npg = (ntok + S::P - 1) / S::P;
+  const uint8_t* fl = selflag + t0l;
+  const float* eb = a.spill + (size_t)c * sm.region + (size_t)t0l * HQ;
+  const int nslot = range_tc_slots<D, HKV, G>(stage_bytes, a.flag_cap);   // >= 2: checked by the caller
+  unsigned char* vslots =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(stage_raw) + 1023) & ~(uintptr_t)1023);
+  unsigned char* bbuf = vslots + (size_t)nslot * VPAGE;                  // two buffers of weights
+  float* lslots = reinterpret_cast<float*>(bbuf + 2 * BBUF);
+  uint64_t* full = reinterpret_cast<uint64_t*>(lslots + (size_t)nslot * (LROWS / 4));
+  uint64_t* mmad = full + kRangeSlotsTC;                                 // [2]: MMAs of a weight buffer done
+  int* plist = reinterpret_cast<int*>(mmad + 2);
+  int* ppage = plist + a.flag_cap / S::P;
+  int* pv_ok = ppage + a.flag_cap / S::P;
+  auto attended = [&](int i) -> bool {
+    const int t = lp0 * S::P + i;
+    return i < ntok && (t < st.s_end || t >= st.ls || fl[i] == 1);
+  };
+  auto b_off = [](int n, int k) -> int {          // byte of B element (row n, token k)
+    return (n >> 3) * 256 + (k >> 3) * 128 + (n & 7) * 16 + (k & 7) * 2;
+  };
+
+  // ---- the pages of my segment with at least one attended token, ascending, and their ids
+  int nlist = 0;
+  #pragma unroll 1
+  for (int j0 = 0; j0 < npg; j0 += S::THREADS) {
+    const int j = j0 + tid;
+    int any = 0;
+    if (j < npg)
+      #pragma unroll 1
+      for (int r = 0; r < S::P && !any; ++r) any = attended(j * S::P + r);
+    int tot;
+    const int pos = block_scan(any, sm.wsum, tot);
+    if (any) {
+      plist[nlist + pos] = j;
+      ppage[nlist + pos] = a.page_table[(size_t)b * a.pt_stride + lp0 + j];
+    }
+    nlist += tot;
+  }
+  if (nlist == 0) {
+    if (tid < HQ) aml[((size_t)b * HQ + tid) * nCTAp + c] = make_float2(-INFINITY, 0.f);
+    fence_proxy_async_global();
+    __syncthreads();
+    return true;
+  }
+  if (warp == 0) tmem_alloc(&sm.tmem, TCOLS);   // (no relinquish: another sequence may allocate again)
+  if (tid == 0) {
+    #pragma unroll 1
+    for (int s = 0; s < nslot; ++s) mbar_init(&full[s], 1);
+    mbar_init(&mmad[0], 1);
+    mbar_init(&mmad[1], 1);
+    mbar_fence_init();
+  }
+  if (tid < HQ) sm.att_m[tid] = -INFINITY;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+  int issued = 0;   // pages whose copies were issued (thread 0)
+  auto issue = [&](int k) {
+    const int s = k % nslot, j = plist[k], page = ppage[k];
+    const bool ok = page >= 0 && (int64_t)page < a.num_pages;
+    pv_ok[s] = ok;
+    mbar_arrive_expect_tx(&full[s], (ok ? VPAGE : 0) + LROWS);
+    if (ok) {
+      const uint64_t pol = l2_evict_first_policy();     // each V row is read once
+      tma_load_2d(vslots + (size_t)s * VPAGE, &a.tmap_v, 0, page * ROWS, &full[s], pol);
+      tma_load_2d(vslots + (size_t)s * VPAGE + VHALF, &a.tmap_v, 64, page * ROWS, &full[s], pol);
+    } else {
+      set_error(a.status, TS_ERR_PAGE_OOB);
+    }
+    bulk_g2s(lslots + (size_t)s * (LROWS / 4), eb + (size_t)j * S::P * HQ, LROWS, &full[s]);
+    ++issued;
+  };
+  if (tid == 0) {
+    fence_proxy_async_global();
+    #pragma unroll 1
+    for (int k = 0; k < min(nslot, nlist); ++k) issue(k);
+  }
+  // a time-out: the copies issued and the MMAs committed land first, then TMEM is freed
+  auto bail = [&](int kdone) -> bool {
+    if (tid == 0) {
+      set_error(a.status, TS_ERR_TIMEOUT);
+      atomicExch(&a.gsync->abort, 1u);
+      #pragma unroll 1
+      for (int kk = kdone; kk < issued; ++kk) mbar_wait(&full[kk % nslot], (kk / nslot) & 1, a.wait_ns);
+      if (kdone > 0) mbar_wait(&mmad[(kdone - 1) & 1], ((kdone - 1) >> 1) & 1, a.wait_ns);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(tmem, TCOLS);
+    }
+    return false;
+  };
+  const bool wt = tid < S::P * HQ;
+  const int wr = tid / HQ, wh = tid % HQ;
+  KahanF lsum;
+  bool started = false;   // the accumulators hold a page (uniform)
+  #pragma unroll 1
+  for (int k = 0; k < nlist; ++k) {
+    const int s = k % nslot, kb = k & 1, j = plist[k];
+    // the weight buffer and the V slot of page k - 2 are free once its MMAs have completed: the
+    // slot takes page k - 2 + nslot
+    bool landed = true;
+    if (tid == 0 && k >= 2) {
+      landed = mbar_wait(&mmad[kb], ((k - 2) >> 1) & 1, a.wait_ns);
+      if (landed && k - 2 + nslot < nlist) issue(k - 2 + nslot);
+    }
+    landed = mbar_wait(&full[s], (k / nslot) & 1, a.wait_ns) && landed;
+    const float* Lp = lslots + (size_t)s * (LROWS / 4);
+    const int nv = min(S::P, ntok - j * S::P);
+    float xl = -INFINITY;
+    bool att = false;
+    if (wt && landed) {
+      att = wr < nv && pv_ok[s] && attended(j * S::P + wr);
+      if (att) xl = Lp[wr * HQ + wh];
+    }
+    const bool need = att && xl - sm.att_m[wh] > kRescaleGap;
+    if (__syncthreads_or(!landed || need)) {
+      if (__syncthreads_or(!landed)) return bail(k);
+      float* Wm = reinterpret_cast<float*>(bbuf + (size_t)kb * BBUF);   // scratch: the page's masked logits
+      if (wt) Wm[tid] = xl;
+      __syncthreads();
+      if (tid < HQ) {
+        float pm = -INFINITY;
+        #pragma unroll 1
+        for (int r = 0; r < S::P; ++r) pm = fmaxf(pm, Wm[r * HQ + tid]);
+        const float m0 = sm.att_m[tid];
+        const float mn = fmaxf(m0, pm);
+        sm.att_c[tid] = m0 == -INFINITY ? 0.f : exp2f(m0 - mn);
+        sm.att_m[tid] = mn;
+      }
+      bool mma_ok = true;
+      if (started && tid == 0) mma_ok = mbar_wait(&mmad[(k - 1) & 1], ((k - 1) >> 1) & 1, a.wait_ns);
+      if (!__syncthreads_and(mma_ok)) return bail(k);
+      if (wt) {
+        lsum.s *= sm.att_c[wh];
+        lsum.c *= sm.att_c[wh];
+      }
+      if (started) {
+        // the accumulators of every query head, scaled by its correction (lanes = columns of d)
+        tc_fence_after();
+        if (warp < 4) {
+          #pragma unroll 1
+          for (int g = 0; g < HKV; ++g)
+#pragma unroll
+            for (int c0 = 0; c0 < 16; c0 += 8) {
+              const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(g * 16 + c0);
+              float r[8];
+              tmem_ld_x8(ta, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int col = c0 + i, jj = col < G ? col : col - G;
+                r[i] *= col < 2 * G ? sm.att_c[g * G + jj] : 1.f;
+              }
+              tmem_st_x8(ta, r);
+            }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+      }
+      __syncthreads();
+    }
+    // ---- the weights into buffer kb as two bf16 terms, rows j (hi) and G + j (lo) of the KV head
+    unsigned char* bk = bbuf + (size_t)kb * BBUF;
+    if (wt) {
+      const float w = att ? exp2f(xl - sm.att_m[wh]) : 0.f;
+      lsum.add(w);
+      const int g = wh / G, jj = wh % G;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
+      *reinterpret_cast<__nv_bfloat16*>(bk + g * BTILE + b_off(jj, wr)) = hi;
+      *reinterpret_cast<__nv_bfloat16*>(bk + g * BTILE + b_off(G + jj, wr)) = lo;
+    }
+    // the weight rows past 2 G and a partial page's V rows past the sequence are zero (a zero
+    // weight times a NaN is a NaN)
+    for (int i = tid; i < HKV * (16 - 2 * G) * 2; i += S::THREADS) {
+      const int g = i / ((16 - 2 * G) * 2), rr = 2 * G + (i / 2) % (16 - 2 * G), kg = i & 1;
+      *reinterpret_cast<uint4*>(bk + g * BTILE + b_off(rr, kg * 8)) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    const bool vok = pv_ok[s] != 0;
+    if (vok && nv < S::P) {
+      unsigned char* vp = vslots + (size_t)s * VPAGE;
+      const int nz = HKV * (S::P - nv);                  // rows (g, token >= nv), both halves, 8 chunks each
+      for (int i = tid; i < nz * 16; i += S::THREADS) {
+        const int row = i / 16, ch = i % 16, g = row / (S::P - nv), t = nv + row % (S::P - nv);
+        *reinterpret_cast<uint4*>(vp + (ch >> 3) * VHALF + (g * S::P + t) * 128 + (ch & 7) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      if (vok) {
+        const uint32_t va = smem_addr(vslots + (size_t)s * VPAGE), ba = smem_addr(bk);
+        #pragma unroll 1
+        for (int g = 0; g < HKV; ++g)
+          umma_bf16(tmem + (uint32_t)(g * 16), sdesc_sw128_mn(va + g * S::P * 128, VHALF, 1024),
+                    sdesc_kmajor_none(ba + g * BTILE, 128, 256), idesc, started);
+      }
+      umma_commit(&mmad[kb]);     // (with no MMA it arrives at once: the phases stay in step)
+    }
+    started = started || vok;
+  }
+  // ---- every MMA done: outputs from TMEM (warps 0..3: lane = column of d), sums, the CTA's partial
+  bool done = true;
+  if (tid == 0) done = mbar_wait(&mmad[(nlist - 1) & 1], ((nlist - 1) >> 1) & 1, a.wait_ns);
+  if (!__syncthreads_and(done)) return bail(nlist);
+  tc_fence_after();
+  float* red = reinterpret_cast<float*>(vslots);                 // [HQ][D] (the slots are spent)
+  float* lred = red + (size_t)HQ * D;                            // [16][HQ]
+  if (warp < 4) {
+    #pragma unroll 1
+    for (int g = 0; g < HKV; ++g) {
+      float r[16];
+      const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(g * 16);
+      tmem_ld_x8(ta, *reinterpret_cast<float(*)[8]>(r));
+      tmem_ld_x8(ta + 8, *reinterpret_cast<float(*)[8]>(r + 8));
+      tmem_wait_ld();
+#pragma unroll
+      for (int jj = 0; jj < G; ++jj)
+        red[(size_t)(g * G + jj) * D + warp * 32 + lane] = started ? r[jj] + r[G + jj] : 0.f;
+    }
+  }
+  if (wt) lred[tid] = lsum.s - lsum.c;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TCOLS);
+  }
+  if (tid == 0) {
+    #pragma unroll 1
+    for (int s = 0; s < nslot; ++s) mbar_inval(&full[s]);
+    mbar_inval(&mmad[0]);
+    mbar_inval(&mmad[1]);
   }
   const int Dq = D / dq;
   #pragma unroll 1
@@ -1634,10 +1943,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         // registers, reduced into the CTA's partials at the end; warps 8.. finish the set-up
         const int nsl = a.nslot_tc;
         float* eb = a.spill + (size_t)c * sm.region;             // [tok_stride][H]
-        if (warp == 2) {
-          tmem_alloc(&sm.tmem, 2 * S::TC_COLS);
-          tmem_relinquish();
-        }
+        if (warp == 2) tmem_alloc(&sm.tmem, 2 * S::TC_COLS);   // (the permit is kept: the range
+                                                                // attention allocates again later)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
@@ -2516,6 +2823,12 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     constexpr int NWG = S::NW / HKV;
     const int gw = warp % HKV, wsl = warp / HKV;
     constexpr bool kRangeGeom = D % 8 == 0 && S::THREADS % (HKV * (D / 8)) == 0 && S::P * HQ <= S::THREADS;
+    // the tensor-core variant: bf16 pools, d = 128 (M = the columns of d), the two weight terms of
+    // the G heads in 16 columns, and its ring (at least two slots) with the outputs' reduction
+    // inside the V slots
+    constexpr bool kRangeTC = S::TC && D == 128 && 2 * G <= 16 && HKV * 16 <= 256 &&
+                              range_tc_slots<D, HKV, G>(kStageMin, kStepFlagCap) >= 2 &&
+                              (HQ * D + S::P * HQ) * 4 <= 2 * HKV * S::P * D * 2;
     if (bal) {
       // top-p sequences that take the range attention: every CTA attends the attended tokens of
       // its own scanned range, when the selection is dense enough that streaming each range's
@@ -2526,8 +2839,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       const int rslots =
           min(kRangeSlots, (stage_bytes - kRangeSlots * 8 - (2 * (a.flag_cap / S::P) + kRangeSlots) * 4) / RSLOT);
       const bool range_ok = kRangeGeom && bal && a.range_attend > 0 && sm.hpw == HKV && !sm.scan_dyn &&
-                            rslots >= 2 &&
-                            HQ * D * 4 + S::P * HQ * 4 <= rslots * RSLOT;
+                            ((kRangeTC && a.tcv) || (rslots >= 2 && HQ * D * 4 + S::P * HQ * 4 <= rslots * RSLOT));
       #pragma unroll 1
       for (int b = 0; b < B; ++b) {
         const SeqState& st = sm.seq[b];
@@ -2568,6 +2880,13 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       if (bal && sm.bal.range_b[b]) {
         const int sgr = sm.my_seg_of[b];
         if (sgr >= 0) {
+          if constexpr (kRangeTC) {
+            if (a.tcv) {
+              if (!range_attend_tc<KT, D, HKV, G>(a, sm, dsm, stage_bytes, selflag, b, sgr, ao, aml, nCTAp, dq))
+                return;
+              continue;
+            }
+          }
           if constexpr (kRangeGeom)
             if (!range_attend<KT, D, HKV, G>(a, sm, dsm, stage_bytes, selflag, b, sgr, ao, aml, nCTAp, dq)) return;
         } else {
@@ -3221,25 +3540,32 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   a.tc = 0;
   a.nslot_tc = 0;
   a.scan_dyn = 0;
+  a.tcv = 0;
   if constexpr (S::TC) {
     // tensor-core scan: 1024-aligned ring of page tiles plus two query-term images
     const int nslot_tc = std::min(kMaxSlots, (dyn - flag_cap - 1024 - 2 * S::TC_BIMG) / S::TC_TILE);
-    if (!ctx->no_tc && nslot_tc >= 2 && (c.phases & kPhScore) && c.k_pool && (reinterpret_cast<uintptr_t>(c.q) & 15) == 0) {
-      auto& cache = ctx->kmaps;   // a few recent pools (one per layer in a decode loop)
+    // the tensor map of a pool, from a cache of recent ones (one per layer and pool in a decode
+    // loop), or null when it cannot be encoded
+    auto pool_map = [&](const void* pool) -> const void* {
+      auto& cache = ctx->kmaps;
+      constexpr int n = (int)(sizeof(cache) / sizeof(cache[0]));
       int hitc = -1;
-      for (int i = 0; i < (int)(sizeof(cache) / sizeof(cache[0])); ++i)
-        if (cache[i].pool == c.k_pool && cache[i].num_pages == cfg.num_pages) hitc = i;
+      for (int i = 0; i < n; ++i)
+        if (cache[i].pool == pool && cache[i].num_pages == cfg.num_pages) hitc = i;
       if (hitc < 0) {
         hitc = ctx->kmap_next;
-        ctx->kmap_next = (ctx->kmap_next + 1) % (int)(sizeof(cache) / sizeof(cache[0]));
+        ctx->kmap_next = (ctx->kmap_next + 1) % n;
         cache[hitc].pool = nullptr;
-        if (encode_kmap(reinterpret_cast<CUtensorMap*>(cache[hitc].map), c.k_pool, cfg.num_pages, D, S::TC_ROWS)) {
-          cache[hitc].pool = c.k_pool;
+        if (encode_kmap(reinterpret_cast<CUtensorMap*>(cache[hitc].map), pool, cfg.num_pages, D, S::TC_ROWS)) {
+          cache[hitc].pool = pool;
           cache[hitc].num_pages = cfg.num_pages;
         }
       }
-      if (cache[hitc].pool == c.k_pool) {
-        std::memcpy(&a.tmap_k, cache[hitc].map, sizeof(CUtensorMap));
+      return cache[hitc].pool == pool ? cache[hitc].map : nullptr;
+    };
+    if (!ctx->no_tc && nslot_tc >= 2 && (c.phases & kPhScore) && c.k_pool && (reinterpret_cast<uintptr_t>(c.q) & 15) == 0) {
+      if (const void* m = pool_map(c.k_pool)) {
+        std::memcpy(&a.tmap_k, m, sizeof(CUtensorMap));
         a.tc = 1;
         a.nslot_tc = nslot_tc;
         // CTAs may claim pages of one or two scanned sequences from a shared counter instead of
@@ -3247,6 +3573,15 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
         // bandwidth differs between SMs, but which CTA sums which pages then varies, so repeated
         // runs may differ in the last bits.
         a.scan_dyn = (ctx->scan_claim && S::TC_PAGES == 1) ? 1 : 0;   // tiles of one page only
+      }
+    }
+    // the V map for the tensor-core range attention of top-p (d = 128, enough staging memory; on
+    // request only: eight MMAs of N = 16 per page measured slower than P.V on the CUDA cores)
+    if (D == 128 && a.tc && c.params.mode == TS_SELECT_TOPP && ctx->range_tc && c.v_pool &&
+        dyn - flag_cap - 2 * kOwnBatch * (int)sizeof(int) >= kStageMin) {
+      if (const void* m = pool_map(c.v_pool)) {
+        std::memcpy(&a.tmap_v, m, sizeof(CUtensorMap));
+        a.tcv = 1;
       }
     }
   }

@@ -89,6 +89,18 @@ __device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, float (&r)[8]) {
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 8 consecutive 32-bit columns of this warp's 32 lanes from registers: lane i of the warp writes
+// row (taddr lane + i), columns col .. col + 7.
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const float (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               "r"(__float_as_uint(r[0])), "r"(__float_as_uint(r[1])), "r"(__float_as_uint(r[2])),
+               "r"(__float_as_uint(r[3])), "r"(__float_as_uint(r[4])), "r"(__float_as_uint(r[5])),
+               "r"(__float_as_uint(r[6])), "r"(__float_as_uint(r[7]))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // ------------------------------------------------------------------- MMA
 
 // Shared-memory matrix descriptor of a K-major, 128-byte-swizzled operand
@@ -104,6 +116,32 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor of a K-major operand without swizzle starting at addr (16-byte
+// aligned): core matrices of 8 rows x 16 bytes (8 elements of K) stored as 128 contiguous bytes,
+// the next 8 elements of K `lbo` bytes on, the next 8 rows `sbo` bytes on.
+__device__ __forceinline__ uint64_t sdesc_kmajor_none(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);          // start address
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;       // leading byte offset: the next 8 of K
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;       // stride byte offset: the next 8 rows
+  d |= (uint64_t)1 << 46;                            // version (swizzle mode 0: none)
+  return d;
+}
+
+// Shared-memory matrix descriptor of an MN-major, 128-byte-swizzled operand starting at addr:
+// rows of 128 bytes hold 64 consecutive elements of the M (or N) dimension, one row per element of
+// K; groups of 8 K-rows are `sbo` bytes apart and the next 64 elements of M are `lbo` bytes on. A
+// tiled TMA load with CU_TENSOR_MAP_SWIZZLE_128B whose rows run along K writes this layout.
+__device__ __forceinline__ uint64_t sdesc_sw128_mn(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);          // start address
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;       // leading byte offset: the next 64 of M
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;       // stride byte offset: the next 8 of K
+  d |= (uint64_t)1 << 46;                            // version
+  d |= (uint64_t)2 << 61;                            // 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor of kind::f16: bf16 A and B (both K-major), fp32 D,
 // M x N tile.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
@@ -113,6 +151,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | ((uint32_t)(N >> 3) << 17)    // N / 8
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
+
+// The same with A MN-major (transposed: M contiguous in shared memory).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_amn(int M, int N) { return idesc_bf16_f32(M, N) | (1u << 15); }
 
 // D[tmem] (+)= A[smem] x B[smem]^T over one K-step of 16, issued by one thread.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
