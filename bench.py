@@ -116,7 +116,8 @@ PHASES = {0: "start", 1: "setup", 5: "lengths", 6: "cache-test", 7: "partition",
           37: "h1-start", 38: "h1-zeroed", 39: "h1-counted", 40: "h1-barrier", 41: "h2-start",
           42: "h2-zeroed", 43: "h2-counted", 44: "h2-barrier", 45: "coarse", 46: "fine", 47: "classified",
           48: "cand-barrier", 49: "cand-fetched", 50: "ranked", 51: "att-q", 52: "att-fixed", 53: "att-own",
-          54: "merge-fetched", 55: "counts"}
+          54: "merge-fetched", 55: "counts", 56: "scanned-last", 57: "votes-last", 58: "classified-last",
+          59: "flags-last"}
 
 
 def print_phases(b, step):
@@ -125,7 +126,10 @@ def print_phases(b, step):
     t0 = ph[0]
     pts = sorted((v - t0, i) for i, v in enumerate(ph) if v and i in PHASES and v >= t0)
     hit = bool(b.hit[b.sp.layers - 1][0])
-    print(f"step {step} hit={hit}: " + " ".join(f"{PHASES[i]} {dt / 1000:.1f}" for dt, i in pts))
+    last = " ".join(f"{PHASES[i - 4]}-cta {ph[i] & 255}" for i in (61, 62, 63) if ph[i])
+    if ph[60]:
+        last += f" most-crossing-per-warp {ph[60] >> 32} (candidates {(ph[60] >> 8) & 0xffffff}, cta {ph[60] & 255})"
+    print(f"step {step} hit={hit}: " + " ".join(f"{PHASES[i]} {dt / 1000:.1f}" for dt, i in pts) + " " + last)
 
 
 # ------------------------------------------------------------ distributed

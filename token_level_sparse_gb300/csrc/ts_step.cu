@@ -509,11 +509,25 @@ struct Smem {
 // histogram started / zeroed / counted (added: 28 + l) / barrier passed; 45 / 46 coarse / fine bins
 // fetched; 47 classified, 48 candidate barrier passed, 49 candidates fetched, 50 ranked; 51
 // attention queries loaded, 52 fixed rows requested, 53 own rows requested; 54 first merge
-// item fetched, 55 counts read. (The marks of waves past the first share slots 5..19 with the
+// item fetched, 55 counts read. Over all CTAs, the latest to finish the tensor-core scan (56), the
+// votes (57), the classification (58) and the selection flags (59); 61..63: which CTA that was
+// for 57..59. (The marks of waves past the first share slots 5..19 with the
 // others; slots 17 and 18 also take the latest start and end over all CTAs.)
 #define TS_MARK(i)                                                     \
   do {                                                                 \
     if (c == 0 && tid == 0 && a.phase_ns) a.phase_ns[i] = globaltimer_ns(); \
+  } while (0)
+// the latest time over all CTAs at which one reaches phase boundary i (the clock only grows, so
+// the slot needs no reset between launches)
+#define TS_LAST(i)                                                                  \
+  do {                                                                              \
+    if (tid == 0 && a.phase_ns) atomicMax(&a.phase_ns[i], (unsigned long long)globaltimer_ns()); \
+  } while (0)
+// and which CTA it was: the low 48 bits of the clock above the CTA index (slot i + 4)
+#define TS_LAST_CTA(i)                                                                         \
+  do {                                                                                         \
+    if (tid == 0 && a.phase_ns)                                                                \
+      atomicMax(&a.phase_ns[(i) + 4], ((globaltimer_ns() & ((1ull << 48) - 1)) << 8) | (unsigned)c); \
   } while (0)
 
 // One wave of the CUDA-core scan (geometries and launches without the tensor-core scan): the
@@ -2266,6 +2280,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           return;
         }
         TS_MARK(2);
+        TS_LAST(56);
         fence_proxy_async_global();
         // the first chunk of my logits (all written by this CTA) comes back into shared memory
         // while the other CTAs finish their scans
@@ -2301,6 +2316,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
   }
 
   TS_MARK(20);
+  TS_LAST(57);
+  TS_LAST_CTA(57);
   // ======================================================================== SELECT
   // (nothing to select when every sequence hits or is empty: no pages were partitioned)
   if ((a.phases & kPhSelect) && sm.ptot > 0) {
@@ -2638,6 +2655,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       }
     }
     TS_MARK(47);
+    TS_LAST(58);
+    TS_LAST_CTA(58);
     if (need_cand || need_tie) {
       if (!grid_sync(a.gsync, a.status, &sm.gepoch, a.wait_ns, a.skip_cta, a.skip_barrier)) return;
     }
@@ -2695,19 +2714,48 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         }
         __syncthreads();                                  // red_i is reused below
       }
-      // tokens of the crossing bin: the warp ranks each against the gathered list
+      // tokens of the crossing bin (at most kCandCap in a sequence): listed in token order, then
+      // dealt out round-robin over the warps, each ranked against the gathered candidates (a
+      // warp's 32 tokens have their votes loaded at once, one per lane)
       if (st.cand) {
+        int* xl = reinterpret_cast<int*>(scand + kCandCap);
+        int nxw = 0;
+        #pragma unroll 1
+        for (int i0 = w0; i0 < w1; i0 += 32) nxw += __popc(__ballot_sync(kFull, i0 + lane < w1 && fl[i0 + lane] == 2));
+        if (lane == 0) sm.red_i[0][warp] = nxw;
+        __syncthreads();
+        int xbase = 0, nx = 0;
+        #pragma unroll 1
+        for (int w = 0; w < S::NW; ++w) {
+          if (w < warp) xbase += sm.red_i[0][w];
+          nx += sm.red_i[0][w];
+        }
         #pragma unroll 1
         for (int i0 = w0; i0 < w1; i0 += 32) {
-          unsigned bal = __ballot_sync(kFull, i0 + lane < w1 && fl[i0 + lane] == 2);
-          while (bal) {
-            const int ii = i0 + __ffs(bal) - 1;
-            bal &= bal - 1u;
-            const uint32_t kk = __float_as_uint(__ldcg(vb + tl0 + ii));
+          const bool cr = i0 + lane < w1 && fl[i0 + lane] == 2;
+          const unsigned bal = __ballot_sync(kFull, cr);
+          const int pos = xbase + __popc(bal & ((1u << lane) - 1u));
+          if (cr && pos < kCandCap) xl[pos] = i0 + lane;
+          xbase += __popc(bal);
+        }
+        __syncthreads();
+        nx = min(nx, kCandCap);
+        int ncross = 0;
+        #pragma unroll 1
+        for (int x0 = warp; x0 < nx; x0 += 32 * S::NW) {
+          const int xi = x0 + lane * S::NW;
+          const int myii = xi < nx ? xl[xi] : -1;
+          const uint32_t mykey = myii >= 0 ? __float_as_uint(__ldcg(vb + tl0 + myii)) : 0u;
+          const int nloc = min(32, (nx - x0 + S::NW - 1) / S::NW);
+          ncross += nloc;
+          #pragma unroll 1
+          for (int q = 0; q < nloc; ++q) {
+            const int ii = __shfl_sync(kFull, myii, q);
+            const uint32_t kk = __shfl_sync(kFull, mykey, q);
             const unsigned long long me = ((unsigned long long)kk << 32) | (0xffffffffu - (uint32_t)(tl0 + ii));
             unsigned above = 0;
             unsigned long long cum = 0;
-            #pragma unroll 1
+            #pragma unroll 8   // independent loads in flight together
             for (int j = lane; j < m_cand; j += 32) {
               const unsigned long long y = scand[j];
               if (y > me) {
@@ -2721,9 +2769,13 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
               cum += __shfl_xor_sync(kFull, cum, d);
             }
             if (lane == 0) fl[ii] = (topp ? (cum < st.mass_rem) : (above < (unsigned)st.k_rem)) ? 1 : 0;
-            __syncwarp();
           }
         }
+        // diagnosis (slot 60): the most crossing tokens one warp ranked, above the candidate count
+        // and the CTA
+        if (lane == 0 && a.phase_ns)
+          atomicMax(&a.phase_ns[60], ((unsigned long long)ncross << 32) | ((unsigned long long)m_cand << 8) | (unsigned)c);
+        __syncthreads();   // every flag decided before the counts below
       }
       TS_MARK(50);
       // counts per warp (all, in [s_end, ls), below s_end), then the list in token order, the list
@@ -2774,6 +2826,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
   }
 
   TS_MARK(23);
+  TS_LAST(59);
+  TS_LAST_CTA(59);
   // With top-p the selected tokens can crowd into a few CTAs' ranges: after one more barrier
   // every CTA takes an equal share of each sequence's selected tokens (the CTAs' lists in
   // order, a fixed assignment) instead of its own
@@ -3451,7 +3505,7 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   const int nslot = std::min(kMaxSlots, (dyn - flag_cap) / S::STAGE_BYTES);
   // (the vote pass keeps (max, 1/sum) per segment and head, one segment's CTA partials and
   // per-warp reductions; the merge one (sequence, head)'s CTA rows)
-  if (nslot < S::MIN_SLOTS || dyn - flag_cap < lvl_bins(0) * 12 || dyn - flag_cap < kCandCap * 8 ||
+  if (nslot < S::MIN_SLOTS || dyn - flag_cap < lvl_bins(0) * 12 || dyn - flag_cap < kCandCap * 12 ||
       dyn - flag_cap < kMaxB * 128 * 12 ||
       dyn - flag_cap < kMaxB * kMaxWaveHeads * 8 + ctx->num_sms * S::PV * ctx->cfg.n_q_heads * 8 + 2 * 16 * 32 * 4 + 16 +
                            kVoteBufs * 16 * kMaxWaveHeads * 4 ||   // vote scratch, then the chunks of 16 logit rows
