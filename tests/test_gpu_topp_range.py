@@ -11,6 +11,9 @@ Checks:
 - trajectories against the oracle on each path (votes, index sets in the tie band, outputs
   within 2e-3 per row, lse within 1e-3);
 - the same step on both paths gives the same index sets and outputs within the tolerance;
+- cache hits of dense selections take the range attention too (the cached part, sinks and window
+  over an even split of the pages, logits computed from K): against the oracle and the gathered
+  attention over trajectories with hits;
 - keys whose norms cycle over every four pages move the running max on many pages (the
   rescale path), against the oracle;
 - the geometries of the other workloads (GQA 7 with 4 KV heads; fp32 pools with d = 64).
@@ -71,6 +74,37 @@ def test_topp_paths_agree(monkeypatch):
                 where = f"{other} step {t} seq {i}"
                 assert np.array_equal(a["idx"][i], b["idx"][i]), f"{where}: index sets differ"
                 check_attention(b["out"][i], b["lse"][i], a["out"][i], a["lse"][i], where)
+
+
+@pytest.mark.parametrize("path", ["range", "gather", "auto"])
+def test_topp_hits_against_the_oracle(path, monkeypatch):
+    # theta 0.9 on a slowly drifting query: most steps hit, and p = 0.95 keeps most tokens
+    _set_path(monkeypatch, path)
+    sp = W.spec(4, n0=(20000, 5000, 33000, 2100), steps=6, top_p=0.95, rho=0.995)
+    rep = run_trajectory(W.generate(sp, DEV), 6)
+    _report(path, rep)
+    assert rep.hits >= 8
+
+
+def test_topp_hit_paths_agree(monkeypatch):
+    sp = W.spec(4, n0=(20000, 5000, 33000, 12000), steps=5, top_p=0.9, rho=0.995)
+    wl = W.generate(sp, DEV)
+    res = {}
+    for path in ("gather", "range"):
+        _set_path(monkeypatch, path)
+        r = GpuRunner(wl)
+        res[path] = [r.step(t) for t in range(5)]
+        r.ctx.close()
+    nhit = 0
+    for t in range(5):
+        a, b = res["gather"][t], res["range"][t]
+        assert np.array_equal(a["hit"], b["hit"]), f"step {t}: cache decisions differ"
+        for i in range(sp.batch):
+            where = f"step {t} seq {i} hit={bool(a['hit'][i])}"
+            assert np.array_equal(a["idx"][i], b["idx"][i]), f"{where}: index sets differ"
+            check_attention(b["out"][i], b["lse"][i], a["out"][i], a["lse"][i], where)
+            nhit += int(a["hit"][i])
+    assert nhit >= 8
 
 
 @pytest.mark.parametrize("path", ["range", "range_tc", "gather"])

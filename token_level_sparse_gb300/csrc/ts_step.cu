@@ -738,45 +738,105 @@ __device__ __noinline__ bool cuda_scan_wave(const StepKArgs& a, Smem& sm, unsign
 }
 
 
+// Ring slots of the range attention (hit: pages of K too) that fit `stage_bytes`, or 0 below two.
+template <typename KT, int D, int HKV, int G, bool HIT>
+__host__ __device__ constexpr int range_slots(int stage_bytes, int flag_cap) {
+  constexpr int VPAGE = HKV * kPage * D * (int)sizeof(KT), LROWS = kPage * HKV * G * 4;
+  constexpr int SLOT = (HIT ? 2 : 1) * VPAGE + 2 * LROWS;
+  const int n = (stage_bytes - kRangeSlots * 8 - (3 * (flag_cap / kPage) + kRangeSlots) * 4) / SLOT;
+  return n < 2 ? 0 : (n > kRangeSlots ? kRangeSlots : n);
+}
+
 // Range attention, for dense selections (top-p keeping a large share of a sequence): I attend the
-// tokens of my own scanned range of sequence b that are selected, sinks or in the window. Their
-// logits are the scan's (base 2, still in my scratch region), so K is not read again; each page
-// with an attended token brings its V rows of every KV head and its 16 logit rows into a ring by
-// bulk copy. Weights are 2^(l - m) against a running max m per head, which moves only when a logit
-// passes it by more than kRescaleGap (then sums and outputs are rescaled once). A thread owns (KV
-// head, 8 columns) for the G query heads of that KV head over a share of each page's tokens, in
-// packed fp32 pairs. The
-// CTA's partial (o, max in natural units, sum) goes where the gathered attention puts it. False
-// after a time-out (recorded, the abort word raised, the copies in flight waited for).
-template <typename KT, int D, int HKV, int G>
+// tokens of a range of pages of sequence b that are selected, sinks or in the window.
+//  * A miss (HIT false): the range is my own scanned segment sgi, the tokens are those flagged
+//    selected, and their logits are the scan's (base 2, still in my scratch region), so K is not
+//    read again; each page with an attended token brings its V rows of every KV head and its 16
+//    logit rows into a ring by bulk copy.
+//  * A hit of the Selection Cache (HIT true): nothing was scanned; the sequence's pages are split
+//    evenly over the CTAs, the tokens are the cached part (an ascending list) with the sinks and
+//    the window, and each page brings its K and V rows; the warps of a KV head compute its 16
+//    tokens' logits for the G heads (as the scan does: base 2, fp32).
+// Weights are 2^(l - m) against a running max m per head, which moves only when a logit passes it
+// by more than kRescaleGap (then sums and outputs are rescaled once). A thread owns (KV head, 8
+// columns) for the G query heads of that KV head over a share of each page's tokens, in packed
+// fp32 pairs. The CTA's partial (o, max in natural units, sum) goes where the gathered attention
+// puts it. False after a time-out (recorded, the abort word raised, the copies in flight waited
+// for).
+template <typename KT, int D, int HKV, int G, bool HIT>
 __device__ __noinline__ bool range_attend(const StepKArgs& a, Smem& sm, unsigned char* stage, int stage_bytes,
                                           const uint8_t* selflag, int b, int sgi, float* ao, float2* aml,
                                           int nCTAp, int dq) {
   using S = StepShape<KT, D, HKV, G>;
   constexpr int HQ = HKV * G, D4 = D / 4, D8 = D / 8, PVT = HKV * D8, NSPL = S::THREADS / PVT;
   constexpr int EPC = KV<KT>::kPerChunk;             // elements of a 16-byte chunk of V
-  constexpr int VPAGE = S::STAGE_BYTES;              // one V page of every KV head, [g][16][D]
+  constexpr int EPL = D / 32;                        // hit scores: dimensions per lane
+  constexpr int NWG = S::NW / HKV;                   // hit scores: warps per KV head
+  constexpr int VPAGE = S::STAGE_BYTES;              // one V (or K) page of every KV head, [g][16][D]
   constexpr int LROWS = S::P * HQ * 4;               // its 16 logit rows [16][H]
-  constexpr int SLOT = VPAGE + 2 * LROWS;            // then the weights [16][H]
+  constexpr int SLOT = (HIT ? 2 : 1) * VPAGE + 2 * LROWS;   // [V][K (hit)][logits][weights]
   static_assert(S::THREADS % PVT == 0 && S::P * HQ <= S::THREADS && SLOT % 16 == 0 && D % 8 == 0 && 8 % EPC == 0,
                 "range attention layout");
   constexpr float kLn2 = 0.693147180559945309f;
-  const int tid = threadIdx.x, c = blockIdx.x, nCTA = gridDim.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, c = blockIdx.x, nCTA = gridDim.x;
   const SeqState& st = sm.seq[b];
-  const int t0l = sm.seg_t0[sgi], lp0 = sm.seg_lp0[sgi], ntok = sm.seg_ntok[sgi];
+  int lp0, ntok;
+  const uint8_t* fl = nullptr;
+  const float* eb = nullptr;
+  if constexpr (HIT) {
+    const int npg_seq = (st.n + S::P - 1) / S::P;
+    const int pa = (int)((int64_t)c * npg_seq / nCTA), pb = (int)((int64_t)(c + 1) * npg_seq / nCTA);
+    lp0 = pa;
+    ntok = max(0, min((pb - pa) * S::P, st.n - pa * S::P));
+  } else {
+    const int t0l = sm.seg_t0[sgi];
+    lp0 = sm.seg_lp0[sgi];
+    ntok = sm.seg_ntok[sgi];
+    fl = selflag + t0l;                                                // my flags of the segment
+    eb = a.spill + (size_t)c * sm.region + (size_t)t0l * HQ;           // its logit rows
+  }
   const int npg = (ntok + S::P - 1) / S::P;
-  const uint8_t* fl = selflag + t0l;                                   // my flags of the segment
-  const float* eb = a.spill + (size_t)c * sm.region + (size_t)t0l * HQ;  // its logit rows
-  const int nslot =
-      min(kRangeSlots, (stage_bytes - kRangeSlots * 8 - (2 * (a.flag_cap / S::P) + kRangeSlots) * 4) / SLOT);
+  const int nslot = range_slots<KT, D, HKV, G, HIT>(stage_bytes, a.flag_cap);   // >= 2: checked by the caller
   uint64_t* bars = reinterpret_cast<uint64_t*>(stage + (size_t)nslot * SLOT);
   int* plist = reinterpret_cast<int*>(bars + kRangeSlots);            // my pages with an attended token
   int* ppage = plist + a.flag_cap / S::P;                              // and their page ids
-  int* pv_ok = ppage + a.flag_cap / S::P;                              // per slot: its V page is valid
+  int* pv_ok = ppage + a.flag_cap / S::P;                              // per slot: its pages are valid
+  uint32_t* pmask = reinterpret_cast<uint32_t*>(pv_ok + kRangeSlots);  // hit: attended tokens per page
   auto attended = [&](int i) -> bool {                                 // token lp0 * 16 + i of the sequence
-    const int t = lp0 * S::P + i;
-    return i < ntok && (t < st.s_end || t >= st.ls || fl[i] == 1);
+    if constexpr (HIT) {
+      return i < ntok && ((pmask[i >> 4] >> (i & 15)) & 1u);
+    } else {
+      const int t = lp0 * S::P + i;
+      return i < ntok && (t < st.s_end || t >= st.ls || fl[i] == 1);
+    }
   };
+  if constexpr (HIT) {
+    // the attended tokens of my pages: sinks, window and the cached part inside my range
+    const int tb = lp0 * S::P;
+    #pragma unroll 1
+    for (int j = tid; j < npg; j += S::THREADS) pmask[j] = 0u;
+    __syncthreads();
+    #pragma unroll 1
+    for (int i = tid; i < ntok; i += S::THREADS)
+      if (tb + i < st.s_end || tb + i >= st.ls) atomicOr(&pmask[i >> 4], 1u << (i & 15));
+    const int32_t* ctb = a.ct + (size_t)b * a.cap + sm.ct_lo[b];
+    const int nct = sm.ct_hi[b] - sm.ct_lo[b];
+    if (warp == 0) {
+      int r1, r2;
+      warp_lower_bound2(ctb, nct, tb, tb + ntok, r1, r2);
+      if (lane == 0) {
+        sm.red_i[0][0] = r1;
+        sm.red_i[0][1] = r2;
+      }
+    }
+    __syncthreads();
+    #pragma unroll 1
+    for (int j = sm.red_i[0][0] + tid; j < sm.red_i[0][1]; j += S::THREADS) {
+      const int i = ctb[j] - tb;
+      atomicOr(&pmask[i >> 4], 1u << (i & 15));
+    }
+    __syncthreads();
+  }
 
   // ---- the pages of my segment with at least one attended token, ascending
   int nlist = 0;
@@ -784,9 +844,14 @@ __device__ __noinline__ bool range_attend(const StepKArgs& a, Smem& sm, unsigned
   for (int j0 = 0; j0 < npg; j0 += S::THREADS) {
     const int j = j0 + tid;
     int any = 0;
-    if (j < npg)
-      #pragma unroll 1
-      for (int r = 0; r < S::P && !any; ++r) any = attended(j * S::P + r);
+    if (j < npg) {
+      if constexpr (HIT) {
+        any = pmask[j] != 0u;
+      } else {
+        #pragma unroll 1
+        for (int r = 0; r < S::P && !any; ++r) any = attended(j * S::P + r);
+      }
+    }
     int tot;
     const int pos = block_scan(any, sm.wsum, tot);
     if (any) {
@@ -814,11 +879,29 @@ __device__ __noinline__ bool range_attend(const StepKArgs& a, Smem& sm, unsigned
     const bool ok = page >= 0 && (int64_t)page < a.num_pages;
     pv_ok[s] = ok;
     unsigned char* dst = stage + (size_t)s * SLOT;
-    mbar_arrive_expect_tx(&bars[s], (ok ? VPAGE : 0) + LROWS);
-    if (ok) bulk_g2s(dst, a.v_pool + (size_t)page * VPAGE, VPAGE, &bars[s]);
-    else set_error(a.status, TS_ERR_PAGE_OOB);
-    bulk_g2s(dst + VPAGE, eb + (size_t)j * S::P * HQ, LROWS, &bars[s]);
+    if constexpr (HIT) {
+      mbar_arrive_expect_tx(&bars[s], ok ? 2 * VPAGE : 0);
+      if (ok) {
+        bulk_g2s(dst, a.v_pool + (size_t)page * VPAGE, VPAGE, &bars[s]);
+        bulk_g2s(dst + VPAGE, a.k_pool + (size_t)page * VPAGE, VPAGE, &bars[s]);
+      }
+    } else {
+      mbar_arrive_expect_tx(&bars[s], (ok ? VPAGE : 0) + LROWS);
+      if (ok) bulk_g2s(dst, a.v_pool + (size_t)page * VPAGE, VPAGE, &bars[s]);
+      bulk_g2s(dst + VPAGE, eb + (size_t)j * S::P * HQ, LROWS, &bars[s]);
+    }
+    if (!ok) set_error(a.status, TS_ERR_PAGE_OOB);
   };
+  // hit scores: warp -> (KV head gw, tokens wsl, wsl + NWG, ...), its G queries in registers
+  const int gw = warp % HKV, wsl = warp / HKV;
+  float qreg[S::GP][EPL];
+  if constexpr (HIT) {
+#pragma unroll
+    for (int h = 0; h < S::GP; ++h)
+#pragma unroll
+      for (int e = 0; e < EPL; ++e)
+        qreg[h][e] = h < G ? a.q[((size_t)b * HQ + gw * G + h) * D + lane * EPL + e] : 0.f;
+  }
   if (tid == 0) {
     fence_proxy_async_global();
     #pragma unroll 1
@@ -838,8 +921,31 @@ __device__ __noinline__ bool range_attend(const StepKArgs& a, Smem& sm, unsigned
     const bool landed = mbar_wait(&bars[s], (k / nslot) & 1, a.wait_ns);
     unsigned char* slot = stage + (size_t)s * SLOT;
     const KT* Vp = reinterpret_cast<const KT*>(slot);
-    const float* Lp = reinterpret_cast<const float*>(slot + VPAGE);
-    float* Wp = reinterpret_cast<float*>(slot + VPAGE + LROWS);
+    float* Lp = reinterpret_cast<float*>(slot + (HIT ? 2 : 1) * VPAGE);
+    float* Wp = Lp + S::P * HQ;
+    if constexpr (HIT) {
+      // the page's logits for every query head (rows past the sequence or of a page outside the
+      // pool are computed but never attended)
+      const KT* Kp = reinterpret_cast<const KT*>(slot + VPAGE);
+      #pragma unroll 1
+      for (int r = wsl; r < S::P; r += NWG) {
+        float kf[EPL];
+        load_elems<KT, EPL>(Kp + ((size_t)gw * S::P + r) * D + lane * EPL, kf);
+        float accq[S::GP];
+#pragma unroll
+        for (int h = 0; h < S::GP; ++h) {
+          float x = 0.f;
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) x = fmaf(qreg[h][e], kf[e], x);
+          accq[h] = x;
+        }
+        int which;
+        const float dot = transpose_reduce<S::GP, 32>(accq, lane, which);
+        if ((lane & (32 / S::GP - 1)) == 0 && which < G)
+          Lp[r * HQ + gw * G + which] = fmaf(dot, a.scale_l2, dot * a.scale_l2_lo);
+      }
+      __syncthreads();
+    }
     float xl = -INFINITY;
     bool att = false;
     if (wt && landed) {
@@ -2883,17 +2989,21 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     constexpr bool kRangeTC = S::TC && D == 128 && 2 * G <= 16 && HKV * 16 <= 256 &&
                               range_tc_slots<D, HKV, G>(kStageMin, kStepFlagCap) >= 2 &&
                               (HQ * D + S::P * HQ) * 4 <= 2 * HKV * S::P * D * 2;
-    if (bal) {
-      // top-p sequences that take the range attention: every CTA attends the attended tokens of
-      // its own scanned range, when the selection is dense enough that streaming each range's
-      // pages beats sharing the tokens out (pages of the busiest range against the even share
-      // of tokens, in the ratio of their measured costs); the same decision in every CTA, from
-      // the per-CTA counts published before the barrier
+    const bool topp_att = a.mode == TS_SELECT_TOPP && (a.phases & kPhSelect) && (a.phases & kPhAttend);
+    if (topp_att) {
+      // top-p sequences that take the range attention (1: a miss over each CTA's scanned range; 2:
+      // a hit over an even split of its pages) when the selection is dense enough that streaming
+      // pages beats sharing the tokens out, in the ratio of their measured costs: for a miss the
+      // pages of the busiest range against the even share of tokens, for a hit all its pages
+      // (K and V) against all its attended tokens. The same decision in every CTA, from the
+      // per-CTA counts published before the barrier and the cache state read at set-up.
       constexpr int RSLOT = S::STAGE_BYTES + 2 * S::P * HQ * 4;
-      const int rslots =
-          min(kRangeSlots, (stage_bytes - kRangeSlots * 8 - (2 * (a.flag_cap / S::P) + kRangeSlots) * 4) / RSLOT);
+      const int rslots = range_slots<KT, D, HKV, G, false>(stage_bytes, a.flag_cap);
       const bool range_ok = kRangeGeom && bal && a.range_attend > 0 && sm.hpw == HKV && !sm.scan_dyn &&
                             ((kRangeTC && a.tcv) || (rslots >= 2 && HQ * D * 4 + S::P * HQ * 4 <= rslots * RSLOT));
+      const bool hit_ok = kRangeGeom && a.range_attend > 0 && a.ct != nullptr &&
+                          range_slots<KT, D, HKV, G, true>(stage_bytes, a.flag_cap) >= 2 &&
+                          HQ * D * 4 + S::P * HQ * 4 <= 2 * (2 * S::STAGE_BYTES + 2 * S::P * HQ * 4);
       #pragma unroll 1
       for (int b = 0; b < B; ++b) {
         const SeqState& st = sm.seq[b];
@@ -2923,6 +3033,12 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
             take = a.range_attend == 2 || (int64_t)umax * 4 * nCTA <= (int64_t)(tot + nfix) * 3;
           }
           __syncthreads();
+        } else if (hit_ok && st.hit && st.n > 0) {
+          const int npg_seq = (st.n + S::P - 1) / S::P;
+          const int nfix = st.s_end + (st.n - st.ls) + (sm.ct_hi[b] - sm.ct_lo[b]);
+          if ((npg_seq + nCTA - 1) / nCTA <= a.flag_cap / S::P &&
+              (a.range_attend == 2 || (int64_t)npg_seq * 5 <= (int64_t)nfix))
+            take = 2;
         }
         if (tid == 0) sm.bal.range_b[b] = take;
       }
@@ -2931,7 +3047,13 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
     #pragma unroll 1
     for (int b = 0; b < B; ++b) {
       const SeqState& st = sm.seq[b];
-      if (bal && sm.bal.range_b[b]) {
+      if (topp_att && sm.bal.range_b[b]) {
+        if (sm.bal.range_b[b] == 2) {          // a hit: every CTA takes its share of the pages
+          if constexpr (kRangeGeom)
+            if (!range_attend<KT, D, HKV, G, true>(a, sm, dsm, stage_bytes, selflag, b, -1, ao, aml, nCTAp, dq))
+              return;
+          continue;
+        }
         const int sgr = sm.my_seg_of[b];
         if (sgr >= 0) {
           if constexpr (kRangeTC) {
@@ -2942,7 +3064,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
             }
           }
           if constexpr (kRangeGeom)
-            if (!range_attend<KT, D, HKV, G>(a, sm, dsm, stage_bytes, selflag, b, sgr, ao, aml, nCTAp, dq)) return;
+            if (!range_attend<KT, D, HKV, G, false>(a, sm, dsm, stage_bytes, selflag, b, sgr, ao, aml, nCTAp, dq))
+              return;
         } else {
           if (tid < HQ) aml[((size_t)b * H + tid) * nCTAp + c] = make_float2(-INFINITY, 0.f);
           fence_proxy_async_global();
