@@ -509,7 +509,8 @@ struct Smem {
 // histogram started / zeroed / counted (added: 28 + l) / barrier passed; 45 / 46 coarse / fine bins
 // fetched; 47 classified, 48 candidate barrier passed, 49 candidates fetched, 50 ranked; 51
 // attention queries loaded, 52 fixed rows requested, 53 own rows requested; 54 first merge
-// item fetched, 55 counts read. Over all CTAs, the latest to finish the tensor-core scan (56), the
+// item fetched, 55 counts read; the first attention round's 9, 10, 16 and its end again in 8, 12,
+// 19 and 31. Over all CTAs, the latest to finish the tensor-core scan (56), the
 // votes (57), the classification (58) and the selection flags (59); 61..63: which CTA that was
 // for 57..59. (The marks of waves past the first share slots 5..19 with the
 // others; slots 17 and 18 also take the latest start and end over all CTAs.)
@@ -3145,6 +3146,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
       for (int k = 0; k < NG; ++k) o[k] = make_float4(0.f, 0.f, 0.f, 0.f);
       int fdone = 0;     // fixed tokens of mine already taken
       int opos = 0;      // next own token (position in my list)
+      bool first_round = true;   // (diagnosis: the first round's marks go to slots 8, 12, 19 and 31)
       int ob0 = 0, ob_end = 0;   // my share's positions [ob0, ob_end) looked up in ob_t / ob_p
       // the K and V rows of every KV head of list entries [j0, j1), 16 bytes per thread and copy
       // (all of them in flight at once), as one commit group
@@ -3243,6 +3245,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           __syncthreads();
         }
         TS_MARK(9);
+        if (first_round) TS_MARK(8);
         if (cnt == 0) break;                          // uniform: same counters in every thread
         // ---- the own tokens' rows, then every row of the round has landed
         __syncthreads();
@@ -3251,6 +3254,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         cp_async_wait_all();
         __syncthreads();
         TS_MARK(10);
+        if (first_round) TS_MARK(12);
         // ---- (1) scores: warp -> (its KV head, tokens wsl, wsl + NWG, ...); lane holds EPL dims,
         // the G dot products are reduced across the warp so that lane `which` ends with head `which`
 #pragma unroll 4   // independent tokens: their loads and shuffle trees overlap
@@ -3297,6 +3301,7 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         }
         __syncthreads();
         TS_MARK(16);
+        if (first_round) TS_MARK(19);
         // ---- (3) outputs: thread -> float4 slices (head, 4 dims)
 #pragma unroll
         for (int k = 0; k < NG; ++k) {
@@ -3342,6 +3347,8 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
           }
         }
         __syncthreads();
+        if (first_round) TS_MARK(31);
+        first_round = false;
       }
       TS_MARK(11);
       // ---- this CTA's partial of every query head (read back by bulk copy after the barrier)
