@@ -649,6 +649,19 @@ def oracle_steps(max_seconds=20.0, min_steps=2, head_groups=None, steps=None, wa
     return times, (c1.user + c1.system) - (c0.user + c0.system), w1 - w0
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu), else the platform's processor string."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:  # noqa: BLE001
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def _oracle_replica(_):
     """One process of the all-cores CPU baseline: its own copy of the 128K trajectory."""
     import torch
@@ -677,7 +690,7 @@ def cpu_baseline_main():
     except Exception:  # noqa: BLE001 - keep the one-core number
         pass
     print(json.dumps({"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                      "threads_available": n, "value_1core": one, "cores_1core": cores1,
+                      "threads_available": n, "cpu_model": cpu_model(), "value_1core": one, "cores_1core": cores1,
                       "sample": f"steps of the 128K trajectory (theta 0.9), full heads, fp64 numpy oracle on "
                                 f"CPU-generated inputs of the same recipe: {nsteps} steps over {n} processes "
                                 f"(one replica each, about 12 s), and {len(times)} steps in one process for "
