@@ -2821,48 +2821,24 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
         }
         __syncthreads();                                  // red_i is reused below
       }
-      // tokens of the crossing bin (at most kCandCap in a sequence): listed in token order, then
-      // dealt out round-robin over the warps, each ranked against the gathered candidates (a
-      // warp's 32 tokens have their votes loaded at once, one per lane)
+      // tokens of the crossing bin: the warp ranks those of its own range against the gathered
+      // candidates (a chunk's crossing tokens have their votes loaded at once, one per lane)
       if (st.cand) {
-        int* xl = reinterpret_cast<int*>(scand + kCandCap);
-        int nxw = 0;
-        #pragma unroll 1
-        for (int i0 = w0; i0 < w1; i0 += 32) nxw += __popc(__ballot_sync(kFull, i0 + lane < w1 && fl[i0 + lane] == 2));
-        if (lane == 0) sm.red_i[0][warp] = nxw;
-        __syncthreads();
-        int xbase = 0, nx = 0;
-        #pragma unroll 1
-        for (int w = 0; w < S::NW; ++w) {
-          if (w < warp) xbase += sm.red_i[0][w];
-          nx += sm.red_i[0][w];
-        }
+        int ncross = 0;
         #pragma unroll 1
         for (int i0 = w0; i0 < w1; i0 += 32) {
           const bool cr = i0 + lane < w1 && fl[i0 + lane] == 2;
-          const unsigned bal = __ballot_sync(kFull, cr);
-          const int pos = xbase + __popc(bal & ((1u << lane) - 1u));
-          if (cr && pos < kCandCap) xl[pos] = i0 + lane;
-          xbase += __popc(bal);
-        }
-        __syncthreads();
-        nx = min(nx, kCandCap);
-        int ncross = 0;
-        #pragma unroll 1
-        for (int x0 = warp; x0 < nx; x0 += 32 * S::NW) {
-          const int xi = x0 + lane * S::NW;
-          const int myii = xi < nx ? xl[xi] : -1;
-          const uint32_t mykey = myii >= 0 ? __float_as_uint(__ldcg(vb + tl0 + myii)) : 0u;
-          const int nloc = min(32, (nx - x0 + S::NW - 1) / S::NW);
-          ncross += nloc;
-          #pragma unroll 1
-          for (int q = 0; q < nloc; ++q) {
-            const int ii = __shfl_sync(kFull, myii, q);
-            const uint32_t kk = __shfl_sync(kFull, mykey, q);
+          const uint32_t mykey = cr ? __float_as_uint(__ldcg(vb + tl0 + i0 + lane)) : 0u;
+          unsigned bal = __ballot_sync(kFull, cr);
+          ncross += __popc(bal);
+          while (bal) {
+            const int src = __ffs(bal) - 1, ii = i0 + src;
+            bal &= bal - 1u;
+            const uint32_t kk = __shfl_sync(kFull, mykey, src);
             const unsigned long long me = ((unsigned long long)kk << 32) | (0xffffffffu - (uint32_t)(tl0 + ii));
             unsigned above = 0;
             unsigned long long cum = 0;
-            #pragma unroll 8   // independent loads in flight together
+            #pragma unroll 8   // independent loads in flight together (a warp may rank dozens of tokens)
             for (int j = lane; j < m_cand; j += 32) {
               const unsigned long long y = scand[j];
               if (y > me) {
@@ -2876,13 +2852,13 @@ __device__ __forceinline__ void step_body(const StepKArgs& a) {
               cum += __shfl_xor_sync(kFull, cum, d);
             }
             if (lane == 0) fl[ii] = (topp ? (cum < st.mass_rem) : (above < (unsigned)st.k_rem)) ? 1 : 0;
+            __syncwarp();
           }
         }
         // diagnosis (slot 60): the most crossing tokens one warp ranked, above the candidate count
         // and the CTA
         if (lane == 0 && a.phase_ns)
           atomicMax(&a.phase_ns[60], ((unsigned long long)ncross << 32) | ((unsigned long long)m_cand << 8) | (unsigned)c);
-        __syncthreads();   // every flag decided before the counts below
       }
       TS_MARK(50);
       // counts per warp (all, in [s_end, ls), below s_end), then the list in token order, the list
@@ -3635,7 +3611,7 @@ ts_status run_step(ts_ctx* ctx, const StepCall& c, cudaStream_t s) {
   const int nslot = std::min(kMaxSlots, (dyn - flag_cap) / S::STAGE_BYTES);
   // (the vote pass keeps (max, 1/sum) per segment and head, one segment's CTA partials and
   // per-warp reductions; the merge one (sequence, head)'s CTA rows)
-  if (nslot < S::MIN_SLOTS || dyn - flag_cap < lvl_bins(0) * 12 || dyn - flag_cap < kCandCap * 12 ||
+  if (nslot < S::MIN_SLOTS || dyn - flag_cap < lvl_bins(0) * 12 || dyn - flag_cap < kCandCap * 8 ||
       dyn - flag_cap < kMaxB * 128 * 12 ||
       dyn - flag_cap < kMaxB * kMaxWaveHeads * 8 + ctx->num_sms * S::PV * ctx->cfg.n_q_heads * 8 + 2 * 16 * 32 * 4 + 16 +
                            kVoteBufs * 16 * kMaxWaveHeads * 4 ||   // vote scratch, then the chunks of 16 logit rows
