@@ -23,7 +23,7 @@ import pytest
 import torch
 
 import workloads as W
-from parity import GpuRunner, check_attention, run_trajectory
+from parity import GpuRunner, check_attention, run_trajectory, tsl
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -141,3 +141,26 @@ def test_topp_fp32_small_heads(path, monkeypatch):
     sp = W.spec(0, steps=4, mode="topp", top_p=0.9, n0=(1024,))
     rep = run_trajectory(W.generate(sp, DEV), 4)
     _report(path, rep)
+
+
+@pytest.mark.parametrize("theta", [2.0, 0.9])
+def test_topp_range_page_outside_the_pool_is_reported(theta, monkeypatch):
+    # one sequence's page table names a page past the pool on a miss step (theta 2.0) and on a
+    # dense hit (theta 0.9, the cached query again): the range attention skips the page and the
+    # status reports it; the next step on a valid table is clean
+    _set_path(monkeypatch, "range")
+    T = tsl()
+    sp = W.spec(4, n0=(3000, 1500, 700, 4000), steps=2, top_p=1.0, needles="lnN2")
+    wl = W.generate(sp, DEV)
+    r = GpuRunner(wl, theta=theta)
+    r.step(0)                                          # fills the cache (a miss)
+    bad = wl.page_table.clone()
+    bad[1, 5] = wl.num_pages + 7
+    r.ctx.decode_step(wl.q[0][0], wl.k_pool[0], wl.v_pool[0], bad, wl.seq_lens(0), r.params, r.idx, r.count,
+                      r.out, r.lse, hit=r.hit, vote=r.vote, cache=r.cache, layer=0)
+    assert r.ctx.status() == T.STATUS_CODE["TS_ERR_PAGE_OOB"]
+    if theta <= 1.0:
+        assert bool(r.hit.cpu().numpy().all())         # the same query: every sequence hit
+    g = r.step(1)                                      # asserts a clean status
+    assert np.all(np.isfinite(g["out"]))
+    r.ctx.close()
