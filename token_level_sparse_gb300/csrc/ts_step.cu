@@ -21,12 +21,16 @@
 //    once the crossing bin holds at most 2048 tokens they are gathered and
 //    ranked exactly (ties go to the lower index; top-p mass in 2^-40 fixed
 //    point). Each CTA then writes its selected tokens as an ascending list into
-//    its spent logit scratch;
+//    a buffer of its own (its logits stay in its scratch);
 //  * attention: every CTA attends its own selected tokens (with top-p an equal
-//    share of every CTA's lists) plus a round-robin share of the sinks, window
-//    and cached indices, gathering K/V rows by bulk copy; per-CTA (max, sum, o)
-//    partials are merged after one more barrier, and the index lists and the
-//    Selection Cache entries are written from the per-CTA lists.
+//    share of every CTA's lists; a batch of top-k sequences: an equal share
+//    over the sequence's group of CTAs) plus a round-robin share of the sinks,
+//    window and cached indices, gathering K/V rows by cp.async. Dense top-p
+//    selections instead attend each CTA's own range of pages (range_attend):
+//    misses from the scan's logits and streamed V pages, cache hits from
+//    streamed K and V pages. Per-CTA (max, sum, o) partials are merged after one
+//    more barrier, and the index lists and the Selection Cache entries are
+//    written from the per-CTA lists.
 // Grid barriers and mbarrier waits are bounded by %globaltimer; on time-out
 // the kernel records TS_ERR_TIMEOUT and returns. The last CTA to leave zeroes
 // the barrier words for the next launch.
