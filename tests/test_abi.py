@@ -61,6 +61,15 @@ def test_validation_before_cuda(lib):
     assert lib.ts_create(ctypes.byref(h), ctypes.byref(bad)) == INVALID
     odd_page = T.Config(32, 8, 128, 8, T.TS_KV_BF16, 1, 10, 10)
     assert lib.ts_create(ctypes.byref(h), ctypes.byref(odd_page)) == T.STATUS_CODE["TS_ERR_UNSUPPORTED"]
+    # one token per page passes validation (here, without a GPU, creation then stops at CUDA), and
+    # its token count is bounded like 16-token pages'
+    token_pages = T.Config(32, 8, 128, 1, T.TS_KV_BF16, 1, 10, 10)
+    rc = lib.ts_create(ctypes.byref(h), ctypes.byref(token_pages))
+    assert rc not in (T.STATUS_CODE["TS_ERR_UNSUPPORTED"], INVALID, T.STATUS_CODE["TS_ERR_SHAPE"])
+    if rc == 0:                                     # (with a GPU the context exists)
+        lib.ts_destroy(h)
+    too_many = T.Config(32, 8, 128, 1, T.TS_KV_BF16, 1, (1 << 30) + 1, 10)
+    assert lib.ts_create(ctypes.byref(h), ctypes.byref(too_many)) == T.STATUS_CODE["TS_ERR_SHAPE"]
     no_kernel = T.Config(24, 8, 96, 16, T.TS_KV_BF16, 1, 10, 10)
     assert lib.ts_create(ctypes.byref(h), ctypes.byref(no_kernel)) == T.STATUS_CODE["TS_ERR_UNSUPPORTED"]
     p = T.params()
