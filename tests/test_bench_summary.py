@@ -62,3 +62,20 @@ def test_committed_traffic_line_is_well_formed():
     m = re.search(r"step_traffic_bytes_per_launch_n128k:\s*([0-9.e+]+)\s+step_source_sha256:\s*([0-9a-f]{64})", text)
     assert m is not None
     assert 270e6 < float(m.group(1)) < 300e6                       # ~K scan + gathers + small writes
+
+
+def test_minimum_bytes_count_the_scan_and_the_selected_v_rows():
+    # the algorithmic bytes count K and V of every selected token; the minimum counts the K scan
+    # and the V rows only (the range attention reuses the scan's logits and reads no K row again)
+    rec = [_rec(1.0, True, scan=2_147_483_648, gather=3_600_000_000), _rec(1.0, False, gather=3_600_000_000)]
+    s = bench.summarise(_bench(), rec, 6668.5)
+    alg = 2_147_483_648 + 2 * 3_600_000_000
+    low = 2_147_483_648 + 2 * 1_800_000_000
+    assert abs(s["step_gbs"] - alg / 2e-3 / 1e9) < 1e-6
+    assert abs(s["min_step_gbs"] - low / 2e-3 / 1e9) < 1e-6
+    assert abs(s["min_frac_of_peak"] - s["min_step_gbs"] / 6668.5) < 1e-12
+    assert s["min_step_gbs"] < s["step_gbs"]
+
+
+def test_cpu_model_is_named():
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
