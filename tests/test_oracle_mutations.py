@@ -44,6 +44,7 @@ MUTATIONS = {
     "prefill causal off by one": ("visible = idx[idx <= n - c + i]", "visible = idx[idx < n - c + i]"),
     "logit sum as max": ("return np.asarray(logits, dtype=np.float64).sum(axis=0)",
                          "return np.asarray(logits, dtype=np.float64).max(axis=0)"),
+    "page size fixed at 16": ("    P = pool.shape[2]\n", "    P = 16\n"),
 }
 
 
